@@ -1,0 +1,538 @@
+#!/usr/bin/env python3
+"""Throughput of the canonical Huffman hot path on one GB300 (or N, weak-scaled).
+
+Default workload: the incremental snapshot delta.  x0 = bf16(N(0, 0.02)) and
+x1 = bf16(x0 + N(0, 1e-4)) of shape [65536, 30518] (2.0e9 elements, 4.0 GB
+each), resident in HBM.  One step is one pass of the whole path:
+  lmc_histogram_bf16(x1, x0)      XOR delta + byte planes + two histograms
+  huff_build_codebook x 2         lengths, canonical codes, decode tables
+  lmc_encode_bf16(x1, x0)         XOR delta + byte planes + encode of both planes
+  lmc_decode_bf16(..., x0)        decode both planes, merge, XOR x0 back in
+value = snapshot bytes (2n) / step time: uncompressed GB/s of a full
+compress + decompress round trip.  Inputs (8 GB) exceed the 129 MB L2, so no
+flush is needed between steps.
+
+--impl reference times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Huffman encode/decode GB/s (uncompressed) at 1 GB300; % HBM roofline; ratio"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {"k_decode_bf16": "decode.cu", "k_encode_bf16": "encode.cu", "k_histogram_bf16": "histogram.cu"}
+
+
+# ------------------------------------------------------------------ environment
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def max_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash(name: str) -> str:
+    src = os.path.join(ROOT, "lossless_huffman_compression_gb300", "csrc", KERNEL_SOURCES[name])
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(name: str, units: float):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        e = j[name]
+        if e.get("source_sha256_16") != kernel_hash(name):
+            return None
+        return float(e["dram_bytes_per_unit"]) * units
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our arm
+class SnapshotPath:
+    """Buffers and the step for the snapshot-delta workload."""
+
+    def __init__(self, x0, x1, chunk, max_len=24):
+        from lossless_huffman_compression_gb300 import _lib, codec
+        self.L = _lib
+        self.codec = codec
+        dev = x1.device
+        self.x0 = x0.reshape(-1).view(torch.int16)
+        self.x1 = x1.reshape(-1).view(torch.int16)
+        self.n = n = self.x1.numel()
+        self.chunk = chunk
+        self.max_len = max_len
+        self.h_hi = torch.zeros(256, dtype=torch.int64, device=dev)
+        self.h_lo = torch.zeros(256, dtype=torch.int64, device=dev)
+        self.cb_hi = codec.Codebook(dev)
+        self.cb_lo = codec.Codebook(dev)
+        cap = _lib.huff_encode_bound(n, max_len)
+        self.p_hi = torch.empty(cap, dtype=torch.uint8, device=dev)
+        self.p_lo = torch.empty(cap, dtype=torch.uint8, device=dev)
+        self.nc = _lib.huff_num_chunks(n, chunk)
+        self.o_hi = torch.empty(self.nc + 1, dtype=torch.int64, device=dev)
+        self.o_lo = torch.empty(self.nc + 1, dtype=torch.int64, device=dev)
+        self.ws = torch.empty(_lib.lmc_workspace_size(n, chunk) // 8 + 2, dtype=torch.int64, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out = torch.empty(n, dtype=torch.int16, device=dev)
+        # kernels launched per step: hist (2 zero + 1), build (2), encode (1 zero + 1), decode (1)
+        self.launches_per_step = 8
+
+    def compress(self, w=None, x0=None):
+        L = self.L
+        w = self.x1 if w is None else w
+        x0 = self.x0 if x0 is None else x0
+        L.lmc_histogram_bf16(w, x0, self.h_hi, self.h_lo)
+        L.huff_build_codebook(self.h_hi, self.cb_hi.buf, self.status, self.max_len, 0)
+        L.huff_build_codebook(self.h_lo, self.cb_lo.buf, self.status, self.max_len, 0)
+        L.lmc_encode_bf16(w, x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.p_hi, self.o_hi, self.p_lo,
+                          self.o_lo, self.ws, self.status)
+
+    def decompress(self, x0=None, out=None):
+        x0 = self.x0 if x0 is None else x0
+        out = self.out if out is None else out
+        self.L.lmc_decode_bf16(self.p_hi, self.o_hi, self.p_lo, self.o_lo, self.n, self.chunk, self.cb_hi.buf,
+                               self.cb_lo.buf, x0, out, self.status)
+
+    def step_with_events(self, ev):
+        L = self.L
+        ev[0].record()
+        L.lmc_histogram_bf16(self.x1, self.x0, self.h_hi, self.h_lo)
+        ev[1].record()
+        L.huff_build_codebook(self.h_hi, self.cb_hi.buf, self.status, self.max_len, 0)
+        L.huff_build_codebook(self.h_lo, self.cb_lo.buf, self.status, self.max_len, 0)
+        ev[2].record()
+        L.lmc_encode_bf16(self.x1, self.x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.p_hi, self.o_hi,
+                          self.p_lo, self.o_lo, self.ws, self.status)
+        ev[3].record()
+        L.lmc_decode_bf16(self.p_hi, self.o_hi, self.p_lo, self.o_lo, self.n, self.chunk, self.cb_hi.buf,
+                          self.cb_lo.buf, self.x0, self.out, self.status)
+        ev[4].record()
+
+    def check(self):
+        torch.cuda.synchronize()
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {self.L.status_string(st)}")
+        if not torch.equal(self.out, self.x1):
+            raise RuntimeError("decoded snapshot differs from x1")
+
+    def sizes(self):
+        T_hi = int(self.o_hi[-1].item())
+        T_lo = int(self.o_lo[-1].item())
+        return T_hi, T_lo
+
+
+def run_ours(args, dist, rank, ws):
+    from lossless_huffman_compression_gb300 import workloads
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    shape = workloads.SNAPSHOT_SHAPE if not args.small else (4096, 30518)
+    x0, x1 = workloads.snapshot_pair(device=dev, shape=shape)
+    path = SnapshotPath(x0, x1, args.chunk)
+    n = path.n
+    snap_bytes = 2 * n
+
+    for _ in range(args.warmup):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        path.step_with_events(ev)
+    path.check()  # lossless and error-free before timing
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(args.steps):
+        path.step_with_events(evs[k])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+    ms_local = t0.elapsed_time(t1) / args.steps
+    ms = max_over_ranks(dist, ms_local, dev)
+    path.check()
+
+    stage_names = ["histogram_bf16_xor", "build_codebook_x2", "encode_bf16_xor", "decode_bf16_xor"]
+    stage_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, nm in enumerate(stage_names)}
+    T_hi, T_lo = path.sizes()
+    C = (T_hi + 7) // 8 + (T_lo + 7) // 8
+    offs = 2 * 8 * (path.nc + 1)
+    peak, peak_kind = hbm_peak()
+    alg = {  # algorithmic bytes per launch
+        "histogram_bf16_xor": 4 * n + 2 * 2048,
+        "build_codebook_x2": 2 * (2048 + 21504),
+        "encode_bf16_xor": 4 * n + C + offs,
+        "decode_bf16_xor": C + offs + 4 * n,
+    }
+    stages = {}
+    for nm in stage_names:
+        t = stage_ms[nm] / 1e3
+        stages[nm] = {"ms": round(stage_ms[nm], 4), "gbs_uncompressed": round(snap_bytes / t / 1e9, 1),
+                      "alg_bytes": int(alg[nm]), "hbm_frac": round(alg[nm] / t / 1e9 / peak, 4)}
+    dom = max(["histogram_bf16_xor", "encode_bf16_xor", "decode_bf16_xor"], key=lambda k: stage_ms[k])
+    kname = {"histogram_bf16_xor": "k_histogram_bf16", "encode_bf16_xor": "k_encode_bf16",
+             "decode_bf16_xor": "k_decode_bf16"}[dom]
+    achieved = alg[dom] / (stage_ms[dom] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": recorded_traffic(kname, 1.0)}
+
+    # extra: encode / decode of the already-materialised delta (codebooks given), outside the step
+    extra = materialised_delta_stages(path, args, peak)
+
+    # quality
+    from lossless_huffman_compression_gb300 import _lib
+    h_hi = path.h_hi.cpu().numpy().astype(np.uint64)
+    h_lo = path.h_lo.cpu().numpy().astype(np.uint64)
+    s_hi = _lib.huff_code_stats(h_hi, path.cb_hi.lengths())
+    s_lo = _lib.huff_code_stats(h_lo, path.cb_lo.lengths())
+    quality = {
+        "payload_ratio": round(snap_bytes / C, 4),
+        "container_ratio": round(snap_bytes / (C + offs + 512), 4),
+        "hi_bits_per_symbol": round(s_hi["mean_len"], 4), "hi_entropy": round(s_hi["entropy_bits"], 4),
+        "lo_bits_per_symbol": round(s_lo["mean_len"], 4), "lo_entropy": round(s_lo["entropy_bits"], 4),
+        "hi_shannon_gap": round(s_hi["shannon_gap"], 5), "lo_shannon_gap": round(s_lo["shannon_gap"], 5),
+    }
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_snapshot(path, x0, x1, args, dist, dev)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_snapshot(x0, x1, args)
+
+    total_units = sum_over_ranks(dist, float(snap_bytes), dev)
+    value = total_units / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "snapshot_delta_bf16_65536x30518" if not args.small else "snapshot_delta_bf16_small",
+                   "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk, "max_len": 24,
+                   "step": "xor+split+hist, build x2, fused encode, fused decode+merge+xor",
+                   "l2": "inputs (8 GB) larger than L2; no flush", "parallelism": f"replicas{ws}"},
+        "roofline": roofline, "stages": stages, "materialised_delta": extra, "quality": quality,
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": path.launches_per_step * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def materialised_delta_stages(path, args, peak):
+    """Encode and decode of the byte-grouped delta d = x1 ^ x0 held in HBM (codebooks given)."""
+    L = path.L
+    n = path.n
+    d = torch.empty_like(path.x1)
+    L.lmc_delta_xor(path.x1, path.x0, d)
+    reps = max(3, min(args.steps, 10))
+    out = {}
+    for nm, fn in (("encode_bf16", lambda: L.lmc_encode_bf16(d, None, path.cb_hi.buf, path.cb_lo.buf, path.chunk,
+                                                             path.p_hi, path.o_hi, path.p_lo, path.o_lo, path.ws,
+                                                             path.status)),
+                   ("decode_bf16", lambda: L.lmc_decode_bf16(path.p_hi, path.o_hi, path.p_lo, path.o_lo, n,
+                                                             path.chunk, path.cb_hi.buf, path.cb_lo.buf, None,
+                                                             path.out, path.status))):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        T_hi, T_lo = path.sizes()
+        C = (T_hi + 7) // 8 + (T_lo + 7) // 8 + 2 * 8 * (path.nc + 1)
+        alg = 2 * n + C
+        out[nm] = {"ms": round(ms, 4), "gbs_uncompressed": round(2 * n / ms / 1e6, 1), "alg_bytes": alg,
+                   "hbm_frac": round(alg / ms / 1e6 / peak, 4)}
+    torch.cuda.synchronize()
+    if not torch.equal(path.out, d):
+        raise RuntimeError("materialised-delta decode differs")
+    if int(path.status.item()) != 0:
+        raise RuntimeError("materialised-delta status")
+    del d
+    return out
+
+
+def e2e_snapshot(path, x0, x1, args, dist, dev):
+    """Same step through the public API with HOST buffers: copies inside the timed region."""
+    L = path.L
+    n = path.n
+    h_x1 = torch.empty(n, dtype=torch.int16, pin_memory=True)
+    h_x0 = torch.empty(n, dtype=torch.int16, pin_memory=True)
+    h_x1.copy_(path.x1)
+    h_x0.copy_(path.x0)
+    T_hi, T_lo = path.sizes()
+    cap_hi = ((T_hi + 31) // 32) * 4
+    cap_lo = ((T_lo + 31) // 32) * 4
+    h_p_hi = torch.empty(path.p_hi.numel(), dtype=torch.uint8, pin_memory=True)
+    h_p_lo = torch.empty(path.p_lo.numel(), dtype=torch.uint8, pin_memory=True)
+    h_o_hi = torch.empty(path.nc + 1, dtype=torch.int64, pin_memory=True)
+    h_o_lo = torch.empty(path.nc + 1, dtype=torch.int64, pin_memory=True)
+    h_out = torch.empty(n, dtype=torch.int16, pin_memory=True)
+    d_x1 = torch.empty_like(path.x1)
+    d_x0 = torch.empty_like(path.x0)
+    steps = max(2, min(args.steps, 5))
+
+    def one():
+        d_x1.copy_(h_x1, non_blocking=True)
+        d_x0.copy_(h_x0, non_blocking=True)
+        path.compress(d_x1, d_x0)
+        h_p_hi[:cap_hi].copy_(path.p_hi[:cap_hi], non_blocking=True)
+        h_p_lo[:cap_lo].copy_(path.p_lo[:cap_lo], non_blocking=True)
+        h_o_hi.copy_(path.o_hi, non_blocking=True)
+        h_o_lo.copy_(path.o_lo, non_blocking=True)
+        # decompress from the host-held streams
+        path.p_hi[:cap_hi].copy_(h_p_hi[:cap_hi], non_blocking=True)
+        path.p_lo[:cap_lo].copy_(h_p_lo[:cap_lo], non_blocking=True)
+        path.o_hi.copy_(h_o_hi, non_blocking=True)
+        path.o_lo.copy_(h_o_lo, non_blocking=True)
+        d_x0.copy_(h_x0, non_blocking=True)
+        path.decompress(d_x0, path.out)
+        h_out.copy_(path.out, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(dist)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(dist, a.elapsed_time(b) / steps, dev)
+    if not torch.equal(h_out, h_x1):
+        raise RuntimeError("e2e round trip differs")
+    total = sum_over_ranks(dist, float(2 * n), dev)
+    h2d = 2 * n * 3 + cap_hi + cap_lo + 2 * 8 * (path.nc + 1)
+    d2h = 2 * n + cap_hi + cap_lo + 2 * 8 * (path.nc + 1)
+    del d_x1, d_x0
+    return {"value": round(total / ms / 1e6, 2), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "lmc_histogram_bf16, huff_build_codebook, lmc_encode_bf16, lmc_decode_bf16 with pinned host "
+                   "inputs, streams copied to host and back"}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_snapshot_step(x0h: np.ndarray, x1h: np.ndarray, chunk: int):
+    """The oracle's full path on one sample: delta, planes, codebooks, encode, decode, merge, re-apply."""
+    import oracle
+    d = oracle.delta_xor(x1h, x0h)
+    hi, lo = oracle.bytegroup_split(d)
+    planes = []
+    for p in (hi, lo):
+        ln = oracle.code_lengths(oracle.histogram(p))
+        cd = oracle.canonical_codes(ln)
+        pay, off = oracle.encode(p, ln, cd, chunk)
+        planes.append(oracle.decode(pay, off, p.size, chunk, ln))
+    back = oracle.delta_xor(oracle.bytegroup_merge(planes[0], planes[1]), x0h)
+    if not np.array_equal(back, x1h):
+        raise RuntimeError("oracle round trip failed")
+
+
+def snapshot_sample(x0, x1, elems):
+    a = x0.reshape(-1)[:elems].view(torch.int16).cpu().numpy().view(np.uint16)
+    b = x1.reshape(-1)[:elems].view(torch.int16).cpu().numpy().view(np.uint16)
+    return a, b
+
+
+def cpu_baseline_snapshot(x0, x1, args):
+    elems = args.cpu_sample
+    a, b = snapshot_sample(x0, x1, elems)
+    t = time.perf_counter()
+    oracle_snapshot_step(a, b, args.chunk)
+    dt = time.perf_counter() - t
+    return {"value": round(2 * elems / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {elems} elements of x0/x1 (the snapshot's own distribution); one sequential pass of "
+                      f"delta, split, histograms, codebooks, encode, decode, merge, re-apply; {dt:.1f} s"}
+
+
+def run_reference(args, dist, rank, ws):
+    """The oracle, as it stands, on a bounded sample per step (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    from lossless_huffman_compression_gb300 import workloads
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    shape = workloads.SNAPSHOT_SHAPE if not args.small else (4096, 30518)
+    x0, x1 = workloads.snapshot_pair(device=dev, shape=shape)
+    elems = args.ref_sample
+    a, b = snapshot_sample(x0, x1, elems)
+    del x0, x1
+    for _ in range(args.warmup):
+        oracle_snapshot_step(a[: elems // 8], b[: elems // 8], args.chunk)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle_snapshot_step(a, b, args.chunk)
+        times.append(time.perf_counter() - t)
+    ms = 1e3 * sum(times) / len(times)
+    value = 2 * elems / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "snapshot_delta_bf16_65536x30518", "chunk_bytes": args.chunk,
+                   "sample_elements": elems},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {elems} elements of x0/x1 per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--chunk", type=int, default=16384)
+    ap.add_argument("--small", action="store_true", help="a 250 MB snapshot instead of 4 GB (quick checks)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=64 << 20, help="elements for the oracle baseline")
+    ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        dist = init_dist(ws, "gloo")
+        run_reference(args, dist, rank, ws)
+        return
+    dist = init_dist(ws, "nccl")
+    run_ours(args, dist, rank, ws)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

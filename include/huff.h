@@ -1,0 +1,309 @@
+/*
+ * huff.h -- C ABI of libhuff: canonical Huffman coding of ML tensor bytes on
+ * one GB300 (sm_103a).
+ *
+ * The calls follow the problem statements of two papers:
+ *   [P1] "Single-stage Huffman encoder for ML compression" (arXiv 2601.10673),
+ *        Overview and Methodology steps 1-4: per-shard Huffman needs frequency
+ *        analysis, codebook generation and codebook transmission for every
+ *        shard; the single-stage scheme counts 8-bit symbols over warm-up
+ *        batches, averages the distributions, builds one codebook once, keeps
+ *        it on every accelerator and encodes later tensors with it alone.
+ *   [P2] "Lossless Compression for LLM Tensor Incremental Snapshots" (arXiv
+ *        2505.09810), Method details / technical framework and the English
+ *        abstract: byte-grouping of bf16 tensors, per-group frequency
+ *        statistics, per-group Huffman trees and codes, decompression as the
+ *        reverse (Huffman-decode, restore the byte groups), and incremental
+ *        delta compression between snapshots.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless their name starts with h_.
+ *   - The caller owns and allocates every buffer.  The library never
+ *     allocates memory, never synchronises the device or the stream, and
+ *     enqueues all its work on `stream` (0 = the legacy default stream).
+ *   - The return value is a huff_status.  It reports argument errors found
+ *     on the host (HUFF_ERR_INVALID_ARG, HUFF_ERR_BUFFER_TOO_SMALL) and
+ *     launch failures (HUFF_ERR_CUDA).  Nothing is enqueued when it is not
+ *     HUFF_OK.
+ *   - Errors found by the GPU while the work runs (a symbol without a code,
+ *     a full output buffer, a corrupt stream, a wait that ran out) are
+ *     written to the caller's device int32 *status: the first error wins,
+ *     later ones are dropped.  The caller zeroes *status before the call and
+ *     reads it after synchronising the stream.  No kernel traps or asserts.
+ *   - n == 0 is valid everywhere.
+ *
+ * Stream format (one byte stream, e.g. an int8 shard or one bf16 byte plane)
+ *   - payload: the canonical code of each symbol appended most significant bit
+ *     first; stream bit k is bit 7 - (k mod 8) of payload byte k / 8; bits
+ *     after the last code up to the end of the last written 32-bit word are 0.
+ *     T = total bits; the stream occupies ceil(T / 8) bytes.
+ *   - chunk_bit_off[c] (uint64, c = 0..n_chunks): bit position where symbol
+ *     c * chunk_bytes starts; chunk_bit_off[n_chunks] = T.  Chunks are not
+ *     padded, so the payload does not depend on chunk_bytes; the offsets are
+ *     the index that lets chunks decode independently.
+ *   - codebook: transmitted as its 256 code lengths only (canonical codes).
+ */
+#ifndef HUFF_H_
+#define HUFF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *huff_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum huff_status {
+    HUFF_OK = 0,
+    HUFF_ERR_INVALID_ARG = -1,            /* bad pointer, size, alignment, flag */
+    HUFF_ERR_BUFFER_TOO_SMALL = -2,       /* output or workspace capacity */
+    HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK = -3, /* encode met a symbol whose length is 0 */
+    HUFF_ERR_CORRUPT_STREAM = -4,         /* decode: invalid code, chunk not ending at its offset, read past payload */
+    HUFF_ERR_TIMEOUT = -5,                /* a bounded device-side wait gave up */
+    HUFF_ERR_CUDA = -6,                   /* a CUDA runtime call or launch failed */
+    HUFF_ERR_INVALID_CODEBOOK = -7        /* codebook not built, or lengths over-subscribe the code space */
+} huff_status;
+
+#define HUFF_MAX_LEN 24          /* longest code the library produces or accepts */
+#define HUFF_MIN_MAX_LEN 8       /* smallest length limit that fits 256 symbols */
+#define HUFF_COVER_ALL 1u        /* raise zero counts to 1 before building (fixed codebooks) */
+#define HUFF_CHUNK_ALIGN 256     /* chunk_bytes must be a positive multiple of this */
+#define HUFF_ALIGN 16            /* alignment (bytes) required of bulk device buffers */
+#define HUFF_LUT_BITS 12         /* first-level decode table index width */
+#define HUFF_CODEBOOK_MAGIC 0x48554642u
+
+/*
+ * Device-resident codebook, built by huff_build_codebook or imported by
+ * huff_codebook_from_lengths.  Allocate sizeof(huff_codebook) bytes of device
+ * memory (16-byte aligned).  len[] is the transmitted form; the rest is
+ * derived from it.  magic == HUFF_CODEBOOK_MAGIC marks a finished codebook.
+ */
+typedef struct huff_codebook {
+    uint32_t magic;            /* HUFF_CODEBOOK_MAGIC once complete */
+    int32_t max_len;           /* length limit it was built with */
+    int32_t n_symbols;         /* symbols with len > 0 */
+    int32_t longest;           /* longest code length present */
+    uint8_t len[256];          /* code length per symbol, 0 = no code */
+    uint32_t code[256];        /* canonical code per symbol, right-aligned */
+    uint32_t bl_count[32];     /* number of codes of each length */
+    uint32_t first_code[32];   /* canonical value of the first code of each length */
+    uint32_t first_index[32];  /* index in sorted_symbols of the first code of each length */
+    uint8_t sorted_symbols[256]; /* symbols ordered by (length, symbol) */
+    uint32_t lut[1u << HUFF_LUT_BITS]; /* decode table: (len << 8) | symbol for codes of <= 12 bits, 0 otherwise */
+} huff_codebook;
+
+/* Per-stream quality figures (host helper). */
+typedef struct huff_stats {
+    uint64_t n;                /* symbols counted */
+    uint64_t total_bits;       /* T = sum_s hist[s] * len[s] */
+    double entropy_bits;       /* H = -sum p log2 p, bits per symbol */
+    double mean_len;           /* T / n */
+    double shannon_gap;        /* (T - n H) / (n H); 0 when n H == 0 */
+} huff_stats;
+
+/* ---------------------------------------------------------------- queries */
+
+/* Library version as 0xMMmmpp. */
+uint32_t huff_version(void);
+
+/* Static text for a status code. */
+const char *huff_status_string(int status);
+
+/* sizeof(huff_codebook), for callers that cannot include this header. */
+size_t huff_codebook_size(void);
+
+/* Worst-case payload bytes for n symbols coded with lengths <= max_len,
+ * rounded up to whole 32-bit words, plus 16 bytes of slack. */
+size_t huff_encode_bound(size_t n, int max_len);
+
+/* Workspace bytes huff_encode needs for n symbols (lookback descriptors and a
+ * tile counter).  chunk_bytes does not change it today; it is an argument so
+ * the format can change without an ABI break. */
+size_t huff_workspace_size(size_t n, size_t chunk_bytes);
+
+/* Number of chunks: ceil(n / chunk_bytes); 0 when n == 0. */
+size_t huff_num_chunks(size_t n, size_t chunk_bytes);
+
+/* ---------------------------------------------------------------- histogram */
+
+/*
+ * huff_histogram -- 256-bin symbol histogram [P1 Methodology step 1; P2
+ * framework stage 2 "frequency statistics"].
+ *   in        n symbols at in[0], in[stride], ..., in[(n-1)*stride]; stride is
+ *             1 (a byte stream, int8 read as its two's-complement byte) or 2
+ *             (one byte plane of a little-endian 16-bit array: pass base for
+ *             the low plane, base + 1 for the high plane).  Any alignment.
+ *   hist      uint64[256], device.  accumulate = 0 overwrites it; accumulate = 1
+ *             adds to it, which is how the averaged warm-up distribution of P1
+ *             Methodology step 2 is formed (the pooled sum; Huffman lengths are
+ *             unchanged by scaling all counts, so the sum gives the mean's
+ *             codebook).
+ */
+int huff_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist,
+                   int accumulate, huff_stream_t stream);
+
+/* ---------------------------------------------------------------- codebook */
+
+/*
+ * huff_build_codebook -- Huffman code lengths and canonical codes from a
+ * histogram [P1 Methodology step 3 "build the Huffman codebook once"; P2 key
+ * design 2 "Huffman tree construction"].  The pages do not fix tie-breaks or a
+ * length limit; the rule used (and reproduced by the CPU oracle) is:
+ *   1. flags & HUFF_COVER_ALL: counts of 0 become 1.
+ *   2. Huffman's procedure: repeatedly join the two smallest nodes by
+ *      (count, id), leaves having id = symbol and new nodes ids 256, 257, ...
+ *   3. Lengths above max_len are repaired with the Adjust_BITS procedure of
+ *      ITU-T T.81 Annex K.3 (without its reserved-code step).
+ *   4. Lengths are handed out again by (count desc, symbol asc).
+ *   5. Canonical codes as in RFC 1951 section 3.2.2.
+ *   6. No present symbol: an empty codebook; one symbol: length 1, code 0.
+ *   hist      uint64[256], device.
+ *   max_len   8..24.
+ *   cb        device huff_codebook, written completely (decode tables too).
+ *   status    device int32; HUFF_ERR_INVALID_CODEBOOK if the build fails.
+ * Runs as one thread block.
+ */
+int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags,
+                        huff_codebook *cb, int32_t *status, huff_stream_t stream);
+
+/*
+ * huff_codebook_from_lengths -- import a transmitted codebook [P1 Key
+ * contributions: the codebook is stored on each accelerator, not exchanged per
+ * batch; it travels once, as 256 lengths].
+ *   h_len     HOST uint8[256]; copied before the call returns.
+ *   max_len   8..24; every length must be <= max_len.
+ *   cb        device huff_codebook; status gets HUFF_ERR_INVALID_CODEBOOK when
+ *             the lengths over-subscribe the code space (Kraft sum > 1).
+ */
+int huff_codebook_from_lengths(const uint8_t *h_len, int max_len, huff_codebook *cb,
+                               int32_t *status, huff_stream_t stream);
+
+/* ---------------------------------------------------------------- encode / decode */
+
+/*
+ * huff_encode -- single-stage encode with a given codebook [P1 Methodology
+ * step 4: tensors are encoded directly with the precomputed codebook; P2
+ * framework stage 3 "Huffman coding", split into parallel tasks].
+ *   in            n symbols, 16-byte aligned.
+ *   cb            device codebook built or imported above.
+ *   chunk_bytes   symbols per chunk, a positive multiple of HUFF_CHUNK_ALIGN.
+ *   payload       16-byte aligned, payload_cap bytes; huff_encode_bound(n,
+ *                 max_len) always suffices.  The stream needs ceil(T/32)*4
+ *                 bytes; a shorter buffer gives HUFF_ERR_BUFFER_TOO_SMALL in
+ *                 *status and a truncated payload.
+ *   chunk_bit_off uint64[n_chunks + 1], device, 8-byte aligned.
+ *   ws, ws_bytes  device workspace of at least huff_workspace_size(n,
+ *                 chunk_bytes) bytes, 16-byte aligned; its contents need not be
+ *                 initialised and are garbage afterwards.  Two encodes that run
+ *                 at the same time need two workspaces.
+ *   status        device int32: HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK,
+ *                 HUFF_ERR_BUFFER_TOO_SMALL, HUFF_ERR_TIMEOUT,
+ *                 HUFF_ERR_INVALID_CODEBOOK.
+ * T = chunk_bit_off[n_chunks] after the stream completes.
+ */
+int huff_encode(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk_bytes,
+                uint8_t *payload, size_t payload_cap, uint64_t *chunk_bit_off,
+                void *ws, size_t ws_bytes, int32_t *status, huff_stream_t stream);
+
+/*
+ * huff_decode -- chunked decode [P2 framework: decompression reads the data,
+ * Huffman-decodes it and restores it; lossless, so the output equals the
+ * encoder's input].
+ *   payload       payload_bytes bytes, 16-byte aligned; reads never pass
+ *                 payload_bytes.
+ *   chunk_bit_off uint64[n_chunks + 1] as written by huff_encode.
+ *   n, chunk_bytes the encoder's values.
+ *   out           n bytes, 16-byte aligned.
+ *   status        HUFF_ERR_CORRUPT_STREAM when a code is invalid, a chunk does
+ *                 not end exactly at the next offset, or an offset lies outside
+ *                 the payload; HUFF_ERR_INVALID_CODEBOOK.
+ */
+int huff_decode(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off,
+                size_t n, size_t chunk_bytes, const huff_codebook *cb, uint8_t *out,
+                int32_t *status, huff_stream_t stream);
+
+/* ---------------------------------------------------------------- LMC byte grouping */
+
+/*
+ * lmc_bytegroup_split -- byte grouping of a 16-bit tensor [P2 framework stage 1
+ * and key design 1; English abstract "byte-grouping"]: hi[i] = w[i] >> 8 (bf16:
+ * sign and the 7 high exponent bits), lo[i] = w[i] & 0xff (lowest exponent bit
+ * and the 7 mantissa bits).  w is little-endian uint16 (the bf16 bit pattern).
+ */
+int lmc_bytegroup_split(const uint16_t *w, size_t n, uint8_t *hi, uint8_t *lo,
+                        huff_stream_t stream);
+
+/* lmc_bytegroup_merge -- inverse of the split [P2 framework, decompression:
+ * "restore the byte groups"]: w[i] = hi[i] << 8 | lo[i]. */
+int lmc_bytegroup_merge(const uint8_t *hi, const uint8_t *lo, size_t n, uint16_t *w,
+                        huff_stream_t stream);
+
+/* lmc_delta_xor -- incremental delta between snapshots [P2 English abstract
+ * "incremental delta compression"; the operator is not given on the pages and
+ * is read as XOR of the bit patterns, which is exact for every value including
+ * NaN, Inf and -0]: out[i] = a[i] ^ b[i].  Self-inverse; out may alias a or b. */
+int lmc_delta_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out,
+                  huff_stream_t stream);
+
+/* ---------------------------------------------------------------- LMC fused bf16 paths */
+
+/*
+ * lmc_histogram_bf16 -- histograms of both byte planes of a bf16 tensor,
+ * optionally of its XOR delta against x0, in one pass (P2 framework stages 1-2
+ * fused).  Equal to lmc_delta_xor + lmc_bytegroup_split + huff_histogram on
+ * each plane.
+ *   w, x0     n uint16 values; x0 may be NULL (no delta).  Any alignment.
+ *   hist_hi, hist_lo  uint64[256] each; accumulate as in huff_histogram.
+ */
+int lmc_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
+                       uint64_t *hist_lo, int accumulate, huff_stream_t stream);
+
+/* Workspace bytes lmc_encode_bf16 needs for n elements. */
+size_t lmc_workspace_size(size_t n, size_t chunk_bytes);
+
+/*
+ * lmc_encode_bf16 -- encode both byte planes of a bf16 tensor (optionally of
+ * its XOR delta against x0) straight from the 16-bit words, each plane with
+ * its own codebook (P2 framework stages 1 and 3 fused).  The outputs are
+ * byte-identical to split + huff_encode per plane: plane streams (payload_hi,
+ * off_hi) and (payload_lo, off_lo) with chunk_bytes elements per chunk.
+ *   w, x0     16-byte aligned; x0 may be NULL.
+ *   other arguments as in huff_encode, once per plane.
+ */
+int lmc_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n,
+                    const huff_codebook *cb_hi, const huff_codebook *cb_lo, size_t chunk_bytes,
+                    uint8_t *payload_hi, size_t cap_hi, uint64_t *off_hi,
+                    uint8_t *payload_lo, size_t cap_lo, uint64_t *off_lo,
+                    void *ws, size_t ws_bytes, int32_t *status, huff_stream_t stream);
+
+/*
+ * lmc_decode_bf16 -- decode both planes and write the 16-bit words, optionally
+ * XOR-ing x0 back in (P2 decompression: Huffman-decode, restore byte groups,
+ * re-apply the delta).  out[i] = (hi[i] << 8 | lo[i]) ^ (x0 ? x0[i] : 0).
+ *   out, x0   16-byte aligned; x0 may be NULL; out may not alias x0.
+ *   other arguments as in huff_decode, once per plane.
+ */
+int lmc_decode_bf16(const uint8_t *payload_hi, size_t bytes_hi, const uint64_t *off_hi,
+                    const uint8_t *payload_lo, size_t bytes_lo, const uint64_t *off_lo,
+                    size_t n, size_t chunk_bytes, const huff_codebook *cb_hi,
+                    const huff_codebook *cb_lo, const uint16_t *x0, uint16_t *out,
+                    int32_t *status, huff_stream_t stream);
+
+/* ---------------------------------------------------------------- host helpers */
+
+/*
+ * huff_code_stats -- quality figures of one stream [P1 Key contributions and
+ * Results: compression is compared against per-shard Huffman and against the
+ * Shannon limit].  h_hist: HOST uint64[256]; h_len: HOST uint8[256] code
+ * lengths.  Returns HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK when a counted symbol has
+ * no code.
+ */
+int huff_code_stats(const uint64_t *h_hist, const uint8_t *h_len, huff_stats *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HUFF_H_ */

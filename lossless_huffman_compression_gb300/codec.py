@@ -1,0 +1,176 @@
+"""Convenience layer over the binding: buffers sized and allocated by torch,
+work done by libhuff's kernels.  Nothing here computes on the host except
+buffer sizes.
+
+    cb = build_codebook(histogram(x))          # per-shard codebook
+    s = encode(x, cb)                          # Stream(payload, off, n, chunk_bytes)
+    y = decode(s, cb)                          # == x
+
+    streams = compress_bf16(x1, x0)            # LMC: XOR delta, byte planes, per-plane codebooks
+    x1_back = decompress_bf16(streams, x0)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import HuffError
+
+DEFAULT_CHUNK = 16384
+
+
+class Codebook:
+    """A device-resident huff_codebook."""
+
+    def __init__(self, device=None):
+        device = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = torch.zeros(_lib.huff_codebook_size(), dtype=torch.uint8, device=device)
+
+    @property
+    def device(self):
+        return self.buf.device
+
+    def lengths(self) -> np.ndarray:
+        """The 256 code lengths: the transmitted form of the codebook."""
+        o = _lib.CODEBOOK_LEN_OFFSET
+        return self.buf[o:o + 256].cpu().numpy().copy()
+
+    def codes(self) -> np.ndarray:
+        o = _lib.CODEBOOK_LEN_OFFSET + 256
+        return self.buf[o:o + 1024].cpu().numpy().view(np.uint32).copy()
+
+
+@dataclass
+class Stream:
+    payload: torch.Tensor  # uint8, capacity >= ceil(T/32)*4
+    off: torch.Tensor      # int64[n_chunks + 1], bit offsets (uint64 in the C ABI)
+    n: int
+    chunk_bytes: int
+
+    def total_bits(self) -> int:
+        return int(self.off[-1].item())
+
+    def nbytes(self) -> int:
+        return (self.total_bits() + 7) // 8
+
+    def n_chunks(self) -> int:
+        return self.off.numel() - 1
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def raise_on_status(status: torch.Tensor, what: str) -> None:
+    st = int(status.item())
+    if st != 0:
+        raise HuffError(what, st)
+
+
+def histogram(x: torch.Tensor, hist: torch.Tensor | None = None, accumulate: bool = False) -> torch.Tensor:
+    if hist is None:
+        hist = torch.zeros(256, dtype=torch.int64, device=x.device)
+    _lib.huff_histogram(x.reshape(-1), hist, accumulate=accumulate)
+    return hist
+
+
+def build_codebook(hist: torch.Tensor, max_len: int = 24, flags: int = 0, cb: Codebook | None = None,
+                   status: torch.Tensor | None = None) -> Codebook:
+    cb = cb or Codebook(hist.device)
+    st = status if status is not None else new_status(hist.device)
+    _lib.huff_build_codebook(hist, cb.buf, st, max_len, flags)
+    if status is None:
+        raise_on_status(st, "huff_build_codebook")
+    return cb
+
+
+def codebook_from_lengths(lengths, max_len: int = 24, device=None) -> Codebook:
+    cb = Codebook(device)
+    st = new_status(cb.device)
+    _lib.huff_codebook_from_lengths(lengths, cb.buf, st, max_len)
+    raise_on_status(st, "huff_codebook_from_lengths")
+    return cb
+
+
+def encode(x: torch.Tensor, cb: Codebook, chunk_bytes: int = DEFAULT_CHUNK, max_len: int = 24,
+           status: torch.Tensor | None = None) -> Stream:
+    flat = x.reshape(-1)
+    n = flat.numel() * flat.element_size()
+    payload = torch.empty(_lib.huff_encode_bound(n, max_len), dtype=torch.uint8, device=x.device)
+    off = torch.empty(_lib.huff_num_chunks(n, chunk_bytes) + 1, dtype=torch.int64, device=x.device)
+    ws = torch.empty(max(_lib.huff_workspace_size(n, chunk_bytes), 16) // 8, dtype=torch.int64, device=x.device)
+    st = status if status is not None else new_status(x.device)
+    _lib.huff_encode(flat, cb.buf, chunk_bytes, payload, off, ws, st, n=n)
+    if status is None:
+        raise_on_status(st, "huff_encode")
+    return Stream(payload, off, n, chunk_bytes)
+
+
+def decode(s: Stream, cb: Codebook, out: torch.Tensor | None = None,
+           status: torch.Tensor | None = None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(max(s.n, 1), dtype=torch.uint8, device=s.payload.device)[: s.n]
+    st = status if status is not None else new_status(s.payload.device)
+    _lib.huff_decode(s.payload, s.off, s.n, s.chunk_bytes, cb.buf, out, st)
+    if status is None:
+        raise_on_status(st, "huff_decode")
+    return out
+
+
+def compress(x: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, max_len: int = 24, flags: int = 0):
+    """Per-shard Huffman: histogram, codebook and encode of one byte stream."""
+    cb = build_codebook(histogram(x), max_len, flags)
+    return cb, encode(x, cb, chunk_bytes, max_len)
+
+
+@dataclass
+class Bf16Streams:
+    cb_hi: Codebook
+    cb_lo: Codebook
+    hi: Stream
+    lo: Stream
+    n: int
+
+
+def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: int = DEFAULT_CHUNK,
+                  max_len: int = 24, flags: int = 0, cb_hi: Codebook | None = None,
+                  cb_lo: Codebook | None = None) -> Bf16Streams:
+    """LMC snapshot compress: optional XOR delta, byte planes, one codebook per plane."""
+    w16 = w.reshape(-1).view(torch.int16)
+    x16 = None if x0 is None else x0.reshape(-1).view(torch.int16)
+    n = w16.numel()
+    dev = w.device
+    if cb_hi is None or cb_lo is None:
+        h_hi = torch.empty(256, dtype=torch.int64, device=dev)
+        h_lo = torch.empty(256, dtype=torch.int64, device=dev)
+        _lib.lmc_histogram_bf16(w16, x16, h_hi, h_lo)
+        st = new_status(dev)
+        cb_hi = build_codebook(h_hi, max_len, flags, status=st)
+        cb_lo = build_codebook(h_lo, max_len, flags, status=st)
+        raise_on_status(st, "huff_build_codebook")
+    cap = _lib.huff_encode_bound(n, max_len)
+    p_hi = torch.empty(cap, dtype=torch.uint8, device=dev)
+    p_lo = torch.empty(cap, dtype=torch.uint8, device=dev)
+    nc = _lib.huff_num_chunks(n, chunk_bytes)
+    o_hi = torch.empty(nc + 1, dtype=torch.int64, device=dev)
+    o_lo = torch.empty(nc + 1, dtype=torch.int64, device=dev)
+    ws = torch.empty(max(_lib.lmc_workspace_size(n, chunk_bytes), 16) // 8, dtype=torch.int64, device=dev)
+    st = new_status(dev)
+    _lib.lmc_encode_bf16(w16, x16, cb_hi.buf, cb_lo.buf, chunk_bytes, p_hi, o_hi, p_lo, o_lo, ws, st)
+    raise_on_status(st, "lmc_encode_bf16")
+    return Bf16Streams(cb_hi, cb_lo, Stream(p_hi, o_hi, n, chunk_bytes), Stream(p_lo, o_lo, n, chunk_bytes), n)
+
+
+def decompress_bf16(s: Bf16Streams, x0: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    dev = s.hi.payload.device
+    if out is None:
+        out = torch.empty(max(s.n, 1), dtype=torch.bfloat16, device=dev)[: s.n]
+    x16 = None if x0 is None else x0.reshape(-1).view(torch.int16)
+    st = new_status(dev)
+    _lib.lmc_decode_bf16(s.hi.payload, s.hi.off, s.lo.payload, s.lo.off, s.n, s.hi.chunk_bytes, s.cb_hi.buf,
+                         s.cb_lo.buf, x16, out.view(torch.int16), st)
+    raise_on_status(st, "lmc_decode_bf16")
+    return out

@@ -1,0 +1,212 @@
+// api.cu -- the extern "C" entry points of libhuff (include/huff.h).
+//
+// Host side only: argument checks, buffer sizing, and launches on the caller's
+// stream.  No allocation, no synchronisation.
+#include <cmath>
+
+#include "common.cuh"
+
+using namespace huffk;
+
+namespace {
+
+constexpr size_t kMaxN = size_t(1) << 40;  // 1 Ti symbols: bit offsets stay far below 2^62
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline cudaStream_t cs(huff_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool chunk_ok(size_t chunk) { return chunk > 0 && chunk % HUFF_CHUNK_ALIGN == 0 && chunk <= (size_t(1) << 31); }
+
+}  // namespace
+
+extern "C" {
+
+uint32_t huff_version(void) { return 0x010000u; }
+
+const char *huff_status_string(int status) {
+    switch (status) {
+        case HUFF_OK: return "ok";
+        case HUFF_ERR_INVALID_ARG: return "invalid argument";
+        case HUFF_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+        case HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK: return "symbol not in codebook";
+        case HUFF_ERR_CORRUPT_STREAM: return "corrupt stream";
+        case HUFF_ERR_TIMEOUT: return "device wait timed out";
+        case HUFF_ERR_CUDA: return "CUDA error";
+        case HUFF_ERR_INVALID_CODEBOOK: return "invalid codebook";
+        default: return "unknown status";
+    }
+}
+
+size_t huff_codebook_size(void) { return sizeof(huff_codebook); }
+
+size_t huff_num_chunks(size_t n, size_t chunk_bytes) {
+    if (chunk_bytes == 0) return 0;
+    return (n + chunk_bytes - 1) / chunk_bytes;
+}
+
+size_t huff_encode_bound(size_t n, int max_len) {
+    if (max_len < 1 || max_len > HUFF_MAX_LEN) max_len = HUFF_MAX_LEN;
+    const size_t words = (n * static_cast<size_t>(max_len) + 31) / 32;
+    return words * 4 + 16;
+}
+
+size_t huff_workspace_size(size_t n, size_t chunk_bytes) {
+    (void)chunk_bytes;
+    return (2 * enc_u8_tiles(n) + 2) * sizeof(uint64_t);
+}
+
+size_t lmc_workspace_size(size_t n, size_t chunk_bytes) {
+    (void)chunk_bytes;
+    return (4 * enc_bf16_tiles(n) + 2) * sizeof(uint64_t);
+}
+
+int huff_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist, int accumulate,
+                   huff_stream_t stream) {
+    if (hist == nullptr || !aligned(hist, 8) || (stride != 1 && stride != 2) || n > kMaxN ||
+        (n > 0 && in == nullptr))
+        return HUFF_ERR_INVALID_ARG;
+    if (!accumulate) {
+        const int st = launch_zero_u64(hist, 256, cs(stream));
+        if (st != HUFF_OK) return st;
+    }
+    if (n == 0) return HUFF_OK;
+    return launch_histogram(in, n, stride, hist, cs(stream));
+}
+
+int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_codebook *cb, int32_t *status,
+                        huff_stream_t stream) {
+    if (hist == nullptr || cb == nullptr || status == nullptr || !aligned(cb, 16) || !aligned(hist, 8) ||
+        max_len < HUFF_MIN_MAX_LEN || max_len > HUFF_MAX_LEN || (flags & ~HUFF_COVER_ALL) != 0)
+        return HUFF_ERR_INVALID_ARG;
+    return launch_build_codebook(hist, max_len, flags, cb, status, cs(stream));
+}
+
+int huff_codebook_from_lengths(const uint8_t *h_len, int max_len, huff_codebook *cb, int32_t *status,
+                               huff_stream_t stream) {
+    if (h_len == nullptr || cb == nullptr || status == nullptr || !aligned(cb, 16) ||
+        max_len < HUFF_MIN_MAX_LEN || max_len > HUFF_MAX_LEN)
+        return HUFF_ERR_INVALID_ARG;
+    for (int s = 0; s < 256; ++s)
+        if (h_len[s] > max_len) return HUFF_ERR_INVALID_ARG;
+    // a pageable source is staged before cudaMemcpyAsync returns, so h_len may be reused at once
+    if (cudaMemcpyAsync(cb->len, h_len, 256, cudaMemcpyHostToDevice, cs(stream)) != cudaSuccess)
+        return HUFF_ERR_CUDA;
+    return launch_codebook_from_lengths(max_len, cb, status, cs(stream));
+}
+
+int huff_encode(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk_bytes, uint8_t *payload,
+                size_t payload_cap, uint64_t *chunk_bit_off, void *ws, size_t ws_bytes, int32_t *status,
+                huff_stream_t stream) {
+    if (cb == nullptr || chunk_bit_off == nullptr || status == nullptr || !chunk_ok(chunk_bytes) || n > kMaxN ||
+        !aligned(cb, 16) || !aligned(chunk_bit_off, 8))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (in == nullptr || payload == nullptr || ws == nullptr || !aligned(in, HUFF_ALIGN) ||
+                  !aligned(payload, HUFF_ALIGN) || !aligned(ws, HUFF_ALIGN)))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && ws_bytes < huff_workspace_size(n, chunk_bytes)) return HUFF_ERR_BUFFER_TOO_SMALL;
+    return launch_encode_u8(in, n, cb, chunk_bytes, payload, payload_cap, chunk_bit_off, ws, status, cs(stream));
+}
+
+int huff_decode(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off, size_t n,
+                size_t chunk_bytes, const huff_codebook *cb, uint8_t *out, int32_t *status,
+                huff_stream_t stream) {
+    if (cb == nullptr || status == nullptr || !chunk_ok(chunk_bytes) || n > kMaxN || !aligned(cb, 16))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (payload == nullptr || chunk_bit_off == nullptr || out == nullptr ||
+                  !aligned(payload, HUFF_ALIGN) || !aligned(out, HUFF_ALIGN) || !aligned(chunk_bit_off, 8)))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_decode_u8(payload, payload_bytes, chunk_bit_off, n, chunk_bytes, cb, out, status, cs(stream));
+}
+
+int lmc_bytegroup_split(const uint16_t *w, size_t n, uint8_t *hi, uint8_t *lo, huff_stream_t stream) {
+    if (n > kMaxN || (n > 0 && (w == nullptr || hi == nullptr || lo == nullptr || !aligned(w, 2))))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_split(w, n, hi, lo, cs(stream));
+}
+
+int lmc_bytegroup_merge(const uint8_t *hi, const uint8_t *lo, size_t n, uint16_t *w, huff_stream_t stream) {
+    if (n > kMaxN || (n > 0 && (w == nullptr || hi == nullptr || lo == nullptr || !aligned(w, 2))))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_merge(hi, lo, n, w, cs(stream));
+}
+
+int lmc_delta_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out, huff_stream_t stream) {
+    if (n > kMaxN || (n > 0 && (a == nullptr || b == nullptr || out == nullptr || !aligned(a, 2) ||
+                                !aligned(b, 2) || !aligned(out, 2))))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_xor(a, b, n, out, cs(stream));
+}
+
+int lmc_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi, uint64_t *hist_lo,
+                       int accumulate, huff_stream_t stream) {
+    if (hist_hi == nullptr || hist_lo == nullptr || hist_hi == hist_lo || !aligned(hist_hi, 8) ||
+        !aligned(hist_lo, 8) || n > kMaxN || (n > 0 && (w == nullptr || !aligned(w, 2))) ||
+        (x0 != nullptr && !aligned(x0, 2)))
+        return HUFF_ERR_INVALID_ARG;
+    if (!accumulate) {
+        int st = launch_zero_u64(hist_hi, 256, cs(stream));
+        if (st == HUFF_OK) st = launch_zero_u64(hist_lo, 256, cs(stream));
+        if (st != HUFF_OK) return st;
+    }
+    if (n == 0) return HUFF_OK;
+    return launch_histogram_bf16(w, x0, n, hist_hi, hist_lo, cs(stream));
+}
+
+int lmc_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
+                    const huff_codebook *cb_lo, size_t chunk_bytes, uint8_t *payload_hi, size_t cap_hi,
+                    uint64_t *off_hi, uint8_t *payload_lo, size_t cap_lo, uint64_t *off_lo, void *ws,
+                    size_t ws_bytes, int32_t *status, huff_stream_t stream) {
+    if (cb_hi == nullptr || cb_lo == nullptr || off_hi == nullptr || off_lo == nullptr || status == nullptr ||
+        !chunk_ok(chunk_bytes) || n > kMaxN || !aligned(cb_hi, 16) || !aligned(cb_lo, 16) ||
+        !aligned(off_hi, 8) || !aligned(off_lo, 8))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (w == nullptr || payload_hi == nullptr || payload_lo == nullptr || ws == nullptr ||
+                  !aligned(w, HUFF_ALIGN) || (x0 != nullptr && !aligned(x0, HUFF_ALIGN)) ||
+                  !aligned(payload_hi, HUFF_ALIGN) || !aligned(payload_lo, HUFF_ALIGN) || !aligned(ws, HUFF_ALIGN)))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && ws_bytes < lmc_workspace_size(n, chunk_bytes)) return HUFF_ERR_BUFFER_TOO_SMALL;
+    return launch_encode_bf16(w, x0, n, cb_hi, cb_lo, chunk_bytes, payload_hi, cap_hi, off_hi, payload_lo, cap_lo,
+                              off_lo, ws, status, cs(stream));
+}
+
+int lmc_decode_bf16(const uint8_t *payload_hi, size_t bytes_hi, const uint64_t *off_hi, const uint8_t *payload_lo,
+                    size_t bytes_lo, const uint64_t *off_lo, size_t n, size_t chunk_bytes,
+                    const huff_codebook *cb_hi, const huff_codebook *cb_lo, const uint16_t *x0, uint16_t *out,
+                    int32_t *status, huff_stream_t stream) {
+    if (cb_hi == nullptr || cb_lo == nullptr || status == nullptr || !chunk_ok(chunk_bytes) || n > kMaxN ||
+        !aligned(cb_hi, 16) || !aligned(cb_lo, 16))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (payload_hi == nullptr || payload_lo == nullptr || off_hi == nullptr || off_lo == nullptr ||
+                  out == nullptr || !aligned(payload_hi, HUFF_ALIGN) || !aligned(payload_lo, HUFF_ALIGN) ||
+                  !aligned(out, HUFF_ALIGN) || (x0 != nullptr && !aligned(x0, HUFF_ALIGN)) ||
+                  !aligned(off_hi, 8) || !aligned(off_lo, 8) || x0 == out))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_decode_bf16(payload_hi, bytes_hi, off_hi, payload_lo, bytes_lo, off_lo, n, chunk_bytes, cb_hi,
+                              cb_lo, x0, out, status, cs(stream));
+}
+
+int huff_code_stats(const uint64_t *h_hist, const uint8_t *h_len, huff_stats *out) {
+    if (h_hist == nullptr || h_len == nullptr || out == nullptr) return HUFF_ERR_INVALID_ARG;
+    huff_stats r{};
+    int st = HUFF_OK;
+    for (int s = 0; s < 256; ++s) {
+        r.n += h_hist[s];
+        r.total_bits += h_hist[s] * h_len[s];
+        if (h_hist[s] > 0 && h_len[s] == 0) st = HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK;
+    }
+    if (r.n > 0) {
+        double h = 0.0;
+        for (int s = 0; s < 256; ++s) {
+            if (h_hist[s] == 0) continue;
+            const double p = static_cast<double>(h_hist[s]) / static_cast<double>(r.n);
+            h -= p * std::log2(p);
+        }
+        r.entropy_bits = h;
+        r.mean_len = static_cast<double>(r.total_bits) / static_cast<double>(r.n);
+        const double nh = static_cast<double>(r.n) * h;
+        r.shannon_gap = nh > 0.0 ? (static_cast<double>(r.total_bits) - nh) / nh : 0.0;
+    }
+    *out = r;
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,263 @@
+// codebook.cu -- code lengths, canonical codes and decode tables, one CTA.
+//
+// "Single-stage Huffman encoder for ML compression" (arXiv 2601.10673),
+// Methodology step 3: the Huffman codebook is built once from the averaged
+// distribution.  "Lossless Compression for LLM Tensor Incremental Snapshots"
+// (arXiv 2505.09810), key design 2: efficient Huffman tree construction.
+//
+// The pages fix neither the tie-break nor a length limit nor how codes are
+// assigned; the rule implemented here is:
+//   (count, id) order with leaves id = symbol and new nodes 256, 257, ...;
+//   ITU-T T.81 Annex K.3 Adjust_BITS repair down to max_len (no reserved
+//   code); lengths handed out again by (count desc, symbol asc);
+//   RFC 1951 3.2.2 canonical codes.
+//
+// GPU design: 256 threads, one per symbol.  The present symbols are ranked by
+// (count, symbol) with an all-pairs comparison (256 x 256 compares spread over
+// the block), which turns Huffman's procedure into the two-queue form: sorted
+// leaves plus a FIFO of new nodes, whose counts come out non-decreasing with
+// increasing ids, so the FIFO is itself in (count, id) order and every step
+// takes the same two nodes as a (count, id) heap would.  The 255 joins are
+// inherently serial and run on one thread (a few microseconds, once per
+// codebook); depths, counting, reassignment, code assignment and the 4096
+// entry decode table are spread over the block.
+#include "common.cuh"
+
+namespace huffk {
+
+namespace {
+
+constexpr int kT = 256;
+
+// Codes, ranks, decode tables and the header from 256 lengths in shared
+// memory.  Requires every length <= max_len <= 24.
+__device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook *cb, int32_t *status) {
+    __shared__ uint32_t blc[34];
+    __shared__ uint32_t fc[34];
+    __shared__ uint32_t fi[34];
+    __shared__ uint8_t srt[256];
+    __shared__ int s_bad, s_nsym, s_longest;
+    const int t = threadIdx.x;
+    if (t < 34) blc[t] = 0;
+    if (t == 0) {
+        s_bad = 0;
+        s_longest = 0;
+    }
+    srt[t] = 0;
+    __syncthreads();
+    const int L = lens[t];
+    if (L > 0) {
+        atomicAdd(&blc[L], 1u);
+        atomicMax(&s_longest, L);
+    }
+    __syncthreads();
+    if (t == 0) {
+        uint64_t code = 0;
+        uint32_t idx = 0;
+        blc[0] = 0;
+        fc[0] = 0;
+        fi[0] = 0;
+        for (int l = 1; l <= 32; ++l) {
+            code = (code + blc[l - 1]) << 1;
+            fc[l] = static_cast<uint32_t>(code);
+            fi[l] = idx;
+            idx += blc[l];
+            if (blc[l] > 0 && code + blc[l] > (1ull << l)) s_bad = 1;  // over-subscribed
+        }
+        s_nsym = static_cast<int>(idx);
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (t == 0) {
+            cb->magic = 0;
+            set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+        }
+        return;
+    }
+    uint32_t code = 0;
+    if (L > 0) {
+        uint32_t r = 0;
+        for (int u = 0; u < t; ++u) r += (lens[u] == L);
+        code = fc[L] + r;
+        srt[fi[L] + r] = static_cast<uint8_t>(t);
+    }
+    cb->len[t] = static_cast<uint8_t>(L);
+    cb->code[t] = code;
+    if (t < 32) {
+        cb->bl_count[t] = blc[t];
+        cb->first_code[t] = fc[t];
+        cb->first_index[t] = fi[t];
+    }
+    __syncthreads();
+    cb->sorted_symbols[t] = srt[t];
+    // first-level decode table: entry i holds the code that the 12-bit window i starts with
+    for (int i = t; i < (1 << HUFF_LUT_BITS); i += kT) {
+        uint32_t e = 0;
+        for (int l = 1; l <= HUFF_LUT_BITS; ++l) {
+            const uint32_t c = static_cast<uint32_t>(i) >> (HUFF_LUT_BITS - l);
+            if (blc[l] > 0 && c >= fc[l] && c - fc[l] < blc[l]) {
+                e = (static_cast<uint32_t>(l) << 8) | srt[fi[l] + (c - fc[l])];
+                break;
+            }
+        }
+        cb->lut[i] = e;
+    }
+    __syncthreads();
+    if (t == 0) {
+        cb->max_len = max_len;
+        cb->n_symbols = s_nsym;
+        cb->longest = s_longest;
+        __threadfence();
+        cb->magic = HUFF_CODEBOOK_MAGIC;
+    }
+}
+
+__global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restrict__ hist, int max_len,
+                                                       unsigned flags, huff_codebook *__restrict__ cb,
+                                                       int32_t *status) {
+    __shared__ uint64_t cnt[256];
+    __shared__ uint64_t leaf_cnt[256];
+    __shared__ uint64_t int_cnt[256];
+    __shared__ uint16_t leaf_parent[256];
+    __shared__ uint16_t int_parent[256];
+    __shared__ uint16_t int_depth[256];
+    __shared__ uint32_t bl[260];
+    __shared__ uint8_t lens[256];
+    __shared__ int s_maxdepth, s_fail;
+
+    const int t = threadIdx.x;
+    uint64_t c = hist[t];
+    if ((flags & HUFF_COVER_ALL) && c == 0) c = 1;
+    cnt[t] = c;
+    bl[t] = 0;
+    if (t < 4) bl[256 + t] = 0;
+    lens[t] = 0;
+    if (t == 0) {
+        s_maxdepth = 0;
+        s_fail = 0;
+    }
+    const int m = __syncthreads_count(c > 0);
+
+    if (m >= 2) {
+        // rank of each present symbol by (count asc, symbol asc)
+        if (c > 0) {
+            int r = 0;
+            for (int u = 0; u < 256; ++u) {
+                const uint64_t cu = cnt[u];
+                r += (cu > 0) && (cu < c || (cu == c && u < t));
+            }
+            leaf_cnt[r] = c;
+        }
+        __syncthreads();
+        if (t == 0) {
+            // two-queue Huffman: leaves (sorted) against new nodes (FIFO); a leaf wins a count tie
+            int li = 0, ii = 0;
+            for (int k = 0; k < m - 1; ++k) {
+                uint64_t sum = 0;
+                for (int pick = 0; pick < 2; ++pick) {
+                    const bool take_leaf = li < m && (ii >= k || leaf_cnt[li] <= int_cnt[ii]);
+                    if (take_leaf) {
+                        leaf_parent[li] = static_cast<uint16_t>(k);
+                        sum += leaf_cnt[li++];
+                    } else {
+                        int_parent[ii] = static_cast<uint16_t>(k);
+                        sum += int_cnt[ii++];
+                    }
+                }
+                int_cnt[k] = sum;
+            }
+            // depths of new nodes: the root is the last one; parents come after children
+            int_depth[m - 2] = 0;
+            for (int k = m - 3; k >= 0; --k) int_depth[k] = int_depth[int_parent[k]] + 1;
+        }
+        __syncthreads();
+        if (t < m) {
+            const int d = int_depth[leaf_parent[t]] + 1;
+            atomicAdd(&bl[d], 1u);
+            atomicMax(&s_maxdepth, d);
+        }
+        __syncthreads();
+        if (t == 0 && s_maxdepth > max_len) {
+            // Adjust_BITS, largest over-long depth first; each move keeps the Kraft sum at 1
+            for (int i = s_maxdepth; i > max_len; --i) {
+                while (bl[i] > 0) {
+                    int j = i - 2;
+                    while (j > 0 && bl[j] == 0) --j;
+                    if (j <= 0) {
+                        s_fail = 1;
+                        break;
+                    }
+                    bl[i] -= 2;
+                    bl[i - 1] += 1;
+                    bl[j + 1] += 2;
+                    bl[j] -= 1;
+                }
+                if (s_fail) break;
+            }
+        }
+        __syncthreads();
+        if (s_fail) {
+            if (t == 0) {
+                cb->magic = 0;
+                set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+            }
+            return;
+        }
+        // hand the lengths out again by (count desc, symbol asc)
+        if (c > 0) {
+            int r = 0;
+            for (int u = 0; u < 256; ++u) {
+                const uint64_t cu = cnt[u];
+                r += (cu > 0) && (cu > c || (cu == c && u < t));
+            }
+            uint32_t cum = 0;
+            for (int L = 1; L <= max_len; ++L) {
+                cum += bl[L];
+                if (static_cast<uint32_t>(r) < cum) {
+                    lens[t] = static_cast<uint8_t>(L);
+                    break;
+                }
+            }
+        }
+    } else if (m == 1) {
+        if (c > 0) lens[t] = 1;
+    }
+    __syncthreads();
+    finish_codebook(lens, max_len, cb, status);
+}
+
+__global__ void __launch_bounds__(kT) k_codebook_from_lengths(int max_len, huff_codebook *__restrict__ cb,
+                                                              int32_t *status) {
+    __shared__ uint8_t lens[256];
+    __shared__ int s_bad;
+    const int t = threadIdx.x;
+    if (t == 0) s_bad = 0;
+    __syncthreads();
+    const int L = cb->len[t];
+    if (L > max_len) s_bad = 1;
+    lens[t] = static_cast<uint8_t>(L);
+    __syncthreads();
+    if (s_bad) {
+        if (t == 0) {
+            cb->magic = 0;
+            set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+        }
+        return;
+    }
+    finish_codebook(lens, max_len, cb, status);
+}
+
+}  // namespace
+
+int launch_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_codebook *cb,
+                          int32_t *status, cudaStream_t s) {
+    k_build_codebook<<<1, kT, 0, s>>>(hist, max_len, flags, cb, status);
+    return launch_status();
+}
+
+int launch_codebook_from_lengths(int max_len, huff_codebook *cb, int32_t *status, cudaStream_t s) {
+    k_codebook_from_lengths<<<1, kT, 0, s>>>(max_len, cb, status);
+    return launch_status();
+}
+
+}  // namespace huffk
