@@ -191,8 +191,8 @@ class SnapshotPath:
         self.ws = torch.empty(_lib.lmc_workspace_size(n, chunk) // 8 + 2, dtype=torch.int64, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty(n, dtype=torch.int16, device=dev)
-        # kernels launched per step: hist (2 zero + 1), build (2), encode (1 zero + 1), decode (1)
-        self.launches_per_step = 8
+        # kernels launched per step: hist (2 zero + 1), build (2), encode (zero + main + fix-up), decode (1)
+        self.launches_per_step = 9
 
     def compress(self, w=None, x0=None):
         L = self.L
@@ -245,7 +245,7 @@ def run_ours(args, dist, rank, ws):
     __graft_entry__.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    shape = workloads.SNAPSHOT_SHAPE if not args.small else (4096, 30518)
+    shape = (args.rows, workloads.SNAPSHOT_SHAPE[1])
     x0, x1 = workloads.snapshot_pair(device=dev, shape=shape)
     path = SnapshotPath(x0, x1, args.chunk)
     n = path.n
@@ -330,7 +330,7 @@ def run_ours(args, dist, rank, ws):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": "snapshot_delta_bf16_65536x30518" if not args.small else "snapshot_delta_bf16_small",
+        "config": {"workload": f"snapshot_delta_bf16_{args.rows}x{workloads.SNAPSHOT_SHAPE[1]}",
                    "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk, "max_len": 24,
                    "step": "xor+split+hist, build x2, fused encode, fused decode+merge+xor",
                    "l2": "inputs (8 GB) larger than L2; no flush", "parallelism": f"replicas{ws}"},
@@ -481,9 +481,9 @@ def run_reference(args, dist, rank, ws):
     oracle.build()
     from lossless_huffman_compression_gb300 import workloads
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    shape = workloads.SNAPSHOT_SHAPE if not args.small else (4096, 30518)
+    shape = (args.rows, workloads.SNAPSHOT_SHAPE[1])
     x0, x1 = workloads.snapshot_pair(device=dev, shape=shape)
-    elems = args.ref_sample
+    elems = min(args.ref_sample, x0.numel())
     a, b = snapshot_sample(x0, x1, elems)
     del x0, x1
     for _ in range(args.warmup):
@@ -499,7 +499,7 @@ def run_reference(args, dist, rank, ws):
         "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": "snapshot_delta_bf16_65536x30518", "chunk_bytes": args.chunk,
+        "config": {"workload": f"snapshot_delta_bf16_{args.rows}x30518", "chunk_bytes": args.chunk,
                    "sample_elements": elems},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"first {elems} elements of x0/x1 per step"},
@@ -515,12 +515,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk", type=int, default=16384)
-    ap.add_argument("--small", action="store_true", help="a 250 MB snapshot instead of 4 GB (quick checks)")
+    ap.add_argument("--rows", type=int, default=65536,
+                    help="snapshot rows of 30518 bf16 (65536 = the 4.0 GB workload; fewer for quick checks)")
+    ap.add_argument("--small", action="store_true", help="same as --rows 4096 (a 250 MB snapshot)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=64 << 20, help="elements for the oracle baseline")
     ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")
     args = ap.parse_args()
+    if args.small:
+        args.rows = 4096
     ws, rank, local = dist_env()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

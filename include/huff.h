@@ -91,7 +91,10 @@ typedef struct huff_codebook {
     uint32_t first_code[32];   /* canonical value of the first code of each length */
     uint32_t first_index[32];  /* index in sorted_symbols of the first code of each length */
     uint8_t sorted_symbols[256]; /* symbols ordered by (length, symbol) */
-    uint32_t lut[1u << HUFF_LUT_BITS]; /* decode table: (len << 8) | symbol for codes of <= 12 bits, 0 otherwise */
+    uint32_t lut[1u << HUFF_LUT_BITS]; /* decode table for the next 12 stream bits: the codes wholly inside
+                                          them, greedily, at most 3: symbols (bits 0-23, first symbol in
+                                          bits 0-7), count (bits 24-25), total length (bits 27-31);
+                                          0 when the first code is longer than 12 bits */
 } huff_codebook;
 
 /* Per-stream quality figures (host helper). */
@@ -118,8 +121,8 @@ size_t huff_codebook_size(void);
  * rounded up to whole 32-bit words, plus 16 bytes of slack. */
 size_t huff_encode_bound(size_t n, int max_len);
 
-/* Workspace bytes huff_encode needs for n symbols (lookback descriptors and a
- * tile counter).  chunk_bytes does not change it today; it is an argument so
+/* Workspace bytes huff_encode needs for n symbols (per 8 KiB tile: a lookback
+ * descriptor and the tile's two boundary words).  chunk_bytes does not change it today; it is an argument so
  * the format can change without an ABI break. */
 size_t huff_workspace_size(size_t n, size_t chunk_bytes);
 
@@ -162,7 +165,9 @@ int huff_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist,
  *   hist      uint64[256], device.
  *   max_len   8..24.
  *   cb        device huff_codebook, written completely (decode tables too).
- *   status    device int32; HUFF_ERR_INVALID_CODEBOOK if the build fails.
+ *   status    device int32; HUFF_ERR_INVALID_CODEBOOK if the build fails: the
+ *             counts (after HUFF_COVER_ALL) must sum below 2^63, which every
+ *             histogram of fewer than 2^63 symbols does.
  * Runs as one thread block.
  */
 int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags,

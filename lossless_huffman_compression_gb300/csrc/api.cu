@@ -3,12 +3,18 @@
 // Host side only: argument checks, buffer sizing, and launches on the caller's
 // stream.  No allocation, no synchronisation.
 #include <cmath>
+#include <cstddef>
 
 #include "common.cuh"
 
 using namespace huffk;
 
 namespace {
+
+// the decode kernels copy the table with 16-byte loads; the binding reads len[] at byte 16
+static_assert(offsetof(huff_codebook, lut) % 16 == 0, "codebook lut must be 16-byte aligned");
+static_assert(offsetof(huff_codebook, len) == 16 && offsetof(huff_codebook, code) == 272, "codebook layout");
+static_assert(sizeof(huff_codebook) % 16 == 0, "codebook size");
 
 constexpr size_t kMaxN = size_t(1) << 40;  // 1 Ti symbols: bit offsets stay far below 2^62
 

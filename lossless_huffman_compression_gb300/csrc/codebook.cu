@@ -90,17 +90,26 @@ __device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook 
     }
     __syncthreads();
     cb->sorted_symbols[t] = srt[t];
-    // first-level decode table: entry i holds the code that the 12-bit window i starts with
+    // first-level decode table: entry i lists the codes that lie wholly inside the 12-bit window i,
+    // greedily from its first bit, at most three: symbols (8 bits each, first in the low byte),
+    // their count << 24 and their total length << 27; 0 when the first code is longer than 12 bits
     for (int i = t; i < (1 << HUFF_LUT_BITS); i += kT) {
-        uint32_t e = 0;
-        for (int l = 1; l <= HUFF_LUT_BITS; ++l) {
-            const uint32_t c = static_cast<uint32_t>(i) >> (HUFF_LUT_BITS - l);
-            if (blc[l] > 0 && c >= fc[l] && c - fc[l] < blc[l]) {
-                e = (static_cast<uint32_t>(l) << 8) | srt[fi[l] + (c - fc[l])];
-                break;
+        uint32_t syms = 0, count = 0, pos = 0;
+        while (count < 3) {
+            bool found = false;
+            for (uint32_t l = 1; l + pos <= HUFF_LUT_BITS; ++l) {
+                const uint32_t c = (static_cast<uint32_t>(i) >> (HUFF_LUT_BITS - pos - l)) & ((1u << l) - 1u);
+                if (blc[l] > 0 && c >= fc[l] && c - fc[l] < blc[l]) {
+                    syms |= static_cast<uint32_t>(srt[fi[l] + (c - fc[l])]) << (8 * count);
+                    ++count;
+                    pos += l;
+                    found = true;
+                    break;
+                }
             }
+            if (!found) break;
         }
-        cb->lut[i] = e;
+        cb->lut[i] = count ? (syms | (count << 24) | (pos << 27)) : 0u;
     }
     __syncthreads();
     if (t == 0) {
@@ -149,6 +158,23 @@ __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restric
             leaf_cnt[r] = c;
         }
         __syncthreads();
+        if (t == 0) {
+            // the counts must sum below 2^63 so that no node count can overflow
+            uint64_t total = 0;
+            for (int u = 0; u < 256; ++u) {
+                const uint64_t nt = total + cnt[u];
+                if (nt < total || nt >= (1ull << 63)) s_fail = 1;
+                total = nt;
+            }
+        }
+        __syncthreads();
+        if (s_fail) {
+            if (t == 0) {
+                cb->magic = 0;
+                set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+            }
+            return;
+        }
         if (t == 0) {
             // two-queue Huffman: leaves (sorted) against new nodes (FIFO); a leaf wins a count tie
             int li = 0, ii = 0;

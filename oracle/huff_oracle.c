@@ -100,6 +100,14 @@ int ref_code_lengths(const uint64_t *hist, int max_len, unsigned flags, uint8_t 
         if (active[s]) ++m;
     }
     if (m == 0) return REF_OK;                       /* C5: empty codebook  */
+    {   /* node counts are sums of leaf counts: the total must stay below 2^63 */
+        uint64_t total = 0;
+        for (int s = 0; s < 256; ++s) {
+            if (total + count[s] < total) return REF_ERR_INVALID_ARG;
+            total += count[s];
+        }
+        if (total >= ((uint64_t)1 << 63)) return REF_ERR_INVALID_ARG;
+    }
     if (max_len < 9 && (uint64_t)m > ((uint64_t)1 << max_len))
         return REF_ERR_INVALID_ARG;                  /* no prefix code fits */
     if (m == 1) {                                    /* C5: one symbol      */

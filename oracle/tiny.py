@@ -63,6 +63,8 @@ def huffman_depths(counts: list[int]) -> dict[int, int]:
 def code_lengths(counts: list[int], max_len: int = 24, flags: int = 0) -> list[int]:
     """Lengths after the max_len repair and the (count desc, symbol asc) reassignment (C4, C5)."""
     cnt = [max(c, 1) if (flags & COVER_ALL) else c for c in counts]
+    if sum(cnt) >= 1 << 63:
+        raise ValueError("counts must sum below 2^63")
     depths = huffman_depths(cnt)
     lengths = [0] * 256
     if not depths:

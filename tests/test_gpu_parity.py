@@ -87,7 +87,7 @@ def _adversarial_hists():
         fib.append(fib[-1] + fib[-2])
     h = np.zeros(256, np.uint64); h[:40] = fib; out.append(h)            # depth 39 before the limit
     h = np.zeros(256, np.uint64); h[100:140] = fib; out.append(h)
-    h = np.array([2 ** min(i, 60) for i in range(256)], dtype=np.uint64); out.append(h)
+    h = np.array([2 ** min(i, 54) for i in range(256)], dtype=np.uint64); out.append(h)  # total just below 2^63
     h = np.zeros(256, np.uint64); h[::2] = 1; out.append(h)
     return out
 
@@ -132,6 +132,17 @@ def test_codebooks_match_oracle(max_len, flags):
         np.testing.assert_array_equal(got_code, cd)
         magic = int(cb[:4].view(np.uint32)[0])
         assert magic == _lib.HUFF_CODEBOOK_MAGIC
+
+
+def test_counts_summing_to_2_63_are_rejected():
+    h = np.zeros(256, np.uint64)
+    h[0] = 1 << 62
+    h[1] = 1 << 62
+    with pytest.raises(oracle.OracleError):
+        oracle.code_lengths(h)
+    with pytest.raises(_lib.HuffError) as e:
+        codec.build_codebook(torch.from_numpy(h.astype(np.int64)).cuda())
+    assert e.value.status == _lib.HUFF_ERR_INVALID_CODEBOOK
 
 
 def test_codebook_from_lengths_round_trip_and_rejects_oversubscription():

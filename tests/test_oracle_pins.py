@@ -154,6 +154,18 @@ def test_special_cases_zero_one_two_symbols():
     assert ln[77] == 1 and ln[3] == 1 and int(ln.sum()) == 2
 
 
+def test_counts_must_sum_below_2_63():
+    h = np.zeros(256, dtype=np.uint64)
+    h[0] = 1 << 62
+    h[1] = (1 << 62) - 1
+    assert int(oracle.code_lengths(h).sum()) == 2
+    h[1] = 1 << 62
+    with pytest.raises(oracle.OracleError):
+        oracle.code_lengths(h)
+    with pytest.raises(ValueError):
+        tiny.code_lengths([int(v) for v in h])
+
+
 def test_one_symbol_stream_round_trip():
     x = np.full(1000, 42, dtype=np.uint8)
     ln, cd, payload, off = oracle.compress_plane(x, 256)
