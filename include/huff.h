@@ -73,6 +73,7 @@ typedef enum huff_status {
 #define HUFF_ALIGN 16            /* alignment (bytes) required of bulk device buffers */
 #define HUFF_LUT_BITS 12         /* first-level decode table index width */
 #define HUFF_CODEBOOK_MAGIC 0x48554642u
+#define HUFF_NOALLOC_MAX_SYMBOLS (1ull << 30) /* largest n huff_encode_noalloc accepts */
 
 /*
  * Device-resident codebook, built by huff_build_codebook or imported by
@@ -211,6 +212,34 @@ int huff_codebook_from_lengths(const uint8_t *h_len, int max_len, huff_codebook 
 int huff_encode(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk_bytes,
                 uint8_t *payload, size_t payload_cap, uint64_t *chunk_bit_off,
                 void *ws, size_t ws_bytes, int32_t *status, huff_stream_t stream);
+
+/*
+ * huff_encode_noalloc -- huff_encode for callers that cannot allocate device
+ * memory.  No counterpart in the papers: it is a deployment convenience.
+ *
+ * huff_encode needs a workspace of huff_workspace_size(n) bytes.  Some callers
+ * have no way to provide one: a process whose device memory is owned entirely
+ * by a framework's pool allocator (third-party cudaMalloc calls fail or break
+ * its accounting), a latency-critical loop that must not call cudaMalloc or
+ * cudaFree because they can synchronise the whole device, or a caller that
+ * only holds the input and output buffers it was handed.  This entry point
+ * takes the same inputs and outputs as huff_encode, without ws, and runs the
+ * same kernels with a workspace that the library keeps in a fixed 2 MiB
+ * device array.  Nothing is allocated per call.
+ *   n             at most HUFF_NOALLOC_MAX_SYMBOLS (2^30) symbols; larger n
+ *                 returns HUFF_ERR_BUFFER_TOO_SMALL and enqueues nothing.
+ *   other arguments as in huff_encode; the output is identical to its output.
+ * The array lives in every GPU that loads the library, until the process
+ * exits.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture.  All calls share the one array:
+ * calls whose work can overlap on the GPU (different streams, or several host
+ * threads) race and corrupt each other's output; serialise them, or use
+ * huff_encode with one workspace per stream.
+ */
+int huff_encode_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk_bytes,
+                        uint8_t *payload, size_t payload_cap, uint64_t *chunk_bit_off, int32_t *status,
+                        huff_stream_t stream);
 
 /*
  * huff_decode -- chunked decode [P2 framework: decompression reads the data,

@@ -32,12 +32,13 @@ HUFF_MAX_LEN = 24
 HUFF_COVER_ALL = 1
 HUFF_CHUNK_ALIGN = 256
 HUFF_CODEBOOK_MAGIC = 0x48554642
+HUFF_NOALLOC_MAX_SYMBOLS = 1 << 30
 CODEBOOK_LEN_OFFSET = 16  # byte offset of len[256] inside huff_codebook
 
 EXPORTS = (
     "huff_version", "huff_status_string", "huff_codebook_size", "huff_encode_bound", "huff_workspace_size",
     "huff_num_chunks", "huff_histogram", "huff_build_codebook", "huff_codebook_from_lengths", "huff_encode",
-    "huff_decode", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
+    "huff_decode", "huff_encode_noalloc", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats",
 )
 
@@ -81,6 +82,7 @@ def load(path: str = LIB_PATH):
         "huff_codebook_from_lengths": (I, [P, I, P, P, P]),
         "huff_encode": (I, [P, S, P, S, P, S, P, P, S, P, P]),
         "huff_decode": (I, [P, S, P, S, S, P, P, P, P]),
+        "huff_encode_noalloc": (I, [P, S, P, S, P, S, P, P, P]),
         "lmc_bytegroup_split": (I, [P, S, P, P, P]),
         "lmc_bytegroup_merge": (I, [P, P, S, P, P]),
         "lmc_delta_xor": (I, [P, P, S, P, P]),
@@ -192,6 +194,16 @@ def huff_encode(inp: torch.Tensor, cb: torch.Tensor, chunk_bytes: int, payload: 
         _dev(inp, "inp"), n, _dev(cb, "cb"), chunk_bytes, _dev(payload, "payload"),
         payload.numel() * payload.element_size(), _dev(off, "off"), _dev(ws, "ws"),
         ws.numel() * ws.element_size(), _dev(status, "status"), _stream(stream)))
+
+
+def huff_encode_noalloc(inp: torch.Tensor, cb: torch.Tensor, chunk_bytes: int, payload: torch.Tensor,
+                        off: torch.Tensor, status: torch.Tensor, n: int | None = None, stream=None):
+    """huff_encode without a workspace argument (the library's built-in scratch is used)."""
+    if n is None:
+        n = inp.numel() * inp.element_size()
+    _check("huff_encode_noalloc", load().huff_encode_noalloc(
+        _dev(inp, "inp"), n, _dev(cb, "cb"), chunk_bytes, _dev(payload, "payload"),
+        payload.numel() * payload.element_size(), _dev(off, "off"), _dev(status, "status"), _stream(stream)))
 
 
 def huff_decode(payload: torch.Tensor, off: torch.Tensor, n: int, chunk_bytes: int, cb: torch.Tensor,

@@ -112,6 +112,19 @@ int huff_encode(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chu
     return launch_encode_u8(in, n, cb, chunk_bytes, payload, payload_cap, chunk_bit_off, ws, status, cs(stream));
 }
 
+int huff_encode_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk_bytes,
+                        uint8_t *payload, size_t payload_cap, uint64_t *chunk_bit_off, int32_t *status,
+                        huff_stream_t stream) {
+    if (cb == nullptr || chunk_bit_off == nullptr || status == nullptr || !chunk_ok(chunk_bytes) ||
+        !aligned(cb, 16) || !aligned(chunk_bit_off, 8))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > HUFF_NOALLOC_MAX_SYMBOLS) return HUFF_ERR_BUFFER_TOO_SMALL;  // beyond the built-in scratch
+    if (n > 0 && (in == nullptr || payload == nullptr || !aligned(in, HUFF_ALIGN) || !aligned(payload, HUFF_ALIGN)))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_encode_u8_noalloc(in, n, cb, chunk_bytes, payload, payload_cap, chunk_bit_off, status,
+                                    cs(stream));
+}
+
 int huff_decode(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off, size_t n,
                 size_t chunk_bytes, const huff_codebook *cb, uint8_t *out, int32_t *status,
                 huff_stream_t stream) {

@@ -146,6 +146,8 @@ size_t enc_bf16_tiles(size_t n);
 int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk,
                      uint8_t *payload, size_t cap, uint64_t *off, void *ws, int32_t *status,
                      cudaStream_t s);
+int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk,
+                             uint8_t *payload, size_t cap, uint64_t *off, int32_t *status, cudaStream_t s);
 int launch_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
                        const huff_codebook *cb_lo, size_t chunk, uint8_t *pay_hi, size_t cap_hi,
                        uint64_t *off_hi, uint8_t *pay_lo, size_t cap_lo, uint64_t *off_lo, void *ws,

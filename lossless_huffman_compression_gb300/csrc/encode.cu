@@ -34,9 +34,17 @@
 //   delta) and encodes the high and low byte planes as two streams in one
 //   pass.  All waits are bounded; a wait that runs out sets HUFF_ERR_TIMEOUT
 //   and the kernel carries on to completion.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace huffk {
+
+// Workspace for huff_encode_noalloc: two 64-bit words per 8 KiB tile, enough
+// for HUFF_NOALLOC_MAX_SYMBOLS symbols.  Every GPU that loads the library
+// keeps these 2 MiB until the process exits; all calls share them.
+constexpr size_t kNoAllocScratchWords = 2 * (HUFF_NOALLOC_MAX_SYMBOLS / kEncU8Tile);
+static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocScratchWords];
 
 namespace {
 
@@ -521,6 +529,31 @@ int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_
     EncPlane p0{cb, reinterpret_cast<uint32_t *>(payload), cap / 4, off, w, w + tiles};
     EncPlane p1 = p0;
     return run_encode<false, false>(in, nullptr, n, p0, p1, chunk, static_cast<uint32_t>(tiles), status, s);
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (host code only sees a host-side stand-in under the array's name).
+static uint64_t *noalloc_scratch_address() {
+    static std::mutex mu;
+    static uint64_t *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<uint64_t *>(p);
+    }
+    return addr[dev];
+}
+
+int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk, uint8_t *payload,
+                             size_t cap, uint64_t *off, int32_t *status, cudaStream_t s) {
+    if (2 * enc_u8_tiles(n) > kNoAllocScratchWords) return HUFF_ERR_BUFFER_TOO_SMALL;
+    uint64_t *ws = noalloc_scratch_address();
+    if (ws == nullptr) return HUFF_ERR_CUDA;
+    // the same path as huff_encode; it zeroes the descriptors it needs before the encode kernel runs
+    return launch_encode_u8(in, n, cb, chunk, payload, cap, off, ws, status, s);
 }
 
 int launch_encode_bf16(const uint16_t *w16, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
