@@ -72,6 +72,7 @@ typedef enum huff_status {
 #define HUFF_CHUNK_ALIGN 256     /* chunk_bytes must be a positive multiple of this */
 #define HUFF_ALIGN 16            /* alignment (bytes) required of bulk device buffers */
 #define HUFF_LUT_BITS 12         /* first-level decode table index width */
+#define HUFF_LUT_SYMS 6          /* most symbols one decode-table entry holds */
 #define HUFF_CODEBOOK_MAGIC 0x48554642u
 #define HUFF_NOALLOC_MAX_SYMBOLS (1ull << 30) /* largest n huff_encode_noalloc accepts */
 
@@ -92,9 +93,9 @@ typedef struct huff_codebook {
     uint32_t first_code[32];   /* canonical value of the first code of each length */
     uint32_t first_index[32];  /* index in sorted_symbols of the first code of each length */
     uint8_t sorted_symbols[256]; /* symbols ordered by (length, symbol) */
-    uint32_t lut[1u << HUFF_LUT_BITS]; /* decode table for the next 12 stream bits: the codes wholly inside
-                                          them, greedily, at most 3: symbols (bits 0-23, first symbol in
-                                          bits 0-7), count (bits 24-25), total length (bits 27-31);
+    uint64_t lut[1u << HUFF_LUT_BITS]; /* decode table for the next 12 stream bits: the codes wholly inside
+                                          them, greedily, at most 6: symbols (bits 0-47, first symbol in
+                                          bits 0-7), count (bits 48-51), total length (bits 52-55);
                                           0 when the first code is longer than 12 bits */
 } huff_codebook;
 

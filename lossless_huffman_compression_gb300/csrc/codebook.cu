@@ -91,16 +91,17 @@ __device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook 
     __syncthreads();
     cb->sorted_symbols[t] = srt[t];
     // first-level decode table: entry i lists the codes that lie wholly inside the 12-bit window i,
-    // greedily from its first bit, at most three: symbols (8 bits each, first in the low byte),
-    // their count << 24 and their total length << 27; 0 when the first code is longer than 12 bits
+    // greedily from its first bit, at most HUFF_LUT_SYMS: symbols (8 bits each, first in the low
+    // byte), their count << 48 and their total length << 52; 0 when the first code is longer than 12 bits
     for (int i = t; i < (1 << HUFF_LUT_BITS); i += kT) {
-        uint32_t syms = 0, count = 0, pos = 0;
-        while (count < 3) {
+        uint64_t syms = 0;
+        uint32_t count = 0, pos = 0;
+        while (count < HUFF_LUT_SYMS) {
             bool found = false;
             for (uint32_t l = 1; l + pos <= HUFF_LUT_BITS; ++l) {
                 const uint32_t c = (static_cast<uint32_t>(i) >> (HUFF_LUT_BITS - pos - l)) & ((1u << l) - 1u);
                 if (blc[l] > 0 && c >= fc[l] && c - fc[l] < blc[l]) {
-                    syms |= static_cast<uint32_t>(srt[fi[l] + (c - fc[l])]) << (8 * count);
+                    syms |= static_cast<uint64_t>(srt[fi[l] + (c - fc[l])]) << (8 * count);
                     ++count;
                     pos += l;
                     found = true;
@@ -109,7 +110,7 @@ __device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook 
             }
             if (!found) break;
         }
-        cb->lut[i] = count ? (syms | (count << 24) | (pos << 27)) : 0u;
+        cb->lut[i] = count ? (syms | (static_cast<uint64_t>(count) << 48) | (static_cast<uint64_t>(pos) << 52)) : 0ull;
     }
     __syncthreads();
     if (t == 0) {

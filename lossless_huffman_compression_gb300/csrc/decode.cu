@@ -7,20 +7,22 @@
 // encoder are those tasks' entry points.
 //
 // GPU design:
-//   * one thread per chunk (byte streams); for the fused bf16 path two
-//     adjacent lanes share a chunk pair, one per byte plane, and swap 8
-//     decoded bytes per round with a pair shuffle to form 16-bit words;
 //   * the codebook's 4096-entry first-level table sits in shared memory; an
-//     entry holds every code that fits completely in the 12-bit window (up
-//     to three symbols, their count and their total length), so short codes
-//     decode several symbols per lookup; codes longer than 12 bits take an
+//     entry lists every code that lies wholly inside a 12-bit window (up to
+//     six symbols, their count and their total length), so short codes decode
+//     several symbols per lookup; codes longer than 12 bits take an
 //     out-of-line canonical search (first_code / bl_count);
 //   * the bit reader keeps 64 bits in a register, refills 32 at a time from a
-//     128-bit queue, and always has the next 16-byte unit of the stream in
-//     flight, so global-memory latency stays off the decode chain; reads
+//     128-bit queue, and always has the next two 16-byte units of the stream
+//     in flight, so global-memory latency stays off the decode chain; reads
 //     never pass the payload's end;
-//   * decoded bytes gather in a 64-bit accumulator and leave as 8-byte
-//     stores; x0 (for the XOR delta) is loaded one group of four rounds ahead.
+//   * byte streams: one thread per chunk, decoded bytes leave as 8-byte stores;
+//   * fused bf16: one thread per chunk pair decodes 64 symbols of each byte
+//     plane per segment into private shared-memory rows (one lookup per loop
+//     iteration, stores predicated, so the lanes of a warp stay in step),
+//     then merges them into 16-bit words, XORs x0 (loaded before the
+//     segment's decode, so its latency hides behind it) and stores 128 bytes;
+//     no barrier couples the threads.
 // Every chunk must end exactly at the next chunk's offset, otherwise
 // HUFF_ERR_CORRUPT_STREAM is reported.
 #include "common.cuh"
@@ -33,7 +35,7 @@ constexpr int kDecBlock = 256;
 
 // 16-byte aligned (and sized) so that arrays of tables keep every lut 16-byte aligned for uint4 copies
 struct __align__(16) DecTables {
-    uint32_t lut[1u << HUFF_LUT_BITS];  // syms (24 bits) | count << 24 | total bits << 27
+    uint64_t lut[1u << HUFF_LUT_BITS];  // syms (48 bits) | count << 48 | total bits << 52
     uint32_t bl_count[32];
     uint32_t first_code[32];
     uint32_t first_index[32];
@@ -49,7 +51,7 @@ __device__ void load_tables(DecTables &T, const huff_codebook *cb) {
     const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
     const uint4 *src = reinterpret_cast<const uint4 *>(cb->lut);
     uint4 *dst = reinterpret_cast<uint4 *>(T.lut);
-    for (int i = tid; i < (1 << HUFF_LUT_BITS) / 4; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < (1 << HUFF_LUT_BITS) / 2; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
     if (tid < 32) {
         T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
         T.first_code[tid] = ok ? cb->first_code[tid] : 0;
@@ -79,11 +81,11 @@ struct BitReader {
     const uint8_t *p;
     size_t nbytes;
     size_t ui;        // next 16-byte unit to fetch
-    uint64_t buf;     // upcoming bits, most significant first
-    int nb;           // valid bits in buf
-    uint64_t qh, ql;  // queued big-endian words not yet in buf
+    uint32_t bh, bl;  // upcoming bits (64, most significant first): bh = first 32
+    int nb;           // valid bits in (bh, bl)
+    uint64_t qh, ql;  // queued big-endian words not yet in the bit buffer
     int qn;           // words left in the queue
-    uint4 nxt;        // the unit after the queue, in flight
+    uint4 nxt, nxt2;  // the two units after the queue, in flight
 
     __device__ __forceinline__ uint4 load_unit(size_t u) const {
         if (u * 16 + 16 <= nbytes) {
@@ -106,7 +108,8 @@ struct BitReader {
         ql <<= 32;
         if (--qn == 0) {
             enqueue(nxt);
-            nxt = load_unit(ui++);
+            nxt = nxt2;
+            nxt2 = load_unit(ui++);
         }
         return w;
     }
@@ -114,77 +117,93 @@ struct BitReader {
         const size_t u = pos >> 7;
         enqueue(load_unit(u));
         nxt = load_unit(u + 1);
-        ui = u + 2;
+        nxt2 = load_unit(u + 2);
+        ui = u + 3;
         for (uint32_t k = 0; k < ((pos >> 5) & 3u); ++k) pop();
-        buf = static_cast<uint64_t>(pop()) << 32;
-        buf |= pop();
-        const int sk = static_cast<int>(pos & 31u);
-        buf <<= sk;
-        nb = 64 - sk;
+        bh = pop();
+        bl = pop();
+        nb = 64;
+        consume(static_cast<uint32_t>(pos & 31u));
+    }
+    // drop `bits` (< 32) leading bits
+    __device__ __forceinline__ void consume(uint32_t bits) {
+        bh = __funnelshift_l(bl, bh, bits);
+        bl <<= bits;
+        nb -= static_cast<int>(bits);
     }
     __device__ __forceinline__ void refill() {
         if (nb <= 32) {
-            buf |= static_cast<uint64_t>(pop()) << (32 - nb);
+            const uint32_t w = pop();
+            const int s = 32 - nb;  // free bits in bl, 0..32
+            if (s == 32) {
+                bh = w;  // nb == 0: every bit of the buffer is free
+            } else {
+                bh |= s ? (w >> (32 - s)) : 0u;
+                bl |= w << s;
+            }
             nb += 32;
         }
     }
-    __device__ __forceinline__ void consume(uint32_t bits) {
-        buf <<= bits;
-        nb -= static_cast<int>(bits);
-    }
+    __device__ __forceinline__ uint64_t top64() const { return (static_cast<uint64_t>(bh) << 32) | bl; }
     // bits consumed from the start of the payload
     __device__ __forceinline__ uint64_t pos() const {
-        return static_cast<uint64_t>(ui - 1) * 128 - 32 * static_cast<uint64_t>(qn) - static_cast<uint64_t>(nb);
+        return static_cast<uint64_t>(ui - 2) * 128 - 32 * static_cast<uint64_t>(qn) - static_cast<uint64_t>(nb);
     }
 };
 
-// Canonical search for a code longer than the table's 12 bits; L = 0 if none matches.
-__device__ __noinline__ uint32_t long_code(uint64_t buf, const DecTables *T, uint32_t *L) {
-    const uint32_t v = static_cast<uint32_t>(buf >> (64 - HUFF_MAX_LEN));
+// Canonical search for a code longer than the table's 12 bits: returns
+// (length << 8) | symbol, length 0 if no code matches.
+__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables *T) {
+    const uint32_t v = top >> (32 - HUFF_MAX_LEN);
     for (int l = HUFF_LUT_BITS + 1; l <= T->longest; ++l) {
         const uint32_t c = v >> (HUFF_MAX_LEN - l);
         const uint32_t d = c - T->first_code[l];
-        if (d < T->bl_count[l]) {
-            *L = static_cast<uint32_t>(l);
-            return T->sorted[T->first_index[l] + d];
-        }
+        if (d < T->bl_count[l]) return (static_cast<uint32_t>(l) << 8) | T->sorted[T->first_index[l] + d];
     }
-    *L = 0;
     return 0;
+}
+
+// The rare case where a table entry holds more symbols than the chunk has
+// left: the total length of its first c symbols.
+__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables *T) {
+    uint32_t bits = 0;
+    for (uint32_t k = 0; k < c; ++k) bits += T->len[(v >> (8 * k)) & 0xffu];
+    return bits;
 }
 
 // Pending decoded bytes: byte k of the stream order is byte k of (a0, a1).
 struct Pend {
     uint64_t a0, a1;
-    int fill;
+    int fill;  // < 8 before a take, <= 7 + HUFF_LUT_SYMS after
 };
 
-// Decode one table lookup's worth of symbols (1..3, never more than rem > 0).
+// Decode one table lookup's worth of symbols (1..HUFF_LUT_SYMS, never more than rem > 0).
 __device__ __forceinline__ void take(BitReader &r, const DecTables &T, Pend &o, int &rem, bool &bad) {
     r.refill();
-    const uint32_t e = T.lut[r.buf >> (64 - HUFF_LUT_BITS)];
-    uint32_t c = (e >> 24) & 3u;
-    uint32_t bits = e >> 27;
-    uint32_t v = e & 0xffffffu;
+    const uint64_t e = T.lut[r.bh >> (32 - HUFF_LUT_BITS)];
+    uint32_t c = static_cast<uint32_t>(e >> 48) & 15u;
+    uint32_t bits = static_cast<uint32_t>(e >> 52) & 15u;
+    uint64_t v = e & 0xffffffffffffull;
     if (c == 0) {
-        uint32_t L;
-        v = long_code(r.buf, &T, &L);
+        const uint32_t lc = long_code(r.bh, &T);
+        uint32_t L = lc >> 8;
         if (L == 0) {
             bad = true;
             L = 1;
         }
+        v = lc & 0xffu;
         c = 1;
         bits = L;
     } else if (static_cast<int>(c) > rem) {
         c = static_cast<uint32_t>(rem);
-        bits = T.len[v & 0xffu] + (c == 2 ? T.len[(v >> 8) & 0xffu] : 0u);
-        v &= c == 1 ? 0xffu : 0xffffu;
+        bits = clamped_bits(v, c, &T);
+        v &= (1ull << (8 * c)) - 1ull;
     }
     r.consume(bits);
     rem -= static_cast<int>(c);
     const int f = o.fill;
-    o.a0 |= static_cast<uint64_t>(v) << (8 * f);
-    if (f + static_cast<int>(c) > 8) o.a1 |= static_cast<uint64_t>(v) >> (8 * (8 - f));
+    o.a0 |= v << (8 * f);
+    if (f + static_cast<int>(c) > 8) o.a1 |= v >> (8 * (8 - f));
     o.fill = f + static_cast<int>(c);
 }
 
@@ -231,26 +250,63 @@ __global__ void __launch_bounds__(kDecBlock) k_decode_u8(const uint8_t *__restri
     int rem = cnt;
     Pend pd{0, 0, 0};
     int written = 0;
-    while (rem > 0) {
-        take(r, T, pd, rem, bad);  // fill < 8 before, <= 10 after
+    while (rem > 0) {  // one lookup per iteration keeps the lanes in step
+        take(r, T, pd, rem, bad);
         if (pd.fill >= 8) {
             *reinterpret_cast<uint64_t *>(o + written) = pd.a0;
             written += 8;
             shift8(pd);
         }
     }
+    while (pd.fill >= 8) {
+        *reinterpret_cast<uint64_t *>(o + written) = pd.a0;
+        written += 8;
+        shift8(pd);
+    }
     for (int k = 0; k < pd.fill; ++k) o[written + k] = static_cast<uint8_t>(pd.a0 >> (8 * k));
     if (bad || r.pos() != end) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
-// Lanes 2c (high plane) and 2c + 1 (low plane) decode chunk c of their plane.
+constexpr int kSegB = 64;                                    // elements per lane per segment
+constexpr int kRowB = kSegB + 8;                              // staging row pitch (spreads the lanes' rows over banks)
+constexpr size_t kBf16Smem = 2 * sizeof(DecTables) + size_t(2) * kDecBlock * kRowB;
+
+// Decode one plane's symbols up to `target` into its staging row (row byte k
+// = stream symbol seg0 + k).  Every iteration does one table lookup and, when
+// 8 bytes are ready, one 8-byte store: the lanes of a warp run the same
+// instructions and only the trip count differs.  Symbols decoded past
+// `target` stay in the accumulator for the next segment.
+__device__ __forceinline__ void decode_row(BitReader &r, const DecTables &T, Pend &pd, int &rem, int &written,
+                                           int target, int seg0, uint8_t *row, bool &bad) {
+    while (written < target) {
+        if (rem > 0) take(r, T, pd, rem, bad);  // fill <= 7 before, <= 13 after
+        if (pd.fill >= 8) {
+            *reinterpret_cast<uint64_t *>(row + (written - seg0)) = pd.a0;
+            written += 8;
+            shift8(pd);
+        } else if (rem == 0) {
+            *reinterpret_cast<uint64_t *>(row + (written - seg0)) = pd.a0;
+            written += pd.fill;
+            pd.fill = 0;
+            pd.a0 = 0;
+        }
+    }
+}
+
+// Each thread owns one chunk pair: per segment it decodes 64 symbols of the
+// high-byte plane, then 64 of the low-byte plane, into two private
+// shared-memory rows, then merges them into 16-bit words, XORs x0 and stores
+// 128 bytes.  Long segments let the lanes' varying symbols-per-lookup even
+// out before the warp's lanes meet again.  No barrier couples the threads, and every lane of a warp runs
+// the same plane at the same time.
 template <bool XOR>
 __global__ void __launch_bounds__(kDecBlock) k_decode_bf16(
     const uint8_t *__restrict__ pay_hi, size_t bytes_hi, const uint64_t *__restrict__ off_hi,
     const uint8_t *__restrict__ pay_lo, size_t bytes_lo, const uint64_t *__restrict__ off_lo, size_t n,
     size_t chunk, const huff_codebook *__restrict__ cb_hi, const huff_codebook *__restrict__ cb_lo,
     const uint16_t *__restrict__ x0, uint16_t *__restrict__ out, int32_t *status) {
-    __shared__ DecTables Tb[2];
+    extern __shared__ __align__(16) uint8_t dsm[];
+    DecTables *Tb = reinterpret_cast<DecTables *>(dsm);
     load_tables(Tb[0], cb_hi);
     load_tables(Tb[1], cb_lo);
     __syncthreads();
@@ -259,81 +315,67 @@ __global__ void __launch_bounds__(kDecBlock) k_decode_bf16(
         return;
     }
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    const size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const size_t c = g >> 1;
-    const int plane = static_cast<int>(g & 1);  // 0: high byte, 1: low byte
-    if (c >= n_chunks) return;                   // both lanes of a pair leave together
-    const unsigned pair = 3u << (threadIdx.x & 30u);
-    const DecTables &T = Tb[plane];
-    const uint8_t *pay = plane ? pay_lo : pay_hi;
-    const size_t nbytes = plane ? bytes_lo : bytes_hi;
-    const uint64_t *off = plane ? off_lo : off_hi;
-    uint64_t start, end;
-    const bool ok = chunk_bounds(off, c, nbytes, start, end);
-    if (!ok) set_status(status, HUFF_ERR_CORRUPT_STREAM);
-    if (__any_sync(pair, !ok)) return;
-    BitReader r;
-    r.p = pay;
-    r.nbytes = nbytes;
-    r.init(start);
+    const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= n_chunks) return;
+    uint64_t sh, eh, sl, el;
+    if (!chunk_bounds(off_hi, c, bytes_hi, sh, eh) || !chunk_bounds(off_lo, c, bytes_lo, sl, el)) {
+        set_status(status, HUFF_ERR_CORRUPT_STREAM);
+        return;
+    }
+    uint8_t *hrow = dsm + 2 * sizeof(DecTables) + static_cast<size_t>(threadIdx.x) * kRowB;
+    uint8_t *lrow = hrow + static_cast<size_t>(kDecBlock) * kRowB;
+    BitReader rh, rl;
+    rh.p = pay_hi;
+    rh.nbytes = bytes_hi;
+    rh.init(sh);
+    rl.p = pay_lo;
+    rl.nbytes = bytes_lo;
+    rl.init(sl);
     const size_t first = c * chunk;
     const int cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
     uint16_t *o = out + first;
     const uint16_t *x = XOR ? x0 + first : nullptr;
     bool bad = false;
-    int rem = cnt;
-    Pend pd{0, 0, 0};
-    // x0 words of this lane (4 elements per round) for the current and the next group of 4 rounds
-    uint64_t xq[4] = {0, 0, 0, 0}, xn[4] = {0, 0, 0, 0};
-    if (XOR) {
+    int remh = cnt, reml = cnt, wh = 0, wl = 0;
+    Pend ph{0, 0, 0}, pl{0, 0, 0};
+    for (int seg0 = 0; seg0 < cnt; seg0 += kSegB) {
+        const int target = cnt - seg0 < kSegB ? cnt : seg0 + kSegB;
+        const bool full = target == seg0 + kSegB;
+        uint4 xq[kSegB / 8];  // x0 of the whole segment, in flight while the planes decode
+        if (XOR && full) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int base = 8 * q + 4 * plane;
-            if (base + 4 <= cnt) xq[q] = __ldcs(reinterpret_cast<const unsigned long long *>(x + base));
+            for (int g = 0; g < kSegB / 8; ++g) xq[g] = __ldcs(reinterpret_cast<const uint4 *>(x + seg0) + g);
         }
-    }
-    for (int k = 0; k < cnt; k += 32) {
-        if (XOR) {
+        decode_row(rh, Tb[0], ph, remh, wh, target, seg0, hrow, bad);
+        decode_row(rl, Tb[1], pl, reml, wl, target, seg0, lrow, bad);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int base = k + 32 + 8 * q + 4 * plane;
-                if (base + 4 <= cnt) xn[q] = __ldcs(reinterpret_cast<const unsigned long long *>(x + base));
-            }
-        }
+        for (int g = 0; g < kSegB / 8; ++g) {
+            const int e0 = seg0 + 8 * g;  // first of this group's 8 elements
+            if (e0 >= target) break;
+            const uint2 h = *reinterpret_cast<const uint2 *>(hrow + 8 * g);
+            const uint2 l = *reinterpret_cast<const uint2 *>(lrow + 8 * g);
+            uint4 v = make_uint4(__byte_perm(l.x, h.x, 0x5140), __byte_perm(l.x, h.x, 0x7362),
+                                 __byte_perm(l.y, h.y, 0x5140), __byte_perm(l.y, h.y, 0x7362));
+            if (e0 + 8 <= target) {
+                if (XOR) {
+                    const uint4 xv = full ? xq[g] : __ldcs(reinterpret_cast<const uint4 *>(x + e0));
+                    v.x ^= xv.x; v.y ^= xv.y; v.z ^= xv.z; v.w ^= xv.w;
+                }
+                __stcs(reinterpret_cast<uint4 *>(o + e0), v);
+            } else {
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int kk = k + 8 * q;
-            if (kk < cnt) {
-                const int want = cnt - kk < 8 ? cnt - kk : 8;
-                while (pd.fill < want) take(r, T, pd, rem, bad);
-                const uint64_t mine = pd.a0;
-                const uint64_t other = __shfl_xor_sync(pair, mine, 1);
-                const uint64_t hi8 = plane ? other : mine;
-                const uint64_t lo8 = plane ? mine : other;
-                // element j = lo byte j | hi byte j << 8; the high lane writes elements 0-3, the low lane 4-7
-                const uint32_t l32 = static_cast<uint32_t>(plane ? lo8 >> 32 : lo8);
-                const uint32_t h32 = static_cast<uint32_t>(plane ? hi8 >> 32 : hi8);
-                uint64_t wv = (static_cast<uint64_t>(__byte_perm(l32, h32, 0x7362)) << 32) |
-                              __byte_perm(l32, h32, 0x5140);
-                const int base = kk + 4 * plane;
-                if (base + 4 <= cnt) {
-                    if (XOR) wv ^= xq[q];
-                    __stcs(reinterpret_cast<unsigned long long *>(o + base), static_cast<unsigned long long>(wv));
-                } else {
-                    for (int j = 0; j < 4 && base + j < cnt; ++j) {
-                        uint16_t v = static_cast<uint16_t>(wv >> (16 * j));
-                        if (XOR) v ^= x[base + j];
-                        o[base + j] = v;
+                for (int k = 0; k < 8; ++k) {
+                    if (e0 + k < target) {
+                        uint16_t val = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+                        if (XOR) val ^= x[e0 + k];
+                        o[e0 + k] = val;
                     }
                 }
-                if (want == 8) shift8(pd);
-                else pd.fill = 0;
             }
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) xq[q] = xn[q];
     }
-    if (bad || r.pos() != end) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+    if (bad || rh.pos() != eh || rl.pos() != el) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
 }  // namespace
@@ -353,13 +395,21 @@ int launch_decode_bf16(const uint8_t *pay_hi, size_t bytes_hi, const uint64_t *o
                        uint16_t *out, int32_t *status, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    const unsigned grid = static_cast<unsigned>((2 * n_chunks + kDecBlock - 1) / kDecBlock);
-    if (x0 != nullptr)
-        k_decode_bf16<true><<<grid, kDecBlock, 0, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n,
-                                                       chunk, cb_hi, cb_lo, x0, out, status);
-    else
-        k_decode_bf16<false><<<grid, kDecBlock, 0, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n,
-                                                        chunk, cb_hi, cb_lo, nullptr, out, status);
+    const unsigned grid = static_cast<unsigned>((n_chunks + kDecBlock - 1) / kDecBlock);
+    if (x0 != nullptr) {
+        if (cudaFuncSetAttribute(k_decode_bf16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kBf16Smem)) != cudaSuccess)
+            return HUFF_ERR_CUDA;
+        k_decode_bf16<true><<<grid, kDecBlock, kBf16Smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo,
+                                                               n, chunk, cb_hi, cb_lo, x0, out, status);
+    } else {
+        if (cudaFuncSetAttribute(k_decode_bf16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kBf16Smem)) != cudaSuccess)
+            return HUFF_ERR_CUDA;
+        k_decode_bf16<false><<<grid, kDecBlock, kBf16Smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo,
+                                                                off_lo, n, chunk, cb_hi, cb_lo, nullptr, out,
+                                                                status);
+    }
     return launch_status();
 }
 
