@@ -19,7 +19,6 @@ constexpr int kEncBf16ElemsPerThread = 16;       // two 16-byte vectors of bf16
 constexpr int kEncBf16Tile = kEncThreads * kEncBf16ElemsPerThread; // 4096 elements
 constexpr int kEncStages = 3;                    // TMA ring depth
 constexpr int kLutRep = 8;                       // copies of the encode table (bank spreading)
-constexpr int kDecThreads = 128;                 // decode CTA size
 constexpr int kHistThreads = 512;
 constexpr int kHistCopies = 32;                  // one histogram copy per lane
 constexpr int kHistPitch = 257;                  // padded copy pitch: copy c of bin b sits in bank (c+b)%32

@@ -31,11 +31,13 @@ namespace huffk {
 
 namespace {
 
-constexpr int kDecBlock = 256;
+constexpr int kSecMax = 2048;  // secondary-table entries per plane
 
 // 16-byte aligned (and sized) so that arrays of tables keep every lut 16-byte aligned for uint4 copies
 struct __align__(16) DecTables {
-    uint64_t lut[1u << HUFF_LUT_BITS];  // syms (48 bits) | count << 48 | total bits << 52
+    uint64_t lut[1u << HUFF_LUT_BITS];  // syms (48 bits) | count << 48 | total bits << 52; 0: first code > 12 bits
+    uint16_t sec[kSecMax];              // codes longer than 12 bits: symbol | length << 8 (0: no code)
+    uint64_t run;                       // the 1-bit code's symbol in all 8 bytes (when there is one)
     uint32_t bl_count[32];
     uint32_t first_code[32];
     uint32_t first_index[32];
@@ -43,32 +45,71 @@ struct __align__(16) DecTables {
     uint8_t len[256];
     int longest;
     int ok;
+    int has_run;    // a 1-bit code exists: 8 leading zero bits are 8 of its symbol
+    int sec_k;      // bits after the 12-bit window that index sec (0: no code is longer than 12 bits)
+    int sec_first;  // first 12-bit prefix of the long codes (they fill the top of the code space)
+    int sec_ok;     // sec holds every long code; otherwise the canonical search decodes them
 };
 static_assert(sizeof(DecTables) % 16 == 0, "table arrays must keep 16-byte alignment");
 
-__device__ void load_tables(DecTables &T, const huff_codebook *cb) {
+// Copy a device codebook into shared tables and build the secondary table
+// for codes longer than the 12-bit window.  Canonical codes place every code
+// longer than 12 bits after all shorter ones, so their 12-bit prefixes are
+// the contiguous range [first_code[13] / 2, 4096); sec holds, per prefix,
+// 2^k entries (k = longest - 12) indexed by the next k bits.  Two barriers.
+__device__ void load_tables(DecTables *Ts, const huff_codebook *const *cbs, int nt) {
     const int tid = threadIdx.x;
-    const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
-    const uint4 *src = reinterpret_cast<const uint4 *>(cb->lut);
-    uint4 *dst = reinterpret_cast<uint4 *>(T.lut);
-    for (int i = tid; i < (1 << HUFF_LUT_BITS) / 2; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
-    if (tid < 32) {
-        T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
-        T.first_code[tid] = ok ? cb->first_code[tid] : 0;
-        T.first_index[tid] = ok ? cb->first_index[tid] : 0;
+    for (int t = 0; t < nt; ++t) {
+        DecTables &T = Ts[t];
+        const huff_codebook *cb = cbs[t];
+        const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
+        const uint4 *src = reinterpret_cast<const uint4 *>(cb->lut);
+        uint4 *dst = reinterpret_cast<uint4 *>(T.lut);
+        for (int i = tid; i < (1 << HUFF_LUT_BITS) / 2; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
+        uint4 *sz = reinterpret_cast<uint4 *>(T.sec);
+        for (int i = tid; i < kSecMax / 8; i += blockDim.x) sz[i] = make_uint4(0, 0, 0, 0);
+        if (tid < 32) {
+            T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
+            T.first_code[tid] = ok ? cb->first_code[tid] : 0;
+            T.first_index[tid] = ok ? cb->first_index[tid] : 0;
+        }
+        for (int i = tid; i < 256; i += blockDim.x) {
+            T.sorted[i] = ok ? cb->sorted_symbols[i] : 0;
+            T.len[i] = ok ? cb->len[i] : 0;
+        }
+        if (tid == 0) {
+            const int longest = ok ? cb->longest : 0;
+            T.longest = longest;
+            T.ok = ok && longest <= HUFF_MAX_LEN;
+            T.has_run = ok && cb->bl_count[1] > 0;
+            T.run = (ok ? static_cast<uint64_t>(cb->sorted_symbols[0]) : 0ull) * 0x0101010101010101ull;
+            const int k = longest > HUFF_LUT_BITS ? longest - HUFF_LUT_BITS : 0;
+            const int first = k ? static_cast<int>(cb->first_code[HUFF_LUT_BITS + 1] >> 1) : (1 << HUFF_LUT_BITS);
+            T.sec_k = k;
+            T.sec_first = first;
+            T.sec_ok = k == 0 || (first <= (1 << HUFF_LUT_BITS) &&
+                                  (static_cast<long long>((1 << HUFF_LUT_BITS) - first) << k) <= kSecMax);
+        }
     }
-    for (int i = tid; i < 256; i += blockDim.x) {
-        T.sorted[i] = ok ? cb->sorted_symbols[i] : 0;
-        T.len[i] = ok ? cb->len[i] : 0;
+    __syncthreads();
+    for (int t = 0; t < nt; ++t) {
+        DecTables &T = Ts[t];
+        if (!T.ok || T.sec_k == 0 || !T.sec_ok) continue;
+        const int k = T.sec_k;
+        const huff_codebook *cb = cbs[t];
+        for (int sym = tid; sym < 256; sym += blockDim.x) {
+            const int L = T.len[sym];
+            if (L <= HUFF_LUT_BITS) continue;
+            const uint32_t base = (cb->code[sym] << (HUFF_LUT_BITS + k - L)) - (static_cast<uint32_t>(T.sec_first) << k);
+            const uint16_t ent = static_cast<uint16_t>(sym | (L << 8));
+            for (uint32_t j = 0; j < (1u << (HUFF_LUT_BITS + k - L)); ++j) T.sec[base + j] = ent;
+        }
     }
-    if (tid == 0) {
-        T.longest = ok ? cb->longest : 0;
-        T.ok = ok && cb->longest <= HUFF_MAX_LEN;
-    }
+    __syncthreads();
 }
 
 // Bytes of a 16-byte unit past the payload's end read as zero.
-__device__ __noinline__ uint4 load_unit_tail(const uint8_t *p, size_t nbytes, size_t u) {
+__device__ __forceinline__ uint4 load_unit_tail(const uint8_t *p, size_t nbytes, size_t u) {
     uint32_t w[4] = {0, 0, 0, 0};
     for (int k = 0; k < 16; ++k) {
         const size_t i = u * 16 + k;
@@ -77,79 +118,20 @@ __device__ __noinline__ uint4 load_unit_tail(const uint8_t *p, size_t nbytes, si
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-struct BitReader {
-    const uint8_t *p;
-    size_t nbytes;
-    size_t ui;        // next 16-byte unit to fetch
-    uint32_t bh, bl;  // upcoming bits (64, most significant first): bh = first 32
-    int nb;           // valid bits in (bh, bl)
-    uint64_t qh, ql;  // queued big-endian words not yet in the bit buffer
-    int qn;           // words left in the queue
-    uint4 nxt, nxt2;  // the two units after the queue, in flight
-
-    __device__ __forceinline__ uint4 load_unit(size_t u) const {
-        if (u * 16 + 16 <= nbytes) {
-            uint4 v;
-            asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "l"(p + u * 16));
-            return v;
-        }
-        return load_unit_tail(p, nbytes, u);
+// Bit reader: 64 upcoming bits in (bh, bl), most significant first; the
+// current 16-byte unit of the stream (raw words, qi = next word) and the one
+// after it, in flight.  The payload pointer and size are passed to every
+// call that may load, so they stay kernel parameters rather than registers.
+__device__ __forceinline__ uint4 load_unit(const uint8_t *p, size_t nbytes, size_t u) {
+    if (u * 16 + 16 <= nbytes) {
+        uint4 v;
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p + u * 16));
+        return v;
     }
-    __device__ __forceinline__ void enqueue(uint4 v) {
-        qh = (static_cast<uint64_t>(bswap32(v.x)) << 32) | bswap32(v.y);
-        ql = (static_cast<uint64_t>(bswap32(v.z)) << 32) | bswap32(v.w);
-        qn = 4;
-    }
-    __device__ __forceinline__ uint32_t pop() {
-        const uint32_t w = static_cast<uint32_t>(qh >> 32);
-        qh = (qh << 32) | (ql >> 32);
-        ql <<= 32;
-        if (--qn == 0) {
-            enqueue(nxt);
-            nxt = nxt2;
-            nxt2 = load_unit(ui++);
-        }
-        return w;
-    }
-    __device__ __forceinline__ void init(uint64_t pos) {
-        const size_t u = pos >> 7;
-        enqueue(load_unit(u));
-        nxt = load_unit(u + 1);
-        nxt2 = load_unit(u + 2);
-        ui = u + 3;
-        for (uint32_t k = 0; k < ((pos >> 5) & 3u); ++k) pop();
-        bh = pop();
-        bl = pop();
-        nb = 64;
-        consume(static_cast<uint32_t>(pos & 31u));
-    }
-    // drop `bits` (< 32) leading bits
-    __device__ __forceinline__ void consume(uint32_t bits) {
-        bh = __funnelshift_l(bl, bh, bits);
-        bl <<= bits;
-        nb -= static_cast<int>(bits);
-    }
-    __device__ __forceinline__ void refill() {
-        if (nb <= 32) {
-            const uint32_t w = pop();
-            const int s = 32 - nb;  // free bits in bl, 0..32
-            if (s == 32) {
-                bh = w;  // nb == 0: every bit of the buffer is free
-            } else {
-                bh |= s ? (w >> (32 - s)) : 0u;
-                bl |= w << s;
-            }
-            nb += 32;
-        }
-    }
-    __device__ __forceinline__ uint64_t top64() const { return (static_cast<uint64_t>(bh) << 32) | bl; }
-    // bits consumed from the start of the payload
-    __device__ __forceinline__ uint64_t pos() const {
-        return static_cast<uint64_t>(ui - 2) * 128 - 32 * static_cast<uint64_t>(qn) - static_cast<uint64_t>(nb);
-    }
-};
+    return load_unit_tail(p, nbytes, u);
+}
 
 // Canonical search for a code longer than the table's 12 bits: returns
 // (length << 8) | symbol, length 0 if no code matches.
@@ -171,46 +153,174 @@ __device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecT
     return bits;
 }
 
-// Pending decoded bytes: byte k of the stream order is byte k of (a0, a1).
-struct Pend {
-    uint64_t a0, a1;
-    int fill;  // < 8 before a take, <= 7 + HUFF_LUT_SYMS after
+// ------------------------------------------------------------------ per-lane plane decoder
+//
+// A lane decodes one chunk of one byte plane into a private ring of RING
+// bytes in shared memory.  The warp works in segments of kSeg symbols per
+// lane: it keeps stepping until every lane has stored its segment, and a lane
+// that is ahead keeps decoding into the ring's free slots instead of idling,
+// so the lanes' varying symbols-per-lookup cost little SIMT efficiency.  Then
+// the warp copies the segment out cooperatively, so global stores are whole
+// sectors.  A step is one straight-line table lookup; only codes longer than
+// the 12-bit window (one secondary-table load) and a chunk's last symbols
+// leave it.
+constexpr int kSeg = 32;       // symbols per lane per segment (multiple of 16)
+constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
+constexpr int kStepMax = 8;    // symbols one step may add (a run of the 1-bit code)
+constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
+static_assert(kRing >= kSeg + 7 + kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
+static_assert(HUFF_LUT_SYMS <= kStepMax, "a table entry must fit one step");
+
+struct PlaneDec {
+    uint32_t bh, bl;  // upcoming bits, most significant first
+    int nb;           // valid bits in (bh, bl); >= 33 after a refill
+    int qi;           // next word of cur
+    uint4 cur;        // current unit (raw little-endian words)
+    size_t ui;        // index of the unit after cur
+    uint64_t a0;      // pending decoded bytes: byte k of the stream order is byte k of a0
+    int fill;         // pending symbols, < 8 between steps
+    int st;           // symbols stored to the ring (a multiple of 8 until the chunk is complete)
+
+    __device__ __forceinline__ void refill(const uint8_t *p, size_t nbytes) {
+        const bool rf = nb <= 32;
+        const uint32_t raw = (qi & 2) ? ((qi & 1) ? cur.w : cur.z) : ((qi & 1) ? cur.y : cur.x);
+        const uint32_t w = rf ? bswap32(raw) : 0u;
+        bh |= __funnelshift_rc(w, 0u, static_cast<uint32_t>(nb));       // w >> nb (0 when nb >= 32)
+        bl |= __funnelshift_lc(0u, w, static_cast<uint32_t>(32 - nb));  // w << (32 - nb)
+        nb += rf ? 32 : 0;
+        qi += rf ? 1 : 0;
+        if (qi == 4) {
+            cur = load_unit(p, nbytes, ui++);
+            qi = 0;
+        }
+    }
+    __device__ __forceinline__ void consume(uint32_t bits) {  // bits < 32
+        bh = __funnelshift_l(bl, bh, bits);
+        bl <<= bits;
+        nb -= static_cast<int>(bits);
+    }
+    __device__ __forceinline__ void start(const uint8_t *p, size_t nbytes, uint64_t pos) {
+        const size_t u = pos >> 7;
+        cur = load_unit(p, nbytes, u);
+        ui = u + 1;
+        qi = static_cast<int>((pos >> 5) & 3u);
+        bh = bl = 0;
+        nb = 0;
+        refill(p, nbytes);
+        refill(p, nbytes);
+        consume(static_cast<uint32_t>(pos & 31u));
+    }
+    // bits consumed from the start of the payload
+    __device__ __forceinline__ uint64_t pos() const {
+        return 32 * (static_cast<uint64_t>(ui - 1) * 4 + static_cast<uint64_t>(qi)) - static_cast<uint64_t>(nb);
+    }
 };
 
-// Decode one table lookup's worth of symbols (1..HUFF_LUT_SYMS, never more than rem > 0).
-__device__ __forceinline__ void take(BitReader &r, const DecTables &T, Pend &o, int &rem, bool &bad) {
-    r.refill();
-    const uint64_t e = T.lut[r.bh >> (32 - HUFF_LUT_BITS)];
-    uint32_t c = static_cast<uint32_t>(e >> 48) & 15u;
-    uint32_t bits = static_cast<uint32_t>(e >> 52) & 15u;
-    uint64_t v = e & 0xffffffffffffull;
+// The rare cases of a step: a code longer than the table's window (or no
+// code at all: a corrupt stream), and an entry with more symbols than the
+// chunk has left.
+__device__ __forceinline__ void step_rare(const DecTables &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
+                                       uint32_t &bits, uint64_t &v, bool &bad) {
     if (c == 0) {
-        const uint32_t lc = long_code(r.bh, &T);
-        uint32_t L = lc >> 8;
+        uint32_t L = 0, sym = 0;
+        if (T.sec_ok) {
+            if (T.sec_k > 0 && static_cast<int>(win) >= T.sec_first) {
+                const int k = T.sec_k;
+                const uint32_t idx = ((win - static_cast<uint32_t>(T.sec_first)) << k) |
+                                     ((top >> (32 - HUFF_LUT_BITS - k)) & ((1u << k) - 1u));
+                const uint32_t e2 = T.sec[idx];
+                L = e2 >> 8;
+                sym = e2 & 0xffu;
+            }
+        } else {
+            const uint32_t lc = long_code(top, &T);
+            L = lc >> 8;
+            sym = lc & 0xffu;
+        }
         if (L == 0) {
             bad = true;
             L = 1;
         }
-        v = lc & 0xffu;
         c = 1;
         bits = L;
-    } else if (static_cast<int>(c) > rem) {
+        v = sym;
+    }
+    if (static_cast<int>(c) > rem) {
         c = static_cast<uint32_t>(rem);
         bits = clamped_bits(v, c, &T);
         v &= (1ull << (8 * c)) - 1ull;
     }
-    r.consume(bits);
-    rem -= static_cast<int>(c);
-    const int f = o.fill;
-    o.a0 |= v << (8 * f);
-    if (f + static_cast<int>(c) > 8) o.a1 |= v >> (8 * (8 - f));
-    o.fill = f + static_cast<int>(c);
 }
 
-__device__ __forceinline__ void shift8(Pend &o) {
-    o.a0 = o.a1;
-    o.a1 = 0;
-    o.fill -= 8;
+// One step: if the chunk has symbols left and the ring has room, one table
+// lookup (or a run of eight 1-bit codes), then at most one 8-byte store.
+// `limit` = the first symbol position whose slot still holds unmerged data.
+template <int RING, bool RUN>
+__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables &T,
+                                     uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
+    // Predicated rather than branched: a lane with nothing to do (its chunk
+    // is complete or its ring is full) takes a step of zero bits and zero
+    // symbols, so the step stays one basic block.
+    const int rem = cnt - s.st - s.fill;
+    const bool go = rem > 0 && s.st + s.fill + kStepMax <= limit;
+    s.refill(p, nbytes);
+    const uint32_t win = s.bh >> (32 - HUFF_LUT_BITS);
+    const uint64_t e = T.lut[win];
+    const uint32_t eh = static_cast<uint32_t>(e >> 32);
+    uint32_t c = (eh >> 16) & 15u;
+    uint32_t bits = eh >> 20;
+    uint64_t v = e & 0xffffffffffffull;
+    if (RUN && s.bh < (1u << 24)) {
+        c = 8;
+        bits = 8;
+        v = run;
+    }
+    if (go && (c == 0 || static_cast<int>(c) > rem)) step_rare(T, win, s.bh, rem, c, bits, v, bad);
+    c = go ? c : 0u;
+    bits = go ? bits : 0u;
+    v = go ? v : 0ull;
+    s.consume(bits);
+    const int f = s.fill;
+    const uint64_t a = s.a0 | (v << (8 * f));
+    const int nf = f + static_cast<int>(c);
+    const bool full = nf >= 8;
+    if (full) *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = a;
+    s.a0 = full ? (v >> 1) >> (63 - 8 * f) : a;  // the bytes that did not fit
+    s.st += full ? 8 : 0;
+    s.fill = full ? nf - 8 : nf;
+}
+
+__device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, size_t nbytes, uint64_t start, int cnt) {
+    if (cnt > 0) s.start(pay, nbytes, start);
+    s.a0 = 0;
+    s.fill = 0;
+    s.st = 0;
+}
+
+// Decode until every lane of the warp has stored symbols [.., need) into its
+// RING-byte ring (a lane whose chunk is complete stores its last partial word).
+template <int RING, bool RUN>
+__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables &T,
+                                               uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
+                                               bool &bad) {
+    const uint64_t run = RUN ? T.run : 0ull;
+    while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
+        step<RING, RUN>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+    if (s.fill > 0 && s.st + s.fill == cnt) {
+        *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
+        s.st = cnt;
+        s.fill = 0;
+        s.a0 = 0;
+    }
+}
+
+template <int RING>
+__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables &T,
+                                             uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
+    if (T.has_run)
+        fill_segment_t<RING, true>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+    else
+        fill_segment_t<RING, false>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
 __device__ __forceinline__ bool chunk_bounds(const uint64_t *off, size_t c, size_t nbytes, uint64_t &start,
@@ -220,162 +330,173 @@ __device__ __forceinline__ bool chunk_bounds(const uint64_t *off, size_t c, size
     return start <= end && end <= static_cast<uint64_t>(nbytes) * 8;
 }
 
-__global__ void __launch_bounds__(kDecBlock) k_decode_u8(const uint8_t *__restrict__ payload, size_t nbytes,
-                                                         const uint64_t *__restrict__ off, size_t n, size_t chunk,
-                                                         const huff_codebook *__restrict__ cb,
-                                                         uint8_t *__restrict__ out, int32_t *status) {
-    __shared__ DecTables T;
-    load_tables(T, cb);
-    __syncthreads();
+// Launch geometry: one lane per chunk (pair), blocks spread over every SM.
+__host__ int decode_block(size_t n_chunks, int sms) {
+    size_t per_sm = (n_chunks + static_cast<size_t>(sms) - 1) / static_cast<size_t>(sms);
+    per_sm = (per_sm + 31) / 32 * 32;
+    return static_cast<int>(per_sm > static_cast<size_t>(kMaxBlock) ? kMaxBlock : per_sm);
+}
+
+// ------------------------------------------------------------------ byte streams
+//
+// Lane ring: 2 * kRing bytes (one plane, twice the slack); swizzled by lane
+// parity so that the copy-out's reads of 8 lanes' segments spread over the banks.
+constexpr int kRingU8 = 2 * kRing;
+constexpr int kSegU8 = 2 * kSeg;
+
+__global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__restrict__ payload, size_t nbytes,
+                                                           const uint64_t *__restrict__ off, size_t n, size_t chunk,
+                                                           const huff_codebook *__restrict__ cb,
+                                                           uint8_t *__restrict__ out, int32_t *status) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    DecTables &T = *reinterpret_cast<DecTables *>(dsm);
+    const huff_codebook *cbs[1] = {cb};
+    load_tables(&T, cbs, 1);
     if (!T.ok) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
         return;
     }
+    const int lane = threadIdx.x & 31;
     const size_t n_chunks = (n + chunk - 1) / chunk;
     const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= n_chunks) return;
-    uint64_t start, end;
-    if (!chunk_bounds(off, c, nbytes, start, end)) {
-        set_status(status, HUFF_ERR_CORRUPT_STREAM);
-        return;
+    const size_t c0 = c - lane;  // the warp's first chunk
+    uint64_t start = 0, end = 0;
+    int cnt = 0;
+    if (c < n_chunks) {
+        if (chunk_bounds(off, c, nbytes, start, end)) {
+            const size_t first = c * chunk;
+            cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
+        } else {
+            set_status(status, HUFF_ERR_CORRUPT_STREAM);
+        }
     }
-    BitReader r;
-    r.p = payload;
-    r.nbytes = nbytes;
-    r.init(start);
-    const size_t first = c * chunk;
-    const int cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
-    uint8_t *o = out + first;
+    uint8_t *rings = dsm + sizeof(DecTables) + static_cast<size_t>(threadIdx.x - lane) * kRingU8;
+    uint8_t *ring = rings + lane * kRingU8;
+    const uint32_t swz = (lane & 1) ? kRingU8 / 2 : 0;
+    PlaneDec s;
+    plane_start(s, payload, nbytes, start, cnt);
     bool bad = false;
-    int rem = cnt;
-    Pend pd{0, 0, 0};
-    int written = 0;
-    while (rem > 0) {  // one lookup per iteration keeps the lanes in step
-        take(r, T, pd, rem, bad);
-        if (pd.fill >= 8) {
-            *reinterpret_cast<uint64_t *>(o + written) = pd.a0;
-            written += 8;
-            shift8(pd);
+    const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
+    for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSegU8) {
+        fill_segment<kRingU8>(s, payload, nbytes, T, ring, swz, cnt, min(cnt, seg0 + kSegU8), seg0 + kRingU8, bad);
+        __syncwarp();
+        // copy-out: 8 lanes' segments per pass, 16 bytes per lane
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int sl = 8 * i + (lane >> 2);
+            const int e0 = seg0 + 16 * (lane & 3);
+            const int cs = __shfl_sync(0xffffffffu, cnt, sl);
+            if (e0 < cs) {
+                const uint8_t *src =
+                    rings + sl * kRingU8 + ((e0 & (kRingU8 - 1)) ^ ((sl & 1) ? kRingU8 / 2 : 0));
+                uint8_t *dst = out + (c0 + sl) * chunk + e0;
+                const uint4 v = *reinterpret_cast<const uint4 *>(src);
+                if (e0 + 16 <= cs) {  // out is 16-byte aligned and chunk a multiple of 256
+                    __stcs(reinterpret_cast<uint4 *>(dst), v);
+                } else {
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    for (int k = 0; k < cs - e0; ++k) dst[k] = static_cast<uint8_t>(w[k >> 2] >> (8 * (k & 3)));
+                }
+            }
         }
+        __syncwarp();
     }
-    while (pd.fill >= 8) {
-        *reinterpret_cast<uint64_t *>(o + written) = pd.a0;
-        written += 8;
-        shift8(pd);
-    }
-    for (int k = 0; k < pd.fill; ++k) o[written + k] = static_cast<uint8_t>(pd.a0 >> (8 * k));
-    if (bad || r.pos() != end) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+    if (cnt > 0 && (bad || s.pos() != off[c + 1])) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
-constexpr int kSegB = 64;                                    // elements per lane per segment
-constexpr int kRowB = kSegB + 8;                              // staging row pitch (spreads the lanes' rows over banks)
-constexpr size_t kBf16Smem = 2 * sizeof(DecTables) + size_t(2) * kDecBlock * kRowB;
-
-// Decode one plane's symbols up to `target` into its staging row (row byte k
-// = stream symbol seg0 + k).  Every iteration does one table lookup and, when
-// 8 bytes are ready, one 8-byte store: the lanes of a warp run the same
-// instructions and only the trip count differs.  Symbols decoded past
-// `target` stay in the accumulator for the next segment.
-__device__ __forceinline__ void decode_row(BitReader &r, const DecTables &T, Pend &pd, int &rem, int &written,
-                                           int target, int seg0, uint8_t *row, bool &bad) {
-    while (written < target) {
-        if (rem > 0) take(r, T, pd, rem, bad);  // fill <= 7 before, <= 13 after
-        if (pd.fill >= 8) {
-            *reinterpret_cast<uint64_t *>(row + (written - seg0)) = pd.a0;
-            written += 8;
-            shift8(pd);
-        } else if (rem == 0) {
-            *reinterpret_cast<uint64_t *>(row + (written - seg0)) = pd.a0;
-            written += pd.fill;
-            pd.fill = 0;
-            pd.a0 = 0;
-        }
-    }
-}
-
-// Each thread owns one chunk pair: per segment it decodes 64 symbols of the
-// high-byte plane, then 64 of the low-byte plane, into two private
-// shared-memory rows, then merges them into 16-bit words, XORs x0 and stores
-// 128 bytes.  Long segments let the lanes' varying symbols-per-lookup even
-// out before the warp's lanes meet again.  No barrier couples the threads, and every lane of a warp runs
-// the same plane at the same time.
+// ------------------------------------------------------------------ fused bf16
+//
+// One lane per chunk pair decodes both planes into two rings (128 bytes per
+// lane: the high ring in the half given by the lane's parity, the low ring in
+// the other; each ring's two 32-byte halves swapped on every second lane
+// pair), then the warp merges 8 lanes' segments per pass: bytes to 16-bit
+// words, XOR x0, 16-byte streaming stores.
 template <bool XOR>
-__global__ void __launch_bounds__(kDecBlock) k_decode_bf16(
+__global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
     const uint8_t *__restrict__ pay_hi, size_t bytes_hi, const uint64_t *__restrict__ off_hi,
     const uint8_t *__restrict__ pay_lo, size_t bytes_lo, const uint64_t *__restrict__ off_lo, size_t n,
     size_t chunk, const huff_codebook *__restrict__ cb_hi, const huff_codebook *__restrict__ cb_lo,
     const uint16_t *__restrict__ x0, uint16_t *__restrict__ out, int32_t *status) {
     extern __shared__ __align__(16) uint8_t dsm[];
     DecTables *Tb = reinterpret_cast<DecTables *>(dsm);
-    load_tables(Tb[0], cb_hi);
-    load_tables(Tb[1], cb_lo);
-    __syncthreads();
+    const huff_codebook *cbs[2] = {cb_hi, cb_lo};
+    load_tables(Tb, cbs, 2);
     if (!Tb[0].ok || !Tb[1].ok) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
         return;
     }
+    const int lane = threadIdx.x & 31;
     const size_t n_chunks = (n + chunk - 1) / chunk;
     const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= n_chunks) return;
-    uint64_t sh, eh, sl, el;
-    if (!chunk_bounds(off_hi, c, bytes_hi, sh, eh) || !chunk_bounds(off_lo, c, bytes_lo, sl, el)) {
-        set_status(status, HUFF_ERR_CORRUPT_STREAM);
-        return;
-    }
-    uint8_t *hrow = dsm + 2 * sizeof(DecTables) + static_cast<size_t>(threadIdx.x) * kRowB;
-    uint8_t *lrow = hrow + static_cast<size_t>(kDecBlock) * kRowB;
-    BitReader rh, rl;
-    rh.p = pay_hi;
-    rh.nbytes = bytes_hi;
-    rh.init(sh);
-    rl.p = pay_lo;
-    rl.nbytes = bytes_lo;
-    rl.init(sl);
-    const size_t first = c * chunk;
-    const int cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
-    uint16_t *o = out + first;
-    const uint16_t *x = XOR ? x0 + first : nullptr;
-    bool bad = false;
-    int remh = cnt, reml = cnt, wh = 0, wl = 0;
-    Pend ph{0, 0, 0}, pl{0, 0, 0};
-    for (int seg0 = 0; seg0 < cnt; seg0 += kSegB) {
-        const int target = cnt - seg0 < kSegB ? cnt : seg0 + kSegB;
-        const bool full = target == seg0 + kSegB;
-        uint4 xq[kSegB / 8];  // x0 of the whole segment, in flight while the planes decode
-        if (XOR && full) {
-#pragma unroll
-            for (int g = 0; g < kSegB / 8; ++g) xq[g] = __ldcs(reinterpret_cast<const uint4 *>(x + seg0) + g);
+    const size_t c0 = c - lane;
+    uint64_t sh = 0, eh = 0, sl = 0, el = 0;
+    int cnt = 0;
+    if (c < n_chunks) {
+        if (chunk_bounds(off_hi, c, bytes_hi, sh, eh) && chunk_bounds(off_lo, c, bytes_lo, sl, el)) {
+            const size_t first = c * chunk;
+            cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
+        } else {
+            set_status(status, HUFF_ERR_CORRUPT_STREAM);
         }
-        decode_row(rh, Tb[0], ph, remh, wh, target, seg0, hrow, bad);
-        decode_row(rl, Tb[1], pl, reml, wl, target, seg0, lrow, bad);
+    }
+    uint8_t *rings = dsm + 2 * sizeof(DecTables) + static_cast<size_t>(threadIdx.x - lane) * (2 * kRing);
+    uint8_t *hring = rings + lane * (2 * kRing) + ((lane & 1) ? kRing : 0);
+    uint8_t *lring = rings + lane * (2 * kRing) + ((lane & 1) ? 0 : kRing);
+    const uint32_t swz = (lane & 2) ? kRing / 2 : 0;
+    PlaneDec h, l;
+    plane_start(h, pay_hi, bytes_hi, sh, cnt);
+    plane_start(l, pay_lo, bytes_lo, sl, cnt);
+    bool bad = false;
+    const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
+    for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSeg) {
+        if (XOR && seg0 < cnt) {
+            const uint16_t *xp = x0 + c * chunk + seg0;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(xp));
+        }
+        const int need = min(cnt, seg0 + kSeg);
+        fill_segment<kRing>(h, pay_hi, bytes_hi, Tb[0], hring, swz, cnt, need, seg0 + kRing, bad);
+        fill_segment<kRing>(l, pay_lo, bytes_lo, Tb[1], lring, swz, cnt, need, seg0 + kRing, bad);
+        __syncwarp();
+        // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane
 #pragma unroll
-        for (int g = 0; g < kSegB / 8; ++g) {
-            const int e0 = seg0 + 8 * g;  // first of this group's 8 elements
-            if (e0 >= target) break;
-            const uint2 h = *reinterpret_cast<const uint2 *>(hrow + 8 * g);
-            const uint2 l = *reinterpret_cast<const uint2 *>(lrow + 8 * g);
-            uint4 v = make_uint4(__byte_perm(l.x, h.x, 0x5140), __byte_perm(l.x, h.x, 0x7362),
-                                 __byte_perm(l.y, h.y, 0x5140), __byte_perm(l.y, h.y, 0x7362));
-            if (e0 + 8 <= target) {
-                if (XOR) {
-                    const uint4 xv = full ? xq[g] : __ldcs(reinterpret_cast<const uint4 *>(x + e0));
-                    v.x ^= xv.x; v.y ^= xv.y; v.z ^= xv.z; v.w ^= xv.w;
-                }
-                __stcs(reinterpret_cast<uint4 *>(o + e0), v);
-            } else {
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int i = 0; i < 4; ++i) {
+            const int q = 8 * i + (lane >> 2);  // source lane
+            const int e0 = seg0 + 8 * (lane & 3);
+            const int cs = __shfl_sync(0xffffffffu, cnt, q);
+            if (e0 < cs) {
+                const uint8_t *qr = rings + q * (2 * kRing);
+                const uint32_t o = (e0 & (kRing - 1)) ^ ((q & 2) ? kRing / 2 : 0);
+                const uint2 hv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? kRing : 0) + o);
+                const uint2 lv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? 0 : kRing) + o);
+                uint4 v = make_uint4(__byte_perm(lv.x, hv.x, 0x5140), __byte_perm(lv.x, hv.x, 0x7362),
+                                     __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
+                const size_t g = (c0 + q) * chunk + e0;  // first element of this group
+                if (e0 + 8 <= cs) {  // x0 and out are 16-byte aligned, chunk a multiple of 256
+                    if (XOR) {
+                        const uint4 xv = __ldcs(reinterpret_cast<const uint4 *>(x0 + g));
+                        v.x ^= xv.x;
+                        v.y ^= xv.y;
+                        v.z ^= xv.z;
+                        v.w ^= xv.w;
+                    }
+                    __stcs(reinterpret_cast<uint4 *>(out + g), v);
+                } else {
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (e0 + k < target) {
-                        uint16_t val = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
-                        if (XOR) val ^= x[e0 + k];
-                        o[e0 + k] = val;
+                    for (int k = 0; k < 8; ++k) {
+                        if (e0 + k < cs) {
+                            uint16_t val = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+                            if (XOR) val ^= x0[g + k];
+                            out[g + k] = val;
+                        }
                     }
                 }
             }
         }
+        __syncwarp();
     }
-    if (bad || rh.pos() != eh || rl.pos() != el) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+    if (cnt > 0 && (bad || h.pos() != off_hi[c + 1] || l.pos() != off_lo[c + 1]))
+        set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
 }  // namespace
@@ -384,8 +505,13 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
                      const huff_codebook *cb, uint8_t *out, int32_t *status, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    const unsigned grid = static_cast<unsigned>((n_chunks + kDecBlock - 1) / kDecBlock);
-    k_decode_u8<<<grid, kDecBlock, 0, s>>>(payload, bytes, off, n, chunk, cb, out, status);
+    const int block = decode_block(n_chunks, dev_info().sms);
+    const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
+    const size_t smem = sizeof(DecTables) + static_cast<size_t>(block) * kRingU8;
+    if (cudaFuncSetAttribute(k_decode_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return HUFF_ERR_CUDA;
+    k_decode_u8<<<grid, block, smem, s>>>(payload, bytes, off, n, chunk, cb, out, status);
     return launch_status();
 }
 
@@ -395,20 +521,21 @@ int launch_decode_bf16(const uint8_t *pay_hi, size_t bytes_hi, const uint64_t *o
                        uint16_t *out, int32_t *status, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    const unsigned grid = static_cast<unsigned>((n_chunks + kDecBlock - 1) / kDecBlock);
+    const int block = decode_block(n_chunks, dev_info().sms);
+    const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
+    const size_t smem = 2 * sizeof(DecTables) + static_cast<size_t>(block) * (2 * kRing);
     if (x0 != nullptr) {
         if (cudaFuncSetAttribute(k_decode_bf16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kBf16Smem)) != cudaSuccess)
+                                 static_cast<int>(smem)) != cudaSuccess)
             return HUFF_ERR_CUDA;
-        k_decode_bf16<true><<<grid, kDecBlock, kBf16Smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo,
-                                                               n, chunk, cb_hi, cb_lo, x0, out, status);
+        k_decode_bf16<true><<<grid, block, smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n, chunk,
+                                                      cb_hi, cb_lo, x0, out, status);
     } else {
         if (cudaFuncSetAttribute(k_decode_bf16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kBf16Smem)) != cudaSuccess)
+                                 static_cast<int>(smem)) != cudaSuccess)
             return HUFF_ERR_CUDA;
-        k_decode_bf16<false><<<grid, kDecBlock, kBf16Smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo,
-                                                                off_lo, n, chunk, cb_hi, cb_lo, nullptr, out,
-                                                                status);
+        k_decode_bf16<false><<<grid, block, smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n,
+                                                       chunk, cb_hi, cb_lo, nullptr, out, status);
     }
     return launch_status();
 }

@@ -174,27 +174,23 @@ struct Packer {
     uint32_t hi, lo;  // pending bits: the low `nb` bits of hi:lo
     uint32_t nb;
     uint32_t w;       // next buffer word
-    bool first_partial;
 
     __device__ __forceinline__ void begin(uint32_t *b, uint32_t start) {
         buf = b;
         hi = lo = 0;
         nb = start & 31u;
         w = start >> 5;
-        first_partial = nb != 0;
     }
+    // Branch-free: a completed word is OR-ed into the (zeroed) buffer under a
+    // predicate, so the lanes of a warp never split on the data.
     __device__ __forceinline__ void push(uint32_t e) {
         hi = __funnelshift_l(lo, hi, e);
         lo = __funnelshift_l(0u, lo, e) | (e >> 8);
         nb += e & 31u;
-        if (nb >= 32) {
-            nb -= 32;
-            const uint32_t word = __funnelshift_r(lo, hi, nb);
-            if (first_partial) atomicOr(&buf[w], word);
-            else buf[w] = word;
-            first_partial = false;
-            ++w;
-        }
+        const bool full = nb >= 32;
+        nb -= full ? 32u : 0u;
+        if (full) atomicOr(&buf[w], __funnelshift_r(lo, hi, nb));
+        w += full ? 1u : 0u;
     }
     __device__ __forceinline__ void finish() {
         if (nb > 0) atomicOr(&buf[w], lo << (32 - nb));
@@ -487,37 +483,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                 const uint32_t excl1 = uint32_t(excl);
                 const uint32_t tot0 = uint32_t(total >> 32);
                 const uint32_t tot1 = uint32_t(total);
-                // each plane's symbols are packed as two independent halves (the second half starts
-                // where the first half's bits end), so up to four packing chains run interleaved
-                constexpr int kHalf = C::kSyms / 2;
-                uint32_t half0 = 0, half1 = 0;
+                Packer pk0, pk1;
+                pk0.begin(bufs, excl0);
+                if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
 #pragma unroll
-                for (int j = 0; j < kHalf; ++j) {
-                    half0 += e0[j] & 31u;
-                    if (BF16) half1 += e1[BF16 ? j : 0] & 31u;
+                for (int j = 0; j < C::kSyms; ++j) {
+                    pk0.push(e0[j]);
+                    if (BF16) pk1.push(e1[BF16 ? j : 0]);
                 }
-                Packer pa0, pb0, pa1, pb1;
-                pa0.begin(bufs, excl0);
-                pb0.begin(bufs, excl0 + half0);
-                if (BF16) {
-                    pa1.begin(bufs + C::kBufWords, excl1);
-                    pb1.begin(bufs + C::kBufWords, excl1 + half1);
-                }
-#pragma unroll
-                for (int j = 0; j < kHalf; ++j) {
-                    pa0.push(e0[j]);
-                    pb0.push(e0[j + kHalf]);
-                    if (BF16) {
-                        pa1.push(e1[BF16 ? j : 0]);
-                        pb1.push(e1[BF16 ? j + kHalf : 0]);
-                    }
-                }
-                pa0.finish();
-                pb0.finish();
-                if (BF16) {
-                    pa1.finish();
-                    pb1.finish();
-                }
+                pk0.finish();
+                if (BF16) pk1.finish();
                 __syncthreads();  // buffers packed
                 // write the tile's words at its global bit offset
                 uint64_t next_run = 0;  // thread 32 p: plane p's offset after this tile
