@@ -520,7 +520,7 @@ def main():
     ap.add_argument("--small", action="store_true", help="same as --rows 4096 (a 250 MB snapshot)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=64 << 20, help="elements for the oracle baseline")
+    ap.add_argument("--cpu-sample", type=int, default=256 << 20, help="elements for the oracle baseline (about 10 s)")
     ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")
     args = ap.parse_args()
     if args.small:
