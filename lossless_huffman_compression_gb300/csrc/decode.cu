@@ -124,10 +124,14 @@ __device__ __forceinline__ uint4 load_unit_tail(const uint8_t *p, size_t nbytes,
 // call that may load, so they stay kernel parameters rather than registers.
 __device__ __forceinline__ uint4 load_unit(const uint8_t *p, size_t nbytes, size_t u) {
     if (u * 16 + 16 <= nbytes) {
+        // a lane reads its chunk 16 bytes at a time over the whole kernel while x0 and the output
+        // stream past: keep the payload's lines in L2 ahead of them (x0 and out are evict-first)
+        uint64_t pol;
+        asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
         uint4 v;
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "l"(p + u * 16));
+                     : "l"(p + u * 16), "l"(pol));
         return v;
     }
     return load_unit_tail(p, nbytes, u);
@@ -449,9 +453,9 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
     bool bad = false;
     const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
     for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSeg) {
-        if (XOR && seg0 < cnt) {
+        if (XOR && seg0 < cnt && (seg0 & 63) == 0) {  // one 128-byte line of x0 per two segments
             const uint16_t *xp = x0 + c * chunk + seg0;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(xp));
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xp));
         }
         const int need = min(cnt, seg0 + kSeg);
         fill_segment<kRing>(h, pay_hi, bytes_hi, Tb[0], hring, swz, cnt, need, seg0 + kRing, bad);
