@@ -4,9 +4,10 @@
 Default workload: the incremental snapshot delta.  x0 = bf16(N(0, 0.02)) and
 x1 = bf16(x0 + N(0, 1e-4)) of shape [65536, 30518] (2.0e9 elements, 4.0 GB
 each), resident in HBM.  One step is one pass of the whole path:
-  lmc_histogram_bf16(x1, x0)      XOR delta + byte planes + two histograms
-  huff_build_codebook x 2         lengths, canonical codes, decode tables
-  lmc_encode_bf16(x1, x0)         XOR delta + byte planes + encode of both planes
+  lmc_histogram_bf16_counted(x1, x0)  XOR delta + byte planes + two histograms
+                                      (+ per-segment counts)
+  huff_build_codebook x 2             lengths, canonical codes, decode tables
+  lmc_encode_bf16_counted(x1, x0)     XOR delta + byte planes + one-pass encode of both planes
   lmc_decode_bf16(..., x0)        decode both planes, merge, XOR x0 back in
 value = snapshot bytes (2n) / step time: uncompressed GB/s of a full
 compress + decompress round trip.  Inputs (8 GB) exceed the 129 MB L2, so no
@@ -189,20 +190,23 @@ class SnapshotPath:
         self.o_hi = torch.empty(self.nc + 1, dtype=torch.int64, device=dev)
         self.o_lo = torch.empty(self.nc + 1, dtype=torch.int64, device=dev)
         self.ws = torch.empty(_lib.lmc_workspace_size(n, chunk) // 8 + 2, dtype=torch.int64, device=dev)
+        self.seg = torch.empty(_lib.lmc_segment_counts_size(n) // 4 + 4, dtype=torch.int32, device=dev)
+        self.ws_counted = torch.empty(_lib.lmc_counted_workspace_size(n) // 8 + 2, dtype=torch.int64, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty(n, dtype=torch.int16, device=dev)
-        # kernels launched per step: hist (2 zero + 1), build (2), encode (zero + main + fix-up), decode (1)
-        self.launches_per_step = 9
+        # kernels launched per step: hist (2 zero + 1), build (2), encode (segment bits + scan + main + fix-up),
+        # decode (1)
+        self.launches_per_step = 10
 
     def compress(self, w=None, x0=None):
         L = self.L
         w = self.x1 if w is None else w
         x0 = self.x0 if x0 is None else x0
-        L.lmc_histogram_bf16(w, x0, self.h_hi, self.h_lo)
+        L.lmc_histogram_bf16_counted(w, x0, self.h_hi, self.h_lo, self.seg)
         L.huff_build_codebook(self.h_hi, self.cb_hi.buf, self.status, self.max_len, 0)
         L.huff_build_codebook(self.h_lo, self.cb_lo.buf, self.status, self.max_len, 0)
-        L.lmc_encode_bf16(w, x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.p_hi, self.o_hi, self.p_lo,
-                          self.o_lo, self.ws, self.status)
+        L.lmc_encode_bf16_counted(w, x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.seg, self.p_hi, self.o_hi,
+                                  self.p_lo, self.o_lo, self.ws_counted, self.status)
 
     def decompress(self, x0=None, out=None):
         x0 = self.x0 if x0 is None else x0
@@ -213,13 +217,13 @@ class SnapshotPath:
     def step_with_events(self, ev):
         L = self.L
         ev[0].record()
-        L.lmc_histogram_bf16(self.x1, self.x0, self.h_hi, self.h_lo)
+        L.lmc_histogram_bf16_counted(self.x1, self.x0, self.h_hi, self.h_lo, self.seg)
         ev[1].record()
         L.huff_build_codebook(self.h_hi, self.cb_hi.buf, self.status, self.max_len, 0)
         L.huff_build_codebook(self.h_lo, self.cb_lo.buf, self.status, self.max_len, 0)
         ev[2].record()
-        L.lmc_encode_bf16(self.x1, self.x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.p_hi, self.o_hi,
-                          self.p_lo, self.o_lo, self.ws, self.status)
+        L.lmc_encode_bf16_counted(self.x1, self.x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.seg, self.p_hi,
+                                  self.o_hi, self.p_lo, self.o_lo, self.ws_counted, self.status)
         ev[3].record()
         L.lmc_decode_bf16(self.p_hi, self.o_hi, self.p_lo, self.o_lo, self.n, self.chunk, self.cb_hi.buf,
                           self.cb_lo.buf, self.x0, self.out, self.status)
@@ -435,7 +439,7 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
     del d_x1, d_x0
     return {"value": round(total / ms / 1e6, 2), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "api": "lmc_histogram_bf16, huff_build_codebook, lmc_encode_bf16, lmc_decode_bf16 with pinned host "
+            "api": "lmc_histogram_bf16_counted, huff_build_codebook, lmc_encode_bf16_counted, lmc_decode_bf16 with pinned host "
                    "inputs, streams copied to host and back"}
 
 

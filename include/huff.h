@@ -314,6 +314,51 @@ int lmc_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n,
                     void *ws, size_t ws_bytes, int32_t *status, huff_stream_t stream);
 
 /*
+ * Counted per-shard path.  When the codebooks are built from the tensor's own
+ * histograms (per-shard mode, P2 framework stages 2-3), the histogram pass
+ * can also record both planes' counts per segment of HUFF_COUNT_SEGMENT
+ * elements.  lmc_encode_bf16_counted then derives every segment's bit offset
+ * as sum(count * length) and encodes in one pass over the input, with no
+ * counting pass and no waiting between CTAs.  Its outputs are byte-identical
+ * to lmc_encode_bf16's.  (A GPU arrangement of the same method; the pages
+ * have no separate step for it.)
+ */
+#define HUFF_COUNT_SEGMENT 131072
+
+/* Bytes of the per-segment counts for n elements: 2048 * ceil(n / HUFF_COUNT_SEGMENT). */
+size_t lmc_segment_counts_size(size_t n);
+
+/* Workspace bytes lmc_encode_bf16_counted needs: 48 * ceil(n / HUFF_COUNT_SEGMENT) + 16. */
+size_t lmc_counted_workspace_size(size_t n);
+
+/*
+ * lmc_histogram_bf16_counted -- lmc_histogram_bf16 that also writes
+ * seg_counts[s][0][b] and seg_counts[s][1][b] (uint32): the counts of symbol
+ * b in the high and low plane of elements [s * HUFF_COUNT_SEGMENT, ...).
+ *   w, x0       16-byte aligned; x0 may be NULL (no delta).
+ *   hist_hi, hist_lo  uint64[256] each, overwritten.
+ *   seg_counts  uint32 array of seg_counts_bytes >= lmc_segment_counts_size(n), 4-byte aligned.
+ */
+int lmc_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
+                               uint64_t *hist_lo, uint32_t *seg_counts, size_t seg_counts_bytes,
+                               huff_stream_t stream);
+
+/*
+ * lmc_encode_bf16_counted -- lmc_encode_bf16 from the per-segment counts of
+ * the same w (and x0) written by lmc_histogram_bf16_counted.  Counts that do
+ * not match the data give a wrong stream (the caller owns that contract);
+ * a symbol without a code still sets HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK.
+ *   ws          ws_bytes >= lmc_counted_workspace_size(n), 16-byte aligned.
+ *   other arguments as in lmc_encode_bf16.
+ */
+int lmc_encode_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n,
+                            const huff_codebook *cb_hi, const huff_codebook *cb_lo, size_t chunk_bytes,
+                            const uint32_t *seg_counts, size_t seg_counts_bytes,
+                            uint8_t *payload_hi, size_t cap_hi, uint64_t *off_hi,
+                            uint8_t *payload_lo, size_t cap_lo, uint64_t *off_lo,
+                            void *ws, size_t ws_bytes, int32_t *status, huff_stream_t stream);
+
+/*
  * lmc_decode_bf16 -- decode both planes and write the 16-bit words, optionally
  * XOR-ing x0 back in (P2 decompression: Huffman-decode, restore byte groups,
  * re-apply the delta).  out[i] = (hi[i] << 8 | lo[i]) ^ (x0 ? x0[i] : 0).

@@ -33,13 +33,15 @@ HUFF_COVER_ALL = 1
 HUFF_CHUNK_ALIGN = 256
 HUFF_CODEBOOK_MAGIC = 0x48554642
 HUFF_NOALLOC_MAX_SYMBOLS = 1 << 30
+HUFF_COUNT_SEGMENT = 131072
 CODEBOOK_LEN_OFFSET = 16  # byte offset of len[256] inside huff_codebook
 
 EXPORTS = (
     "huff_version", "huff_status_string", "huff_codebook_size", "huff_encode_bound", "huff_workspace_size",
     "huff_num_chunks", "huff_histogram", "huff_build_codebook", "huff_codebook_from_lengths", "huff_encode",
     "huff_decode", "huff_encode_noalloc", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
-    "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats",
+    "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
+    "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted",
 )
 
 
@@ -90,6 +92,10 @@ def load(path: str = LIB_PATH):
         "lmc_encode_bf16": (I, [P, P, S, P, P, S, P, S, P, P, S, P, P, S, P, P]),
         "lmc_decode_bf16": (I, [P, S, P, P, S, P, S, S, P, P, P, P, P, P]),
         "huff_code_stats": (I, [P, P, ctypes.POINTER(HuffStats)]),
+        "lmc_segment_counts_size": (S, [S]),
+        "lmc_counted_workspace_size": (S, [S]),
+        "lmc_histogram_bf16_counted": (I, [P, P, S, P, P, P, S, P]),
+        "lmc_encode_bf16_counted": (I, [P, P, S, P, P, S, P, S, P, S, P, P, S, P, P, S, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -152,6 +158,14 @@ def huff_workspace_size(n: int, chunk_bytes: int) -> int:
 
 def lmc_workspace_size(n: int, chunk_bytes: int) -> int:
     return int(load().lmc_workspace_size(n, chunk_bytes))
+
+
+def lmc_segment_counts_size(n: int) -> int:
+    return int(load().lmc_segment_counts_size(n))
+
+
+def lmc_counted_workspace_size(n: int) -> int:
+    return int(load().lmc_counted_workspace_size(n))
 
 
 def huff_num_chunks(n: int, chunk_bytes: int) -> int:
@@ -242,6 +256,25 @@ def lmc_encode_bf16(w: torch.Tensor, x0: torch.Tensor | None, cb_hi: torch.Tenso
                     off_lo: torch.Tensor, ws: torch.Tensor, status: torch.Tensor, stream=None):
     _check("lmc_encode_bf16", load().lmc_encode_bf16(
         _dev(w, "w"), _dev(x0, "x0"), w.numel(), _dev(cb_hi, "cb_hi"), _dev(cb_lo, "cb_lo"), chunk_bytes,
+        _dev(payload_hi, "payload_hi"), payload_hi.numel() * payload_hi.element_size(), _dev(off_hi, "off_hi"),
+        _dev(payload_lo, "payload_lo"), payload_lo.numel() * payload_lo.element_size(), _dev(off_lo, "off_lo"),
+        _dev(ws, "ws"), ws.numel() * ws.element_size(), _dev(status, "status"), _stream(stream)))
+
+
+def lmc_histogram_bf16_counted(w: torch.Tensor, x0: torch.Tensor | None, hist_hi: torch.Tensor,
+                               hist_lo: torch.Tensor, seg_counts: torch.Tensor, stream=None):
+    _check("lmc_histogram_bf16_counted", load().lmc_histogram_bf16_counted(
+        _dev(w, "w"), _dev(x0, "x0"), w.numel(), _dev(hist_hi, "hist_hi"), _dev(hist_lo, "hist_lo"),
+        _dev(seg_counts, "seg_counts"), seg_counts.numel() * seg_counts.element_size(), _stream(stream)))
+
+
+def lmc_encode_bf16_counted(w: torch.Tensor, x0: torch.Tensor | None, cb_hi: torch.Tensor, cb_lo: torch.Tensor,
+                            chunk_bytes: int, seg_counts: torch.Tensor, payload_hi: torch.Tensor,
+                            off_hi: torch.Tensor, payload_lo: torch.Tensor, off_lo: torch.Tensor, ws: torch.Tensor,
+                            status: torch.Tensor, stream=None):
+    _check("lmc_encode_bf16_counted", load().lmc_encode_bf16_counted(
+        _dev(w, "w"), _dev(x0, "x0"), w.numel(), _dev(cb_hi, "cb_hi"), _dev(cb_lo, "cb_lo"), chunk_bytes,
+        _dev(seg_counts, "seg_counts"), seg_counts.numel() * seg_counts.element_size(),
         _dev(payload_hi, "payload_hi"), payload_hi.numel() * payload_hi.element_size(), _dev(off_hi, "off_hi"),
         _dev(payload_lo, "payload_lo"), payload_lo.numel() * payload_lo.element_size(), _dev(off_lo, "off_lo"),
         _dev(ws, "ws"), ws.numel() * ws.element_size(), _dev(status, "status"), _stream(stream)))

@@ -143,24 +143,33 @@ def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: 
     x16 = None if x0 is None else x0.reshape(-1).view(torch.int16)
     n = w16.numel()
     dev = w.device
-    if cb_hi is None or cb_lo is None:
-        h_hi = torch.empty(256, dtype=torch.int64, device=dev)
-        h_lo = torch.empty(256, dtype=torch.int64, device=dev)
-        _lib.lmc_histogram_bf16(w16, x16, h_hi, h_lo)
-        st = new_status(dev)
-        cb_hi = build_codebook(h_hi, max_len, flags, status=st)
-        cb_lo = build_codebook(h_lo, max_len, flags, status=st)
-        raise_on_status(st, "huff_build_codebook")
     cap = _lib.huff_encode_bound(n, max_len)
     p_hi = torch.empty(cap, dtype=torch.uint8, device=dev)
     p_lo = torch.empty(cap, dtype=torch.uint8, device=dev)
     nc = _lib.huff_num_chunks(n, chunk_bytes)
     o_hi = torch.empty(nc + 1, dtype=torch.int64, device=dev)
     o_lo = torch.empty(nc + 1, dtype=torch.int64, device=dev)
-    ws = torch.empty(max(_lib.lmc_workspace_size(n, chunk_bytes), 16) // 8, dtype=torch.int64, device=dev)
-    st = new_status(dev)
-    _lib.lmc_encode_bf16(w16, x16, cb_hi.buf, cb_lo.buf, chunk_bytes, p_hi, o_hi, p_lo, o_lo, ws, st)
-    raise_on_status(st, "lmc_encode_bf16")
+    if cb_hi is None or cb_lo is None:
+        # per-shard: the histogram pass records per-segment counts, so the encode makes one pass
+        h_hi = torch.empty(256, dtype=torch.int64, device=dev)
+        h_lo = torch.empty(256, dtype=torch.int64, device=dev)
+        seg = torch.empty(max(_lib.lmc_segment_counts_size(n), 4) // 4, dtype=torch.int32, device=dev)
+        _lib.lmc_histogram_bf16_counted(w16, x16, h_hi, h_lo, seg)
+        st = new_status(dev)
+        cb_hi = build_codebook(h_hi, max_len, flags, status=st)
+        cb_lo = build_codebook(h_lo, max_len, flags, status=st)
+        raise_on_status(st, "huff_build_codebook")
+        ws = torch.empty(max(_lib.lmc_counted_workspace_size(n), 16) // 8, dtype=torch.int64, device=dev)
+        st = new_status(dev)
+        _lib.lmc_encode_bf16_counted(w16, x16, cb_hi.buf, cb_lo.buf, chunk_bytes, seg, p_hi, o_hi, p_lo, o_lo, ws,
+                                     st)
+        raise_on_status(st, "lmc_encode_bf16_counted")
+    else:
+        # fixed codebooks: the encode counts each segment's bits itself
+        ws = torch.empty(max(_lib.lmc_workspace_size(n, chunk_bytes), 16) // 8, dtype=torch.int64, device=dev)
+        st = new_status(dev)
+        _lib.lmc_encode_bf16(w16, x16, cb_hi.buf, cb_lo.buf, chunk_bytes, p_hi, o_hi, p_lo, o_lo, ws, st)
+        raise_on_status(st, "lmc_encode_bf16")
     return Bf16Streams(cb_hi, cb_lo, Stream(p_hi, o_hi, n, chunk_bytes), Stream(p_lo, o_lo, n, chunk_bytes), n)
 
 

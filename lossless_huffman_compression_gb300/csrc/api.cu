@@ -13,6 +13,7 @@ namespace {
 
 // the decode kernels copy the table with 16-byte loads; the binding reads len[] at byte 16
 static_assert(offsetof(huff_codebook, lut) % 16 == 0, "codebook lut must be 16-byte aligned");
+static_assert(HUFF_COUNT_SEGMENT == huffk::kDirSegElems, "counted segment size");
 static_assert(offsetof(huff_codebook, len) == 16 && offsetof(huff_codebook, code) == 272, "codebook layout");
 static_assert(sizeof(huff_codebook) % 16 == 0, "codebook size");
 
@@ -185,6 +186,48 @@ int lmc_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n, const huff_
     if (n > 0 && ws_bytes < lmc_workspace_size(n, chunk_bytes)) return HUFF_ERR_BUFFER_TOO_SMALL;
     return launch_encode_bf16(w, x0, n, cb_hi, cb_lo, chunk_bytes, payload_hi, cap_hi, off_hi, payload_lo, cap_lo,
                               off_lo, ws, status, cs(stream));
+}
+
+size_t lmc_segment_counts_size(size_t n) {
+    return static_cast<size_t>(huffk::kSegCountWords) * 4 * ((n + HUFF_COUNT_SEGMENT - 1) / HUFF_COUNT_SEGMENT);
+}
+
+size_t lmc_counted_workspace_size(size_t n) { return 48 * ((n + HUFF_COUNT_SEGMENT - 1) / HUFF_COUNT_SEGMENT) + 16; }
+
+int lmc_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
+                               uint64_t *hist_lo, uint32_t *seg_counts, size_t seg_counts_bytes,
+                               huff_stream_t stream) {
+    if (hist_hi == nullptr || hist_lo == nullptr || hist_hi == hist_lo || !aligned(hist_hi, 8) ||
+        !aligned(hist_lo, 8) || n > kMaxN)
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (w == nullptr || seg_counts == nullptr || !aligned(w, HUFF_ALIGN) ||
+                  (x0 != nullptr && !aligned(x0, HUFF_ALIGN)) || !aligned(seg_counts, 4)))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && seg_counts_bytes < lmc_segment_counts_size(n)) return HUFF_ERR_BUFFER_TOO_SMALL;
+    int st = launch_zero_u64(hist_hi, 256, cs(stream));
+    if (st == HUFF_OK) st = launch_zero_u64(hist_lo, 256, cs(stream));
+    if (st != HUFF_OK || n == 0) return st;
+    return launch_histogram_bf16_counted(w, x0, n, hist_hi, hist_lo, seg_counts, cs(stream));
+}
+
+int lmc_encode_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
+                            const huff_codebook *cb_lo, size_t chunk_bytes, const uint32_t *seg_counts,
+                            size_t seg_counts_bytes, uint8_t *payload_hi, size_t cap_hi, uint64_t *off_hi,
+                            uint8_t *payload_lo, size_t cap_lo, uint64_t *off_lo, void *ws, size_t ws_bytes,
+                            int32_t *status, huff_stream_t stream) {
+    if (cb_hi == nullptr || cb_lo == nullptr || off_hi == nullptr || off_lo == nullptr || status == nullptr ||
+        !chunk_ok(chunk_bytes) || n > kMaxN || !aligned(cb_hi, 16) || !aligned(cb_lo, 16) ||
+        !aligned(off_hi, 8) || !aligned(off_lo, 8))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (w == nullptr || payload_hi == nullptr || payload_lo == nullptr || ws == nullptr ||
+                  seg_counts == nullptr || !aligned(w, HUFF_ALIGN) || (x0 != nullptr && !aligned(x0, HUFF_ALIGN)) ||
+                  !aligned(payload_hi, HUFF_ALIGN) || !aligned(payload_lo, HUFF_ALIGN) || !aligned(ws, HUFF_ALIGN) ||
+                  !aligned(seg_counts, 4)))
+        return HUFF_ERR_INVALID_ARG;
+    if (n > 0 && (ws_bytes < lmc_counted_workspace_size(n) || seg_counts_bytes < lmc_segment_counts_size(n)))
+        return HUFF_ERR_BUFFER_TOO_SMALL;
+    return launch_encode_bf16_counted(w, x0, n, cb_hi, cb_lo, chunk_bytes, seg_counts, payload_hi, cap_hi, off_hi,
+                                      payload_lo, cap_lo, off_lo, ws, status, cs(stream));
 }
 
 int lmc_decode_bf16(const uint8_t *payload_hi, size_t bytes_hi, const uint64_t *off_hi, const uint8_t *payload_lo,

@@ -18,6 +18,12 @@ constexpr int kEncU8Tile = kEncThreads * kEncU8SymsPerThread;     // 8192 symbol
 constexpr int kEncBf16ElemsPerThread = 16;       // two 16-byte vectors of bf16
 constexpr int kEncBf16Tile = kEncThreads * kEncBf16ElemsPerThread; // 4096 elements
 constexpr int kEncStages = 3;                    // TMA ring depth
+// Counted (per-shard) bf16 path: the histogram pass records each plane's
+// counts per segment of kDirSegTiles encode tiles, so the encode knows every
+// segment's bit offset before it starts and reads its input once.
+constexpr int kDirSegTiles = 32;
+constexpr size_t kDirSegElems = size_t(kDirSegTiles) * kEncBf16Tile;  // 131072 bf16 elements
+constexpr int kSegCountWords = 512;                                   // [hi 256 | lo 256] per segment
 constexpr int kLutRep = 8;                       // copies of the encode table (bank spreading)
 constexpr int kHistThreads = 512;
 constexpr int kHistCopies = 32;                  // one histogram copy per lane
@@ -170,6 +176,12 @@ int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_
                      cudaStream_t s);
 int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk,
                              uint8_t *payload, size_t cap, uint64_t *off, int32_t *status, cudaStream_t s);
+int launch_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
+                                  uint64_t *hist_lo, uint32_t *seg_counts, cudaStream_t s);
+int launch_encode_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
+                               const huff_codebook *cb_lo, size_t chunk, const uint32_t *seg_counts,
+                               uint8_t *pay_hi, size_t cap_hi, uint64_t *off_hi, uint8_t *pay_lo, size_t cap_lo,
+                               uint64_t *off_lo, void *ws, int32_t *status, cudaStream_t s);
 int launch_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
                        const huff_codebook *cb_lo, size_t chunk, uint8_t *pay_hi, size_t cap_hi,
                        uint64_t *off_hi, uint8_t *pay_lo, size_t cap_lo, uint64_t *off_lo, void *ws,

@@ -546,6 +546,279 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
     }
 }
 
+// ------------------------------------------------------------------ counted path (bf16, per shard)
+//
+// When the histogram pass has recorded each plane's counts per segment of
+// kDirSegTiles tiles, every segment's bit count is sum(count * length): a
+// scan gives each segment's offset before the encode starts.  The encode then
+// reads its input once (no counting pass) and no CTA waits for another.
+
+// Bits of each segment per plane: one warp per segment.
+__global__ void k_seg_bits(const uint32_t *__restrict__ seg_counts, uint32_t n_seg, const huff_codebook *cb_hi,
+                           const huff_codebook *cb_lo, uint64_t *__restrict__ bits, int32_t *status) {
+    __shared__ uint8_t len[kSegCountWords];
+    for (int i = threadIdx.x; i < kSegCountWords; i += blockDim.x) {
+        const huff_codebook *cb = i < 256 ? cb_hi : cb_lo;
+        len[i] = cb->magic == HUFF_CODEBOOK_MAGIC ? cb->len[i & 255] : 0;
+    }
+    __syncthreads();
+    const uint32_t seg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (seg >= n_seg) return;
+    const uint32_t *h = seg_counts + static_cast<size_t>(seg) * kSegCountWords;
+    uint64_t b0 = 0, b1 = 0;
+    bool missing = false;
+#pragma unroll
+    for (int j = lane; j < 256; j += 32) {
+        const uint32_t c0 = h[j], c1 = h[256 + j];
+        const uint32_t l0 = len[j], l1 = len[256 + j];
+        b0 += static_cast<uint64_t>(c0) * l0;
+        b1 += static_cast<uint64_t>(c1) * l1;
+        missing |= (c0 && !l0) || (c1 && !l1);
+    }
+    b0 = warp_sum_u64(b0);
+    b1 = warp_sum_u64(b1);
+    if (__any_sync(0xffffffffu, missing) && lane == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
+    if (lane == 0) {
+        bits[seg] = b0;
+        bits[n_seg + seg] = b1;
+    }
+}
+
+// Inclusive prefix of the segment bit counts, as the lookback descriptors the
+// fix-up kernel reads (flag: inclusive prefix).  One CTA, rounds of 1024 x 8.
+__global__ void __launch_bounds__(1024) k_seg_scan(const uint64_t *__restrict__ bits, uint32_t n_seg,
+                                                   uint64_t *__restrict__ desc_hi, uint64_t *__restrict__ desc_lo) {
+    __shared__ uint64_t wsum[2][32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t carry[2] = {0, 0};
+    for (uint32_t base = 0; base < n_seg; base += 1024 * 8) {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint64_t v[8], t = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t i = base + tid * 8 + j;
+                v[j] = i < n_seg ? bits[p * size_t(n_seg) + i] : 0;
+                t += v[j];
+            }
+            uint64_t incl = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) wsum[p][warp] = incl;
+            __syncthreads();
+            uint64_t before = carry[p], all = carry[p];
+            for (int w = 0; w < 32; ++w) {
+                before += w < warp ? wsum[p][w] : 0;
+                all += wsum[p][w];
+            }
+            uint64_t run = before + incl - t;
+            uint64_t *desc = p == 0 ? desc_hi : desc_lo;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t i = base + tid * 8 + j;
+                run += v[j];
+                if (i < n_seg) desc[i] = kFlagPrefix | run;
+            }
+            carry[p] = all;
+            __syncthreads();
+        }
+    }
+}
+
+template <bool BF16, bool XOR>
+struct CountedCfg {
+    using C = EncCfg<BF16, XOR>;
+    static constexpr size_t kSmem = C::kMiscBytes + C::kRingBytes + C::kLutBytes + C::kBufBytes;
+};
+
+// Job q: tile q % kDirSegTiles of this CTA's segment number q / kDirSegTiles
+// (segments are dealt round robin over the grid).
+template <bool BF16, bool XOR>
+__device__ __forceinline__ void issue_counted_job(uint8_t *ring, Misc *ms, uint32_t q, uint32_t n_seg,
+                                                  uint32_t n_tiles, const uint8_t *in, const uint8_t *in2, size_t n) {
+    using C = EncCfg<BF16, XOR>;
+    const uint32_t seg = blockIdx.x + (q / kDirSegTiles) * gridDim.x;
+    if (seg >= n_seg) return;  // the consumers stop before this job
+    const int s = static_cast<int>(q % kStages);
+    const uint32_t t = seg * kDirSegTiles + q % kDirSegTiles;
+    uint32_t bytes = 0;
+    size_t first = 0;
+    if (t < n_tiles) {
+        first = static_cast<size_t>(t) * C::kTileSyms;
+        const size_t cnt = n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms);
+        bytes = static_cast<uint32_t>(cnt * (BF16 ? 2 : 1)) & ~15u;
+    }
+    mbar_arrive_expect_tx(&ms->full[s], bytes * C::kInputs);
+    if (bytes) {
+        const uint64_t pol = l2_policy_evict_first();
+        const size_t src = first * (BF16 ? 2 : 1);
+        uint8_t *dst = ring + size_t(s) * C::kInputs * C::kTileBytes;
+        bulk_g2s_hint(dst, in + src, bytes, &ms->full[s], pol);
+        if (XOR) bulk_g2s_hint(dst + C::kTileBytes, in2 + src, bytes, &ms->full[s], pol);
+    }
+}
+
+// One pass per tile: lookup, block scan, pack, shifted write-out; a segment
+// starts at the offset in its predecessor's descriptor.
+template <bool BF16, bool XOR>
+__global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *__restrict__ in,
+                                                             const uint8_t *__restrict__ in2, size_t n, EncPlane p0,
+                                                             EncPlane p1, size_t chunk, uint32_t n_tiles,
+                                                             uint32_t n_seg, int32_t *status) {
+    using C = EncCfg<BF16, XOR>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Misc *ms = reinterpret_cast<Misc *>(smem);
+    uint8_t *ring = smem + C::kMiscBytes;
+    uint32_t *lut = reinterpret_cast<uint32_t *>(ring + C::kRingBytes);
+    uint32_t *bufs = lut + C::kPlanes * C::kLutWords;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    if (tid == 0) ms->bad_codebook = 0;
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < C::kPlanes; ++p) {
+        const huff_codebook *cb = p == 0 ? p0.cb : p1.cb;
+        const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
+        if (!ok && tid == 0) ms->bad_codebook = 1;
+        for (int i = tid; i < C::kLutWords; i += kThreads) {
+            const int s = i / kLutRep;
+            const uint32_t L = ok ? cb->len[s] : 0u;
+            lut[p * C::kLutWords + i] = (L >= 1 && L <= HUFF_MAX_LEN) ? ((cb->code[s] << 8) | L) : 0u;
+        }
+    }
+    for (int i = tid; i < C::kPlanes * C::kBufWords; i += kThreads) bufs[i] = 0;
+    uint32_t issued = 0;  // next job to issue (thread 0 only)
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&ms->full[s], 1);
+        fence_mbar_init();
+        for (; issued < uint32_t(kStages); ++issued)
+            issue_counted_job<BF16, XOR>(ring, ms, issued, n_seg, n_tiles, in, in2, n);
+    }
+    __syncthreads();
+    if (ms->bad_codebook && tid == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+    const uint32_t *lut_r = lut + (lane & (kLutRep - 1));
+    uint32_t mn_all = 0xffffffffu;
+
+    for (uint32_t r = 0;; ++r) {
+        const uint32_t seg = blockIdx.x + r * gridDim.x;
+        if (seg >= n_seg) break;
+        const uint32_t t_first = seg * kDirSegTiles;
+        const int seg_tiles =
+            static_cast<int>(n_tiles - t_first < uint32_t(kDirSegTiles) ? n_tiles - t_first : kDirSegTiles);
+        if (tid < C::kPlanes) {  // this segment's offset: the inclusive prefix of the one before
+            const EncPlane &P = tid == 0 ? p0 : p1;
+            ms->run[tid] = seg ? (P.desc[seg - 1] & kValueMask) : 0;
+            ms->carry[tid] = 0;
+            ms->seg_head[tid] = 0;
+        }
+        // (the first tile's barriers order these writes before their readers)
+        for (int k = 0; k < kDirSegTiles; ++k) {
+            const uint32_t q = r * kDirSegTiles + k;
+            const int s = static_cast<int>(q % kStages);
+            if (!mbar_wait(&ms->full[s], (q / kStages) & 1u) && tid == 0) set_status(status, HUFF_ERR_TIMEOUT);
+            if (k < seg_tiles) {
+                const uint32_t t = t_first + k;
+                const size_t first = static_cast<size_t>(t) * C::kTileSyms;
+                const int tile_n = static_cast<int>(n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms));
+                uint32_t wv[8];
+                read_tile<BF16, XOR>(ring + size_t(s) * C::kInputs * C::kTileBytes, tid, first, tile_n, in, in2, wv);
+                const int nvalid = tile_n - tid * C::kSyms < 0
+                                       ? 0
+                                       : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
+                uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
+                lookup<BF16, XOR>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
+                if (nvalid > 0) mn_all = min(mn_all, mn);
+                const uint64_t mine = (static_cast<uint64_t>(b0) << 32) | b1;
+                uint64_t incl = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (lane == 31) ms->warp_sum[warp] = incl;
+                __syncthreads();  // stage s consumed; warp sums ready
+                if (tid == 0) issue_counted_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
+                uint64_t before = 0, total = 0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) {
+                    const uint64_t ws = ms->warp_sum[w];
+                    before += w < warp ? ws : 0;
+                    total += ws;
+                }
+                const uint64_t excl = before + incl - mine;
+                const uint32_t excl0 = uint32_t(excl >> 32);
+                const uint32_t excl1 = uint32_t(excl);
+                const uint32_t tot0 = uint32_t(total >> 32);
+                const uint32_t tot1 = uint32_t(total);
+                Packer pk0, pk1;
+                pk0.begin(bufs, excl0);
+                if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
+#pragma unroll
+                for (int j = 0; j < C::kSyms; ++j) {
+                    pk0.push(e0[j]);
+                    if (BF16) pk1.push(e1[BF16 ? j : 0]);
+                }
+                pk0.finish();
+                if (BF16) pk1.finish();
+                __syncthreads();  // buffers packed
+                uint64_t next_run = 0;  // thread 32 p: plane p's offset after this tile
+#pragma unroll
+                for (int p = 0; p < C::kPlanes; ++p) {
+                    const EncPlane &P = p == 0 ? p0 : p1;
+                    const uint32_t *buf = bufs + p * C::kBufWords;
+                    const uint64_t pre = ms->run[p];
+                    const uint32_t ph = static_cast<uint32_t>(pre & 31u);
+                    const uint64_t g0 = pre >> 5;
+                    const uint32_t tot = p == 0 ? tot0 : tot1;
+                    const uint32_t nfull = (ph + tot) >> 5;
+                    for (uint32_t i = (ph ? 1u : 0u) + tid; i < nfull; i += kThreads)
+                        put_word(P.payload, P.cap_words, g0 + i, shifted_word(buf, i, ph), status);
+                    const size_t g = first + size_t(tid) * C::kSyms;
+                    if (nvalid > 0 && g % chunk == 0) P.off[g / chunk] = pre + (p == 0 ? excl0 : excl1);
+                    if (tid == 32 * p) {
+                        const uint32_t head = ph ? shifted_word(buf, 0, ph) : 0u;
+                        uint32_t combined = head;
+                        if (ph) {
+                            if (k == 0) {
+                                ms->seg_head[p] = head;  // the segment's first word: the fix-up kernel's
+                            } else {
+                                combined |= ms->carry[p];
+                                if (nfull >= 1) put_word(P.payload, P.cap_words, g0, combined, status);
+                            }
+                        }
+                        uint32_t tail = 0;
+                        if ((ph + tot) & 31u) tail = nfull == 0 ? (ph ? combined : buf[0]) : shifted_word(buf, nfull, ph);
+                        ms->carry[p] = tail;  // read only by this thread
+                        next_run = pre + tot;
+                        if (k == seg_tiles - 1) P.edge[seg] = (static_cast<uint64_t>(ms->seg_head[p]) << 32) | tail;
+                    }
+                }
+                __syncthreads();  // everyone has read the buffers and the running offsets
+                if (tid == 0) ms->run[0] = next_run;
+                if (BF16 && tid == 32) ms->run[1] = next_run;
+#pragma unroll
+                for (int p = 0; p < C::kPlanes; ++p) {
+                    uint32_t *buf = bufs + p * C::kBufWords;
+                    const uint32_t used = ((p == 0 ? tot0 : tot1) + 31u) / 32u + 1u;
+                    for (uint32_t i = tid; i < used; i += kThreads) buf[i] = 0;
+                }
+            } else {
+                __syncthreads();  // stage s consumed (an empty job)
+                if (tid == 0) issue_counted_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
+            }
+        }
+        __syncthreads();  // the segment's last offsets are read before the next segment resets them
+    }
+    if (mn_all == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
+}
+
 // Boundary words: the word where segment t-1 ends and segment t begins holds
 // bits of both; the stream's last, partial word holds the end of the last
 // segment.
@@ -672,6 +945,52 @@ int launch_encode_bf16(const uint16_t *w16, const uint16_t *x0, size_t n, const 
         return run_encode<true, true>(a, reinterpret_cast<const uint8_t *>(x0), n, p0, p1, chunk,
                                       static_cast<uint32_t>(tiles), ctr, status, s);
     return run_encode<true, false>(a, nullptr, n, p0, p1, chunk, static_cast<uint32_t>(tiles), ctr, status, s);
+}
+
+int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
+                               const huff_codebook *cb_lo, size_t chunk, const uint32_t *seg_counts,
+                               uint8_t *pay_hi, size_t cap_hi, uint64_t *off_hi, uint8_t *pay_lo, size_t cap_lo,
+                               uint64_t *off_lo, void *ws, int32_t *status, cudaStream_t s) {
+    if (n == 0) {
+        k_encode_empty<<<1, 1, 0, s>>>(off_hi, off_lo);
+        return launch_status();
+    }
+    const size_t tiles = enc_bf16_tiles(n);
+    const size_t segs = (tiles + kDirSegTiles - 1) / kDirSegTiles;
+    uint64_t *w = static_cast<uint64_t *>(ws);
+    // layout: desc_hi, desc_lo, edge_hi, edge_lo, bits (2 x segs)
+    EncPlane p0{cb_hi, reinterpret_cast<uint32_t *>(pay_hi), cap_hi / 4, off_hi, w, w + 2 * segs};
+    EncPlane p1{cb_lo, reinterpret_cast<uint32_t *>(pay_lo), cap_lo / 4, off_lo, w + segs, w + 3 * segs};
+    uint64_t *bits = w + 4 * segs;
+    const unsigned nb = static_cast<unsigned>((segs * 32 + 255) / 256);
+    k_seg_bits<<<nb, 256, 0, s>>>(seg_counts, static_cast<uint32_t>(segs), cb_hi, cb_lo, bits, status);
+    if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
+    k_seg_scan<<<1, 1024, 0, s>>>(bits, static_cast<uint32_t>(segs), p0.desc, p1.desc);
+    if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
+    const uint8_t *a = reinterpret_cast<const uint8_t *>(w16);
+    const uint8_t *b = reinterpret_cast<const uint8_t *>(x0);
+    const DevInfo d = dev_info();
+    auto run = [&](auto kern, size_t smem) -> int {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+            return HUFF_ERR_CUDA;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
+            per_sm < 1)
+            return HUFF_ERR_CUDA;
+        size_t grid = static_cast<size_t>(d.sms) * per_sm;
+        if (grid > segs) grid = segs;
+        kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, b, n, p0, p1, chunk, static_cast<uint32_t>(tiles),
+                                                               static_cast<uint32_t>(segs), status);
+        return cudaGetLastError() == cudaSuccess ? HUFF_OK : HUFF_ERR_CUDA;
+    };
+    int st = x0 != nullptr ? run(k_encode_counted<true, true>, CountedCfg<true, true>::kSmem)
+                           : run(k_encode_counted<true, false>, CountedCfg<true, false>::kSmem);
+    if (st != HUFF_OK) return st;
+    const size_t n_chunks = (n + chunk - 1) / chunk;
+    k_encode_fixup<<<static_cast<unsigned>((segs + 127) / 128), 128, 0, s>>>(p0, p1, 2, static_cast<uint32_t>(segs),
+                                                                            n_chunks, status);
+    return launch_status();
 }
 
 }  // namespace huffk

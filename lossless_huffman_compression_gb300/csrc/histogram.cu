@@ -169,6 +169,80 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16(const uint16_t 
     flush_copies(sh + kHistCopies * kHistPitch, hist_lo);
 }
 
+// Both byte planes, per segment of kDirSegElems elements: each CTA takes whole
+// segments; after a segment it folds its 32 copies into the segment's 512
+// counts (high plane, then low plane), zeroes them, and keeps a running total
+// per bin for the whole-tensor histograms.  Folding costs 0.25 shared-memory
+// accesses per element.  w and x0 are 16-byte aligned.
+template <bool XOR>
+__global__ void __launch_bounds__(kHistThreads) k_histogram_bf16_counted(const uint16_t *__restrict__ w,
+                                                                         const uint16_t *__restrict__ x0, size_t n,
+                                                                         uint64_t *__restrict__ hist_hi,
+                                                                         uint64_t *__restrict__ hist_lo,
+                                                                         uint32_t *__restrict__ seg_counts,
+                                                                         uint32_t n_seg) {
+    static_assert(kHistThreads == kSegCountWords, "one thread per (plane, bin)");
+    extern __shared__ uint32_t sh[];
+    const int tid = threadIdx.x;
+    for (int i = tid; i < 2 * kHistCopies * kHistPitch; i += blockDim.x) sh[i] = 0;
+    __syncthreads();
+    uint32_t *hi = sh + (tid & 31) * kHistPitch;
+    uint32_t *lo = hi + kHistCopies * kHistPitch;
+    uint32_t *fold = sh + (tid >> 8) * kHistCopies * kHistPitch + (tid & 255);  // this thread's bin, copy 0
+    uint64_t total = 0;
+    for (uint32_t seg = blockIdx.x; seg < n_seg; seg += gridDim.x) {
+        const size_t first = static_cast<size_t>(seg) * kDirSegElems;
+        const size_t cnt = n - first < kDirSegElems ? n - first : kDirSegElems;
+        const size_t nv = cnt / 8;
+        const uint4 *vw = reinterpret_cast<const uint4 *>(w + first);
+        const uint4 *vx = reinterpret_cast<const uint4 *>(XOR ? x0 + first : w + first);
+        size_t i = tid;
+        for (; i + 3 * kHistThreads < nv; i += 4 * kHistThreads) {
+            uint4 a[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[j] = __ldcs(vw + i + j * kHistThreads);
+            if (XOR) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 c = __ldcs(vx + i + j * kHistThreads);
+                    a[j].x ^= c.x; a[j].y ^= c.y; a[j].z ^= c.z; a[j].w ^= c.w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                count_pair(hi, lo, a[j].x); count_pair(hi, lo, a[j].y);
+                count_pair(hi, lo, a[j].z); count_pair(hi, lo, a[j].w);
+            }
+        }
+        for (; i < nv; i += kHistThreads) {
+            uint4 a = __ldcs(vw + i);
+            if (XOR) {
+                const uint4 c = __ldcs(vx + i);
+                a.x ^= c.x; a.y ^= c.y; a.z ^= c.z; a.w ^= c.w;
+            }
+            count_pair(hi, lo, a.x); count_pair(hi, lo, a.y); count_pair(hi, lo, a.z); count_pair(hi, lo, a.w);
+        }
+        for (size_t e = nv * 8 + tid; e < cnt; e += kHistThreads) {
+            const uint32_t v = w[first + e] ^ (XOR ? x0[first + e] : 0);
+            atomicAdd(&lo[v & 0xffu], 1u);
+            atomicAdd(&hi[v >> 8], 1u);
+        }
+        __syncthreads();
+        uint32_t s = 0;
+#pragma unroll 8
+        for (int c = 0; c < kHistCopies; ++c) {
+            s += fold[c * kHistPitch];
+            fold[c * kHistPitch] = 0;
+        }
+        seg_counts[static_cast<size_t>(seg) * kSegCountWords + tid] = s;
+        total += s;
+        __syncthreads();
+    }
+    if (total)
+        atomicAdd(reinterpret_cast<unsigned long long *>(tid < 256 ? &hist_hi[tid] : &hist_lo[tid - 256]),
+                  static_cast<unsigned long long>(total));
+}
+
 __global__ void k_zero_u64(uint64_t *p, size_t count) {
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
          i += static_cast<size_t>(gridDim.x) * blockDim.x)
@@ -240,6 +314,24 @@ int launch_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint6
     } else {
         if ((st = hist_grid(k_histogram_bf16<false>, smem, n / 16 + 1, &grid)) != HUFF_OK) return st;
         k_histogram_bf16<false><<<grid, kHistThreads, smem, s>>>(w, nullptr, n, hist_hi, hist_lo);
+    }
+    return launch_status();
+}
+
+int launch_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
+                                  uint64_t *hist_lo, uint32_t *seg_counts, cudaStream_t s) {
+    const size_t smem = 2 * kHistCopies * kHistPitch * sizeof(uint32_t);
+    const size_t n_seg = (n + kDirSegElems - 1) / kDirSegElems;
+    int grid = 1, st;
+    if (x0 != nullptr) {
+        if ((st = hist_grid(k_histogram_bf16_counted<true>, smem, n_seg * kHistThreads, &grid)) != HUFF_OK) return st;
+        k_histogram_bf16_counted<true><<<grid, kHistThreads, smem, s>>>(w, x0, n, hist_hi, hist_lo, seg_counts,
+                                                                         static_cast<uint32_t>(n_seg));
+    } else {
+        if ((st = hist_grid(k_histogram_bf16_counted<false>, smem, n_seg * kHistThreads, &grid)) != HUFF_OK)
+            return st;
+        k_histogram_bf16_counted<false><<<grid, kHistThreads, smem, s>>>(w, nullptr, n, hist_hi, hist_lo,
+                                                                          seg_counts, static_cast<uint32_t>(n_seg));
     }
     return launch_status();
 }

@@ -1,0 +1,129 @@
+"""The counted per-shard bf16 path (per-segment counts from the histogram
+pass, one-pass encode) against the oracle and against the two-pass encode,
+element by element, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_huffman_compression_gb300 import _lib, codec
+from gpu_util import assert_stream_equal, host, oracle_codebook
+
+pytestmark = pytest.mark.gpu
+
+SEG = _lib.HUFF_COUNT_SEGMENT
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    _lib.load()
+    assert torch.cuda.is_available()
+
+
+def _pair(n, rng, sigma_noise=1e-4):
+    x0 = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32)).to(torch.bfloat16)
+    x1 = (x0.float() + torch.from_numpy(rng.normal(0, sigma_noise, n).astype(np.float32))).to(torch.bfloat16)
+    return x0, x1
+
+
+def _counted(dx1, dx0, chunk, cb_hi=None, cb_lo=None):
+    n = dx1.numel()
+    w16 = dx1.view(torch.int16)
+    x16 = None if dx0 is None else dx0.view(torch.int16)
+    hh = torch.empty(256, dtype=torch.int64, device="cuda")
+    hl = torch.empty(256, dtype=torch.int64, device="cuda")
+    seg = torch.full((max(_lib.lmc_segment_counts_size(n), 4) // 4,), -1, dtype=torch.int32, device="cuda")
+    _lib.lmc_histogram_bf16_counted(w16, x16, hh, hl, seg)
+    if cb_hi is None:
+        cb_hi = codec.build_codebook(hh)
+        cb_lo = codec.build_codebook(hl)
+    cap = _lib.huff_encode_bound(n, 24)
+    nc = _lib.huff_num_chunks(n, chunk)
+    p_hi = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    p_lo = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    o_hi = torch.empty(nc + 1, dtype=torch.int64, device="cuda")
+    o_lo = torch.empty(nc + 1, dtype=torch.int64, device="cuda")
+    ws = torch.empty(max(_lib.lmc_counted_workspace_size(n), 16) // 8, dtype=torch.int64, device="cuda")
+    st = codec.new_status()
+    _lib.lmc_encode_bf16_counted(w16, x16, cb_hi.buf, cb_lo.buf, chunk, seg, p_hi, o_hi, p_lo, o_lo, ws, st)
+    torch.cuda.synchronize()
+    return (hh, hl, seg, cb_hi, cb_lo, codec.Stream(p_hi, o_hi, n, chunk), codec.Stream(p_lo, o_lo, n, chunk),
+            int(st.item()))
+
+
+@pytest.mark.parametrize("n", [1, 8, 4097, SEG - 1, SEG, SEG + 1, 3 * SEG + 4097, 1_000_003])
+@pytest.mark.parametrize("delta", [False, True])
+@pytest.mark.parametrize("chunk", [256, 16384])
+def test_counted_matches_oracle_and_two_pass(n, delta, chunk):
+    rng = np.random.default_rng(n * 2 + delta)
+    x0, x1 = _pair(n, rng)
+    w = x1.view(torch.int16).numpy().view(np.uint16)
+    if delta:
+        w = oracle.delta_xor(w, x0.view(torch.int16).numpy().view(np.uint16))
+    hi, lo = oracle.bytegroup_split(w)
+    dx1, dx0 = x1.cuda(), (x0.cuda() if delta else None)
+    hh, hl, seg, cb_hi, cb_lo, s_hi, s_lo, st = _counted(dx1, dx0, chunk)
+    assert st == 0
+    np.testing.assert_array_equal(host(hh).astype(np.uint64), oracle.histogram(hi))
+    np.testing.assert_array_equal(host(hl).astype(np.uint64), oracle.histogram(lo))
+    counts = host(seg).view(np.uint32)
+    n_seg = (n + SEG - 1) // SEG
+    for s in range(n_seg):
+        np.testing.assert_array_equal(counts[s * 512:s * 512 + 256].astype(np.uint64),
+                                      oracle.histogram(hi[s * SEG:(s + 1) * SEG]))
+        np.testing.assert_array_equal(counts[s * 512 + 256:s * 512 + 512].astype(np.uint64),
+                                      oracle.histogram(lo[s * SEG:(s + 1) * SEG]))
+    for plane, cb, stream in ((hi, cb_hi, s_hi), (lo, cb_lo, s_lo)):
+        ln, cd = oracle_codebook(oracle.histogram(plane))
+        np.testing.assert_array_equal(cb.lengths(), ln)
+        pay, off = oracle.encode(plane, ln, cd, chunk)
+        assert_stream_equal(stream, pay, off)
+    # byte-identical to the two-pass encode with the same codebooks
+    two = codec.compress_bf16(dx1, dx0, chunk, cb_hi=cb_hi, cb_lo=cb_lo)
+    for a, b in ((two.hi, s_hi), (two.lo, s_lo)):
+        assert torch.equal(a.off, b.off)
+        nb = (a.total_bits() + 7) // 8
+        assert torch.equal(a.payload[:nb], b.payload[:nb])
+    back = codec.decompress_bf16(codec.Bf16Streams(cb_hi, cb_lo, s_hi, s_lo, n), dx0)
+    assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
+
+
+def test_counted_compress_bf16_round_trip_wide_noise():
+    # larger noise: longer codes and more long (> 12 bit) codes in the low plane
+    rng = np.random.default_rng(7)
+    x0, x1 = _pair(2 * SEG + 333, rng, sigma_noise=3e-3)
+    s = codec.compress_bf16(x1.cuda(), x0.cuda(), 4096)
+    back = codec.decompress_bf16(s, x0.cuda())
+    assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
+
+
+def test_counted_symbol_without_code_sets_status():
+    rng = np.random.default_rng(11)
+    x0, x1 = _pair(SEG + 5, rng)
+    # codebooks from a histogram that lacks most symbols
+    h = torch.zeros(256, dtype=torch.int64, device="cuda")
+    h[0] = 10
+    h[1] = 3
+    cb = codec.build_codebook(h)
+    *_, st = _counted(x1.cuda(), x0.cuda(), 4096, cb_hi=cb, cb_lo=cb)
+    assert st == _lib.HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK
+
+
+def test_counted_argument_errors():
+    n = 4096
+    w = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    hh = torch.zeros(256, dtype=torch.int64, device="cuda")
+    hl = torch.zeros(256, dtype=torch.int64, device="cuda")
+    seg = torch.zeros(512, dtype=torch.int32, device="cuda")
+    small = torch.zeros(100, dtype=torch.int32, device="cuda")
+    with pytest.raises(_lib.HuffError) as e:
+        _lib.lmc_histogram_bf16_counted(w[:n], None, hh, hl, small)
+    assert e.value.status == _lib.HUFF_ERR_BUFFER_TOO_SMALL
+    with pytest.raises(_lib.HuffError) as e:
+        _lib.lmc_histogram_bf16_counted(w[1:n + 1], None, hh, hl, seg)  # 2-byte offset: not 16-byte aligned
+    assert e.value.status == _lib.HUFF_ERR_INVALID_ARG
+    with pytest.raises(_lib.HuffError) as e:
+        _lib.lmc_histogram_bf16_counted(w[:n], None, hh, hh, seg)
+    assert e.value.status == _lib.HUFF_ERR_INVALID_ARG
