@@ -80,7 +80,7 @@ struct EncCfg {
     static constexpr size_t kBufBytes = size_t(kPlanes) * kBufWords * 4;
     static constexpr size_t kCntBytes = size_t(kSegTiles) * kThreads * 4;
     static constexpr size_t kSmem = kMiscBytes + kRingBytes + kLutBytes + kBufBytes + kCntBytes;
-    static_assert(kTileSyms * (BF16 ? 2 : 1) == kTileBytes, "tile geometry");
+    static_assert(kTileSyms * (BF16 ? 2 : 1) == kTileBytes && kTileSyms <= 8192, "tile geometry");
 };
 
 struct Misc {
@@ -92,6 +92,8 @@ struct Misc {
     uint32_t seg_head[2];    // [plane] the segment's bits in its first, partial word
     uint32_t segq[2];        // segment of round r at [r & 1]
     int32_t bad_codebook;
+    uint64_t chunk_q;        // the current tile's first element is element chunk_r of chunk chunk_q
+    uint32_t chunk_r;
 };
 static_assert(sizeof(Misc) <= 512, "misc area");
 
@@ -167,35 +169,79 @@ __device__ uint64_t lookback(const uint64_t *desc, uint32_t t, int lane, int32_t
 // tile-local bit buffer from bit `start` on.  The pending bits sit in the
 // 64-bit pair (hi, lo); since len < 32, 32-bit funnel shifts move them, and
 // the entry itself serves as the shift count (funnel shifts use its low 5
-// bits).  Words wholly inside this thread's bits are stored; the partial
-// words at either end are OR-ed (the buffer is zero before packing).
+// bits).  A word wholly inside this thread's bits is stored under a
+// predicate (no branch, no atomic); the first word, which may hold bits of
+// earlier threads, is kept in a register and OR-ed in by finish() together
+// with the last, partial word (the buffer is zero before packing).
 struct Packer {
     uint32_t *buf;
     uint32_t hi, lo;  // pending bits: the low `nb` bits of hi:lo
     uint32_t nb;
     uint32_t w;       // next buffer word
+    uint32_t w0;      // the first word
+    uint32_t head;    // the first word's bits, once complete
+    bool first;       // the first word is not complete yet
 
     __device__ __forceinline__ void begin(uint32_t *b, uint32_t start) {
         buf = b;
         hi = lo = 0;
         nb = start & 31u;
-        w = start >> 5;
+        w = w0 = start >> 5;
+        head = 0;
+        first = true;
     }
-    // Branch-free: a completed word is OR-ed into the (zeroed) buffer under a
-    // predicate, so the lanes of a warp never split on the data.
     __device__ __forceinline__ void push(uint32_t e) {
         hi = __funnelshift_l(lo, hi, e);
         lo = __funnelshift_l(0u, lo, e) | (e >> 8);
         nb += e & 31u;
         const bool full = nb >= 32;
         nb -= full ? 32u : 0u;
-        if (full) atomicOr(&buf[w], __funnelshift_r(lo, hi, nb));
+        const uint32_t word = __funnelshift_r(lo, hi, nb);
+        if (full && !first) buf[w] = word;
+        head = (full && first) ? word : head;
+        first = first && !full;
         w += full ? 1u : 0u;
     }
     __device__ __forceinline__ void finish() {
+        if (!first) atomicOr(&buf[w0], head);
         if (nb > 0) atomicOr(&buf[w], lo << (32 - nb));
     }
 };
+
+// Chunk starts among a tile's per-thread groups.  Chunks are multiples of 256
+// elements and a thread's group is 16 or 32, so a group starts a chunk or lies
+// inside one.  With the tile's position in its chunk (q, r) kept by thread 0,
+// a thread's distance d = r + first-of-group < chunk + 8192 (a tile is at
+// most 8192 symbols) is divided exactly by a multiply-high when chunk < 8192
+// (magic = ceil(2^32 / chunk); exact since d * chunk < 2^32) or by one
+// compare when chunk >= 8192 (then d < 2 chunk).
+struct ChunkDiv {
+    uint32_t chunk;  // < 2^31
+    uint32_t magic;  // 0 when chunk >= 8192
+    __device__ __forceinline__ uint32_t div(uint32_t d) const {
+        return magic ? __umulhi(d, magic) : (d >= chunk ? 1u : 0u);
+    }
+};
+
+__host__ inline ChunkDiv make_chunk_div(size_t chunk) {
+    const uint32_t c = static_cast<uint32_t>(chunk);
+    return ChunkDiv{c, c < 8192 ? static_cast<uint32_t>(((1ull << 32) + c - 1) / c) : 0u};
+}
+
+// Thread 0, before a tile: its first element's chunk and offset in it
+// (incrementally from the previous tile of the same segment).
+__device__ __forceinline__ void chunk_position(Misc *ms, const ChunkDiv &cd, size_t first, bool seg_start,
+                                               uint32_t tile_syms) {
+    if (seg_start) {
+        ms->chunk_q = first / cd.chunk;
+        ms->chunk_r = static_cast<uint32_t>(first % cd.chunk);
+    } else {
+        const uint32_t d = ms->chunk_r + tile_syms;
+        const uint32_t k = cd.div(d);
+        ms->chunk_q += k;
+        ms->chunk_r = d - k * cd.chunk;
+    }
+}
 
 // Global word i of a tile whose bits start at phase ph, from the tile-local buffer.
 __device__ __forceinline__ uint32_t shifted_word(const uint32_t *buf, uint32_t i, uint32_t ph) {
@@ -330,7 +376,7 @@ __device__ __forceinline__ void lookup(const uint32_t *lut_r, const uint32_t (&w
 
 template <bool BF16, bool XOR>
 __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restrict__ in, const uint8_t *__restrict__ in2,
-                                                     size_t n, EncPlane p0, EncPlane p1, size_t chunk,
+                                                     size_t n, EncPlane p0, EncPlane p1, ChunkDiv cdiv,
                                                      uint32_t n_tiles, unsigned *seg_ctr, int32_t *status) {
     using C = EncCfg<BF16, XOR>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -469,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                     if (lane >= o) incl += y;
                 }
                 if (lane == 31) ms->warp_sum[warp] = incl;
+                if (tid == 0) chunk_position(ms, cdiv, first, k == 0, C::kTileSyms);
                 __syncthreads();  // stage s consumed; warp sums ready
                 if (tid == 0) issue_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
                 uint64_t before = 0, total = 0;
@@ -508,7 +555,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                     for (uint32_t i = (ph ? 1u : 0u) + tid; i < nfull; i += kThreads)
                         put_word(P.payload, P.cap_words, g0 + i, shifted_word(buf, i, ph), status);
                     const size_t g = first + size_t(tid) * C::kSyms;
-                    if (nvalid > 0 && g % chunk == 0) P.off[g / chunk] = pre + (p == 0 ? excl0 : excl1);
+                    if (nvalid > 0) {
+                        const uint32_t d = ms->chunk_r + static_cast<uint32_t>(tid) * C::kSyms;
+                        const uint32_t kq = cdiv.div(d);
+                        if (kq * cdiv.chunk == d) P.off[ms->chunk_q + kq] = pre + (p == 0 ? excl0 : excl1);
+                    }
                     if (tid == 32 * p) {
                         // the word this tile starts in, and the one it ends in
                         const uint32_t head = ph ? shifted_word(buf, 0, ph) : 0u;
@@ -667,7 +718,7 @@ __device__ __forceinline__ void issue_counted_job(uint8_t *ring, Misc *ms, uint3
 template <bool BF16, bool XOR>
 __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *__restrict__ in,
                                                              const uint8_t *__restrict__ in2, size_t n, EncPlane p0,
-                                                             EncPlane p1, size_t chunk, uint32_t n_tiles,
+                                                             EncPlane p1, ChunkDiv cdiv, uint32_t n_tiles,
                                                              uint32_t n_seg, int32_t *status) {
     using C = EncCfg<BF16, XOR>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -743,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *_
                     if (lane >= o) incl += y;
                 }
                 if (lane == 31) ms->warp_sum[warp] = incl;
+                if (tid == 0) chunk_position(ms, cdiv, first, k == 0, C::kTileSyms);
                 __syncthreads();  // stage s consumed; warp sums ready
                 if (tid == 0) issue_counted_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
                 uint64_t before = 0, total = 0;
@@ -781,7 +833,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *_
                     for (uint32_t i = (ph ? 1u : 0u) + tid; i < nfull; i += kThreads)
                         put_word(P.payload, P.cap_words, g0 + i, shifted_word(buf, i, ph), status);
                     const size_t g = first + size_t(tid) * C::kSyms;
-                    if (nvalid > 0 && g % chunk == 0) P.off[g / chunk] = pre + (p == 0 ? excl0 : excl1);
+                    if (nvalid > 0) {
+                        const uint32_t d = ms->chunk_r + static_cast<uint32_t>(tid) * C::kSyms;
+                        const uint32_t kq = cdiv.div(d);
+                        if (kq * cdiv.chunk == d) P.off[ms->chunk_q + kq] = pre + (p == 0 ? excl0 : excl1);
+                    }
                     if (tid == 32 * p) {
                         const uint32_t head = ph ? shifted_word(buf, 0, ph) : 0u;
                         uint32_t combined = head;
@@ -862,8 +918,8 @@ int run_encode(const uint8_t *in, const uint8_t *in2, size_t n, EncPlane p0, Enc
     if (grid > n_seg) grid = n_seg;
     // segments are claimed in order by CTAs that are already running, so every segment a
     // lookback waits for belongs to a resident CTA and the grid needs no co-residency
-    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(in, in2, n, p0, p1, chunk, n_tiles, seg_ctr,
-                                                                  status);
+    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(in, in2, n, p0, p1, make_chunk_div(chunk), n_tiles,
+                                                                  seg_ctr, status);
     if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
     const size_t n_chunks = (n + chunk - 1) / chunk;
     k_encode_fixup<<<(n_seg + 255) / 256, 256, 0, s>>>(p0, p1, C::kPlanes, n_seg, n_chunks, status);
@@ -980,7 +1036,8 @@ int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n
             return HUFF_ERR_CUDA;
         size_t grid = static_cast<size_t>(d.sms) * per_sm;
         if (grid > segs) grid = segs;
-        kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, b, n, p0, p1, chunk, static_cast<uint32_t>(tiles),
+        kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, b, n, p0, p1, make_chunk_div(chunk),
+                                                               static_cast<uint32_t>(tiles),
                                                                static_cast<uint32_t>(segs), status);
         return cudaGetLastError() == cudaSuccess ? HUFF_OK : HUFF_ERR_CUDA;
     };
