@@ -202,6 +202,22 @@ struct Packer {
         first = first && !full;
         w += full ? 1u : 0u;
     }
+    // Two codes at once when together they are at most 31 bits.
+    __device__ __forceinline__ void push2(uint32_t ea, uint32_t eb) {
+        const uint32_t lb = eb & 31u;
+        const uint32_t L = (ea & 31u) + lb;
+        const uint32_t code = ((ea >> 8) << lb) | (eb >> 8);
+        hi = __funnelshift_l(lo, hi, L);
+        lo = (lo << L) | code;
+        nb += L;
+        const bool full = nb >= 32;
+        nb -= full ? 32u : 0u;
+        const uint32_t word = __funnelshift_r(lo, hi, nb);
+        if (full && !first) buf[w] = word;
+        head = (full && first) ? word : head;
+        first = first && !full;
+        w += full ? 1u : 0u;
+    }
     __device__ __forceinline__ void finish() {
         if (!first) atomicOr(&buf[w0], head);
         if (nb > 0) atomicOr(&buf[w], lo << (32 - nb));
@@ -533,10 +549,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                 Packer pk0, pk1;
                 pk0.begin(bufs, excl0);
                 if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
+                // pairs of codes at most 31 bits long go in one step; a warp with a longer pair
+                // anywhere packs its codes one by one
+                uint32_t longest_pair = 0;
 #pragma unroll
-                for (int j = 0; j < C::kSyms; ++j) {
-                    pk0.push(e0[j]);
-                    if (BF16) pk1.push(e1[BF16 ? j : 0]);
+                for (int j = 0; j < C::kSyms; j += 2) {
+                    longest_pair = max(longest_pair, (e0[j] & 31u) + (e0[j + 1] & 31u));
+                    if (BF16) longest_pair = max(longest_pair, (e1[BF16 ? j : 0] & 31u) + (e1[BF16 ? j + 1 : 0] & 31u));
+                }
+                if (__any_sync(0xffffffffu, longest_pair > 31u)) {
+#pragma unroll
+                    for (int j = 0; j < C::kSyms; ++j) {
+                        pk0.push(e0[j]);
+                        if (BF16) pk1.push(e1[BF16 ? j : 0]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C::kSyms; j += 2) {
+                        pk0.push2(e0[j], e0[j + 1]);
+                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0]);
+                    }
                 }
                 pk0.finish();
                 if (BF16) pk1.finish();
@@ -812,10 +844,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *_
                 Packer pk0, pk1;
                 pk0.begin(bufs, excl0);
                 if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
+                // pairs of codes at most 31 bits long go in one step; a warp with a longer pair
+                // anywhere packs its codes one by one
+                uint32_t longest_pair = 0;
 #pragma unroll
-                for (int j = 0; j < C::kSyms; ++j) {
-                    pk0.push(e0[j]);
-                    if (BF16) pk1.push(e1[BF16 ? j : 0]);
+                for (int j = 0; j < C::kSyms; j += 2) {
+                    longest_pair = max(longest_pair, (e0[j] & 31u) + (e0[j + 1] & 31u));
+                    if (BF16) longest_pair = max(longest_pair, (e1[BF16 ? j : 0] & 31u) + (e1[BF16 ? j + 1 : 0] & 31u));
+                }
+                if (__any_sync(0xffffffffu, longest_pair > 31u)) {
+#pragma unroll
+                    for (int j = 0; j < C::kSyms; ++j) {
+                        pk0.push(e0[j]);
+                        if (BF16) pk1.push(e1[BF16 ? j : 0]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C::kSyms; j += 2) {
+                        pk0.push2(e0[j], e0[j + 1]);
+                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0]);
+                    }
                 }
                 pk0.finish();
                 if (BF16) pk1.finish();
