@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Huffman encode/decode GB/s (uncompressed) at 1 GB300; % HBM roofline; ratio"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = {"k_decode_bf16": "decode.cu", "k_encode_bf16": "encode.cu", "k_histogram_bf16": "histogram.cu"}
+KERNEL_SOURCES = {"k_decode_bf16": "decode.cu", "k_encode_counted": "encode.cu", "k_histogram_bf16_counted": "histogram.cu"}
 
 
 # ------------------------------------------------------------------ environment
@@ -296,12 +296,12 @@ def run_ours(args, dist, rank, ws):
         stages[nm] = {"ms": round(stage_ms[nm], 4), "gbs_uncompressed": round(snap_bytes / t / 1e9, 1),
                       "alg_bytes": int(alg[nm]), "hbm_frac": round(alg[nm] / t / 1e9 / peak, 4)}
     dom = max(["histogram_bf16_xor", "encode_bf16_xor", "decode_bf16_xor"], key=lambda k: stage_ms[k])
-    kname = {"histogram_bf16_xor": "k_histogram_bf16", "encode_bf16_xor": "k_encode_bf16",
+    kname = {"histogram_bf16_xor": "k_histogram_bf16_counted", "encode_bf16_xor": "k_encode_counted",
              "decode_bf16_xor": "k_decode_bf16"}[dom]
     achieved = alg[dom] / (stage_ms[dom] / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                "traffic": recorded_traffic(kname, 1.0)}
+                "traffic": recorded_traffic(kname, float(n))}
 
     # extra: encode / decode of the already-materialised delta (codebooks given), outside the step
     extra = materialised_delta_stages(path, args, peak)
