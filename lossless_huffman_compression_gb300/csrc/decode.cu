@@ -33,11 +33,14 @@ namespace {
 
 constexpr int kSecMax = 2048;  // secondary-table entries per plane
 
-// 16-byte aligned (and sized) so that arrays of tables keep every lut 16-byte aligned for uint4 copies
+// Shared decode tables of one codebook for a W-bit window (W = 12: the
+// codebook's own table; W = 13: built from it in the prologue).  16-byte
+// aligned and sized, so tables placed back to back stay aligned.
+template <int W>
 struct __align__(16) DecTables {
-    uint64_t lut[1u << HUFF_LUT_BITS];  // syms (48 bits) | count << 48 | total bits << 52; 0: first code > 12 bits
-    uint16_t sec[kSecMax];              // codes longer than 12 bits: symbol | length << 8 (0: no code)
-    uint64_t run;                       // the 1-bit code's symbol in all 8 bytes (when there is one)
+    uint64_t lut[1u << W];  // syms (48 bits) | count << 48 | total bits << 52; 0: first code > W bits
+    uint16_t sec[kSecMax];  // codes longer than W bits: symbol | length << 8 (0: no code)
+    uint64_t run;           // the 1-bit code's symbol in all 8 bytes (when there is one)
     uint32_t bl_count[32];
     uint32_t first_code[32];
     uint32_t first_index[32];
@@ -46,66 +49,91 @@ struct __align__(16) DecTables {
     int longest;
     int ok;
     int has_run;    // a 1-bit code exists: 8 leading zero bits are 8 of its symbol
-    int sec_k;      // bits after the 12-bit window that index sec (0: no code is longer than 12 bits)
-    int sec_first;  // first 12-bit prefix of the long codes (they fill the top of the code space)
+    int sec_k;      // bits after the W-bit window that index sec (0: no code is longer than W bits)
+    int sec_first;  // first W-bit prefix of the long codes (they fill the top of the code space)
     int sec_ok;     // sec holds every long code; otherwise the canonical search decodes them
 };
-static_assert(sizeof(DecTables) % 16 == 0, "table arrays must keep 16-byte alignment");
+static_assert(sizeof(DecTables<12>) % 16 == 0 && sizeof(DecTables<13>) % 16 == 0, "tables keep 16-byte alignment");
 
-// Copy a device codebook into shared tables and build the secondary table
-// for codes longer than the 12-bit window.  Canonical codes place every code
-// longer than 12 bits after all shorter ones, so their 12-bit prefixes are
-// the contiguous range [first_code[13] / 2, 4096); sec holds, per prefix,
-// 2^k entries (k = longest - 12) indexed by the next k bits.  Two barriers.
-__device__ void load_tables(DecTables *Ts, const huff_codebook *const *cbs, int nt) {
+constexpr size_t kBf16Tables = sizeof(DecTables<12>) + sizeof(DecTables<13>);
+
+// Phase 1 of loading a codebook: the W-bit table, the canonical arrays and
+// the header.  For W = 13 an entry is the 12-bit entry of its first 12 bits
+// plus, when it holds fewer than the maximum number of symbols, the one code
+// that ends exactly at the 13th bit (a code ending earlier would already be
+// in the 12-bit entry, and no code is shorter than 1 bit).
+template <int W>
+__device__ void load_table_a(DecTables<W> &T, const huff_codebook *cb) {
+    static_assert(W == HUFF_LUT_BITS || W == HUFF_LUT_BITS + 1, "12- or 13-bit window");
     const int tid = threadIdx.x;
-    for (int t = 0; t < nt; ++t) {
-        DecTables &T = Ts[t];
-        const huff_codebook *cb = cbs[t];
-        const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
+    const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
+    if (W == HUFF_LUT_BITS) {
         const uint4 *src = reinterpret_cast<const uint4 *>(cb->lut);
         uint4 *dst = reinterpret_cast<uint4 *>(T.lut);
-        for (int i = tid; i < (1 << HUFF_LUT_BITS) / 2; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
-        uint4 *sz = reinterpret_cast<uint4 *>(T.sec);
-        for (int i = tid; i < kSecMax / 8; i += blockDim.x) sz[i] = make_uint4(0, 0, 0, 0);
-        if (tid < 32) {
-            T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
-            T.first_code[tid] = ok ? cb->first_code[tid] : 0;
-            T.first_index[tid] = ok ? cb->first_index[tid] : 0;
-        }
-        for (int i = tid; i < 256; i += blockDim.x) {
-            T.sorted[i] = ok ? cb->sorted_symbols[i] : 0;
-            T.len[i] = ok ? cb->len[i] : 0;
-        }
-        if (tid == 0) {
-            const int longest = ok ? cb->longest : 0;
-            T.longest = longest;
-            T.ok = ok && longest <= HUFF_MAX_LEN;
-            T.has_run = ok && cb->bl_count[1] > 0;
-            T.run = (ok ? static_cast<uint64_t>(cb->sorted_symbols[0]) : 0ull) * 0x0101010101010101ull;
-            const int k = longest > HUFF_LUT_BITS ? longest - HUFF_LUT_BITS : 0;
-            const int first = k ? static_cast<int>(cb->first_code[HUFF_LUT_BITS + 1] >> 1) : (1 << HUFF_LUT_BITS);
-            T.sec_k = k;
-            T.sec_first = first;
-            T.sec_ok = k == 0 || (first <= (1 << HUFF_LUT_BITS) &&
-                                  (static_cast<long long>((1 << HUFF_LUT_BITS) - first) << k) <= kSecMax);
+        for (int i = tid; i < (1 << W) / 2; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
+    } else {
+        for (int i = tid; i < (1 << W); i += blockDim.x) {
+            uint64_t e = 0;
+            if (ok) {
+                e = cb->lut[i >> 1];
+                const uint32_t c = static_cast<uint32_t>(e >> 48) & 15u;
+                const uint32_t bits = static_cast<uint32_t>(e >> 52) & 15u;
+                if (c < HUFF_LUT_SYMS) {
+                    const uint32_t r = static_cast<uint32_t>(W) - bits;  // 1..W
+                    const uint32_t v = static_cast<uint32_t>(i) & ((1u << r) - 1u);
+                    const uint32_t nc = cb->bl_count[r];
+                    const uint32_t d = v - cb->first_code[r];
+                    if (nc != 0 && d < nc) {
+                        const uint64_t sym = cb->sorted_symbols[cb->first_index[r] + d];
+                        e = (e & 0xffffffffffffull) | (sym << (8 * c)) | (static_cast<uint64_t>(c + 1) << 48) |
+                            (static_cast<uint64_t>(W) << 52);
+                    }
+                }
+            }
+            T.lut[i] = e;
         }
     }
-    __syncthreads();
-    for (int t = 0; t < nt; ++t) {
-        DecTables &T = Ts[t];
-        if (!T.ok || T.sec_k == 0 || !T.sec_ok) continue;
-        const int k = T.sec_k;
-        const huff_codebook *cb = cbs[t];
-        for (int sym = tid; sym < 256; sym += blockDim.x) {
-            const int L = T.len[sym];
-            if (L <= HUFF_LUT_BITS) continue;
-            const uint32_t base = (cb->code[sym] << (HUFF_LUT_BITS + k - L)) - (static_cast<uint32_t>(T.sec_first) << k);
-            const uint16_t ent = static_cast<uint16_t>(sym | (L << 8));
-            for (uint32_t j = 0; j < (1u << (HUFF_LUT_BITS + k - L)); ++j) T.sec[base + j] = ent;
-        }
+    uint4 *sz = reinterpret_cast<uint4 *>(T.sec);
+    for (int i = tid; i < kSecMax / 8; i += blockDim.x) sz[i] = make_uint4(0, 0, 0, 0);
+    if (tid < 32) {
+        T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
+        T.first_code[tid] = ok ? cb->first_code[tid] : 0;
+        T.first_index[tid] = ok ? cb->first_index[tid] : 0;
     }
-    __syncthreads();
+    for (int i = tid; i < 256; i += blockDim.x) {
+        T.sorted[i] = ok ? cb->sorted_symbols[i] : 0;
+        T.len[i] = ok ? cb->len[i] : 0;
+    }
+    if (tid == 0) {
+        const int longest = ok ? cb->longest : 0;
+        T.longest = longest;
+        T.ok = ok && longest <= HUFF_MAX_LEN;
+        T.has_run = ok && cb->bl_count[1] > 0;
+        T.run = (ok ? static_cast<uint64_t>(cb->sorted_symbols[0]) : 0ull) * 0x0101010101010101ull;
+        const int k = longest > W ? longest - W : 0;
+        const int first = k ? static_cast<int>(cb->first_code[W + 1] >> 1) : (1 << W);
+        T.sec_k = k;
+        T.sec_first = first;
+        T.sec_ok = k == 0 || (first <= (1 << W) && (static_cast<long long>((1 << W) - first) << k) <= kSecMax);
+    }
+}
+
+// Phase 2 (after a barrier): the secondary table for codes longer than the
+// window.  Canonical codes place every code longer than W bits after all
+// shorter ones, so their W-bit prefixes are the contiguous range
+// [first_code[W + 1] / 2, 2^W); sec holds, per prefix, 2^k entries
+// (k = longest - W) indexed by the next k bits.
+template <int W>
+__device__ void load_table_b(DecTables<W> &T, const huff_codebook *cb) {
+    if (!T.ok || T.sec_k == 0 || !T.sec_ok) return;
+    const int k = T.sec_k;
+    for (int sym = threadIdx.x; sym < 256; sym += blockDim.x) {
+        const int L = T.len[sym];
+        if (L <= W) continue;
+        const uint32_t base = (cb->code[sym] << (W + k - L)) - (static_cast<uint32_t>(T.sec_first) << k);
+        const uint16_t ent = static_cast<uint16_t>(sym | (L << 8));
+        for (uint32_t j = 0; j < (1u << (W + k - L)); ++j) T.sec[base + j] = ent;
+    }
 }
 
 // Bytes of a 16-byte unit past the payload's end read as zero.
@@ -137,11 +165,12 @@ __device__ __forceinline__ uint4 load_unit(const uint8_t *p, size_t nbytes, size
     return load_unit_tail(p, nbytes, u);
 }
 
-// Canonical search for a code longer than the table's 12 bits: returns
+// Canonical search for a code longer than the table's W bits: returns
 // (length << 8) | symbol, length 0 if no code matches.
-__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables *T) {
+template <int W>
+__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W> *T) {
     const uint32_t v = top >> (32 - HUFF_MAX_LEN);
-    for (int l = HUFF_LUT_BITS + 1; l <= T->longest; ++l) {
+    for (int l = W + 1; l <= T->longest; ++l) {
         const uint32_t c = v >> (HUFF_MAX_LEN - l);
         const uint32_t d = c - T->first_code[l];
         if (d < T->bl_count[l]) return (static_cast<uint32_t>(l) << 8) | T->sorted[T->first_index[l] + d];
@@ -151,7 +180,8 @@ __device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables *T) {
 
 // The rare case where a table entry holds more symbols than the chunk has
 // left: the total length of its first c symbols.
-__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables *T) {
+template <int W>
+__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables<W> *T) {
     uint32_t bits = 0;
     for (uint32_t k = 0; k < c; ++k) bits += T->len[(v >> (8 * k)) & 0xffu];
     return bits;
@@ -223,7 +253,8 @@ struct PlaneDec {
 // The rare cases of a step: a code longer than the table's window (or no
 // code at all: a corrupt stream), and an entry with more symbols than the
 // chunk has left.
-__device__ __forceinline__ void step_rare(const DecTables &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
+template <int W>
+__device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
                                        uint32_t &bits, uint64_t &v, bool &bad) {
     if (c == 0) {
         uint32_t L = 0, sym = 0;
@@ -231,7 +262,7 @@ __device__ __forceinline__ void step_rare(const DecTables &T, uint32_t win, uint
             if (T.sec_k > 0 && static_cast<int>(win) >= T.sec_first) {
                 const int k = T.sec_k;
                 const uint32_t idx = ((win - static_cast<uint32_t>(T.sec_first)) << k) |
-                                     ((top >> (32 - HUFF_LUT_BITS - k)) & ((1u << k) - 1u));
+                                     ((top >> (32 - W - k)) & ((1u << k) - 1u));
                 const uint32_t e2 = T.sec[idx];
                 L = e2 >> 8;
                 sym = e2 & 0xffu;
@@ -259,8 +290,8 @@ __device__ __forceinline__ void step_rare(const DecTables &T, uint32_t win, uint
 // One step: if the chunk has symbols left and the ring has room, one table
 // lookup (or a run of eight 1-bit codes), then at most one 8-byte store.
 // `limit` = the first symbol position whose slot still holds unmerged data.
-template <int RING, bool RUN>
-__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables &T,
+template <int RING, bool RUN, int W>
+__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
     // Predicated rather than branched: a lane with nothing to do (its chunk
     // is complete or its ring is full) takes a step of zero bits and zero
@@ -268,7 +299,7 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     const int rem = cnt - s.st - s.fill;
     const bool go = rem > 0 && s.st + s.fill + kStepMax <= limit;
     s.refill(p, nbytes);
-    const uint32_t win = s.bh >> (32 - HUFF_LUT_BITS);
+    const uint32_t win = s.bh >> (32 - W);
     const uint64_t e = T.lut[win];
     const uint32_t eh = static_cast<uint32_t>(e >> 32);
     uint32_t c = (eh >> 16) & 15u;
@@ -303,13 +334,13 @@ __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, siz
 
 // Decode until every lane of the warp has stored symbols [.., need) into its
 // RING-byte ring (a lane whose chunk is complete stores its last partial word).
-template <int RING, bool RUN>
-__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables &T,
+template <int RING, bool RUN, int W>
+__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                                uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
                                                bool &bad) {
     const uint64_t run = RUN ? T.run : 0ull;
     while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
-        step<RING, RUN>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+        step<RING, RUN, W>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
     if (s.fill > 0 && s.st + s.fill == cnt) {
         *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
         s.st = cnt;
@@ -318,13 +349,13 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
     }
 }
 
-template <int RING>
-__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables &T,
+template <int RING, int W>
+__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                              uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
     if (T.has_run)
-        fill_segment_t<RING, true>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, true, W>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
     else
-        fill_segment_t<RING, false>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, false, W>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
 __device__ __forceinline__ bool chunk_bounds(const uint64_t *off, size_t c, size_t nbytes, uint64_t &start,
@@ -353,9 +384,11 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
                                                            const huff_codebook *__restrict__ cb,
                                                            uint8_t *__restrict__ out, int32_t *status) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    DecTables &T = *reinterpret_cast<DecTables *>(dsm);
-    const huff_codebook *cbs[1] = {cb};
-    load_tables(&T, cbs, 1);
+    DecTables<13> &T = *reinterpret_cast<DecTables<13> *>(dsm);
+    load_table_a(T, cb);
+    __syncthreads();
+    load_table_b(T, cb);
+    __syncthreads();
     if (!T.ok) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
         return;
@@ -374,7 +407,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
             set_status(status, HUFF_ERR_CORRUPT_STREAM);
         }
     }
-    uint8_t *rings = dsm + sizeof(DecTables) + static_cast<size_t>(threadIdx.x - lane) * kRingU8;
+    uint8_t *rings = dsm + sizeof(DecTables<13>) + static_cast<size_t>(threadIdx.x - lane) * kRingU8;
     uint8_t *ring = rings + lane * kRingU8;
     const uint32_t swz = (lane & 1) ? kRingU8 / 2 : 0;
     PlaneDec s;
@@ -422,10 +455,16 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
     size_t chunk, const huff_codebook *__restrict__ cb_hi, const huff_codebook *__restrict__ cb_lo,
     const uint16_t *__restrict__ x0, uint16_t *__restrict__ out, int32_t *status) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    DecTables *Tb = reinterpret_cast<DecTables *>(dsm);
-    const huff_codebook *cbs[2] = {cb_hi, cb_lo};
-    load_tables(Tb, cbs, 2);
-    if (!Tb[0].ok || !Tb[1].ok) {
+    // high plane: the codebook's 12-bit table; low plane: a 13-bit table
+    DecTables<12> &Th = *reinterpret_cast<DecTables<12> *>(dsm);
+    DecTables<13> &Tl = *reinterpret_cast<DecTables<13> *>(dsm + sizeof(DecTables<12>));
+    load_table_a(Th, cb_hi);
+    load_table_a(Tl, cb_lo);
+    __syncthreads();
+    load_table_b(Th, cb_hi);
+    load_table_b(Tl, cb_lo);
+    __syncthreads();
+    if (!Th.ok || !Tl.ok) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
         return;
     }
@@ -443,7 +482,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
             set_status(status, HUFF_ERR_CORRUPT_STREAM);
         }
     }
-    uint8_t *rings = dsm + 2 * sizeof(DecTables) + static_cast<size_t>(threadIdx.x - lane) * (2 * kRing);
+    uint8_t *rings = dsm + kBf16Tables + static_cast<size_t>(threadIdx.x - lane) * (2 * kRing);
     uint8_t *hring = rings + lane * (2 * kRing) + ((lane & 1) ? kRing : 0);
     uint8_t *lring = rings + lane * (2 * kRing) + ((lane & 1) ? 0 : kRing);
     const uint32_t swz = (lane & 2) ? kRing / 2 : 0;
@@ -458,8 +497,8 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
             asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xp));
         }
         const int need = min(cnt, seg0 + kSeg);
-        fill_segment<kRing>(h, pay_hi, bytes_hi, Tb[0], hring, swz, cnt, need, seg0 + kRing, bad);
-        fill_segment<kRing>(l, pay_lo, bytes_lo, Tb[1], lring, swz, cnt, need, seg0 + kRing, bad);
+        fill_segment<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
+        fill_segment<kRing>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
         __syncwarp();
         // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane
 #pragma unroll
@@ -511,7 +550,7 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
     const size_t n_chunks = (n + chunk - 1) / chunk;
     const int block = decode_block(n_chunks, dev_info().sms);
     const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
-    const size_t smem = sizeof(DecTables) + static_cast<size_t>(block) * kRingU8;
+    const size_t smem = sizeof(DecTables<13>) + static_cast<size_t>(block) * kRingU8;
     if (cudaFuncSetAttribute(k_decode_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return HUFF_ERR_CUDA;
@@ -527,7 +566,7 @@ int launch_decode_bf16(const uint8_t *pay_hi, size_t bytes_hi, const uint64_t *o
     const size_t n_chunks = (n + chunk - 1) / chunk;
     const int block = decode_block(n_chunks, dev_info().sms);
     const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
-    const size_t smem = 2 * sizeof(DecTables) + static_cast<size_t>(block) * (2 * kRing);
+    const size_t smem = kBf16Tables + static_cast<size_t>(block) * (2 * kRing);
     if (x0 != nullptr) {
         if (cudaFuncSetAttribute(k_decode_bf16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
