@@ -200,9 +200,9 @@ __device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecT
 // leave it.
 constexpr int kSeg = 32;       // symbols per lane per segment (multiple of 16)
 constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
-constexpr int kStepMax = 8;    // symbols one step may add (a run of the 1-bit code)
+constexpr int kStepMax = 8;    // symbols a table step may add (a run step: twice that)
 constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
-static_assert(kRing >= kSeg + 7 + kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
+static_assert(kRing >= kSeg + 7 + 2 * kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
 static_assert(HUFF_LUT_SYMS <= kStepMax, "a table entry must fit one step");
 
 struct PlaneDec {
@@ -288,16 +288,18 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
 }
 
 // One step: if the chunk has symbols left and the ring has room, one table
-// lookup (or a run of eight 1-bit codes), then at most one 8-byte store.
+// lookup (or, for a plane with a 1-bit code, a run of 16 or 8 of that code
+// when the next 16 or 8 bits are zero), then at most two 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
 template <int RING, bool RUN, int W>
 __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
+    constexpr int kMax = RUN ? 2 * kStepMax : kStepMax;  // symbols one step may add
     // Predicated rather than branched: a lane with nothing to do (its chunk
     // is complete or its ring is full) takes a step of zero bits and zero
     // symbols, so the step stays one basic block.
     const int rem = cnt - s.st - s.fill;
-    const bool go = rem > 0 && s.st + s.fill + kStepMax <= limit;
+    const bool go = rem > 0 && s.st + s.fill + kMax <= limit;
     s.refill(p, nbytes);
     const uint32_t win = s.bh >> (32 - W);
     const uint64_t e = T.lut[win];
@@ -305,10 +307,12 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     uint32_t c = (eh >> 16) & 15u;
     uint32_t bits = eh >> 20;
     uint64_t v = e & 0xffffffffffffull;
-    if (RUN && s.bh < (1u << 24)) {
-        c = 8;
-        bits = 8;
-        v = run;
+    if (RUN) {
+        const bool r16 = s.bh < (1u << 16) && rem >= 16;
+        const bool r8 = s.bh < (1u << 24);
+        c = r16 ? 16u : (r8 ? 8u : c);
+        bits = r16 ? 16u : (r8 ? 8u : bits);
+        v = (r16 || r8) ? run : v;
     }
     if (go && (c == 0 || static_cast<int>(c) > rem)) step_rare(T, win, s.bh, rem, c, bits, v, bad);
     c = go ? c : 0u;
@@ -320,9 +324,11 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     const int nf = f + static_cast<int>(c);
     const bool full = nf >= 8;
     if (full) *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = a;
-    s.a0 = full ? (v >> 1) >> (63 - 8 * f) : a;  // the bytes that did not fit
-    s.st += full ? 8 : 0;
-    s.fill = full ? nf - 8 : nf;
+    if (RUN && nf >= 16) *reinterpret_cast<uint64_t *>(ring + (((s.st + 8) & (RING - 1)) ^ swz)) = run;
+    s.a0 = full ? (v >> 1) >> (63 - 8 * f) : a;  // the bytes that did not fit (all run bytes after a 16-run)
+    const int done = (RUN && nf >= 16) ? 16 : (full ? 8 : 0);
+    s.st += done;
+    s.fill = nf - done;
 }
 
 __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, size_t nbytes, uint64_t start, int cnt) {
@@ -378,6 +384,8 @@ __host__ int decode_block(size_t n_chunks, int sms) {
 // parity so that the copy-out's reads of 8 lanes' segments spread over the banks.
 constexpr int kRingU8 = 2 * kRing;
 constexpr int kSegU8 = 2 * kSeg;
+static_assert(kRingU8 >= kSegU8 + 7 + 2 * kStepMax && (kRingU8 & (kRingU8 - 1)) == 0 && kSegU8 % 16 == 0,
+              "byte-stream ring geometry");
 
 __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__restrict__ payload, size_t nbytes,
                                                            const uint64_t *__restrict__ off, size_t n, size_t chunk,
