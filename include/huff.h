@@ -282,6 +282,24 @@ int lmc_bytegroup_merge(const uint8_t *hi, const uint8_t *lo, size_t n, uint16_t
 int lmc_delta_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out,
                   huff_stream_t stream);
 
+/*
+ * lmc_bytegroup_split_w / lmc_bytegroup_merge_w -- byte planes of W-byte
+ * words, W = 1, 2, 4 or 8: P2's byte grouping (framework stage 1, key design
+ * 1) for other element widths (fp32: 4 planes, fp16 and bf16: 2, fp8: 1,
+ * fp64: 8).  Plane p holds byte W-1-p of every word, most significant first;
+ * for W = 2 plane 0 is lmc_bytegroup_split's hi.  Each plane is then an
+ * ordinary byte stream for huff_histogram / huff_encode.
+ *   in, out     n words of W bytes, little endian; any alignment (16-byte
+ *               aligned pointers with n % 16 == 0 take the vector path).
+ *   planes      plane p at planes + p * plane_stride (plane_stride >= n bytes, a
+ *               multiple of 16 for the vector path); must not overlap in/out.
+ *   width       1, 2, 4 or 8, else HUFF_ERR_INVALID_ARG.
+ */
+int lmc_bytegroup_split_w(const void *in, size_t n, int width, uint8_t *planes, size_t plane_stride,
+                          huff_stream_t stream);
+int lmc_bytegroup_merge_w(const uint8_t *planes, size_t n, int width, size_t plane_stride, void *out,
+                          huff_stream_t stream);
+
 /* ---------------------------------------------------------------- LMC fused bf16 paths */
 
 /*

@@ -41,7 +41,8 @@ EXPORTS = (
     "huff_num_chunks", "huff_histogram", "huff_build_codebook", "huff_codebook_from_lengths", "huff_encode",
     "huff_decode", "huff_encode_noalloc", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
-    "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted",
+    "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
+    "lmc_bytegroup_merge_w",
 )
 
 
@@ -93,6 +94,8 @@ def load(path: str = LIB_PATH):
         "lmc_decode_bf16": (I, [P, S, P, P, S, P, S, S, P, P, P, P, P, P]),
         "huff_code_stats": (I, [P, P, ctypes.POINTER(HuffStats)]),
         "lmc_segment_counts_size": (S, [S]),
+        "lmc_bytegroup_split_w": (I, [P, S, I, P, S, P]),
+        "lmc_bytegroup_merge_w": (I, [P, S, I, S, P, P]),
         "lmc_counted_workspace_size": (S, [S]),
         "lmc_histogram_bf16_counted": (I, [P, P, S, P, P, P, S, P]),
         "lmc_encode_bf16_counted": (I, [P, P, S, P, P, S, P, S, P, S, P, P, S, P, P, S, P, P]),
@@ -259,6 +262,24 @@ def lmc_encode_bf16(w: torch.Tensor, x0: torch.Tensor | None, cb_hi: torch.Tenso
         _dev(payload_hi, "payload_hi"), payload_hi.numel() * payload_hi.element_size(), _dev(off_hi, "off_hi"),
         _dev(payload_lo, "payload_lo"), payload_lo.numel() * payload_lo.element_size(), _dev(off_lo, "off_lo"),
         _dev(ws, "ws"), ws.numel() * ws.element_size(), _dev(status, "status"), _stream(stream)))
+
+
+def lmc_bytegroup_split_w(x: torch.Tensor, width: int, planes: torch.Tensor, plane_stride: int, stream=None):
+    """Plane p (byte width-1-p of each width-byte word of x) at planes[p * plane_stride:]."""
+    nbytes = x.numel() * x.element_size()
+    if nbytes % width:
+        raise ValueError("tensor size is not a whole number of words")
+    _check("lmc_bytegroup_split_w", load().lmc_bytegroup_split_w(_dev(x, "x"), nbytes // width, width,
+                                                                 _dev(planes, "planes"), plane_stride,
+                                                                 _stream(stream)))
+
+
+def lmc_bytegroup_merge_w(planes: torch.Tensor, width: int, plane_stride: int, out: torch.Tensor, stream=None):
+    nbytes = out.numel() * out.element_size()
+    if nbytes % width:
+        raise ValueError("tensor size is not a whole number of words")
+    _check("lmc_bytegroup_merge_w", load().lmc_bytegroup_merge_w(_dev(planes, "planes"), nbytes // width, width,
+                                                                 plane_stride, _dev(out, "out"), _stream(stream)))
 
 
 def lmc_histogram_bf16_counted(w: torch.Tensor, x0: torch.Tensor | None, hist_hi: torch.Tensor,

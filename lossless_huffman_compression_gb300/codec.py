@@ -183,3 +183,61 @@ def decompress_bf16(s: Bf16Streams, x0: torch.Tensor | None = None, out: torch.T
                          s.cb_lo.buf, x16, out.view(torch.int16), st)
     raise_on_status(st, "lmc_decode_bf16")
     return out
+
+
+@dataclass
+class PlaneStreams:
+    """A tensor of width-byte words as byte planes (most significant first), one stream each."""
+    width: int
+    n: int                 # words
+    dtype: torch.dtype
+    shape: tuple
+    planes: list           # [(Codebook, Stream)] for plane 0 .. width-1
+
+
+def _plane_stride(n: int) -> int:
+    return max(16, (n + 15) // 16 * 16)
+
+
+def _xor_words(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor) -> None:
+    """out = a ^ b on the tensors' bit patterns (lmc_delta_xor on their 16-bit view)."""
+    if (a.numel() * a.element_size()) % 2:
+        raise ValueError("the XOR delta needs an even number of bytes")
+    _lib.lmc_delta_xor(a.reshape(-1).view(torch.int16), b.reshape(-1).view(torch.int16),
+                       out.reshape(-1).view(torch.int16))
+
+
+def compress_planes(x: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: int = DEFAULT_CHUNK,
+                    max_len: int = 24, flags: int = 0, codebooks: list | None = None) -> PlaneStreams:
+    """Byte grouping for any element width (fp32: 4 planes, fp16/bf16: 2, fp8: 1, fp64: 8), optionally of the
+    XOR delta against x0, then one canonical Huffman stream per plane (per-plane codebooks, or the given ones)."""
+    width = x.element_size()
+    flat = x.reshape(-1)
+    n = flat.numel()
+    src = flat
+    if x0 is not None:
+        src = torch.empty_like(flat)
+        _xor_words(flat, x0, src)
+    ps = _plane_stride(n)
+    planes = torch.empty(width * ps, dtype=torch.uint8, device=x.device)
+    _lib.lmc_bytegroup_split_w(src, width, planes, ps)
+    out = []
+    for p in range(width):
+        pl = planes[p * ps: p * ps + n]
+        cb = codebooks[p] if codebooks is not None else build_codebook(histogram(pl), max_len, flags)
+        out.append((cb, encode(pl, cb, chunk_bytes, max_len)))
+    return PlaneStreams(width, n, x.dtype, tuple(x.shape), out)
+
+
+def decompress_planes(s: PlaneStreams, x0: torch.Tensor | None = None) -> torch.Tensor:
+    dev = s.planes[0][1].payload.device
+    ps = _plane_stride(s.n)
+    planes = torch.empty(s.width * ps, dtype=torch.uint8, device=dev)
+    for p, (cb, st) in enumerate(s.planes):
+        decode(st, cb, out=planes[p * ps: p * ps + s.n])
+    out = torch.empty(s.shape, dtype=s.dtype, device=dev)
+    _lib.lmc_bytegroup_merge_w(planes, s.width, ps, out.reshape(-1))
+    if x0 is not None:
+        _xor_words(out, x0, out)
+    return out
+

@@ -156,6 +156,22 @@ int lmc_delta_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out,
     return launch_xor(a, b, n, out, cs(stream));
 }
 
+int lmc_bytegroup_split_w(const void *in, size_t n, int width, uint8_t *planes, size_t plane_stride,
+                          huff_stream_t stream) {
+    if ((width != 1 && width != 2 && width != 4 && width != 8) || n > kMaxN || plane_stride < n ||
+        (n > 0 && (in == nullptr || planes == nullptr)))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_split_w(static_cast<const uint8_t *>(in), n, width, planes, plane_stride, cs(stream));
+}
+
+int lmc_bytegroup_merge_w(const uint8_t *planes, size_t n, int width, size_t plane_stride, void *out,
+                          huff_stream_t stream) {
+    if ((width != 1 && width != 2 && width != 4 && width != 8) || n > kMaxN || plane_stride < n ||
+        (n > 0 && (out == nullptr || planes == nullptr)))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_merge_w(planes, n, width, plane_stride, static_cast<uint8_t *>(out), cs(stream));
+}
+
 int lmc_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi, uint64_t *hist_lo,
                        int accumulate, huff_stream_t stream) {
     if (hist_hi == nullptr || hist_lo == nullptr || hist_hi == hist_lo || !aligned(hist_hi, 8) ||

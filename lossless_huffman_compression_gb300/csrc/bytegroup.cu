@@ -100,6 +100,87 @@ __global__ void __launch_bounds__(kStreamThreads) k_xor(const uint16_t *a, const
     for (size_t i = done + tid; i < n; i += stride) out[i] = static_cast<uint16_t>(a[i] ^ b[i]);
 }
 
+// Byte planes of W-byte words (W = 1, 2, 4, 8): plane p holds byte W-1-p of
+// every word (most significant first, so for IEEE floats plane 0 is the sign
+// and the high exponent bits).  Plane p starts at planes + p * ps (ps >= n).  A thread moves 16
+// words at a time: W 16-byte loads, one 16-byte store per plane.
+template <int W>
+__device__ __forceinline__ uint32_t byte_of(const uint32_t (&r)[4 * W], int b) {
+    return (r[b >> 2] >> (8 * (b & 3))) & 0xffu;
+}
+
+template <int W>
+__global__ void __launch_bounds__(kStreamThreads) k_split_w(const uint8_t *__restrict__ in, size_t n,
+                                                            uint8_t *__restrict__ planes, size_t ps) {
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t done = 0;
+    if (aligned16(in) && aligned16(planes) && n % 16 == 0 && ps % 16 == 0) {
+        const size_t nv = n / 16;
+        for (size_t v = tid; v < nv; v += stride) {
+            uint32_t r[4 * W];
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(in + (v * 16) * W) + j);
+                r[4 * j] = a.x; r[4 * j + 1] = a.y; r[4 * j + 2] = a.z; r[4 * j + 3] = a.w;
+            }
+#pragma unroll
+            for (int p = 0; p < W; ++p) {
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    o[q] = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[q] |= byte_of<W>(r, (4 * q + i) * W + (W - 1 - p)) << (8 * i);
+                }
+                __stcs(reinterpret_cast<uint4 *>(planes + p * ps + v * 16), make_uint4(o[0], o[1], o[2], o[3]));
+            }
+        }
+        done = nv * 16;
+    }
+    for (size_t i = done + tid; i < n; i += stride)
+#pragma unroll
+        for (int p = 0; p < W; ++p) planes[p * ps + i] = in[i * W + (W - 1 - p)];
+}
+
+template <int W>
+__global__ void __launch_bounds__(kStreamThreads) k_merge_w(const uint8_t *__restrict__ planes, size_t n,
+                                                            size_t ps, uint8_t *__restrict__ out) {
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t done = 0;
+    if (aligned16(out) && aligned16(planes) && n % 16 == 0 && ps % 16 == 0) {
+        const size_t nv = n / 16;
+        for (size_t v = tid; v < nv; v += stride) {
+            uint32_t pl[4 * W];  // 16 bytes of each plane
+#pragma unroll
+            for (int p = 0; p < W; ++p) {
+                const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(planes + p * ps + v * 16));
+                pl[4 * p] = a.x; pl[4 * p + 1] = a.y; pl[4 * p + 2] = a.z; pl[4 * p + 3] = a.w;
+            }
+#pragma unroll
+            for (int j = 0; j < W; ++j) {  // output vector j: bytes 16 j .. 16 j + 15 of the 16 words
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    o[q] = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int b = 16 * j + 4 * q + i;  // byte b of the block = byte b % W of word b / W
+                        const int p = W - 1 - b % W;
+                        o[q] |= byte_of<W>(pl, 16 * p + b / W) << (8 * i);
+                    }
+                }
+                __stcs(reinterpret_cast<uint4 *>(out + (v * 16) * W) + j, make_uint4(o[0], o[1], o[2], o[3]));
+            }
+        }
+        done = nv * 16;
+    }
+    for (size_t i = done + tid; i < n; i += stride)
+#pragma unroll
+        for (int p = 0; p < W; ++p) out[i * W + (W - 1 - p)] = planes[p * ps + i];
+}
+
 }  // namespace
 
 int launch_split(const uint16_t *w, size_t n, uint8_t *hi, uint8_t *lo, cudaStream_t s) {
@@ -117,6 +198,32 @@ int launch_merge(const uint8_t *hi, const uint8_t *lo, size_t n, uint16_t *w, cu
 int launch_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     k_xor<<<stream_grid(n / 8 + 1), kStreamThreads, 0, s>>>(a, b, n, out);
+    return launch_status();
+}
+
+int launch_split_w(const uint8_t *in, size_t n, int width, uint8_t *planes, size_t ps, cudaStream_t s) {
+    if (n == 0) return HUFF_OK;
+    const unsigned g = stream_grid(n / 16 + 1);
+    switch (width) {
+        case 1: k_split_w<1><<<g, kStreamThreads, 0, s>>>(in, n, planes, ps); break;
+        case 2: k_split_w<2><<<g, kStreamThreads, 0, s>>>(in, n, planes, ps); break;
+        case 4: k_split_w<4><<<g, kStreamThreads, 0, s>>>(in, n, planes, ps); break;
+        case 8: k_split_w<8><<<g, kStreamThreads, 0, s>>>(in, n, planes, ps); break;
+        default: return HUFF_ERR_INVALID_ARG;
+    }
+    return launch_status();
+}
+
+int launch_merge_w(const uint8_t *planes, size_t n, int width, size_t ps, uint8_t *out, cudaStream_t s) {
+    if (n == 0) return HUFF_OK;
+    const unsigned g = stream_grid(n / 16 + 1);
+    switch (width) {
+        case 1: k_merge_w<1><<<g, kStreamThreads, 0, s>>>(planes, n, ps, out); break;
+        case 2: k_merge_w<2><<<g, kStreamThreads, 0, s>>>(planes, n, ps, out); break;
+        case 4: k_merge_w<4><<<g, kStreamThreads, 0, s>>>(planes, n, ps, out); break;
+        case 8: k_merge_w<8><<<g, kStreamThreads, 0, s>>>(planes, n, ps, out); break;
+        default: return HUFF_ERR_INVALID_ARG;
+    }
     return launch_status();
 }
 

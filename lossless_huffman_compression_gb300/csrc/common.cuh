@@ -195,6 +195,8 @@ int launch_decode_bf16(const uint8_t *pay_hi, size_t bytes_hi, const uint64_t *o
 int launch_split(const uint16_t *w, size_t n, uint8_t *hi, uint8_t *lo, cudaStream_t s);
 int launch_merge(const uint8_t *hi, const uint8_t *lo, size_t n, uint16_t *w, cudaStream_t s);
 int launch_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out, cudaStream_t s);
+int launch_split_w(const uint8_t *in, size_t n, int width, uint8_t *planes, size_t ps, cudaStream_t s);
+int launch_merge_w(const uint8_t *planes, size_t n, int width, size_t ps, uint8_t *out, cudaStream_t s);
 
 inline int launch_status() {
     cudaError_t e = cudaGetLastError();

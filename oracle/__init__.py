@@ -194,6 +194,25 @@ def bytegroup_merge(hi, lo) -> np.ndarray:
     return w[:n]
 
 
+def bytegroup_split_w(data, width: int) -> list:
+    """Byte planes of width-byte little-endian words (P2 byte grouping for other
+    element widths): plane p is byte width-1-p of every word, most significant first."""
+    b = np.ascontiguousarray(np.asarray(data).view(np.uint8).reshape(-1))
+    assert b.size % width == 0
+    words = b.reshape(-1, width)
+    return [np.ascontiguousarray(words[:, width - 1 - p]) for p in range(width)]
+
+
+def bytegroup_merge_w(planes) -> np.ndarray:
+    """The words' bytes (little endian) from their byte planes, most significant plane first."""
+    width = len(planes)
+    n = np.asarray(planes[0]).size
+    out = np.empty((n, width), dtype=np.uint8)
+    for p in range(width):
+        out[:, width - 1 - p] = np.asarray(planes[p], dtype=np.uint8)
+    return out.reshape(-1)
+
+
 def delta_xor(a, b) -> np.ndarray:
     """C9: bitwise XOR of two 16-bit snapshots."""
     a16 = np.ascontiguousarray(np.asarray(a).view(np.uint16).reshape(-1))

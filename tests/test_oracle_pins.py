@@ -407,3 +407,42 @@ def test_c_oracle_matches_python_tiny_oracle(seed):
     assert payload.tobytes() == tp and [int(v) for v in off] == toff
     assert tiny.decode(tp, toff, n, cb, tl) == x.tobytes()
     assert oracle.entropy(h) == pytest.approx(tiny.entropy([int(v) for v in h]), rel=1e-12)
+
+
+# ------------------------------------------------------------------ byte planes of other widths (P2 byte grouping)
+def test_bytegroup_split_w_ieee_encodings():
+    # IEEE 754 encodings of exact values, most significant byte first
+    cases = [
+        (np.array([1.0], dtype=np.float32), [0x3F, 0x80, 0x00, 0x00]),
+        (np.array([-2.0], dtype=np.float32), [0xC0, 0x00, 0x00, 0x00]),
+        (np.array([0.1], dtype=np.float32), [0x3D, 0xCC, 0xCC, 0xCD]),
+        (np.array([np.inf], dtype=np.float32), [0x7F, 0x80, 0x00, 0x00]),
+        (np.array([1.0], dtype=np.float64), [0x3F, 0xF0, 0, 0, 0, 0, 0, 0]),
+        (np.array([-0.5], dtype=np.float16), [0xB8, 0x00]),
+    ]
+    for x, want in cases:
+        planes = oracle.bytegroup_split_w(x, x.itemsize)
+        assert [int(p[0]) for p in planes] == want
+
+
+def test_bytegroup_split_w_width2_equals_c_split_on_all_patterns():
+    w = np.arange(1 << 16, dtype=np.uint16)
+    hi, lo = oracle.bytegroup_split(w)
+    p0, p1 = oracle.bytegroup_split_w(w, 2)
+    assert np.array_equal(p0, hi) and np.array_equal(p1, lo)
+
+
+@pytest.mark.parametrize("width", [1, 2, 4, 8])
+def test_bytegroup_merge_w_inverts_split(width):
+    rng = np.random.default_rng(width)
+    b = rng.integers(0, 256, 1000 * width, dtype=np.uint8)
+    planes = oracle.bytegroup_split_w(b, width)
+    assert len(planes) == width and all(p.size == 1000 for p in planes)
+    assert np.array_equal(oracle.bytegroup_merge_w(planes), b)
+
+
+def test_fp32_plane0_holds_the_sign_bit():
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 1, 10000).astype(np.float32)
+    p0 = oracle.bytegroup_split_w(x, 4)[0]
+    assert np.array_equal(p0 >> 7, np.signbit(x).astype(np.uint8))
