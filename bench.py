@@ -312,6 +312,7 @@ def run_ours(args, dist, rank, ws):
 
     # extra: encode / decode of the already-materialised delta (codebooks given), outside the step
     extra = materialised_delta_stages(path, args, peak)
+    planes_fp32 = byte_planes_stage(args, peak) if not args.no_extras else None
 
     # quality
     from lossless_huffman_compression_gb300 import _lib
@@ -344,11 +345,46 @@ def run_ours(args, dist, rank, ws):
                    "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk, "max_len": 24,
                    "step": "xor+split+hist with segment counts, build x2, one-pass fused encode, fused decode+merge+xor",
                    "l2": "inputs (8 GB) larger than L2; no flush", "parallelism": f"replicas{ws}"},
-        "roofline": roofline, "stages": stages, "materialised_delta": extra, "quality": quality,
+        "roofline": roofline, "stages": stages, "materialised_delta": extra, "byte_planes_fp32": planes_fp32,
+        "quality": quality,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": path.launches_per_step * args.steps, "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def byte_planes_stage(args, peak):
+    """Byte grouping for another width: a 1 GiB fp32 tensor (the weights recipe in fp32) as 4 byte planes,
+    compressed and decompressed through codec.compress_planes / decompress_planes (per-plane codebooks)."""
+    from lossless_huffman_compression_gb300 import codec, workloads
+    shape = (args.rows // 4, 16384) if args.rows < 65536 else (16384, 16384)
+    x = workloads.bf16_weights(device="cuda", shape=shape, dtype=torch.float32)
+    nbytes = x.numel() * 4
+    s = codec.compress_planes(x, chunk_bytes=args.chunk)
+    back = codec.decompress_planes(s)
+    if not torch.equal(back.view(torch.int32), x.view(torch.int32)):
+        raise RuntimeError("fp32 byte-plane round trip differs")
+    reps = 3
+    res = {}
+    for nm, fn in (("compress", lambda: codec.compress_planes(x, chunk_bytes=args.chunk)),
+                   ("decompress", lambda: codec.decompress_planes(s))):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        res[nm] = {"ms": round(ms, 3), "gbs_uncompressed": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    payload = sum((st.total_bits() + 7) // 8 for _, st in s.planes)
+    res.update({"shape": list(shape), "dtype": "fp32", "planes": 4, "ratio": round(nbytes / payload, 4),
+                "plane_bits_per_symbol": [round(st.total_bits() / x.numel(), 4) for _, st in s.planes],
+                "api": "codec.compress_planes / decompress_planes (status checked per plane)"})
+    del x, s, back
+    torch.cuda.empty_cache()
+    return res
 
 
 def materialised_delta_stages(path, args, peak):
@@ -529,6 +565,7 @@ def main():
                     help="snapshot rows of 30518 bf16 (65536 = the 4.0 GB workload; fewer for quick checks)")
     ap.add_argument("--small", action="store_true", help="same as --rows 4096 (a 250 MB snapshot)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the fp32 byte-plane measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=256 << 20, help="elements for the oracle baseline (about 10 s)")
     ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")

@@ -176,6 +176,31 @@ int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags,
                         huff_codebook *cb, int32_t *status, huff_stream_t stream);
 
 /*
+ * Drift-adaptive refresh of a fixed codebook.  P1 builds its codebook once
+ * from warm-up statistics and names distribution drift as the limitation of
+ * that scheme, with adaptive codebooks as future work.  For a shard about to
+ * be encoded with cb, huff_drift_check measures how far cb is from the
+ * shard's own statistics and huff_build_codebook_if rebuilds cb from the
+ * shard's histogram only when the check said so, without a host round trip.
+ *
+ * huff_drift_check -- with h the shard's histogram (n symbols, entropy H bits
+ * per symbol), T = sum h[s] * len[s] its cost under cb and B = n * max(H, 1)
+ * (the entropy bound, and at least one bit per symbol for any Huffman code
+ * of bytes):  gap = (T - B) / B, +infinity when a present symbol has no
+ * code, 0 for an empty shard.  Writes *flag = (gap > threshold) and, if gap
+ * is not NULL, *gap (double).  All pointers device; threshold >= 0.
+ */
+int huff_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag,
+                     double *gap, huff_stream_t stream);
+
+/*
+ * huff_build_codebook_if -- huff_build_codebook when *flag != 0 (a device
+ * word, e.g. from huff_drift_check); otherwise cb is left as it is.
+ */
+int huff_build_codebook_if(const uint64_t *hist, const uint32_t *flag, int max_len, unsigned flags,
+                           huff_codebook *cb, int32_t *status, huff_stream_t stream);
+
+/*
  * huff_codebook_from_lengths -- import a transmitted codebook [P1 Key
  * contributions: the codebook is stored on each accelerator, not exchanged per
  * batch; it travels once, as 256 lengths].

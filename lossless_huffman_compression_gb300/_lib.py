@@ -42,7 +42,7 @@ EXPORTS = (
     "huff_decode", "huff_encode_noalloc", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
     "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
-    "lmc_bytegroup_merge_w",
+    "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if",
 )
 
 
@@ -94,6 +94,8 @@ def load(path: str = LIB_PATH):
         "lmc_decode_bf16": (I, [P, S, P, P, S, P, S, S, P, P, P, P, P, P]),
         "huff_code_stats": (I, [P, P, ctypes.POINTER(HuffStats)]),
         "lmc_segment_counts_size": (S, [S]),
+        "huff_drift_check": (I, [P, P, ctypes.c_double, P, P, P]),
+        "huff_build_codebook_if": (I, [P, P, I, ctypes.c_uint, P, P, P]),
         "lmc_bytegroup_split_w": (I, [P, S, I, P, S, P]),
         "lmc_bytegroup_merge_w": (I, [P, S, I, S, P, P]),
         "lmc_counted_workspace_size": (S, [S]),
@@ -262,6 +264,19 @@ def lmc_encode_bf16(w: torch.Tensor, x0: torch.Tensor | None, cb_hi: torch.Tenso
         _dev(payload_hi, "payload_hi"), payload_hi.numel() * payload_hi.element_size(), _dev(off_hi, "off_hi"),
         _dev(payload_lo, "payload_lo"), payload_lo.numel() * payload_lo.element_size(), _dev(off_lo, "off_lo"),
         _dev(ws, "ws"), ws.numel() * ws.element_size(), _dev(status, "status"), _stream(stream)))
+
+
+def huff_drift_check(hist: torch.Tensor, cb: torch.Tensor, threshold: float, flag: torch.Tensor,
+                     gap: torch.Tensor | None = None, stream=None):
+    _check("huff_drift_check", load().huff_drift_check(_dev(hist, "hist"), _dev(cb, "cb"), float(threshold),
+                                                       _dev(flag, "flag"), _dev(gap, "gap"), _stream(stream)))
+
+
+def huff_build_codebook_if(hist: torch.Tensor, flag: torch.Tensor, cb: torch.Tensor, status: torch.Tensor,
+                           max_len: int = HUFF_MAX_LEN, flags: int = 0, stream=None):
+    _check("huff_build_codebook_if", load().huff_build_codebook_if(
+        _dev(hist, "hist"), _dev(flag, "flag"), max_len, flags, _dev(cb, "cb"), _dev(status, "status"),
+        _stream(stream)))
 
 
 def lmc_bytegroup_split_w(x: torch.Tensor, width: int, planes: torch.Tensor, plane_stride: int, stream=None):

@@ -241,3 +241,26 @@ def decompress_planes(s: PlaneStreams, x0: torch.Tensor | None = None) -> torch.
         _xor_words(out, x0, out)
     return out
 
+
+class DriftAdaptiveCodebook:
+    """A fixed codebook that is rebuilt from a shard's own histogram when the shard drifts too far from it
+    (huff_drift_check + huff_build_codebook_if; no host round trip).  The flag of the last check stays on
+    the device in `refreshed`; read it (one sync) to know whether the transmitted lengths changed."""
+
+    def __init__(self, cb: Codebook, threshold: float = 0.02, max_len: int = 24, flags: int = _lib.HUFF_COVER_ALL):
+        self.cb = cb
+        self.threshold = threshold
+        self.max_len = max_len
+        self.flags = flags
+        dev = cb.device
+        self.refreshed = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.gap = torch.zeros(1, dtype=torch.float64, device=dev)
+        self.status = new_status(dev)
+        self.hist = torch.zeros(256, dtype=torch.int64, device=dev)
+
+    def encode(self, x: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK) -> Stream:
+        histogram(x, self.hist)
+        _lib.huff_drift_check(self.hist, self.cb.buf, self.threshold, self.refreshed, self.gap)
+        _lib.huff_build_codebook_if(self.hist, self.refreshed, self.cb.buf, self.status, self.max_len, self.flags)
+        return encode(x, self.cb, chunk_bytes, self.max_len)
+

@@ -84,7 +84,24 @@ int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_
     if (hist == nullptr || cb == nullptr || status == nullptr || !aligned(cb, 16) || !aligned(hist, 8) ||
         max_len < HUFF_MIN_MAX_LEN || max_len > HUFF_MAX_LEN || (flags & ~HUFF_COVER_ALL) != 0)
         return HUFF_ERR_INVALID_ARG;
-    return launch_build_codebook(hist, max_len, flags, cb, status, cs(stream));
+    return launch_build_codebook(hist, max_len, flags, cb, status, nullptr, cs(stream));
+}
+
+int huff_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag, double *gap,
+                     huff_stream_t stream) {
+    if (hist == nullptr || cb == nullptr || flag == nullptr || !aligned(hist, 8) || !aligned(cb, 16) ||
+        !aligned(flag, 4) || (gap != nullptr && !aligned(gap, 8)) || !(threshold >= 0.0))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_drift_check(hist, cb, threshold, flag, gap, cs(stream));
+}
+
+int huff_build_codebook_if(const uint64_t *hist, const uint32_t *flag, int max_len, unsigned flags,
+                           huff_codebook *cb, int32_t *status, huff_stream_t stream) {
+    if (hist == nullptr || flag == nullptr || cb == nullptr || status == nullptr || !aligned(cb, 16) ||
+        !aligned(hist, 8) || !aligned(flag, 4) || max_len < HUFF_MIN_MAX_LEN || max_len > HUFF_MAX_LEN ||
+        (flags & ~HUFF_COVER_ALL) != 0)
+        return HUFF_ERR_INVALID_ARG;
+    return launch_build_codebook(hist, max_len, flags, cb, status, flag, cs(stream));
 }
 
 int huff_codebook_from_lengths(const uint8_t *h_len, int max_len, huff_codebook *cb, int32_t *status,

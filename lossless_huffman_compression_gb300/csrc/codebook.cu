@@ -124,7 +124,8 @@ __device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook 
 
 __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restrict__ hist, int max_len,
                                                        unsigned flags, huff_codebook *__restrict__ cb,
-                                                       int32_t *status) {
+                                                       int32_t *status, const uint32_t *__restrict__ when) {
+    if (when != nullptr && *when == 0) return;  // conditional rebuild: the codebook stays as it is
     __shared__ uint64_t cnt[256];
     __shared__ uint64_t leaf_cnt[256];
     __shared__ uint64_t int_cnt[256];
@@ -253,6 +254,64 @@ __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restric
     finish_codebook(lens, max_len, cb, status);
 }
 
+// Drift of a shard against the codebook in use (P1 Limitations: a fixed
+// codebook degrades when the distribution drifts; refreshing it is P1's
+// future work).  The shard costs T = sum h * len bits under the codebook;
+// its own entropy bounds any code from below by n H bits, and a Huffman
+// code of bytes by n bits (at least one bit per symbol), so the bound is
+// B = n max(H, 1).  gap = (T - B) / B; a symbol without a code makes the gap
+// infinite; an empty shard has gap 0.  *flag = gap > threshold.
+__global__ void __launch_bounds__(kT) k_drift_check(const uint64_t *__restrict__ hist,
+                                                    const huff_codebook *__restrict__ cb, double threshold,
+                                                    uint32_t *__restrict__ flag, double *__restrict__ gap_out) {
+    __shared__ uint64_t s_n[kT / 32], s_bits[kT / 32];
+    __shared__ double s_h[kT / 32];
+    __shared__ int s_missing;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (t == 0) s_missing = 0;
+    __syncthreads();
+    const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
+    const uint64_t h = hist[t];
+    const uint64_t L = ok ? cb->len[t] : 0;
+    if (h > 0 && L == 0) s_missing = 1;
+    uint64_t n = h, bits = h * L;
+    for (int o = 16; o > 0; o >>= 1) {
+        n += __shfl_xor_sync(0xffffffffu, n, o);
+        bits += __shfl_xor_sync(0xffffffffu, bits, o);
+    }
+    if (lane == 0) {
+        s_n[warp] = n;
+        s_bits[warp] = bits;
+    }
+    __syncthreads();
+    uint64_t N = 0, T = 0;
+    for (int w = 0; w < kT / 32; ++w) {
+        N += s_n[w];
+        T += s_bits[w];
+    }
+    double e = 0.0;  // -p log2 p of this symbol
+    if (h > 0) {
+        const double p = static_cast<double>(h) / static_cast<double>(N);
+        e = -p * log2(p);
+    }
+    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+    if (lane == 0) s_h[warp] = e;
+    __syncthreads();
+    if (t == 0) {
+        double H = 0.0;
+        for (int w = 0; w < kT / 32; ++w) H += s_h[w];
+        double g = 0.0;
+        if (s_missing) {
+            g = __longlong_as_double(0x7ff0000000000000ll);  // +infinity
+        } else if (N > 0) {
+            const double B = static_cast<double>(N) * (H > 1.0 ? H : 1.0);
+            g = (static_cast<double>(T) - B) / B;
+        }
+        if (gap_out != nullptr) *gap_out = g;
+        *flag = g > threshold ? 1u : 0u;
+    }
+}
+
 __global__ void __launch_bounds__(kT) k_codebook_from_lengths(int max_len, huff_codebook *__restrict__ cb,
                                                               int32_t *status) {
     __shared__ uint8_t lens[256];
@@ -277,8 +336,14 @@ __global__ void __launch_bounds__(kT) k_codebook_from_lengths(int max_len, huff_
 }  // namespace
 
 int launch_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_codebook *cb,
-                          int32_t *status, cudaStream_t s) {
-    k_build_codebook<<<1, kT, 0, s>>>(hist, max_len, flags, cb, status);
+                          int32_t *status, const uint32_t *when, cudaStream_t s) {
+    k_build_codebook<<<1, kT, 0, s>>>(hist, max_len, flags, cb, status, when);
+    return launch_status();
+}
+
+int launch_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag,
+                       double *gap, cudaStream_t s) {
+    k_drift_check<<<1, kT, 0, s>>>(hist, cb, threshold, flag, gap);
     return launch_status();
 }
 

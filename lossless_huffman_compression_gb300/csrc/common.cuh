@@ -166,7 +166,9 @@ int launch_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist,
 int launch_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
                           uint64_t *hist_lo, cudaStream_t s);
 int launch_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_codebook *cb,
-                          int32_t *status, cudaStream_t s);
+                          int32_t *status, const uint32_t *when, cudaStream_t s);
+int launch_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag,
+                       double *gap, cudaStream_t s);
 int launch_codebook_from_lengths(int max_len, huff_codebook *cb, int32_t *status, cudaStream_t s);
 
 size_t enc_u8_tiles(size_t n);

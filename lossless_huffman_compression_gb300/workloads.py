@@ -85,18 +85,19 @@ def fixed_codebook_shard(k: int, warmup: bool, device="cpu", shape=None) -> torc
     return out.view(shape)
 
 
-def bf16_weights(device="cpu", shape=BF16_WEIGHTS_SHAPE, seed: int = 3) -> torch.Tensor:
-    """bf16 N(0, 0.02) with 1e-4 outliers of magnitude U(0.5, 4) and random sign."""
+def bf16_weights(device="cpu", shape=BF16_WEIGHTS_SHAPE, seed: int = 3, dtype=torch.bfloat16) -> torch.Tensor:
+    """bf16 N(0, 0.02) with 1e-4 outliers of magnitude U(0.5, 4) and random sign (the same recipe in
+    another float dtype with `dtype`, e.g. the fp32 byte-plane measurement)."""
     n = int(math.prod(shape))
     g = _gen(seed, device)
-    out = torch.empty(n, dtype=torch.bfloat16, device=device)
+    out = torch.empty(n, dtype=dtype, device=device)
     for s in range(0, n, _BLOCK):
         e = min(n, s + _BLOCK)
         x = torch.randn(e - s, generator=g, device=device).mul_(0.02)
         mask = torch.rand(e - s, generator=g, device=device) < 1e-4
         sign = torch.where(torch.rand(e - s, generator=g, device=device) < 0.5, -1.0, 1.0)
         mag = torch.rand(e - s, generator=g, device=device).mul_(3.5).add_(0.5)
-        out[s:e] = torch.where(mask, sign * mag, x).to(torch.bfloat16)
+        out[s:e] = torch.where(mask, sign * mag, x).to(dtype)
     return out.view(shape)
 
 

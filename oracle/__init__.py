@@ -194,6 +194,28 @@ def bytegroup_merge(hi, lo) -> np.ndarray:
     return w[:n]
 
 
+def drift_gap(hist, lengths) -> float:
+    """Drift of a shard against a codebook (P1 Limitations: distribution drift under a fixed codebook):
+    T = sum h * len bits under the codebook, bound B = n * max(H, 1) with H the shard's own entropy
+    (at least one bit per symbol for a Huffman code of bytes); gap = (T - B) / B, infinite when a
+    present symbol has no code, 0 for an empty shard."""
+    h = np.asarray(hist, dtype=np.uint64)
+    ln = np.asarray(lengths, dtype=np.uint64)
+    if np.any((h > 0) & (ln == 0)):
+        return float("inf")
+    n = int(h.sum())
+    if n == 0:
+        return 0.0
+    T = sum(int(a) * int(b) for a, b in zip(h, ln))
+    H = 0.0
+    for c in h:
+        if c:
+            p = float(c) / n
+            H -= p * np.log2(p)
+    B = n * max(H, 1.0)
+    return (T - B) / B
+
+
 def bytegroup_split_w(data, width: int) -> list:
     """Byte planes of width-byte little-endian words (P2 byte grouping for other
     element widths): plane p is byte width-1-p of every word, most significant first."""

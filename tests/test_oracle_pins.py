@@ -446,3 +446,28 @@ def test_fp32_plane0_holds_the_sign_bit():
     x = rng.normal(0, 1, 10000).astype(np.float32)
     p0 = oracle.bytegroup_split_w(x, 4)[0]
     assert np.array_equal(p0 >> 7, np.signbit(x).astype(np.uint8))
+
+
+# ------------------------------------------------------------------ drift of a shard against a fixed codebook
+def test_drift_gap_closed_forms():
+    L = np.zeros(256, dtype=np.uint8)
+    # uniform over 256 symbols with 8-bit codes: T = 8 n = n H
+    assert oracle.drift_gap(np.full(256, 10), np.full(256, 8)) == 0.0
+    # dyadic (1/2, 1/4, 1/8, 1/8) with lengths (1, 2, 3, 3): T / n = H = 1.75
+    h = np.zeros(256, dtype=np.uint64)
+    h[:4] = [4, 2, 1, 1]
+    L[:4] = [1, 2, 3, 3]
+    assert oracle.drift_gap(h, L) == pytest.approx(0.0, abs=1e-15)
+    # uniform over 4 symbols (H = 2) with the same lengths: T / n = 9 / 4, gap 1/8
+    h[:4] = [5, 5, 5, 5]
+    assert oracle.drift_gap(h, L) == pytest.approx(0.125, rel=1e-15)
+    # (0.9, 0.1) with two 1-bit codes: H = 0.469 < 1, so the bound is one bit per symbol: gap 0
+    h2 = np.zeros(256, dtype=np.uint64)
+    h2[:2] = [9, 1]
+    L2 = np.zeros(256, dtype=np.uint8)
+    L2[:2] = [1, 1]
+    assert oracle.drift_gap(h2, L2) == 0.0
+    # a present symbol without a code: infinite; an empty shard: 0
+    h2[7] = 1
+    assert oracle.drift_gap(h2, L2) == float("inf")
+    assert oracle.drift_gap(np.zeros(256), L2) == 0.0
