@@ -313,6 +313,7 @@ def run_ours(args, dist, rank, ws):
     # extra: encode / decode of the already-materialised delta (codebooks given), outside the step
     extra = materialised_delta_stages(path, args, peak)
     planes_fp32 = byte_planes_stage(args, peak) if not args.no_extras else None
+    drift = drift_stage(args) if not args.no_extras else None
 
     # quality
     from lossless_huffman_compression_gb300 import _lib
@@ -345,7 +346,7 @@ def run_ours(args, dist, rank, ws):
                    "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk, "max_len": 24,
                    "step": "xor+split+hist with segment counts, build x2, one-pass fused encode, fused decode+merge+xor",
                    "l2": "inputs (8 GB) larger than L2; no flush", "parallelism": f"replicas{ws}"},
-        "roofline": roofline, "stages": stages, "materialised_delta": extra, "byte_planes_fp32": planes_fp32,
+        "roofline": roofline, "stages": stages, "materialised_delta": extra, "byte_planes_fp32": planes_fp32, "drift_adaptive": drift,
         "quality": quality,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": path.launches_per_step * args.steps, "clocks": clk,
     }
@@ -360,13 +361,14 @@ def byte_planes_stage(args, peak):
     shape = (args.rows // 4, 16384) if args.rows < 65536 else (16384, 16384)
     x = workloads.bf16_weights(device="cuda", shape=shape, dtype=torch.float32)
     nbytes = x.numel() * 4
-    s = codec.compress_planes(x, chunk_bytes=args.chunk)
+    chunk = 4096  # a plane of 2^28 bytes in 4 KiB chunks: 65536 chunks, enough lanes for every SM
+    s = codec.compress_planes(x, chunk_bytes=chunk)
     back = codec.decompress_planes(s)
     if not torch.equal(back.view(torch.int32), x.view(torch.int32)):
         raise RuntimeError("fp32 byte-plane round trip differs")
     reps = 3
     res = {}
-    for nm, fn in (("compress", lambda: codec.compress_planes(x, chunk_bytes=args.chunk)),
+    for nm, fn in (("compress", lambda: codec.compress_planes(x, chunk_bytes=chunk)),
                    ("decompress", lambda: codec.decompress_planes(s))):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -379,10 +381,44 @@ def byte_planes_stage(args, peak):
         ms = a.elapsed_time(b) / reps
         res[nm] = {"ms": round(ms, 3), "gbs_uncompressed": round(nbytes / (ms / 1e3) / 1e9, 1)}
     payload = sum((st.total_bits() + 7) // 8 for _, st in s.planes)
-    res.update({"shape": list(shape), "dtype": "fp32", "planes": 4, "ratio": round(nbytes / payload, 4),
+    res.update({"shape": list(shape), "dtype": "fp32", "planes": 4, "chunk_bytes": chunk,
+                "ratio": round(nbytes / payload, 4),
                 "plane_bits_per_symbol": [round(st.total_bits() / x.numel(), 4) for _, st in s.planes],
                 "api": "codec.compress_planes / decompress_planes (status checked per plane)"})
     del x, s, back
+    torch.cuda.empty_cache()
+    return res
+
+
+def drift_stage(args):
+    """Fixed vs drift-adaptive codebook on the sweep stream's first segments (kinds cycle every segment):
+    codebook from the first 64 MiB with every symbol covered; adaptive = refresh when a segment's drift gap
+    exceeds 2 % (huff_drift_check + huff_build_codebook_if before each segment's encode)."""
+    from lossless_huffman_compression_gb300 import _lib, codec, workloads
+    nseg = 20 if args.rows >= 65536 else 5
+    seg = workloads.SWEEP_SEGMENT_BYTES
+    segs = [workloads.sweep_segment(k, device="cuda").view(torch.uint8) for k in range(nseg)]
+    head = segs[0][: 64 << 20]
+    res = {"segments": nseg, "segment_bytes": seg, "threshold": 0.02, "chunk_bytes": args.chunk}
+    for mode in ("fixed", "adaptive"):
+        cb = codec.build_codebook(codec.histogram(head), 24, _lib.HUFF_COVER_ALL)
+        ad = codec.DriftAdaptiveCodebook(cb, threshold=0.02) if mode == "adaptive" else None
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        bits, refreshes = 0, 0
+        for x in segs:
+            s = ad.encode(x, args.chunk) if ad else codec.encode(x, cb, args.chunk)
+            bits += s.total_bits()
+            if ad:
+                refreshes += int(ad.refreshed.item())
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        res[mode] = {"ratio": round(nseg * seg * 8 / bits, 4), "refreshes": refreshes, "ms": round(ms, 2),
+                     "gbs": round(nseg * seg / (ms / 1e3) / 1e9, 1)}
+    del segs, head
     torch.cuda.empty_cache()
     return res
 
@@ -565,7 +601,7 @@ def main():
                     help="snapshot rows of 30518 bf16 (65536 = the 4.0 GB workload; fewer for quick checks)")
     ap.add_argument("--small", action="store_true", help="same as --rows 4096 (a 250 MB snapshot)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the fp32 byte-plane measurement")
+    ap.add_argument("--no-extras", action="store_true", help="skip the fp32 byte-plane and drift measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=256 << 20, help="elements for the oracle baseline (about 10 s)")
     ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")
