@@ -590,6 +590,100 @@ def run_reference(args, dist, rank, ws):
     print(json.dumps(line), flush=True)
 
 
+def _timed(fn, reps):
+    fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def run_workload(args):
+    """One JSON line per stage for the four other workloads (parity cases, measured for the record):
+    per_shard (int8 1 MiB), fixed_codebook (16 warm-up + 64 test int8 shards), bf16_weights (1 GiB,
+    2 planes), sweep (16 GiB int8, chunk sizes 16 KiB .. 1 MiB).  GB/s of uncompressed bytes; codec API
+    calls (status checked per call)."""
+    from lossless_huffman_compression_gb300 import _lib, codec, workloads
+    import oracle
+    torch.cuda.set_device(0)
+    peak, peak_kind = hbm_peak()
+    reps = max(3, args.steps)
+    out = {"metric": METRIC, "workload": args.workload, "n_gpus": 1, "data": "synthetic", "peak_gbs": peak,
+           "peak_source": peak_kind}
+    if args.workload == "per_shard":
+        x = workloads.per_shard_int8(device="cuda").view(torch.uint8)
+        n = x.numel()
+        cb, s = codec.compress(x, args.chunk)
+        comp = _timed(lambda: codec.compress(x, args.chunk), reps)
+        dec = _timed(lambda: codec.decode(s, cb), reps)
+        h = oracle.histogram(x.cpu().numpy())
+        out.update({"elements": n, "chunk_bytes": args.chunk, "l2": "1 MiB: L2-resident, latency-bound",
+                    "compress_us": round(comp * 1e3, 1), "decode_us": round(dec * 1e3, 1),
+                    "compress_gbs": round(n / comp / 1e6, 2), "decode_gbs": round(n / dec / 1e6, 2),
+                    "ratio": round(8 * n / s.total_bits(), 4), "entropy_bits": round(oracle.entropy(h), 4),
+                    "mean_len": round(s.total_bits() / n, 4)})
+    elif args.workload == "fixed_codebook":
+        hist = torch.zeros(256, dtype=torch.int64, device="cuda")
+        for k in range(workloads.WARMUP_SHARDS):
+            codec.histogram(workloads.fixed_codebook_shard(k, warmup=True, device="cuda"), hist, accumulate=True)
+        cb = codec.build_codebook(hist, 24, _lib.HUFF_COVER_ALL)
+        shards = [workloads.fixed_codebook_shard(k, warmup=False, device="cuda").view(torch.uint8).reshape(-1)
+                  for k in range(workloads.TEST_SHARDS)]
+        n = sum(x.numel() for x in shards)
+        streams = [codec.encode(x, cb, args.chunk) for x in shards]
+        enc = _timed(lambda: [codec.encode(x, cb, args.chunk) for x in shards], 3)
+        dec = _timed(lambda: [codec.decode(st, cb) for st in streams], 3)
+        fixed_bits = sum(st.total_bits() for st in streams)
+        shard_bits, nh = 0, 0.0
+        for x in shards:
+            h = codec.histogram(x).cpu().numpy().astype(np.uint64)
+            ln = codec.build_codebook(torch.from_numpy(h.astype(np.int64)).cuda()).lengths()
+            shard_bits += oracle.total_bits(h, ln)
+            nh += oracle.entropy(h) * x.numel()
+        out.update({"elements": n, "shards": len(shards), "chunk_bytes": args.chunk,
+                    "encode_gbs": round(n / enc / 1e6, 1), "decode_gbs": round(n / dec / 1e6, 1),
+                    "ratio": round(8 * n / fixed_bits, 4),
+                    "gap_vs_per_shard_huffman": round((fixed_bits - shard_bits) / shard_bits, 5),
+                    "gap_vs_entropy": round((fixed_bits - nh) / nh, 5)})
+    elif args.workload == "bf16_weights":
+        x = workloads.bf16_weights(device="cuda")
+        n = x.numel()
+        s = codec.compress_bf16(x, None, args.chunk)
+        comp = _timed(lambda: codec.compress_bf16(x, None, args.chunk), reps)
+        dec = _timed(lambda: codec.decompress_bf16(s), reps)
+        C = s.hi.nbytes() + s.lo.nbytes()
+        out.update({"elements": n, "chunk_bytes": args.chunk, "compress_gbs": round(2 * n / comp / 1e6, 1),
+                    "decode_gbs": round(2 * n / dec / 1e6, 1),
+                    "decode_hbm_frac": round((C + 4 * n) / (dec / 1e3) / 1e9 / peak, 4),
+                    "ratio": round(2 * n / C, 4),
+                    "bits_per_symbol": [round(s.hi.total_bits() / n, 4), round(s.lo.total_bits() / n, 4)]})
+    elif args.workload == "sweep":
+        seg = workloads.SWEEP_SEGMENT_BYTES
+        n = workloads.SWEEP_SEGMENTS * seg
+        x = torch.empty(n, dtype=torch.uint8, device="cuda")
+        for k in range(workloads.SWEEP_SEGMENTS):
+            x[k * seg:(k + 1) * seg] = workloads.sweep_segment(k, device="cuda").view(torch.uint8)
+        cb = codec.build_codebook(codec.histogram(x[: 64 << 20]), 24, _lib.HUFF_COVER_ALL)
+        res = {}
+        dst = torch.empty_like(x)
+        for chunk in (16 << 10, 64 << 10, 256 << 10, 1 << 20):
+            st = codec.encode(x, cb, chunk)
+            enc = _timed(lambda: codec.encode(x, cb, chunk), 2)
+            dec = _timed(lambda: codec.decode(st, cb, out=dst), 2)
+            C = st.nbytes()
+            res[str(chunk)] = {"encode_gbs": round(n / enc / 1e6, 1), "decode_gbs": round(n / dec / 1e6, 1),
+                               "decode_hbm_frac": round((C + n) / (dec / 1e3) / 1e9 / peak, 4),
+                               "ratio": round(n / C, 4)}
+            del st
+        out.update({"elements": n, "per_chunk_size": res})
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -602,6 +696,8 @@ def main():
     ap.add_argument("--small", action="store_true", help="same as --rows 4096 (a 250 MB snapshot)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the fp32 byte-plane and drift measurements")
+    ap.add_argument("--workload", choices=["snapshot", "per_shard", "fixed_codebook", "bf16_weights", "sweep"],
+                    default="snapshot", help="snapshot = the default benchmark line; the others print their own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=256 << 20, help="elements for the oracle baseline (about 10 s)")
     ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")
@@ -611,6 +707,9 @@ def main():
     ws, rank, local = dist_env()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.workload != "snapshot":
+        run_workload(args)
+        return
     if args.impl == "reference":
         dist = init_dist(ws, "gloo")
         run_reference(args, dist, rank, ws)
