@@ -314,7 +314,22 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
         bits = r16 ? 16u : (r8 ? 8u : bits);
         v = (r16 || r8) ? run : v;
     }
-    if (go && (c == 0 || static_cast<int>(c) > rem)) step_rare(T, win, s.bh, rem, c, bits, v, bad);
+    const bool simple = c != 0 && static_cast<int>(c) <= rem;
+    if (go && !simple) step_rare(T, win, s.bh, rem, c, bits, v, bad);
+    if (!RUN) {
+        // a second, dependent lookup on the bits after the first entry, taken when the first entry was
+        // simple (at least 20 valid bits remain) and the two entries together are at most 8 symbols
+        // within the chunk; otherwise those bits wait for the next step
+        const uint32_t top2 = __funnelshift_l(s.bl, s.bh, bits);
+        const uint64_t e2 = T.lut[top2 >> (32 - W)];
+        const uint32_t eh2 = static_cast<uint32_t>(e2 >> 32);
+        const uint32_t c2 = (eh2 >> 16) & 15u;
+        const bool take2 = simple && c2 != 0 && c + c2 <= static_cast<uint32_t>(kStepMax) &&
+                           static_cast<int>(c + c2) <= rem;
+        v |= take2 ? (e2 & 0xffffffffffffull) << (8 * c) : 0ull;
+        bits += take2 ? (eh2 >> 20) : 0u;
+        c += take2 ? c2 : 0u;
+    }
     c = go ? c : 0u;
     bits = go ? bits : 0u;
     v = go ? v : 0ull;
