@@ -203,10 +203,8 @@ struct Packer {
         w += full ? 1u : 0u;
     }
     // Two codes at once when together they are at most 31 bits.
-    __device__ __forceinline__ void push2(uint32_t ea, uint32_t eb) {
-        const uint32_t lb = eb & 31u;
-        const uint32_t L = (ea & 31u) + lb;
-        const uint32_t code = ((ea >> 8) << lb) | (eb >> 8);
+    __device__ __forceinline__ void push2(uint32_t ea, uint32_t eb, uint32_t L) {  // L = both lengths
+        const uint32_t code = ((ea >> 8) << (eb & 31u)) | (eb >> 8);
         hi = __funnelshift_l(lo, hi, L);
         lo = (lo << L) | code;
         nb += L;
@@ -338,7 +336,7 @@ __device__ __forceinline__ void read_tile(const uint8_t *stage, int tid, size_t 
 
 // (code << 8 | len) of this thread's symbols; symbols past the tile's end get 0.
 // mn ends at 0 when a valid symbol has no code.
-template <bool BF16, bool XOR>
+template <bool BF16, bool XOR, bool COUNT>
 __device__ __forceinline__ void lookup(const uint32_t *lut_r, const uint32_t (&wv)[8], bool full, int nvalid,
                                        uint32_t (&e0)[EncCfg<BF16, XOR>::kSyms],
                                        uint32_t (&e1)[BF16 ? EncCfg<BF16, XOR>::kSyms : 1], uint32_t &bits0,
@@ -356,13 +354,15 @@ __device__ __forceinline__ void lookup(const uint32_t *lut_r, const uint32_t (&w
                 mn = min(mn, min(hi, lo));
                 e0[k] = hi;
                 e1[BF16 ? k : 0] = lo;
-                bits0 += hi & 31u;
-                bits1 += lo & 31u;
+                if (COUNT) {
+                    bits0 += hi & 31u;
+                    bits1 += lo & 31u;
+                }
             } else {
                 const uint32_t v = lut_r[__byte_perm(wv[k >> 2], 0, 0x4440 + (k & 3)) * kLutRep];
                 mn = min(mn, v);
                 e0[k] = v;
-                bits0 += v & 31u;
+                if (COUNT) bits0 += v & 31u;
             }
         }
     } else {
@@ -376,15 +376,17 @@ __device__ __forceinline__ void lookup(const uint32_t *lut_r, const uint32_t (&w
                 else mn = min(mn, min(hi, lo));
                 e0[k] = hi;
                 e1[BF16 ? k : 0] = lo;
-                bits0 += hi & 31u;
-                bits1 += lo & 31u;
+                if (COUNT) {
+                    bits0 += hi & 31u;
+                    bits1 += lo & 31u;
+                }
             } else {
                 const uint32_t sym = (wv[k >> 2] >> (8 * (k & 3))) & 0xffu;
                 uint32_t v = lut_r[sym * kLutRep];
                 if (k >= nvalid) v = 0;
                 else mn = min(mn, v);
                 e0[k] = v;
-                bits0 += v & 31u;
+                if (COUNT) bits0 += v & 31u;
             }
         }
     }
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                                        ? 0
                                        : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
                 uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
-                lookup<BF16, XOR>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
+                lookup<BF16, XOR, true>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
                 if (nvalid > 0) mn_all = min(mn_all, mn);
                 cnt[k * kThreads + tid] = (b0 << 16) | b1;
                 sum0 += b0;
@@ -520,7 +522,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                                        ? 0
                                        : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
                 uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
-                lookup<BF16, XOR>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
+                lookup<BF16, XOR, false>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
+                // each pair's total length, once: the bit counts, the pair check and the packing use it
+                uint32_t L0[C::kSyms / 2], L1[BF16 ? C::kSyms / 2 : 1], longest_pair = 0;
+#pragma unroll
+                for (int j = 0; j < C::kSyms / 2; ++j) {
+                    L0[j] = (e0[2 * j] & 31u) + (e0[2 * j + 1] & 31u);
+                    b0 += L0[j];
+                    longest_pair = max(longest_pair, L0[j]);
+                    if (BF16) {
+                        L1[BF16 ? j : 0] = (e1[BF16 ? 2 * j : 0] & 31u) + (e1[BF16 ? 2 * j + 1 : 0] & 31u);
+                        b1 += L1[BF16 ? j : 0];
+                        longest_pair = max(longest_pair, L1[BF16 ? j : 0]);
+                    }
+                }
                 // block scan of the counts kept from pass 1
                 const uint32_t c = cnt[k * kThreads + tid];
                 const uint64_t mine = (static_cast<uint64_t>(c >> 16) << 32) | (c & 0xffffu);
@@ -551,12 +566,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                 if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
                 // pairs of codes at most 31 bits long go in one step; a warp with a longer pair
                 // anywhere packs its codes one by one
-                uint32_t longest_pair = 0;
-#pragma unroll
-                for (int j = 0; j < C::kSyms; j += 2) {
-                    longest_pair = max(longest_pair, (e0[j] & 31u) + (e0[j + 1] & 31u));
-                    if (BF16) longest_pair = max(longest_pair, (e1[BF16 ? j : 0] & 31u) + (e1[BF16 ? j + 1 : 0] & 31u));
-                }
                 if (__any_sync(0xffffffffu, longest_pair > 31u)) {
 #pragma unroll
                     for (int j = 0; j < C::kSyms; ++j) {
@@ -566,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
                 } else {
 #pragma unroll
                     for (int j = 0; j < C::kSyms; j += 2) {
-                        pk0.push2(e0[j], e0[j + 1]);
-                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0]);
+                        pk0.push2(e0[j], e0[j + 1], L0[j / 2]);
+                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0], L1[BF16 ? j / 2 : 0]);
                     }
                 }
                 pk0.finish();
@@ -816,7 +825,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *_
                                        ? 0
                                        : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
                 uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
-                lookup<BF16, XOR>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
+                lookup<BF16, XOR, false>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
+                // each pair's total length, once: the bit counts, the pair check and the packing use it
+                uint32_t L0[C::kSyms / 2], L1[BF16 ? C::kSyms / 2 : 1], longest_pair = 0;
+#pragma unroll
+                for (int j = 0; j < C::kSyms / 2; ++j) {
+                    L0[j] = (e0[2 * j] & 31u) + (e0[2 * j + 1] & 31u);
+                    b0 += L0[j];
+                    longest_pair = max(longest_pair, L0[j]);
+                    if (BF16) {
+                        L1[BF16 ? j : 0] = (e1[BF16 ? 2 * j : 0] & 31u) + (e1[BF16 ? 2 * j + 1 : 0] & 31u);
+                        b1 += L1[BF16 ? j : 0];
+                        longest_pair = max(longest_pair, L1[BF16 ? j : 0]);
+                    }
+                }
                 if (nvalid > 0) mn_all = min(mn_all, mn);
                 const uint64_t mine = (static_cast<uint64_t>(b0) << 32) | b1;
                 uint64_t incl = mine;
@@ -846,12 +868,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *_
                 if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
                 // pairs of codes at most 31 bits long go in one step; a warp with a longer pair
                 // anywhere packs its codes one by one
-                uint32_t longest_pair = 0;
-#pragma unroll
-                for (int j = 0; j < C::kSyms; j += 2) {
-                    longest_pair = max(longest_pair, (e0[j] & 31u) + (e0[j + 1] & 31u));
-                    if (BF16) longest_pair = max(longest_pair, (e1[BF16 ? j : 0] & 31u) + (e1[BF16 ? j + 1 : 0] & 31u));
-                }
                 if (__any_sync(0xffffffffu, longest_pair > 31u)) {
 #pragma unroll
                     for (int j = 0; j < C::kSyms; ++j) {
@@ -861,8 +877,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *_
                 } else {
 #pragma unroll
                     for (int j = 0; j < C::kSyms; j += 2) {
-                        pk0.push2(e0[j], e0[j + 1]);
-                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0]);
+                        pk0.push2(e0[j], e0[j + 1], L0[j / 2]);
+                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0], L1[BF16 ? j / 2 : 0]);
                     }
                 }
                 pk0.finish();
