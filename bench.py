@@ -115,36 +115,54 @@ def recorded_traffic(name: str, units: float):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms.
+
+    start() returns once the first sample has arrived, so that sampling is
+    already running when the timed region opens; begin()/end() bracket that
+    region on the host clock, and the summary keeps the samples taken inside
+    it (all samples only if none fell inside, which the summary says)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
         self.thread = None
+        self.first = threading.Event()
+        self.t_begin = None
+        self.t_end = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        self.first.wait(timeout=10.0)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+            self.first.set()
+
+    def begin(self):
+        self.t_begin = time.monotonic()
+
+    def end(self):
+        self.t_end = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return None
+        time.sleep(self.period_ms / 1000.0)  # one more sample after the region
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -152,24 +170,29 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for t, ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                rows.append((t, float(f[1]), float(f[2]), f[5:9]))
             except ValueError:
                 continue
-            for nm, v in zip(names, f[5:9]):
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t_begin is not None and self.t_end is not None
+                  and self.t_begin <= r[0] <= self.t_end]
+        window = "timed region" if inside else "around the timed region"
+        use = inside or rows
+        reasons = set()
+        for r in use:
+            for nm, v in zip(names, r[3]):
                 if v.lower() == "active":
                     reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "samples": len(use), "window": window, "period_ms": self.period_ms, "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ our arm
@@ -274,11 +297,13 @@ def run_ours(args, dist, rank, ws):
     clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    clocks.begin()
     t0.record()
     for k in range(args.steps):
         path.step_with_events(evs[k])
     t1.record()
     torch.cuda.synchronize()
+    clocks.end()
     barrier(dist)
     clk = clocks.stop()
     ms_local = t0.elapsed_time(t1) / args.steps
@@ -687,7 +712,7 @@ def run_workload(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk", type=int, default=16384)
