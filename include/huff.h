@@ -389,8 +389,9 @@ int lmc_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, 
 /*
  * lmc_encode_bf16_counted -- lmc_encode_bf16 from the per-segment counts of
  * the same w (and x0) written by lmc_histogram_bf16_counted.  Counts that do
- * not match the data give a wrong stream (the caller owns that contract);
- * a symbol without a code still sets HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK.
+ * not match the data give a wrong stream; when a segment's bits differ from
+ * the bits its counts give, status gets HUFF_ERR_INVALID_ARG.  A symbol
+ * without a code still sets HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK.
  *   ws          ws_bytes >= lmc_counted_workspace_size(n), 16-byte aligned.
  *   other arguments as in lmc_encode_bf16.
  */

@@ -721,222 +721,430 @@ __global__ void __launch_bounds__(1024) k_seg_scan(const uint64_t *__restrict__ 
     }
 }
 
-template <bool BF16, bool XOR>
-struct CountedCfg {
-    using C = EncCfg<BF16, XOR>;
-    static constexpr size_t kSmem = C::kMiscBytes + C::kRingBytes + C::kLutBytes + C::kBufBytes;
-};
+// One warp per segment.  With every segment's bit offset known before the
+// launch, a segment depends on no other segment and on no other warp, so a
+// warp encodes whole segments alone, tile after tile (512 elements, 16 per
+// lane), with its own bulk-copy ring and bit buffers: no block barrier on
+// the path.  Per tile:
+//   * lookups: the code table has a 256-byte row per byte value, holding 32
+//     (code, length) slots: slot 16 p + lane % 16 for plane p.  One byte
+//     permute makes the entry's address from an input byte and the lane's
+//     slot, and the 16 lanes of a half-warp always read 16 different bank
+//     pairs, whatever the symbols;
+//   * the codes of consecutive symbols are joined into groups of 2, 4 or 8
+//     while every group of the warp fits in 31 bits (one warp vote per plane
+//     and tile picks the largest such size); a group is appended as one code;
+//   * a warp scan of the lanes' bit counts gives each lane its start bit;
+//     each lane stores the words it completes, and after that ORs its last,
+//     partial word into the buffer.  The first word a lane completes holds
+//     zeros where earlier lanes' bits go; those lanes OR their last words
+//     into it afterwards.  The word the tile ends in is zeroed first, since
+//     no lane completes it;
+//   * complete words go out byte-swapped at the tile's global word; the word
+//     the tile ends in stays in a register and lane 0 of the next tile starts
+//     its bits behind it.
+namespace wenc {
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kLaneElems = 16;
+constexpr int kTile = 32 * kLaneElems;                                 // 512 elements
+constexpr uint32_t kTilesPerSeg = static_cast<uint32_t>(kDirSegElems / kTile);  // 256
+constexpr int kStages = 3;
+constexpr int kStageBytes = 2 * kTile * 2;                             // the tile of w, then of x0
+constexpr int kBufWords = 392;                                         // a tile's bits of one plane
+constexpr size_t kTableBytes = 256 * 256;
+constexpr size_t kRingBytes = size_t(kWarps) * kStages * kStageBytes;
+constexpr size_t kBufBytes = size_t(kWarps) * 2 * kBufWords * 4;
+constexpr size_t kBarBytes = size_t(kWarps) * kStages * 8;
+constexpr size_t kProdBytes = size_t(kWarps) * 32;                     // lane 0's copy-job cursor per warp
+constexpr size_t kSmem = kTableBytes + kRingBytes + kBufBytes + kBarBytes + kProdBytes;
+static_assert(kDirSegElems % kTile == 0, "segments of whole tiles");
+static_assert((kBufWords - 1) * 32 >= 31 + kTile * HUFF_MAX_LEN + 32 && kBufWords % 4 == 0,
+              "tile buffer, and a last slot no tile uses");
+static_assert(kSmem <= 227 * 1024, "one CTA per SM");
+static_assert(kProdBytes % 16 == 0, "cursor slots");
+}  // namespace wenc
 
-// Job q: tile q % kDirSegTiles of this CTA's segment number q / kDirSegTiles
-// (segments are dealt round robin over the grid).
-template <bool BF16, bool XOR>
-__device__ __forceinline__ void issue_counted_job(uint8_t *ring, Misc *ms, uint32_t q, uint32_t n_seg,
-                                                  uint32_t n_tiles, const uint8_t *in, const uint8_t *in2, size_t n) {
-    using C = EncCfg<BF16, XOR>;
-    const uint32_t seg = blockIdx.x + (q / kDirSegTiles) * gridDim.x;
-    if (seg >= n_seg) return;  // the consumers stop before this job
-    const int s = static_cast<int>(q % kStages);
-    const uint32_t t = seg * kDirSegTiles + q % kDirSegTiles;
-    uint32_t bytes = 0;
-    size_t first = 0;
-    if (t < n_tiles) {
-        first = static_cast<size_t>(t) * C::kTileSyms;
-        const size_t cnt = n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms);
-        bytes = static_cast<uint32_t>(cnt * (BF16 ? 2 : 1)) & ~15u;
-    }
-    mbar_arrive_expect_tx(&ms->full[s], bytes * C::kInputs);
-    if (bytes) {
-        const uint64_t pol = l2_policy_evict_first();
-        const size_t src = first * (BF16 ? 2 : 1);
-        uint8_t *dst = ring + size_t(s) * C::kInputs * C::kTileBytes;
-        bulk_g2s_hint(dst, in + src, bytes, &ms->full[s], pol);
-        if (XOR) bulk_g2s_hint(dst + C::kTileBytes, in2 + src, bytes, &ms->full[s], pol);
+// Table entry at byte address a (row = byte value, slot from the permute).
+__device__ __forceinline__ uint2 wtab(const uint8_t *tab, uint32_t a) {
+    return *reinterpret_cast<const uint2 *>(tab + a);
+}
+
+// Byte-permute selectors: byte 0 <- the lane's slot offset, byte 1 <- the
+// symbol byte (row), bytes 2-3 <- zero.  Element 2j of a lane is the low half
+// of its word j: high plane byte 1, low plane byte 0; element 2j+1 the high
+// half: bytes 3 and 2.
+constexpr uint32_t kSelHiA = 0x5514, kSelHiB = 0x5534, kSelLoA = 0x5504, kSelLoB = 0x5524;
+
+// (code, length) of each pair of a lane's symbols in both planes; symbols at
+// or past nvalid count as empty codes when RAGGED.
+template <bool RAGGED>
+__device__ __forceinline__ void wlookup(const uint8_t *tab, const uint32_t (&wv)[8], uint32_t kbh, uint32_t kbl,
+                                        int nvalid, uint32_t (&m)[2][8], uint32_t (&L)[2][8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint2 ha = wtab(tab, __byte_perm(wv[j], kbh, kSelHiA));
+        uint2 hb = wtab(tab, __byte_perm(wv[j], kbh, kSelHiB));
+        uint2 la = wtab(tab, __byte_perm(wv[j], kbl, kSelLoA));
+        uint2 lb = wtab(tab, __byte_perm(wv[j], kbl, kSelLoB));
+        if (RAGGED) {
+            if (2 * j >= nvalid) ha = la = make_uint2(0u, 0u);
+            if (2 * j + 1 >= nvalid) hb = lb = make_uint2(0u, 0u);
+        }
+        m[0][j] = (ha.x << hb.y) | hb.x;  // meaningful while the pair fits 32 bits
+        L[0][j] = ha.y + hb.y;
+        m[1][j] = (la.x << lb.y) | lb.x;
+        L[1][j] = la.y + lb.y;
     }
 }
 
-// One pass per tile: lookup, block scan, pack, shifted write-out; a segment
-// starts at the offset in its predecessor's descriptor.
-template <bool BF16, bool XOR>
-__global__ void __launch_bounds__(kThreads, 2) k_encode_counted(const uint8_t *__restrict__ in,
-                                                             const uint8_t *__restrict__ in2, size_t n, EncPlane p0,
-                                                             EncPlane p1, ChunkDiv cdiv, uint32_t n_tiles,
-                                                             uint32_t n_seg, int32_t *status) {
-    using C = EncCfg<BF16, XOR>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    Misc *ms = reinterpret_cast<Misc *>(smem);
-    uint8_t *ring = smem + C::kMiscBytes;
-    uint32_t *lut = reinterpret_cast<uint32_t *>(ring + C::kRingBytes);
-    uint32_t *bufs = lut + C::kPlanes * C::kLutWords;
+// A lane's bits of one plane in one tile.  Pending bits: the low nb bits of
+// hi:lo (nb < 32 between appends); append(code, len) takes len <= 31.
+struct WPacker {
+    uint32_t hi, lo, nb, w;
+    // A word that is not complete yet goes to the buffer's last slot, which no
+    // tile uses: a plain store instead of a branch.
+    __device__ __forceinline__ void append(uint32_t *buf, uint32_t code, uint32_t len) {
+        hi = __funnelshift_l(lo, hi, len);
+        lo = (lo << len) | code;
+        nb += len;
+        const bool full = nb >= 32;
+        nb &= 31u;
+        buf[full ? w : uint32_t(wenc::kBufWords - 1)] = __funnelshift_r(lo, hi, nb);
+        w += full ? 1u : 0u;
+    }
+    // The last, partial word (an OR of zero when there is none).
+    __device__ __forceinline__ void tail(uint32_t *buf) const {
+        atomicOr(&buf[w], nb ? lo << (32u - nb) : 0u);
+    }
+};
 
+// A lane's 16 elements (32 bytes, XOR x0 for the delta) straight from global
+// memory; bytes at or past tile_n elements read as zero.
+template <bool XOR>
+__device__ __forceinline__ void wload_global(const uint8_t *in, const uint8_t *in2, size_t first, int lane,
+                                             int tile_n, uint32_t (&wv)[8]) {
+    const size_t b0 = (first + static_cast<size_t>(lane) * wenc::kLaneElems) * 2;
+    if (tile_n == wenc::kTile) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(in + b0);
+        const uint4 c = *reinterpret_cast<const uint4 *>(in + b0 + 16);
+        wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+        wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+        if (XOR) {
+            const uint4 d = *reinterpret_cast<const uint4 *>(in2 + b0);
+            const uint4 e = *reinterpret_cast<const uint4 *>(in2 + b0 + 16);
+            wv[0] ^= d.x; wv[1] ^= d.y; wv[2] ^= d.z; wv[3] ^= d.w;
+            wv[4] ^= e.x; wv[5] ^= e.y; wv[6] ^= e.z; wv[7] ^= e.w;
+        }
+    } else {
+        const int tile_bytes = tile_n * 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wv[j] = 0;
+        for (int kk = 0; kk < 32; ++kk) {
+            const int bb = lane * 32 + kk;
+            if (bb >= tile_bytes) break;
+            uint32_t v = in[first * 2 + bb];
+            if (XOR) v ^= in2[first * 2 + bb];
+            wv[kk >> 2] |= v << (8 * (kk & 3));
+        }
+    }
+}
+
+// Appends a lane's 16 symbols of one plane in the largest group size that fits
+// 31 bits for every lane of the warp (warp-uniform branches).
+template <bool XOR>
+__device__ __forceinline__ void wpack(WPacker &pk, uint32_t *buf, const uint32_t (&m)[8], const uint32_t (&L)[8],
+                                      const uint8_t *tab, uint32_t kb, uint32_t sel_a, uint32_t sel_b,
+                                      const uint8_t *in, const uint8_t *in2, size_t first, int lane, int tile_n,
+                                      int nvalid) {
+    uint32_t Q[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) Q[q] = L[2 * q] + L[2 * q + 1];
+    const uint32_t O0 = Q[0] + Q[1], O1 = Q[2] + Q[3];
+    if (!__any_sync(0xffffffffu, max(O0, O1) > 31u)) {
+        uint32_t M4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) M4[q] = (m[2 * q] << L[2 * q + 1]) | m[2 * q + 1];
+        pk.append(buf, (M4[0] << Q[1]) | M4[1], O0);
+        pk.append(buf, (M4[2] << Q[3]) | M4[3], O1);
+    } else if (!__any_sync(0xffffffffu, max(max(Q[0], Q[1]), max(Q[2], Q[3])) > 31u)) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pk.append(buf, (m[2 * q] << L[2 * q + 1]) | m[2 * q + 1], Q[q]);
+    } else {
+        uint32_t lmax = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lmax = max(lmax, L[j]);
+        if (!__any_sync(0xffffffffu, lmax > 31u)) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pk.append(buf, m[j], L[j]);
+        } else {
+            // some pair is longer than 31 bits: one symbol at a time, read and looked up again
+            uint32_t wv[8];
+            wload_global<XOR>(in, in2, first, lane, tile_n, wv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint2 a = wtab(tab, __byte_perm(wv[j], kb, sel_a));
+                uint2 b = wtab(tab, __byte_perm(wv[j], kb, sel_b));
+                if (2 * j >= nvalid) a = make_uint2(0u, 0u);
+                if (2 * j + 1 >= nvalid) b = make_uint2(0u, 0u);
+                pk.append(buf, a.x, a.y);
+                pk.append(buf, b.x, b.y);
+            }
+        }
+    }
+}
+
+// Lane 0's copy jobs: this warp's tiles in order, into the ring stages in turn.
+struct WProducer {
+    uint32_t seg, left, stage, last_bytes;
+    size_t first;  // the next tile's first element
+    template <bool XOR>
+    __device__ __forceinline__ void issue(uint8_t *ring, uint64_t *bar, uint32_t nw, uint32_t n_seg, uint32_t n_tiles,
+                                          const uint8_t *in, const uint8_t *in2, uint64_t pol) {
+        if (seg >= n_seg) return;  // no tiles left: the consumer stops before this job
+        // every tile is whole but the input's last one
+        const uint32_t bytes = (left == 1 && seg == n_seg - 1) ? last_bytes : uint32_t(wenc::kTile * 2);
+        uint8_t *dst = ring + stage * wenc::kStageBytes;
+        mbar_arrive_expect_tx(&bar[stage], bytes * (XOR ? 2u : 1u));
+        if (bytes) {
+            bulk_g2s_hint(dst, in + first * 2, bytes, &bar[stage], pol);
+            if (XOR) bulk_g2s_hint(dst + wenc::kTile * 2, in2 + first * 2, bytes, &bar[stage], pol);
+        }
+        stage = stage + 1 == uint32_t(wenc::kStages) ? 0u : stage + 1;
+        first += wenc::kTile;
+        if (--left == 0) {
+            seg += nw;
+            first = static_cast<size_t>(seg) * kDirSegElems;
+            const uint32_t rest = n_tiles - seg * wenc::kTilesPerSeg;
+            left = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
+        }
+    }
+};
+
+// Complete words [skip, nfull) of a tile's buffer to dst (byte-swapped: the
+// stream is a byte sequence, most significant bit first).
+__device__ __forceinline__ void wwrite(uint32_t *dst, const uint32_t *buf, uint32_t skip, uint32_t nfull, int lane) {
+#pragma unroll 1
+    for (uint32_t i = skip + lane; i < nfull; i += 32) dst[i] = bswap32(buf[i]);
+}
+
+template <bool XOR>
+__global__ void __launch_bounds__(wenc::kThreads, 1)
+    k_encode_counted(const uint8_t *__restrict__ in, const uint8_t *__restrict__ in2, size_t n, EncPlane p0,
+                     EncPlane p1, ChunkDiv cdiv, uint32_t n_tiles, uint32_t n_seg, int32_t *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    const uint8_t *tab = smem;
+    uint8_t *ring = smem + wenc::kTableBytes + size_t(warp) * wenc::kStages * wenc::kStageBytes;
+    uint32_t *buf0 = reinterpret_cast<uint32_t *>(smem + wenc::kTableBytes + wenc::kRingBytes) + warp * 2 * wenc::kBufWords;
+    uint32_t *buf1 = buf0 + wenc::kBufWords;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + wenc::kTableBytes + wenc::kRingBytes + wenc::kBufBytes) + warp * wenc::kStages;
 
-    if (tid == 0) ms->bad_codebook = 0;
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < C::kPlanes; ++p) {
-        const huff_codebook *cb = p == 0 ? p0.cb : p1.cb;
-        const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
-        if (!ok && tid == 0) ms->bad_codebook = 1;
-        for (int i = tid; i < C::kLutWords; i += kThreads) {
-            const int s = i / kLutRep;
-            const uint32_t L = ok ? cb->len[s] : 0u;
-            lut[p * C::kLutWords + i] = (L >= 1 && L <= HUFF_MAX_LEN) ? ((cb->code[s] << 8) | L) : 0u;
-        }
+    // code table: row = byte value, slot = 16 plane + copy; entry (code, length), (0, 0) without a code
+    const bool ok0 = p0.cb->magic == HUFF_CODEBOOK_MAGIC, ok1 = p1.cb->magic == HUFF_CODEBOOK_MAGIC;
+    for (int i = tid; i < 256 * 32; i += wenc::kThreads) {
+        const int sym = i >> 5;
+        const bool lo_plane = (i & 31) >= 16;
+        const huff_codebook *cb = lo_plane ? p1.cb : p0.cb;
+        const uint32_t len = (lo_plane ? ok1 : ok0) ? cb->len[sym] : 0u;
+        const bool has = len >= 1 && len <= HUFF_MAX_LEN;
+        reinterpret_cast<uint2 *>(smem)[i] = make_uint2(has ? cb->code[sym] : 0u, has ? len : 0u);
     }
-    for (int i = tid; i < C::kPlanes * C::kBufWords; i += kThreads) bufs[i] = 0;
-    uint32_t issued = 0;  // next job to issue (thread 0 only)
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&ms->full[s], 1);
+    if (tid == 0 && !(ok0 && ok1)) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+    if (lane == 0) {
+        for (int s = 0; s < wenc::kStages; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
-        for (; issued < uint32_t(kStages); ++issued)
-            issue_counted_job<BF16, XOR>(ring, ms, issued, n_seg, n_tiles, in, in2, n);
     }
-    __syncthreads();
-    if (ms->bad_codebook && tid == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
-    const uint32_t *lut_r = lut + (lane & (kLutRep - 1));
-    uint32_t mn_all = 0xffffffffu;
+    __syncthreads();  // the table and the barriers are ready
+
+    const uint32_t nw = gridDim.x * wenc::kWarps;
+    const uint32_t gw = static_cast<uint32_t>(warp) * gridDim.x + blockIdx.x;  // round r: segment r nw + gw
+    const uint64_t pol = l2_policy_evict_first();
+    const uint32_t last_n = static_cast<uint32_t>(n - static_cast<size_t>(n_tiles - 1) * wenc::kTile);  // 1..512
+    // lane 0's copy-job cursor lives in shared memory: registers are the scarce resource here
+    WProducer *prod = reinterpret_cast<WProducer *>(smem + wenc::kTableBytes + wenc::kRingBytes + wenc::kBufBytes +
+                                                    wenc::kBarBytes) + warp;
+    if (lane == 0) {
+        WProducer pc;
+        pc.seg = gw;
+        pc.stage = 0;
+        pc.last_bytes = (last_n * 2) & ~15u;
+        pc.first = static_cast<size_t>(gw) * kDirSegElems;
+        pc.left = 0;
+        if (gw < n_seg) {
+            const uint32_t rest = n_tiles - gw * wenc::kTilesPerSeg;
+            pc.left = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
+        }
+        for (int s = 0; s < wenc::kStages; ++s) pc.issue<XOR>(ring, bar, nw, n_seg, n_tiles, in, in2, pol);
+        *prod = pc;
+    }
+    const uint32_t kbh = static_cast<uint32_t>(lane & 15) << 3;
+    const uint32_t kbl = kbh + 128u;
+    uint32_t cstage = 0, cphase = 0;
 
     for (uint32_t r = 0;; ++r) {
-        const uint32_t seg = blockIdx.x + r * gridDim.x;
+        const uint32_t seg = r * nw + gw;
         if (seg >= n_seg) break;
-        const uint32_t t_first = seg * kDirSegTiles;
-        const int seg_tiles =
-            static_cast<int>(n_tiles - t_first < uint32_t(kDirSegTiles) ? n_tiles - t_first : kDirSegTiles);
-        if (tid < C::kPlanes) {  // this segment's offset: the inclusive prefix of the one before
-            const EncPlane &P = tid == 0 ? p0 : p1;
-            ms->run[tid] = seg ? (P.desc[seg - 1] & kValueMask) : 0;
-            ms->carry[tid] = 0;
-            ms->seg_head[tid] = 0;
-        }
-        // (the first tile's barriers order these writes before their readers)
-        for (int k = 0; k < kDirSegTiles; ++k) {
-            const uint32_t q = r * kDirSegTiles + k;
-            const int s = static_cast<int>(q % kStages);
-            if (!mbar_wait(&ms->full[s], (q / kStages) & 1u) && tid == 0) set_status(status, HUFF_ERR_TIMEOUT);
-            if (k < seg_tiles) {
-                const uint32_t t = t_first + k;
-                const size_t first = static_cast<size_t>(t) * C::kTileSyms;
-                const int tile_n = static_cast<int>(n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms));
-                uint32_t wv[8];
-                read_tile<BF16, XOR>(ring + size_t(s) * C::kInputs * C::kTileBytes, tid, first, tile_n, in, in2, wv);
-                const int nvalid = tile_n - tid * C::kSyms < 0
-                                       ? 0
-                                       : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
-                uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
-                lookup<BF16, XOR, false>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
-                // each pair's total length, once: the bit counts, the pair check and the packing use it
-                uint32_t L0[C::kSyms / 2], L1[BF16 ? C::kSyms / 2 : 1], longest_pair = 0;
-#pragma unroll
-                for (int j = 0; j < C::kSyms / 2; ++j) {
-                    L0[j] = (e0[2 * j] & 31u) + (e0[2 * j + 1] & 31u);
-                    b0 += L0[j];
-                    longest_pair = max(longest_pair, L0[j]);
-                    if (BF16) {
-                        L1[BF16 ? j : 0] = (e1[BF16 ? 2 * j : 0] & 31u) + (e1[BF16 ? 2 * j + 1 : 0] & 31u);
-                        b1 += L1[BF16 ? j : 0];
-                        longest_pair = max(longest_pair, L1[BF16 ? j : 0]);
-                    }
+        const uint32_t t0 = seg * wenc::kTilesPerSeg;
+        const uint32_t tiles = n_tiles - t0 < wenc::kTilesPerSeg ? n_tiles - t0 : wenc::kTilesPerSeg;
+        // Bit positions inside the segment are 32-bit (a segment has at most 131072 * 24 bits): pos =
+        // the segment's phase in its first word + bits so far; word pos >> 5 of the segment is global
+        // word (start >> 5) + (pos >> 5).
+        const uint64_t start0 = seg ? (p0.desc[seg - 1] & kValueMask) : 0;
+        const uint64_t start1 = seg ? (p1.desc[seg - 1] & kValueMask) : 0;
+        uint32_t *const dst0 = p0.payload + (start0 >> 5);
+        uint32_t *const dst1 = p1.payload + (start1 >> 5);
+        // bits this segment may write before its plane's capacity ends
+        const uint64_t room0 = start0 >> 5 < p0.cap_words ? (p0.cap_words - (start0 >> 5)) * 32 : 0;
+        const uint64_t room1 = start1 >> 5 < p1.cap_words ? (p1.cap_words - (start1 >> 5)) * 32 : 0;
+        const uint32_t lim0 = room0 < 0xffffffffull ? static_cast<uint32_t>(room0) : 0xffffffffu;
+        const uint32_t lim1 = room1 < 0xffffffffull ? static_cast<uint32_t>(room1) : 0xffffffffu;
+        uint32_t pos0 = static_cast<uint32_t>(start0 & 31u), pos1 = static_cast<uint32_t>(start1 & 31u);
+        uint32_t carry0 = 0, carry1 = 0, head0 = 0, head1 = 0;
+        const size_t seg_first = static_cast<size_t>(t0) * wenc::kTile;
+        // the next chunk start: to_next elements ahead, chunk number next_q
+        const uint32_t cr = static_cast<uint32_t>(seg_first % cdiv.chunk);
+        uint64_t next_q = seg_first / cdiv.chunk + (cr ? 1u : 0u);
+        uint32_t to_next = cr ? cdiv.chunk - cr : 0u;
+        for (uint32_t k = 0; k < tiles; ++k) {
+            const int tile_n = t0 + k == n_tiles - 1 ? static_cast<int>(last_n) : wenc::kTile;
+            if (!mbar_wait(&bar[cstage], cphase) && lane == 0) set_status(status, HUFF_ERR_TIMEOUT);
+            const uint8_t *st = ring + cstage * wenc::kStageBytes;
+            uint32_t wv[8];
+            {
+                const uint4 a = *reinterpret_cast<const uint4 *>(st + lane * 32);
+                const uint4 c = *reinterpret_cast<const uint4 *>(st + lane * 32 + 16);
+                wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+                wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+                if (XOR) {
+                    const uint4 d = *reinterpret_cast<const uint4 *>(st + wenc::kTile * 2 + lane * 32);
+                    const uint4 e = *reinterpret_cast<const uint4 *>(st + wenc::kTile * 2 + lane * 32 + 16);
+                    wv[0] ^= d.x; wv[1] ^= d.y; wv[2] ^= d.z; wv[3] ^= d.w;
+                    wv[4] ^= e.x; wv[5] ^= e.y; wv[6] ^= e.z; wv[7] ^= e.w;
                 }
-                if (nvalid > 0) mn_all = min(mn_all, mn);
-                const uint64_t mine = (static_cast<uint64_t>(b0) << 32) | b1;
-                uint64_t incl = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                if (lane == 31) ms->warp_sum[warp] = incl;
-                if (tid == 0) chunk_position(ms, cdiv, first, k == 0, C::kTileSyms);
-                __syncthreads();  // stage s consumed; warp sums ready
-                if (tid == 0) issue_counted_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
-                uint64_t before = 0, total = 0;
-#pragma unroll
-                for (int w = 0; w < kThreads / 32; ++w) {
-                    const uint64_t ws = ms->warp_sum[w];
-                    before += w < warp ? ws : 0;
-                    total += ws;
-                }
-                const uint64_t excl = before + incl - mine;
-                const uint32_t excl0 = uint32_t(excl >> 32);
-                const uint32_t excl1 = uint32_t(excl);
-                const uint32_t tot0 = uint32_t(total >> 32);
-                const uint32_t tot1 = uint32_t(total);
-                Packer pk0, pk1;
-                pk0.begin(bufs, excl0);
-                if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
-                // pairs of codes at most 31 bits long go in one step; a warp with a longer pair
-                // anywhere packs its codes one by one
-                if (__any_sync(0xffffffffu, longest_pair > 31u)) {
-#pragma unroll
-                    for (int j = 0; j < C::kSyms; ++j) {
-                        pk0.push(e0[j]);
-                        if (BF16) pk1.push(e1[BF16 ? j : 0]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < C::kSyms; j += 2) {
-                        pk0.push2(e0[j], e0[j + 1], L0[j / 2]);
-                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0], L1[BF16 ? j / 2 : 0]);
-                    }
-                }
-                pk0.finish();
-                if (BF16) pk1.finish();
-                __syncthreads();  // buffers packed
-                uint64_t next_run = 0;  // thread 32 p: plane p's offset after this tile
-#pragma unroll
-                for (int p = 0; p < C::kPlanes; ++p) {
-                    const EncPlane &P = p == 0 ? p0 : p1;
-                    const uint32_t *buf = bufs + p * C::kBufWords;
-                    const uint64_t pre = ms->run[p];
-                    const uint32_t ph = static_cast<uint32_t>(pre & 31u);
-                    const uint64_t g0 = pre >> 5;
-                    const uint32_t tot = p == 0 ? tot0 : tot1;
-                    const uint32_t nfull = (ph + tot) >> 5;
-                    for (uint32_t i = (ph ? 1u : 0u) + tid; i < nfull; i += kThreads)
-                        put_word(P.payload, P.cap_words, g0 + i, shifted_word(buf, i, ph), status);
-                    const size_t g = first + size_t(tid) * C::kSyms;
-                    if (nvalid > 0) {
-                        const uint32_t d = ms->chunk_r + static_cast<uint32_t>(tid) * C::kSyms;
-                        const uint32_t kq = cdiv.div(d);
-                        if (kq * cdiv.chunk == d) P.off[ms->chunk_q + kq] = pre + (p == 0 ? excl0 : excl1);
-                    }
-                    if (tid == 32 * p) {
-                        const uint32_t head = ph ? shifted_word(buf, 0, ph) : 0u;
-                        uint32_t combined = head;
-                        if (ph) {
-                            if (k == 0) {
-                                ms->seg_head[p] = head;  // the segment's first word: the fix-up kernel's
-                            } else {
-                                combined |= ms->carry[p];
-                                if (nfull >= 1) put_word(P.payload, P.cap_words, g0, combined, status);
-                            }
-                        }
-                        uint32_t tail = 0;
-                        if ((ph + tot) & 31u) tail = nfull == 0 ? (ph ? combined : buf[0]) : shifted_word(buf, nfull, ph);
-                        ms->carry[p] = tail;  // read only by this thread
-                        next_run = pre + tot;
-                        if (k == seg_tiles - 1) P.edge[seg] = (static_cast<uint64_t>(ms->seg_head[p]) << 32) | tail;
-                    }
-                }
-                __syncthreads();  // everyone has read the buffers and the running offsets
-                if (tid == 0) ms->run[0] = next_run;
-                if (BF16 && tid == 32) ms->run[1] = next_run;
-#pragma unroll
-                for (int p = 0; p < C::kPlanes; ++p) {
-                    uint32_t *buf = bufs + p * C::kBufWords;
-                    const uint32_t used = ((p == 0 ? tot0 : tot1) + 31u) / 32u + 1u;
-                    for (uint32_t i = tid; i < used; i += kThreads) buf[i] = 0;
-                }
-            } else {
-                __syncthreads();  // stage s consumed (an empty job)
-                if (tid == 0) issue_counted_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
             }
+            const int nvalid = tile_n - lane * wenc::kLaneElems < 0
+                                   ? 0
+                                   : (tile_n - lane * wenc::kLaneElems > wenc::kLaneElems ? wenc::kLaneElems
+                                                                                          : tile_n - lane * wenc::kLaneElems);
+            if (tile_n < wenc::kTile) {
+                // the last tile: bytes past the bulk copy's 16-byte multiple come from global memory
+                const size_t first = seg_first + static_cast<size_t>(k) * wenc::kTile;
+                const int tile_bytes = tile_n * 2, tma_bytes = tile_bytes & ~15;
+                for (int kk = 0; kk < 32; ++kk) {
+                    const int bb = lane * 32 + kk;
+                    if (bb < tma_bytes) continue;
+                    uint32_t v = 0;
+                    if (bb < tile_bytes) {
+                        v = in[first * 2 + bb];
+                        if (XOR) v ^= in2[first * 2 + bb];
+                    }
+                    wv[kk >> 2] = (wv[kk >> 2] & ~(0xffu << (8 * (kk & 3)))) | (v << (8 * (kk & 3)));
+                }
+            }
+            __syncwarp();  // every lane has read the stage
+            if (lane == 0) {
+                WProducer pc = *prod;
+                pc.issue<XOR>(ring, bar, nw, n_seg, n_tiles, in, in2, pol);
+                *prod = pc;
+            }
+            cstage = cstage + 1 == uint32_t(wenc::kStages) ? 0u : cstage + 1;
+            cphase ^= cstage == 0 ? 1u : 0u;
+
+            uint32_t m[2][8], L[2][8];
+            if (tile_n == wenc::kTile)
+                wlookup<false>(tab, wv, kbh, kbl, wenc::kLaneElems, m, L);
+            else
+                wlookup<true>(tab, wv, kbh, kbl, nvalid, m, L);
+            uint32_t b0 = 0, b1 = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                b0 += L[0][j];
+                b1 += L[1][j];
+            }
+            // warp scan of (high plane bits << 16 | low plane bits): a lane has at most
+            // 16 * 24 bits per plane, a warp at most 12288
+            const uint32_t mine = (b0 << 16) | b1;
+            uint32_t incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            const uint32_t excl = incl - mine;
+            const uint32_t ex0 = excl >> 16, ex1 = excl & 0xffffu, tot0 = tot >> 16, tot1 = tot & 0xffffu;
+
+            // chunk starts in this tile (chunks are multiples of 256 elements, so a chunk starts
+            // at the first element of some lane)
+            if (to_next < wenc::kTile) {
+                do {
+                    if (static_cast<uint32_t>(lane) * wenc::kLaneElems == to_next && to_next < uint32_t(tile_n)) {
+                        p0.off[next_q] = start0 + (pos0 - (start0 & 31u)) + ex0;
+                        p1.off[next_q] = start1 + (pos1 - (start1 & 31u)) + ex1;
+                    }
+                    to_next += cdiv.chunk;
+                    ++next_q;
+                } while (to_next < wenc::kTile);
+            }
+            to_next -= wenc::kTile;
+
+            const uint32_t ph0 = pos0 & 31u, ph1 = pos1 & 31u;
+            const uint32_t end0 = ph0 + tot0, end1 = ph1 + tot1;
+            // the words the tile ends in: no lane completes them (all lanes store the same zero)
+            buf0[end0 >> 5] = 0;
+            buf1[end1 >> 5] = 0;
+            WPacker q0, q1;
+            {
+                const uint32_t s0 = ph0 + ex0, s1 = ph1 + ex1;
+                q0.hi = q1.hi = 0;
+                q0.nb = s0 & 31u;
+                q0.w = s0 >> 5;
+                q1.nb = s1 & 31u;
+                q1.w = s1 >> 5;
+                // lane 0 starts with the previous tile's bits of the word it starts in
+                q0.lo = lane == 0 ? __funnelshift_rc(carry0, 0u, 32u - ph0) : 0u;
+                q1.lo = lane == 0 ? __funnelshift_rc(carry1, 0u, 32u - ph1) : 0u;
+            }
+            {
+                const size_t first = seg_first + static_cast<size_t>(k) * wenc::kTile;
+                wpack<XOR>(q0, buf0, m[0], L[0], tab, kbh, kSelHiA, kSelHiB, in, in2, first, lane, tile_n, nvalid);
+                wpack<XOR>(q1, buf1, m[1], L[1], tab, kbl, kSelLoA, kSelLoB, in, in2, first, lane, tile_n, nvalid);
+            }
+            __syncwarp();  // whole words stored
+            q0.tail(buf0);
+            q1.tail(buf1);
+            __syncwarp();  // partial words ORed in
+            const uint32_t nf0 = end0 >> 5, nf1 = end1 >> 5;
+            // a segment's first word, when it starts inside one, is the fix-up kernel's to write
+            const uint32_t sk0 = (k == 0 && ph0) ? 1u : 0u, sk1 = (k == 0 && ph1) ? 1u : 0u;
+            if (pos0 + tot0 <= lim0 && pos1 + tot1 <= lim1) {
+                wwrite(dst0 + (pos0 >> 5), buf0, sk0, nf0, lane);
+                wwrite(dst1 + (pos1 >> 5), buf1, sk1, nf1, lane);
+            } else if (lane == 0) {
+                set_status(status, HUFF_ERR_BUFFER_TOO_SMALL);
+            }
+            if (k == 0) {
+                head0 = ph0 ? buf0[0] : 0u;
+                head1 = ph1 ? buf1[0] : 0u;
+            }
+            carry0 = buf0[nf0];  // zero when the tile ends on a word boundary
+            carry1 = buf1[nf1];
+            pos0 += tot0;
+            pos1 += tot1;
+            __syncwarp();  // buffers read before the next tile writes them
         }
-        __syncthreads();  // the segment's last offsets are read before the next segment resets them
+        if (lane == 0) {
+            p0.edge[seg] = (static_cast<uint64_t>(head0) << 32) | carry0;
+            p1.edge[seg] = (static_cast<uint64_t>(head1) << 32) | carry1;
+            // the bits written must be the bits the counts gave this segment
+            if (start0 - (start0 & 31u) + pos0 != (p0.desc[seg] & kValueMask) ||
+                start1 - (start1 & 31u) + pos1 != (p1.desc[seg] & kValueMask))
+                set_status(status, HUFF_ERR_INVALID_ARG);
+        }
     }
-    if (mn_all == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
 }
 
 // Boundary words: the word where segment t-1 ends and segment t begins holds
@@ -1090,23 +1298,19 @@ int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n
     const uint8_t *a = reinterpret_cast<const uint8_t *>(w16);
     const uint8_t *b = reinterpret_cast<const uint8_t *>(x0);
     const DevInfo d = dev_info();
-    auto run = [&](auto kern, size_t smem) -> int {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+    const size_t wtiles = (n + wenc::kTile - 1) / wenc::kTile;
+    auto run = [&](auto kern) -> int {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(wenc::kSmem)) !=
             cudaSuccess)
             return HUFF_ERR_CUDA;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
-            per_sm < 1)
-            return HUFF_ERR_CUDA;
-        size_t grid = static_cast<size_t>(d.sms) * per_sm;
+        // one CTA of 16 warps per SM; a warp takes whole segments, so fewer CTAs when there are few
+        size_t grid = static_cast<size_t>(d.sms);
         if (grid > segs) grid = segs;
-        kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, b, n, p0, p1, make_chunk_div(chunk),
-                                                               static_cast<uint32_t>(tiles),
-                                                               static_cast<uint32_t>(segs), status);
+        kern<<<static_cast<unsigned>(grid), wenc::kThreads, wenc::kSmem, s>>>(
+            a, b, n, p0, p1, make_chunk_div(chunk), static_cast<uint32_t>(wtiles), static_cast<uint32_t>(segs), status);
         return cudaGetLastError() == cudaSuccess ? HUFF_OK : HUFF_ERR_CUDA;
     };
-    int st = x0 != nullptr ? run(k_encode_counted<true, true>, CountedCfg<true, true>::kSmem)
-                           : run(k_encode_counted<true, false>, CountedCfg<true, false>::kSmem);
+    int st = x0 != nullptr ? run(k_encode_counted<true>) : run(k_encode_counted<false>);
     if (st != HUFF_OK) return st;
     const size_t n_chunks = (n + chunk - 1) / chunk;
     k_encode_fixup<<<static_cast<unsigned>((segs + 127) / 128), 128, 0, s>>>(p0, p1, 2, static_cast<uint32_t>(segs),

@@ -127,3 +127,62 @@ def test_counted_argument_errors():
     with pytest.raises(_lib.HuffError) as e:
         _lib.lmc_histogram_bf16_counted(w[:n], None, hh, hh, seg)
     assert e.value.status == _lib.HUFF_ERR_INVALID_ARG
+
+
+def _long_code_plane(n, rng):
+    """Bytes with geometric counts (code lengths up to about 19 bits) where the rarest
+    symbols sit next to each other, so some pairs of codes are longer than 31 bits."""
+    counts = [1 << (18 - k) for k in range(1, 13)]
+    vals = np.concatenate([np.full(c, k + 1, np.uint8) for k, c in enumerate(counts)])
+    vals = np.concatenate([vals, np.zeros(n - vals.size, np.uint8)])
+    rng.shuffle(vals)
+    pos = rng.choice(n // 2 - 1, 40, replace=False) * 2
+    vals[pos] = rng.integers(14, 20, 40)
+    vals[pos + 1] = rng.integers(14, 20, 40)
+    return vals
+
+
+def test_counted_long_code_pairs():
+    # pairs of codes longer than 31 bits make warps take the one-code-at-a-time path; ragged last tile
+    n = 3 * SEG + 1000
+    rng = np.random.default_rng(21)
+    hi_b, lo_b = _long_code_plane(n, rng), _long_code_plane(n, rng)
+    w = (hi_b.astype(np.uint16) << 8) | lo_b
+    x1 = torch.from_numpy(w.view(np.int16).copy()).view(torch.bfloat16)
+    hi, lo = oracle.bytegroup_split(w)
+    hh, hl, seg, cb_hi, cb_lo, s_hi, s_lo, st = _counted(x1.cuda(), None, 4096)
+    assert st == 0
+    for plane, cb, stream in ((hi, cb_hi, s_hi), (lo, cb_lo, s_lo)):
+        ln, cd = oracle_codebook(oracle.histogram(plane))
+        pair_len = ln[plane[: n // 2 * 2]].astype(np.int64).reshape(-1, 2).sum(1)
+        assert pair_len.max() > 31  # the case under test is present
+        np.testing.assert_array_equal(cb.lengths(), ln)
+        pay, off = oracle.encode(plane, ln, cd, 4096)
+        assert_stream_equal(stream, pay, off)
+    back = codec.decompress_bf16(codec.Bf16Streams(cb_hi, cb_lo, s_hi, s_lo, n), None)
+    assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
+
+
+def test_counted_counts_of_other_data_set_status():
+    # counts recorded for x, encode of x reversed (same symbols, other per-segment counts)
+    n = 4 * SEG
+    rng = np.random.default_rng(5)
+    x0, x1 = _pair(n, rng, sigma_noise=3e-3)
+    dx1 = x1.cuda()
+    w16 = dx1.view(torch.int16)
+    hh = torch.empty(256, dtype=torch.int64, device="cuda")
+    hl = torch.empty(256, dtype=torch.int64, device="cuda")
+    seg = torch.empty(_lib.lmc_segment_counts_size(n) // 4, dtype=torch.int32, device="cuda")
+    _lib.lmc_histogram_bf16_counted(w16, None, hh, hl, seg)
+    cb_hi, cb_lo = codec.build_codebook(hh), codec.build_codebook(hl)
+    other = torch.flip(w16, [0]).contiguous()
+    cap = _lib.huff_encode_bound(n, 24)
+    nc = _lib.huff_num_chunks(n, 4096)
+    p_hi = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    p_lo = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    o_hi = torch.empty(nc + 1, dtype=torch.int64, device="cuda")
+    o_lo = torch.empty(nc + 1, dtype=torch.int64, device="cuda")
+    ws = torch.empty(_lib.lmc_counted_workspace_size(n) // 8 + 2, dtype=torch.int64, device="cuda")
+    st = codec.new_status()
+    _lib.lmc_encode_bf16_counted(other, None, cb_hi.buf, cb_lo.buf, 4096, seg, p_hi, o_hi, p_lo, o_lo, ws, st)
+    assert int(st.item()) == _lib.HUFF_ERR_INVALID_ARG
