@@ -200,7 +200,7 @@ __device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecT
 // leave it.
 constexpr int kSeg = 32;       // symbols per lane per segment (multiple of 16)
 constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
-constexpr int kStepMax = 8;    // symbols a table step may add (a run step: twice that)
+constexpr int kStepMax = 8;    // symbols a table step may add (a run step: up to 32, within the ring's room)
 constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
 static_assert(kRing >= kSeg + 7 + 2 * kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
 static_assert(HUFF_LUT_SYMS <= kStepMax, "a table entry must fit one step");
@@ -228,9 +228,9 @@ struct PlaneDec {
             qi = 0;
         }
     }
-    __device__ __forceinline__ void consume(uint32_t bits) {  // bits < 32
-        bh = __funnelshift_l(bl, bh, bits);
-        bl <<= bits;
+    __device__ __forceinline__ void consume(uint32_t bits) {  // bits <= 32
+        bh = __funnelshift_lc(bl, bh, bits);
+        bl = __funnelshift_lc(0u, bl, bits);
         nb -= static_cast<int>(bits);
     }
     __device__ __forceinline__ void start(const uint8_t *p, size_t nbytes, uint64_t pos) {
@@ -288,18 +288,19 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
 }
 
 // One step: if the chunk has symbols left and the ring has room, one table
-// lookup (or, for a plane with a 1-bit code, a run of 16 or 8 of that code
-// when the next 16 or 8 bits are zero), then at most two 8-byte stores.
+// lookup, or, for a plane with a 1-bit code, a run of that code as long as
+// the zero bits on top of the window (up to 32, the chunk's rest and the
+// ring's room) when that beats a lookup; then up to four 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
 template <int RING, bool RUN, int W>
 __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
-    constexpr int kMax = RUN ? 2 * kStepMax : kStepMax;  // symbols one step may add
     // Predicated rather than branched: a lane with nothing to do (its chunk
     // is complete or its ring is full) takes a step of zero bits and zero
     // symbols, so the step stays one basic block.
     const int rem = cnt - s.st - s.fill;
-    const bool go = rem > 0 && s.st + s.fill + kMax <= limit;
+    const int room = limit - s.st - s.fill;
+    const bool go = rem > 0 && room >= kStepMax;
     s.refill(p, nbytes);
     const uint32_t win = s.bh >> (32 - W);
     const uint64_t e = T.lut[win];
@@ -307,12 +308,16 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     uint32_t c = (eh >> 16) & 15u;
     uint32_t bits = eh >> 20;
     uint64_t v = e & 0xffffffffffffull;
+    bool is_run = false;
     if (RUN) {
-        const bool r16 = s.bh < (1u << 16) && rem >= 16;
-        const bool r8 = s.bh < (1u << 24);
-        c = r16 ? 16u : (r8 ? 8u : c);
-        bits = r16 ? 16u : (r8 ? 8u : bits);
-        v = (r16 || r8) ? run : v;
+        // the 1-bit code is all zeros: clz(bh) symbols of it are next (bh holds >= 33 valid bits)
+        const int cr = min(min(static_cast<int>(__clz(s.bh)), rem), room);
+        // at least 8 (more than a lookup gives), so a run always completes the pending word and the
+        // first stored word takes run bytes in every position the pending bytes leave
+        is_run = cr >= kStepMax;
+        c = is_run ? static_cast<uint32_t>(cr) : c;
+        bits = is_run ? static_cast<uint32_t>(cr) : bits;
+        v = is_run ? run : v;
     }
     const bool simple = c != 0 && static_cast<int>(c) <= rem;
     if (go && !simple) step_rare(T, win, s.bh, rem, c, bits, v, bad);
@@ -339,11 +344,16 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     const int nf = f + static_cast<int>(c);
     const bool full = nf >= 8;
     if (full) *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = a;
-    if (RUN && nf >= 16) *reinterpret_cast<uint64_t *>(ring + (((s.st + 8) & (RING - 1)) ^ swz)) = run;
-    s.a0 = full ? (v >> 1) >> (63 - 8 * f) : a;  // the bytes that did not fit (all run bytes after a 16-run)
-    const int done = (RUN && nf >= 16) ? 16 : (full ? 8 : 0);
-    s.st += done;
-    s.fill = nf - done;
+    if (RUN) {
+        if (nf >= 16) *reinterpret_cast<uint64_t *>(ring + (((s.st + 8) & (RING - 1)) ^ swz)) = run;
+        if (nf >= 24) *reinterpret_cast<uint64_t *>(ring + (((s.st + 16) & (RING - 1)) ^ swz)) = run;
+        if (nf >= 32) *reinterpret_cast<uint64_t *>(ring + (((s.st + 24) & (RING - 1)) ^ swz)) = run;
+    }
+    // the bytes that did not fit: a lookup's last nf - 8 bytes, or nf % 8 run bytes
+    const int keep = (RUN && is_run) ? 8 * (nf & 7) : 8 * f;
+    s.a0 = full ? (v >> 1) >> (63 - keep) : a;
+    s.st += nf & ~7;
+    s.fill = nf & 7;
 }
 
 __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, size_t nbytes, uint64_t start, int cnt) {
@@ -523,7 +533,17 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
         fill_segment<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
         fill_segment<kRing>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
         __syncwarp();
-        // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane
+        // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane; the four passes'
+        // x0 loads are issued together, ahead of the shared-memory reads
+        uint4 xv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q = 8 * i + (lane >> 2);
+            const int e0 = seg0 + 8 * (lane & 3);
+            xv[i] = make_uint4(0, 0, 0, 0);
+            if (XOR && e0 + 8 <= __shfl_sync(0xffffffffu, cnt, q))
+                xv[i] = __ldcs(reinterpret_cast<const uint4 *>(x0 + (c0 + q) * chunk + e0));
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int q = 8 * i + (lane >> 2);  // source lane
@@ -538,13 +558,10 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
                                      __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
                 const size_t g = (c0 + q) * chunk + e0;  // first element of this group
                 if (e0 + 8 <= cs) {  // x0 and out are 16-byte aligned, chunk a multiple of 256
-                    if (XOR) {
-                        const uint4 xv = __ldcs(reinterpret_cast<const uint4 *>(x0 + g));
-                        v.x ^= xv.x;
-                        v.y ^= xv.y;
-                        v.z ^= xv.z;
-                        v.w ^= xv.w;
-                    }
+                    v.x ^= xv[i].x;
+                    v.y ^= xv[i].y;
+                    v.z ^= xv[i].z;
+                    v.w ^= xv[i].w;
                     __stcs(reinterpret_cast<uint4 *>(out + g), v);
                 } else {
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};

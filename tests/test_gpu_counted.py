@@ -186,3 +186,30 @@ def test_counted_counts_of_other_data_set_status():
     st = codec.new_status()
     _lib.lmc_encode_bf16_counted(other, None, cb_hi.buf, cb_lo.buf, 4096, seg, p_hi, o_hi, p_lo, o_lo, ws, st)
     assert int(st.item()) == _lib.HUFF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("run_byte", [0x00, 0x3C, 0xFF])
+def test_runs_of_a_nonzero_one_bit_symbol(run_byte):
+    # the high plane is mostly one byte value (a 1-bit code) in runs of every length; decode
+    # emits long runs of that code at once, whatever the byte is
+    n = 2 * SEG + 777
+    rng = np.random.default_rng(run_byte)
+    hi_b = np.full(n, run_byte, np.uint8)
+    breaks = rng.random(n) < rng.choice([0.01, 0.05, 0.2], n)
+    hi_b[breaks] = rng.integers(0, 256, int(breaks.sum()))
+    lo_b = rng.integers(0, 256, n).astype(np.uint8)
+    w = (hi_b.astype(np.uint16) << 8) | lo_b
+    x1 = torch.from_numpy(w.view(np.int16).copy()).view(torch.bfloat16)
+    hi, lo = oracle.bytegroup_split(w)
+    for chunk in (256, 4096):
+        hh, hl, seg, cb_hi, cb_lo, s_hi, s_lo, st = _counted(x1.cuda(), None, chunk)
+        assert st == 0
+        ln, cd = oracle_codebook(oracle.histogram(hi))
+        assert ln[run_byte] == 1
+        pay, off = oracle.encode(hi, ln, cd, chunk)
+        assert_stream_equal(s_hi, pay, off)
+        back = codec.decompress_bf16(codec.Bf16Streams(cb_hi, cb_lo, s_hi, s_lo, n), None)
+        assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
+        # the byte-stream decoder on the high plane alone
+        cb, s = codec.compress(torch.from_numpy(hi).cuda(), chunk)
+        assert torch.equal(codec.decode(s, cb).cpu(), torch.from_numpy(hi))
