@@ -7,22 +7,25 @@
 // encoder are those tasks' entry points.
 //
 // GPU design:
-//   * the codebook's 4096-entry first-level table sits in shared memory; an
-//     entry lists every code that lies wholly inside a 12-bit window (up to
-//     six symbols, their count and their total length), so short codes decode
-//     several symbols per lookup; codes longer than 12 bits take an
-//     out-of-line canonical search (first_code / bl_count);
-//   * the bit reader keeps 64 bits in a register, refills 32 at a time from a
-//     128-bit queue, and always has the next two 16-byte units of the stream
-//     in flight, so global-memory latency stays off the decode chain; reads
-//     never pass the payload's end;
-//   * byte streams: one thread per chunk, decoded bytes leave as 8-byte stores;
-//   * fused bf16: one thread per chunk pair decodes 64 symbols of each byte
-//     plane per segment into private shared-memory rows (one lookup per loop
-//     iteration, stores predicated, so the lanes of a warp stay in step),
-//     then merges them into 16-bit words, XORs x0 (loaded before the
-//     segment's decode, so its latency hides behind it) and stores 128 bytes;
-//     no barrier couples the threads.
+//   * one lane per chunk (per chunk pair for bf16), every lane of the grid
+//     resident at once; the block size follows the chunk count;
+//   * shared tables per plane: a window table of 2^W 64-bit entries (W = 12
+//     for the high plane, 13 for the low plane and byte streams), each
+//     listing the codes wholly inside the next W bits (up to six symbols,
+//     their count and total length), a secondary table for longer codes and
+//     the canonical arrays for a search when that table would not fit;
+//   * the bit reader keeps 64 bits in two registers and refills 32 at a time
+//     from a queue of the current 16-byte unit of the stream; reads never
+//     pass the payload's end;
+//   * a step is one predicated basic block: a table lookup plus a second,
+//     dependent one when both fit 8 symbols, or, on a plane with a 1-bit
+//     code, a run of that code as long as the zero bits on top of the window
+//     (up to 32);
+//   * decoded bytes go to per-lane shared rings in segments; the warp steps
+//     until every lane has its segment (a lane that is ahead decodes into
+//     the ring's free part), then merges 8 lanes' segments per pass into
+//     16-bit words, XORs x0 (prefetched to L2 before the segments' decode;
+//     a merge's four loads issued together) and stores 16 bytes per lane.
 // Every chunk must end exactly at the next chunk's offset, otherwise
 // HUFF_ERR_CORRUPT_STREAM is reported.
 #include "common.cuh"
@@ -146,10 +149,11 @@ __device__ __forceinline__ uint4 load_unit_tail(const uint8_t *p, size_t nbytes,
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Bit reader: 64 upcoming bits in (bh, bl), most significant first; the
-// current 16-byte unit of the stream (raw words, qi = next word) and the one
-// after it, in flight.  The payload pointer and size are passed to every
-// call that may load, so they stay kernel parameters rather than registers.
+// Bit reader: 64 upcoming bits in (bh, bl), most significant first, and the
+// words of the current 16-byte unit of the stream not taken yet (a queue: the
+// next word is always cur.x).  The payload pointer and size are passed to
+// every call that may load, so they stay kernel parameters rather than
+// registers.
 __device__ __forceinline__ uint4 load_unit(const uint8_t *p, size_t nbytes, size_t u) {
     if (u * 16 + 16 <= nbytes) {
         // a lane reads its chunk 16 bytes at a time over the whole kernel while x0 and the output
@@ -208,8 +212,8 @@ static_assert(HUFF_LUT_SYMS <= kStepMax, "a table entry must fit one step");
 struct PlaneDec {
     uint32_t bh, bl;  // upcoming bits, most significant first
     int nb;           // valid bits in (bh, bl); >= 33 after a refill
-    int qi;           // next word of cur
-    uint4 cur;        // current unit (raw little-endian words)
+    int qi;           // words of the current unit taken so far
+    uint4 cur;        // the current unit's words not taken yet, from cur.x on (raw little-endian)
     size_t ui;        // index of the unit after cur
     uint64_t a0;      // pending decoded bytes: byte k of the stream order is byte k of a0
     int fill;         // pending symbols, < 8 between steps
@@ -217,11 +221,16 @@ struct PlaneDec {
 
     __device__ __forceinline__ void refill(const uint8_t *p, size_t nbytes) {
         const bool rf = nb <= 32;
-        const uint32_t raw = (qi & 2) ? ((qi & 1) ? cur.w : cur.z) : ((qi & 1) ? cur.y : cur.x);
-        const uint32_t w = rf ? bswap32(raw) : 0u;
+        // cur.x is always the next word; a refill moves the queue down one word
+        const uint32_t w = rf ? bswap32(cur.x) : 0u;
         bh |= __funnelshift_rc(w, 0u, static_cast<uint32_t>(nb));       // w >> nb (0 when nb >= 32)
         bl |= __funnelshift_lc(0u, w, static_cast<uint32_t>(32 - nb));  // w << (32 - nb)
         nb += rf ? 32 : 0;
+        if (rf) {
+            cur.x = cur.y;
+            cur.y = cur.z;
+            cur.z = cur.w;
+        }
         qi += rf ? 1 : 0;
         if (qi == 4) {
             cur = load_unit(p, nbytes, ui++);
@@ -238,6 +247,11 @@ struct PlaneDec {
         cur = load_unit(p, nbytes, u);
         ui = u + 1;
         qi = static_cast<int>((pos >> 5) & 3u);
+        for (int k = 0; k < qi; ++k) {  // words of the unit before the start
+            cur.x = cur.y;
+            cur.y = cur.z;
+            cur.z = cur.w;
+        }
         bh = bl = 0;
         nb = 0;
         refill(p, nbytes);
