@@ -6,7 +6,7 @@ x1 = bf16(x0 + N(0, 1e-4)) of shape [65536, 30518] (2.0e9 elements, 4.0 GB
 each), resident in HBM.  One step is one pass of the whole path:
   lmc_histogram_bf16_counted(x1, x0)  XOR delta + byte planes + two histograms
                                       (+ per-segment counts)
-  huff_build_codebook x 2             lengths, canonical codes, decode tables
+  huff_build_codebooks (both planes)  lengths, canonical codes, decode tables
   lmc_encode_bf16_counted(x1, x0)     XOR delta + byte planes + one-pass encode of both planes
   lmc_decode_bf16(..., x0)        decode both planes, merge, XOR x0 back in
 value = snapshot bytes (2n) / step time: uncompressed GB/s of a full
@@ -209,10 +209,10 @@ class SnapshotPath:
         self.n = n = self.x1.numel()
         self.chunk = chunk
         self.max_len = max_len
-        self.h_hi = torch.zeros(256, dtype=torch.int64, device=dev)
-        self.h_lo = torch.zeros(256, dtype=torch.int64, device=dev)
-        self.cb_hi = codec.Codebook(dev)
-        self.cb_lo = codec.Codebook(dev)
+        self.hists = torch.zeros((2, 256), dtype=torch.int64, device=dev)  # high plane, low plane
+        self.h_hi, self.h_lo = self.hists[0], self.hists[1]
+        self.cbs = torch.zeros((2, _lib.huff_codebook_size()), dtype=torch.uint8, device=dev)
+        self.cb_hi, self.cb_lo = codec.Codebook(buf=self.cbs[0]), codec.Codebook(buf=self.cbs[1])
         cap = _lib.huff_encode_bound(n, max_len)
         self.p_hi = torch.empty(cap, dtype=torch.uint8, device=dev)
         self.p_lo = torch.empty(cap, dtype=torch.uint8, device=dev)
@@ -224,17 +224,16 @@ class SnapshotPath:
         self.ws_counted = torch.empty(_lib.lmc_counted_workspace_size(n) // 8 + 2, dtype=torch.int64, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty(n, dtype=torch.int16, device=dev)
-        # kernels launched per step: hist (2 zero + 1), build (2), encode (segment bits + scan + main + fix-up),
-        # decode (1)
-        self.launches_per_step = 10
+        # kernels launched per step: hist (1 zero of both adjacent histograms + 1), build (1 for both planes),
+        # encode (segment bits + scan + main + fix-up), decode (1)
+        self.launches_per_step = 8
 
     def compress(self, w=None, x0=None):
         L = self.L
         w = self.x1 if w is None else w
         x0 = self.x0 if x0 is None else x0
         L.lmc_histogram_bf16_counted(w, x0, self.h_hi, self.h_lo, self.seg)
-        L.huff_build_codebook(self.h_hi, self.cb_hi.buf, self.status, self.max_len, 0)
-        L.huff_build_codebook(self.h_lo, self.cb_lo.buf, self.status, self.max_len, 0)
+        L.huff_build_codebooks(self.hists, self.cbs, self.status, self.max_len, 0)
         L.lmc_encode_bf16_counted(w, x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.seg, self.p_hi, self.o_hi,
                                   self.p_lo, self.o_lo, self.ws_counted, self.status)
 
@@ -249,8 +248,7 @@ class SnapshotPath:
         ev[0].record()
         L.lmc_histogram_bf16_counted(self.x1, self.x0, self.h_hi, self.h_lo, self.seg)
         ev[1].record()
-        L.huff_build_codebook(self.h_hi, self.cb_hi.buf, self.status, self.max_len, 0)
-        L.huff_build_codebook(self.h_lo, self.cb_lo.buf, self.status, self.max_len, 0)
+        L.huff_build_codebooks(self.hists, self.cbs, self.status, self.max_len, 0)
         ev[2].record()
         L.lmc_encode_bf16_counted(self.x1, self.x0, self.cb_hi.buf, self.cb_lo.buf, self.chunk, self.seg, self.p_hi,
                                   self.o_hi, self.p_lo, self.o_lo, self.ws_counted, self.status)
@@ -542,7 +540,7 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
     del d_x1, d_x0
     return {"value": round(total / ms / 1e6, 2), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "api": "lmc_histogram_bf16_counted, huff_build_codebook, lmc_encode_bf16_counted, lmc_decode_bf16 with pinned host "
+            "api": "lmc_histogram_bf16_counted, huff_build_codebooks, lmc_encode_bf16_counted, lmc_decode_bf16 with pinned host "
                    "inputs, streams copied to host and back"}
 
 

@@ -176,6 +176,18 @@ int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags,
                         huff_codebook *cb, int32_t *status, huff_stream_t stream);
 
 /*
+ * huff_build_codebooks -- huff_build_codebook for `count` histograms in one
+ * launch (one thread block each): cbs[k] from hists[256 k .. 256 k + 255].
+ * Used for the two byte planes of a bf16 tensor.
+ *   hists     uint64[count * 256], device, 8-byte aligned.
+ *   count     0..65535 (0: nothing is enqueued).
+ *   cbs       huff_codebook[count], device, 16-byte aligned, contiguous.
+ *   other arguments and status as in huff_build_codebook (status is shared).
+ */
+int huff_build_codebooks(const uint64_t *hists, size_t count, int max_len, unsigned flags,
+                         huff_codebook *cbs, int32_t *status, huff_stream_t stream);
+
+/*
  * Drift-adaptive refresh of a fixed codebook.  P1 builds its codebook once
  * from warm-up statistics and names distribution drift as the limitation of
  * that scheme, with adaptive codebooks as future work.  For a shard about to

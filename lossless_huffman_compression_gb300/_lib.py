@@ -42,7 +42,7 @@ EXPORTS = (
     "huff_decode", "huff_encode_noalloc", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
     "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
-    "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if",
+    "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if", "huff_build_codebooks",
 )
 
 
@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH):
         "huff_num_chunks": (S, [S, S]),
         "huff_histogram": (I, [P, S, S, P, I, P]),
         "huff_build_codebook": (I, [P, I, ctypes.c_uint, P, P, P]),
+        "huff_build_codebooks": (I, [P, S, I, ctypes.c_uint, P, P, P]),
         "huff_codebook_from_lengths": (I, [P, I, P, P, P]),
         "huff_encode": (I, [P, S, P, S, P, S, P, P, S, P, P]),
         "huff_decode": (I, [P, S, P, S, S, P, P, P, P]),
@@ -194,6 +195,18 @@ def huff_build_codebook(hist: torch.Tensor, cb: torch.Tensor, status: torch.Tens
     _check("huff_build_codebook", load().huff_build_codebook(_dev(hist, "hist"), max_len, flags, _dev(cb, "cb"),
                                                              _dev(status, "status"), _stream(stream)))
     return cb
+
+
+def huff_build_codebooks(hists: torch.Tensor, cbs: torch.Tensor, status: torch.Tensor, max_len: int = HUFF_MAX_LEN,
+                         flags: int = 0, stream=None) -> torch.Tensor:
+    """hists: int64 [count, 256]; cbs: uint8 [count, huff_codebook_size()], contiguous."""
+    count = hists.numel() // 256
+    if hists.numel() != 256 * count or cbs.numel() != count * huff_codebook_size():
+        raise ValueError("hists must be [count, 256] and cbs [count, codebook size]")
+    _check("huff_build_codebooks", load().huff_build_codebooks(_dev(hists, "hists"), count, max_len, flags,
+                                                               _dev(cbs, "cbs"), _dev(status, "status"),
+                                                               _stream(stream)))
+    return cbs
 
 
 def huff_codebook_from_lengths(lengths, cb: torch.Tensor, status: torch.Tensor, max_len: int = HUFF_MAX_LEN,

@@ -25,7 +25,10 @@ DEFAULT_CHUNK = 16384
 class Codebook:
     """A device-resident huff_codebook."""
 
-    def __init__(self, device=None):
+    def __init__(self, device=None, buf: torch.Tensor | None = None):
+        if buf is not None:  # a row of a [count, size] block built by build_codebooks
+            self.buf = buf
+            return
         device = torch.device("cuda") if device is None else torch.device(device)
         self.buf = torch.zeros(_lib.huff_codebook_size(), dtype=torch.uint8, device=device)
 
@@ -85,6 +88,18 @@ def build_codebook(hist: torch.Tensor, max_len: int = 24, flags: int = 0, cb: Co
     if status is None:
         raise_on_status(st, "huff_build_codebook")
     return cb
+
+
+def build_codebooks(hists: torch.Tensor, max_len: int = 24, flags: int = 0,
+                    status: torch.Tensor | None = None) -> list[Codebook]:
+    """One codebook per row of hists ([count, 256]), built in one launch."""
+    count = hists.shape[0]
+    bufs = torch.zeros((count, _lib.huff_codebook_size()), dtype=torch.uint8, device=hists.device)
+    st = status if status is not None else new_status(hists.device)
+    _lib.huff_build_codebooks(hists, bufs, st, max_len, flags)
+    if status is None:
+        raise_on_status(st, "huff_build_codebooks")
+    return [Codebook(buf=bufs[k]) for k in range(count)]
 
 
 def codebook_from_lengths(lengths, max_len: int = 24, device=None) -> Codebook:
@@ -151,14 +166,13 @@ def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: 
     o_lo = torch.empty(nc + 1, dtype=torch.int64, device=dev)
     if cb_hi is None or cb_lo is None:
         # per-shard: the histogram pass records per-segment counts, so the encode makes one pass
-        h_hi = torch.empty(256, dtype=torch.int64, device=dev)
-        h_lo = torch.empty(256, dtype=torch.int64, device=dev)
+        hists = torch.empty((2, 256), dtype=torch.int64, device=dev)
+        h_hi, h_lo = hists[0], hists[1]
         seg = torch.empty(max(_lib.lmc_segment_counts_size(n), 4) // 4, dtype=torch.int32, device=dev)
         _lib.lmc_histogram_bf16_counted(w16, x16, h_hi, h_lo, seg)
         st = new_status(dev)
-        cb_hi = build_codebook(h_hi, max_len, flags, status=st)
-        cb_lo = build_codebook(h_lo, max_len, flags, status=st)
-        raise_on_status(st, "huff_build_codebook")
+        cb_hi, cb_lo = build_codebooks(hists, max_len, flags, status=st)
+        raise_on_status(st, "huff_build_codebooks")
         ws = torch.empty(max(_lib.lmc_counted_workspace_size(n), 16) // 8, dtype=torch.int64, device=dev)
         st = new_status(dev)
         _lib.lmc_encode_bf16_counted(w16, x16, cb_hi.buf, cb_lo.buf, chunk_bytes, seg, p_hi, o_hi, p_lo, o_lo, ws,

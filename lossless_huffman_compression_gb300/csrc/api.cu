@@ -18,6 +18,7 @@ static_assert(offsetof(huff_codebook, len) == 16 && offsetof(huff_codebook, code
 static_assert(sizeof(huff_codebook) % 16 == 0, "codebook size");
 
 constexpr size_t kMaxN = size_t(1) << 40;  // 1 Ti symbols: bit offsets stay far below 2^62
+constexpr size_t kMaxCodebooks = 65535;     // one CTA per codebook in one launch
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline cudaStream_t cs(huff_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -85,6 +86,16 @@ int huff_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_
         max_len < HUFF_MIN_MAX_LEN || max_len > HUFF_MAX_LEN || (flags & ~HUFF_COVER_ALL) != 0)
         return HUFF_ERR_INVALID_ARG;
     return launch_build_codebook(hist, max_len, flags, cb, status, nullptr, cs(stream));
+}
+
+int huff_build_codebooks(const uint64_t *hists, size_t count, int max_len, unsigned flags, huff_codebook *cbs,
+                         int32_t *status, huff_stream_t stream) {
+    if (count == 0) return HUFF_OK;
+    if (hists == nullptr || cbs == nullptr || status == nullptr || !aligned(cbs, 16) || !aligned(hists, 8) ||
+        count > kMaxCodebooks || max_len < HUFF_MIN_MAX_LEN || max_len > HUFF_MAX_LEN ||
+        (flags & ~HUFF_COVER_ALL) != 0)
+        return HUFF_ERR_INVALID_ARG;
+    return launch_build_codebooks(hists, count, max_len, flags, cbs, status, nullptr, cs(stream));
 }
 
 int huff_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag, double *gap,
@@ -237,8 +248,10 @@ int lmc_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, 
                   (x0 != nullptr && !aligned(x0, HUFF_ALIGN)) || !aligned(seg_counts, 4)))
         return HUFF_ERR_INVALID_ARG;
     if (n > 0 && seg_counts_bytes < lmc_segment_counts_size(n)) return HUFF_ERR_BUFFER_TOO_SMALL;
-    int st = launch_zero_u64(hist_hi, 256, cs(stream));
-    if (st == HUFF_OK) st = launch_zero_u64(hist_lo, 256, cs(stream));
+    // both histograms zeroed by one launch when they are adjacent
+    const bool adjacent = hist_lo == hist_hi + 256;
+    int st = launch_zero_u64(hist_hi, adjacent ? 512 : 256, cs(stream));
+    if (st == HUFF_OK && !adjacent) st = launch_zero_u64(hist_lo, 256, cs(stream));
     if (st != HUFF_OK || n == 0) return st;
     return launch_histogram_bf16_counted(w, x0, n, hist_hi, hist_lo, seg_counts, cs(stream));
 }

@@ -92,23 +92,34 @@ __device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook 
     cb->sorted_symbols[t] = srt[t];
     // first-level decode table: entry i lists the codes that lie wholly inside the 12-bit window i,
     // greedily from its first bit, at most HUFF_LUT_SYMS: symbols (8 bits each, first in the low
-    // byte), their count << 48 and their total length << 52; 0 when the first code is longer than 12 bits
+    // byte), their count << 48 and their total length << 52; 0 when the first code is longer than 12 bits.
+    // Built in two passes: first the code that starts each window (its symbol and length, 0 when it
+    // is longer than 12 bits), then each entry as a chain through that table: after pos bits, the
+    // window shifted left by pos (zeros behind) starts with the next code exactly when that code's
+    // length is at most 12 - pos, since then all its bits are real bits of the window.
+    __shared__ uint16_t first_code_of[1 << HUFF_LUT_BITS];  // symbol | length << 8
+    for (int i = t; i < (1 << HUFF_LUT_BITS); i += kT) {
+        uint32_t e = 0;
+        for (uint32_t l = 1; l <= HUFF_LUT_BITS; ++l) {
+            const uint32_t c = static_cast<uint32_t>(i) >> (HUFF_LUT_BITS - l);
+            if (blc[l] > 0 && c >= fc[l] && c - fc[l] < blc[l]) {
+                e = srt[fi[l] + (c - fc[l])] | (l << 8);
+                break;
+            }
+        }
+        first_code_of[i] = static_cast<uint16_t>(e);
+    }
+    __syncthreads();
     for (int i = t; i < (1 << HUFF_LUT_BITS); i += kT) {
         uint64_t syms = 0;
         uint32_t count = 0, pos = 0;
         while (count < HUFF_LUT_SYMS) {
-            bool found = false;
-            for (uint32_t l = 1; l + pos <= HUFF_LUT_BITS; ++l) {
-                const uint32_t c = (static_cast<uint32_t>(i) >> (HUFF_LUT_BITS - pos - l)) & ((1u << l) - 1u);
-                if (blc[l] > 0 && c >= fc[l] && c - fc[l] < blc[l]) {
-                    syms |= static_cast<uint64_t>(srt[fi[l] + (c - fc[l])]) << (8 * count);
-                    ++count;
-                    pos += l;
-                    found = true;
-                    break;
-                }
-            }
-            if (!found) break;
+            const uint32_t e = first_code_of[(static_cast<uint32_t>(i) << pos) & ((1u << HUFF_LUT_BITS) - 1u)];
+            const uint32_t l = e >> 8;
+            if (l == 0 || l + pos > HUFF_LUT_BITS) break;
+            syms |= static_cast<uint64_t>(e & 0xffu) << (8 * count);
+            ++count;
+            pos += l;
         }
         cb->lut[i] = count ? (syms | (static_cast<uint64_t>(count) << 48) | (static_cast<uint64_t>(pos) << 52)) : 0ull;
     }
@@ -122,10 +133,13 @@ __device__ void finish_codebook(const uint8_t *lens, int max_len, huff_codebook 
     }
 }
 
-__global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restrict__ hist, int max_len,
-                                                       unsigned flags, huff_codebook *__restrict__ cb,
+// One CTA per codebook: CTA b builds cbs[b] from hists[256 b .. 256 b + 255].
+__global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restrict__ hists, int max_len,
+                                                       unsigned flags, huff_codebook *__restrict__ cbs,
                                                        int32_t *status, const uint32_t *__restrict__ when) {
     if (when != nullptr && *when == 0) return;  // conditional rebuild: the codebook stays as it is
+    const uint64_t *hist = hists + 256 * static_cast<size_t>(blockIdx.x);
+    huff_codebook *cb = cbs + blockIdx.x;
     __shared__ uint64_t cnt[256];
     __shared__ uint64_t leaf_cnt[256];
     __shared__ uint64_t int_cnt[256];
@@ -140,6 +154,7 @@ __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restric
     uint64_t c = hist[t];
     if ((flags & HUFF_COVER_ALL) && c == 0) c = 1;
     cnt[t] = c;
+    int_cnt[t] = 0;
     bl[t] = 0;
     if (t < 4) bl[256 + t] = 0;
     lens[t] = 0;
@@ -160,15 +175,21 @@ __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restric
             leaf_cnt[r] = c;
         }
         __syncthreads();
-        if (t == 0) {
-            // the counts must sum below 2^63 so that no node count can overflow
-            uint64_t total = 0;
-            for (int u = 0; u < 256; ++u) {
-                const uint64_t nt = total + cnt[u];
-                if (nt < total || nt >= (1ull << 63)) s_fail = 1;
-                total = nt;
+        {
+            // the counts must sum below 2^63 so that no node count can overflow: sum the high and
+            // low 32-bit halves separately (no overflow in either), then compare
+            uint64_t h = c >> 32, l = c & 0xffffffffull;
+            for (int o = 16; o > 0; o >>= 1) {
+                h += __shfl_xor_sync(0xffffffffu, h, o);
+                l += __shfl_xor_sync(0xffffffffu, l, o);
+            }
+            if ((t & 31) == 0) {
+                atomicAdd(reinterpret_cast<unsigned long long *>(&int_cnt[0]), static_cast<unsigned long long>(h));
+                atomicAdd(reinterpret_cast<unsigned long long *>(&int_cnt[1]), static_cast<unsigned long long>(l));
             }
         }
+        __syncthreads();
+        if (t == 0 && int_cnt[0] + (int_cnt[1] >> 32) >= (1ull << 31)) s_fail = 1;
         __syncthreads();
         if (s_fail) {
             if (t == 0) {
@@ -194,11 +215,37 @@ __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restric
                 }
                 int_cnt[k] = sum;
             }
-            // depths of new nodes: the root is the last one; parents come after children
-            int_depth[m - 2] = 0;
-            for (int k = m - 3; k >= 0; --k) int_depth[k] = int_depth[int_parent[k]] + 1;
         }
         __syncthreads();
+        {
+            // depths of new nodes by pointer jumping: the root is node m - 2 (its own ancestor, depth 0);
+            // after round r a node's depth counts its first 2^r ancestors and anc skips to the next ones
+            __shared__ uint16_t anc[256];
+            const int k = t;
+            uint32_t dk = 0, ak = 0;
+            if (k < m - 1) {
+                ak = k == m - 2 ? static_cast<uint32_t>(k) : int_parent[k];
+                dk = k == m - 2 ? 0u : 1u;
+                int_depth[k] = static_cast<uint16_t>(dk);
+                anc[k] = static_cast<uint16_t>(ak);
+            }
+            __syncthreads();
+            for (int r = 0; r < 8; ++r) {  // 2^8 >= 255 ancestors
+                uint32_t nd = dk, na = ak;
+                if (k < m - 1) {
+                    nd = dk + int_depth[ak];
+                    na = anc[ak];
+                }
+                __syncthreads();
+                if (k < m - 1) {
+                    dk = nd;
+                    ak = na;
+                    int_depth[k] = static_cast<uint16_t>(dk);
+                    anc[k] = static_cast<uint16_t>(ak);
+                }
+                __syncthreads();
+            }
+        }
         if (t < m) {
             const int d = int_depth[leaf_parent[t]] + 1;
             atomicAdd(&bl[d], 1u);
@@ -337,7 +384,13 @@ __global__ void __launch_bounds__(kT) k_codebook_from_lengths(int max_len, huff_
 
 int launch_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_codebook *cb,
                           int32_t *status, const uint32_t *when, cudaStream_t s) {
-    k_build_codebook<<<1, kT, 0, s>>>(hist, max_len, flags, cb, status, when);
+    return launch_build_codebooks(hist, 1, max_len, flags, cb, status, when, s);
+}
+
+int launch_build_codebooks(const uint64_t *hists, size_t count, int max_len, unsigned flags, huff_codebook *cbs,
+                           int32_t *status, const uint32_t *when, cudaStream_t s) {
+    if (count == 0) return HUFF_OK;
+    k_build_codebook<<<static_cast<unsigned>(count), kT, 0, s>>>(hists, max_len, flags, cbs, status, when);
     return launch_status();
 }
 

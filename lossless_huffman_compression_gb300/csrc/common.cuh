@@ -167,6 +167,8 @@ int launch_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint6
                           uint64_t *hist_lo, cudaStream_t s);
 int launch_build_codebook(const uint64_t *hist, int max_len, unsigned flags, huff_codebook *cb,
                           int32_t *status, const uint32_t *when, cudaStream_t s);
+int launch_build_codebooks(const uint64_t *hists, size_t count, int max_len, unsigned flags, huff_codebook *cbs,
+                           int32_t *status, const uint32_t *when, cudaStream_t s);
 int launch_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag,
                        double *gap, cudaStream_t s);
 int launch_codebook_from_lengths(int max_len, huff_codebook *cb, int32_t *status, cudaStream_t s);

@@ -362,3 +362,32 @@ def test_fused_bf16_specials_round_trip():
     s = codec.compress_bf16(vals.cuda(), x0.cuda(), 256)
     back = codec.decompress_bf16(s, x0.cuda())
     assert torch.equal(back.view(torch.int16).cpu(), vals.view(torch.int16))
+
+
+def test_build_codebooks_batch_equals_single_builds():
+    rng = np.random.default_rng(17)
+    hists = []
+    for k in range(5):
+        h = rng.integers(0, 1000, 256).astype(np.int64)
+        h[rng.random(256) < 0.3 * k / 4] = 0  # some symbols absent
+        hists.append(h)
+    hists[3][:] = 0
+    hists[3][7] = 5  # one symbol
+    hists[4][:] = 0  # empty
+    H = torch.from_numpy(np.stack(hists)).cuda()
+    cbs = codec.build_codebooks(H, 24, 0)
+    for k in range(5):
+        one = codec.build_codebook(H[k].clone(), 24, 0)
+        assert torch.equal(cbs[k].buf, one.buf)
+        np.testing.assert_array_equal(cbs[k].lengths(), oracle.code_lengths(hists[k].astype(np.uint64), 24))
+
+
+def test_build_codebooks_arguments():
+    H = torch.zeros((2, 256), dtype=torch.int64, device="cuda")
+    bufs = torch.zeros((2, _lib.huff_codebook_size()), dtype=torch.uint8, device="cuda")
+    st = codec.new_status()
+    with pytest.raises(_lib.HuffError) as e:
+        _lib.huff_build_codebooks(H, bufs, st, 40, 0)  # max_len out of range
+    assert e.value.status == _lib.HUFF_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        _lib.huff_build_codebooks(H, bufs[:1], st, 24, 0)
