@@ -308,7 +308,7 @@ def run_ours(args, dist, rank, ws):
     units_per_s, ms = whole_job(dist, float(2 * n), ms_local, dev)
     path.check()
 
-    stage_names = ["histogram_bf16_xor", "build_codebook_x2", "encode_bf16_xor", "decode_bf16_xor"]
+    stage_names = ["histogram_bf16_xor", "build_codebooks", "encode_bf16_xor", "decode_bf16_xor"]
     stage_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, nm in enumerate(stage_names)}
     T_hi, T_lo = path.sizes()
     C = (T_hi + 7) // 8 + (T_lo + 7) // 8
@@ -316,7 +316,7 @@ def run_ours(args, dist, rank, ws):
     peak, peak_kind = hbm_peak()
     alg = {  # algorithmic bytes per launch
         "histogram_bf16_xor": 4 * n + 2 * 2048,
-        "build_codebook_x2": 2 * (2048 + 21504),
+        "build_codebooks": 2 * (2048 + 21504),
         "encode_bf16_xor": 4 * n + C + offs,
         "decode_bf16_xor": C + offs + 4 * n,
     }
@@ -337,6 +337,8 @@ def run_ours(args, dist, rank, ws):
     extra = materialised_delta_stages(path, args, peak)
     planes_fp32 = byte_planes_stage(args, peak) if not args.no_extras else None
     drift = drift_stage(args) if not args.no_extras else None
+    loopback = loopback_stage(args) if not args.no_extras else None
+    bank = bank_stage(args) if not args.no_extras else None
 
     # quality
     from lossless_huffman_compression_gb300 import _lib
@@ -367,9 +369,11 @@ def run_ours(args, dist, rank, ws):
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": f"snapshot_delta_bf16_{args.rows}x{workloads.SNAPSHOT_SHAPE[1]}",
                    "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk, "max_len": 24,
-                   "step": "xor+split+hist with segment counts, build x2, one-pass fused encode, fused decode+merge+xor",
+                   "step": "xor+split+hist with segment counts, both codebooks in one launch, one-pass fused encode, "
+                           "fused decode+merge+xor",
                    "l2": "inputs (8 GB) larger than L2; no flush", "parallelism": f"replicas{ws}"},
-        "roofline": roofline, "stages": stages, "materialised_delta": extra, "byte_planes_fp32": planes_fp32, "drift_adaptive": drift,
+        "roofline": roofline, "stages": stages, "materialised_delta": extra, "byte_planes_fp32": planes_fp32,
+        "drift_adaptive": drift, "loopback": loopback, "codebook_bank": bank,
         "quality": quality,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": path.launches_per_step * args.steps, "clocks": clk,
     }
@@ -443,6 +447,136 @@ def drift_stage(args):
                      "gbs": round(nseg * seg / (ms / 1e3) / 1e9, 1)}
     del segs, head
     torch.cuda.empty_cache()
+    return res
+
+
+def _replay_ms(fn, reps):
+    """Milliseconds per call of fn, replayed from a CUDA graph (launch costs out of the way); plain
+    launches when capture is not possible.  Returns (ms, "graph" | "launches")."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    how = "graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        run = g.replay
+    except Exception:
+        torch.cuda.synchronize()
+        run, how = fn, "launches"
+    for _ in range(3):
+        run()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps, how
+
+
+def loopback_stage(args):
+    """The one-GPU loopback of compressed communication: a message of int8 (the fixed-codebook
+    workload's shards) goes encode -> device-to-device copy of the stream (its size read on the
+    device) -> decode.  Fixed codebook (built once from 4 warm-up shards) against the per-shard
+    pipeline, which also counts, builds a codebook and sends it with the stream.  Chunks of 1 KiB
+    and 16 KiB: the decode runs one lane per chunk, so small messages want small chunks."""
+    from lossless_huffman_compression_gb300 import _lib, codec, workloads
+    hist = torch.zeros(256, dtype=torch.int64, device="cuda")
+    for k in range(4):
+        codec.histogram(workloads.fixed_codebook_shard(k, warmup=True, device="cuda"), hist, accumulate=True)
+    cb = codec.build_codebook(hist, 24, _lib.HUFF_COVER_ALL)
+    src = workloads.fixed_codebook_shard(0, warmup=False, device="cuda").reshape(-1).view(torch.uint8)
+    big = torch.cat([src] * 16)  # 256 MiB
+    res = {"sizes": []}
+    for size, chunk in [(z, c) for z in (64 << 10, 1 << 20, 16 << 20, 256 << 20) for c in (1024, 16384)]:
+        x = big[:size]
+        cap = _lib.huff_encode_bound(size, 24)
+        nc = _lib.huff_num_chunks(size, chunk)
+        pay, pay2 = (torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(2))
+        off, off2 = (torch.empty(nc + 1, dtype=torch.int64, device="cuda") for _ in range(2))
+        ws = torch.empty(max(_lib.huff_workspace_size(size, chunk), 16) // 8, dtype=torch.int64, device="cuda")
+        out = torch.empty_like(x)
+        st = codec.new_status()
+        h2 = torch.zeros(256, dtype=torch.int64, device="cuda")
+        cb_own, cb_sent = codec.Codebook(), codec.Codebook()
+
+        def fixed():
+            _lib.huff_encode(x, cb.buf, chunk, pay, off, ws, st)
+            _lib.huff_stream_copy(pay, off, pay2, off2, st)
+            _lib.huff_decode(pay2, off2, size, chunk, cb.buf, out, st)
+
+        def per_shard():
+            _lib.huff_histogram(x, h2)
+            _lib.huff_build_codebook(h2, cb_own.buf, st)
+            _lib.huff_encode(x, cb_own.buf, chunk, pay, off, ws, st)
+            cb_sent.buf.copy_(cb_own.buf)  # the codebook travels with the stream
+            _lib.huff_stream_copy(pay, off, pay2, off2, st)
+            _lib.huff_decode(pay2, off2, size, chunk, cb_sent.buf, out, st)
+
+        reps = 200 if size <= (1 << 20) else (40 if size <= (16 << 20) else 8)
+        ms_f, how_f = _replay_ms(fixed, reps)
+        ok_f = bool(torch.equal(out, x)) and int(st.item()) == 0
+        bits_f = int(off2[-1].item())
+        out.zero_()
+        ms_p, how_p = _replay_ms(per_shard, reps)
+        ok_p = bool(torch.equal(out, x)) and int(st.item()) == 0
+        res["sizes"].append({
+            "bytes": size, "chunk_bytes": chunk, "fixed_us": round(ms_f * 1e3, 1), "per_shard_us": round(ms_p * 1e3, 1),
+            "fixed_gbs": round(size / (ms_f / 1e3) / 1e9, 1), "ratio_fixed": round(size * 8 / bits_f, 4),
+            "timing": how_f if how_f == how_p else f"{how_f}/{how_p}", "lossless": ok_f and ok_p})
+    del big, src
+    torch.cuda.empty_cache()
+    return res
+
+
+def bank_stage(args):
+    """Per-tensor-type codebook bank: 16 warm-up shards of each type observed, every type's codebook
+    built in one launch, 8 test shards of each type encoded with their own type's codebook; compared
+    with one codebook of all types pooled and with each shard's own codebook."""
+    from lossless_huffman_compression_gb300 import _lib, codec, workloads
+    types = workloads.TENSOR_TYPES
+    bank = codec.CodebookBank(types)
+    for t in types:
+        for k in range(16):
+            bank.observe(t, workloads.tensor_type_shard(t, k, warmup=True, device="cuda"))
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    bank.build()
+    b.record()
+    torch.cuda.synchronize()
+    build_ms = a.elapsed_time(b)
+    pooled = codec.build_codebook(bank.hists.sum(0), 24, _lib.HUFF_COVER_ALL)
+    res = {"types": list(types), "warmup_shards": 16, "test_shards": 8, "build_ms": round(build_ms, 4),
+           "ratio": {}}
+    enc_ms, enc_bytes = 0.0, 0
+    for t in types:
+        tot = {"own_type": 0, "pooled": 0, "per_shard": 0}
+        nbytes = 0
+        for k in range(8):
+            x = workloads.tensor_type_shard(t, k, warmup=False, device="cuda").reshape(-1).view(torch.uint8)
+            nbytes += x.numel()
+            a.record()
+            s = bank.encode(t, x)
+            b.record()
+            torch.cuda.synchronize()
+            enc_ms += a.elapsed_time(b)
+            enc_bytes += x.numel()
+            tot["own_type"] += s.total_bits()
+            tot["pooled"] += codec.encode(x, pooled).total_bits()
+            tot["per_shard"] += codec.encode(x, codec.build_codebook(codec.histogram(x))).total_bits()
+            assert torch.equal(bank.decode(t, s), x)
+        res["ratio"][t] = {kk: round(nbytes * 8 / v, 4) for kk, v in tot.items()}
+    res["encode_gbs"] = round(enc_bytes / (enc_ms / 1e3) / 1e9, 1)
+    res["encode_timing"] = "per call, including the status read"
     return res
 
 

@@ -280,6 +280,28 @@ int huff_encode_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, si
                         huff_stream_t stream);
 
 /*
+ * huff_stream_copy -- copy a compressed stream to other device buffers, its
+ * size read on the device ["Single-stage Huffman encoder for ML compression",
+ * Practical impact: compressed tensors travel between accelerators that hold
+ * the same fixed codebook, so nothing but the stream is exchanged].  With one
+ * GPU this is the loopback link: encode -> copy -> decode with no host round
+ * trip (the host never needs T).
+ *   payload, chunk_bit_off, n_chunks   a stream as huff_encode writes it;
+ *                 payload 16-byte aligned, payload_bytes long.
+ *   dst_payload   dst_cap bytes, 16-byte aligned, not the source; receives
+ *                 the stream through the end of its last 32-bit word:
+ *                 min(4 ceil(T / 32), payload_bytes) bytes, T =
+ *                 chunk_bit_off[n_chunks].
+ *   dst_off       uint64[n_chunks + 1], 8-byte aligned, not the source.
+ *   status        HUFF_ERR_BUFFER_TOO_SMALL when dst_cap is below that size;
+ *                 HUFF_ERR_CORRUPT_STREAM when T > 8 payload_bytes.  Either
+ *                 way nothing is copied.
+ */
+int huff_stream_copy(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off,
+                     size_t n_chunks, uint8_t *dst_payload, size_t dst_cap, uint64_t *dst_off,
+                     int32_t *status, huff_stream_t stream);
+
+/*
  * huff_decode -- chunked decode [P2 framework: decompression reads the data,
  * Huffman-decodes it and restores it; lossless, so the output equals the
  * encoder's input].

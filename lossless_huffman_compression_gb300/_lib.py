@@ -43,6 +43,7 @@ EXPORTS = (
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
     "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
     "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if", "huff_build_codebooks",
+    "huff_stream_copy",
 )
 
 
@@ -83,6 +84,7 @@ def load(path: str = LIB_PATH):
         "huff_histogram": (I, [P, S, S, P, I, P]),
         "huff_build_codebook": (I, [P, I, ctypes.c_uint, P, P, P]),
         "huff_build_codebooks": (I, [P, S, I, ctypes.c_uint, P, P, P]),
+        "huff_stream_copy": (I, [P, S, P, S, P, S, P, P, P]),
         "huff_codebook_from_lengths": (I, [P, I, P, P, P]),
         "huff_encode": (I, [P, S, P, S, P, S, P, P, S, P, P]),
         "huff_decode": (I, [P, S, P, S, S, P, P, P, P]),
@@ -207,6 +209,21 @@ def huff_build_codebooks(hists: torch.Tensor, cbs: torch.Tensor, status: torch.T
                                                                _dev(cbs, "cbs"), _dev(status, "status"),
                                                                _stream(stream)))
     return cbs
+
+
+def huff_stream_copy(payload: torch.Tensor, off: torch.Tensor, dst_payload: torch.Tensor, dst_off: torch.Tensor,
+                     status: torch.Tensor, stream=None) -> None:
+    """Copy a stream (payload bytes up to its device-side size, and its offsets) to dst buffers."""
+    n_chunks = off.numel() - 1
+    if n_chunks < 0 or dst_off.numel() != off.numel():
+        raise ValueError("dst_off must have as many entries as off")
+    _check("huff_stream_copy", load().huff_stream_copy(_dev(payload, "payload"),
+                                                       payload.numel() * payload.element_size(), _dev(off, "off"),
+                                                       n_chunks,
+                                                       _dev(dst_payload, "dst_payload"),
+                                                       dst_payload.numel() * dst_payload.element_size(),
+                                                       _dev(dst_off, "dst_off"), _dev(status, "status"),
+                                                       _stream(stream)))
 
 
 def huff_codebook_from_lengths(lengths, cb: torch.Tensor, status: torch.Tensor, max_len: int = HUFF_MAX_LEN,

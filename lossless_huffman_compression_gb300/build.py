@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libhuff.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "histogram.cu", "codebook.cu", "encode.cu", "decode.cu", "bytegroup.cu"]
+SOURCES = ["api.cu", "histogram.cu", "codebook.cu", "encode.cu", "decode.cu", "bytegroup.cu", "stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

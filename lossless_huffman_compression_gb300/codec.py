@@ -102,6 +102,60 @@ def build_codebooks(hists: torch.Tensor, max_len: int = 24, flags: int = 0,
     return [Codebook(buf=bufs[k]) for k in range(count)]
 
 
+def stream_copy(s: Stream, dst_payload: torch.Tensor | None = None, dst_off: torch.Tensor | None = None,
+                status: torch.Tensor | None = None) -> Stream:
+    """The stream in other device buffers (the loopback link of one GPU): payload bytes up to the
+    stream's size, read on the device, and the offsets."""
+    if dst_payload is None:
+        dst_payload = torch.empty_like(s.payload)
+    if dst_off is None:
+        dst_off = torch.empty_like(s.off)
+    st = status if status is not None else new_status(s.payload.device)
+    _lib.huff_stream_copy(s.payload, s.off, dst_payload, dst_off, st)
+    if status is None:
+        raise_on_status(st, "huff_stream_copy")
+    return Stream(dst_payload, dst_off, s.n, s.chunk_bytes)
+
+
+class CodebookBank:
+    """One fixed codebook per tensor type ("Single-stage Huffman encoder for ML
+    compression", Methodology 1-3: symbol statistics are recorded per tensor
+    type -- activations, gradients, weights -- over warm-up batches, and one
+    codebook is built from each type's averaged distribution; a tensor is then
+    encoded with its type's codebook).  observe() counts a warm-up tensor into
+    its type's histogram on the device; build() makes every type's codebook in
+    one launch (every symbol gets a code, so later tensors never miss one);
+    encode/decode pick the codebook by type."""
+
+    def __init__(self, types, device=None, max_len: int = 24):
+        self.types = list(types)
+        if len(set(self.types)) != len(self.types) or not self.types:
+            raise ValueError("tensor types must be distinct and at least one")
+        self._index = {t: i for i, t in enumerate(self.types)}
+        device = torch.device("cuda") if device is None else torch.device(device)
+        self.max_len = max_len
+        self.hists = torch.zeros((len(self.types), 256), dtype=torch.int64, device=device)
+        self.codebooks: list[Codebook] | None = None
+
+    def observe(self, kind, x: torch.Tensor) -> None:
+        histogram(x.reshape(-1).view(torch.uint8), self.hists[self._index[kind]], accumulate=True)
+
+    def build(self) -> list[Codebook]:
+        self.codebooks = build_codebooks(self.hists, self.max_len, _lib.HUFF_COVER_ALL)
+        return self.codebooks
+
+    def codebook(self, kind) -> Codebook:
+        if self.codebooks is None:
+            raise RuntimeError("CodebookBank.build() has not run")
+        return self.codebooks[self._index[kind]]
+
+    def encode(self, kind, x: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK) -> Stream:
+        return encode(x, self.codebook(kind), chunk_bytes, self.max_len)
+
+    def decode(self, kind, s: Stream, out: torch.Tensor | None = None) -> torch.Tensor:
+        return decode(s, self.codebook(kind), out=out)
+
+
 def codebook_from_lengths(lengths, max_len: int = 24, device=None) -> Codebook:
     cb = Codebook(device)
     st = new_status(cb.device)

@@ -98,6 +98,17 @@ int huff_build_codebooks(const uint64_t *hists, size_t count, int max_len, unsig
     return launch_build_codebooks(hists, count, max_len, flags, cbs, status, nullptr, cs(stream));
 }
 
+int huff_stream_copy(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off, size_t n_chunks,
+                     uint8_t *dst_payload, size_t dst_cap, uint64_t *dst_off, int32_t *status,
+                     huff_stream_t stream) {
+    if (payload == nullptr || chunk_bit_off == nullptr || dst_payload == nullptr || dst_off == nullptr ||
+        status == nullptr || !aligned(payload, HUFF_ALIGN) || !aligned(dst_payload, HUFF_ALIGN) ||
+        !aligned(chunk_bit_off, 8) || !aligned(dst_off, 8) || dst_off == chunk_bit_off || dst_payload == payload)
+        return HUFF_ERR_INVALID_ARG;
+    return launch_stream_copy(payload, payload_bytes, chunk_bit_off, n_chunks, dst_payload, dst_cap, dst_off, status,
+                              cs(stream));
+}
+
 int huff_drift_check(const uint64_t *hist, const huff_codebook *cb, double threshold, uint32_t *flag, double *gap,
                      huff_stream_t stream) {
     if (hist == nullptr || cb == nullptr || flag == nullptr || !aligned(hist, 8) || !aligned(cb, 16) ||

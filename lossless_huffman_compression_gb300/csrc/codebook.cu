@@ -199,21 +199,36 @@ __global__ void __launch_bounds__(kT) k_build_codebook(const uint64_t *__restric
             return;
         }
         if (t == 0) {
-            // two-queue Huffman: leaves (sorted) against new nodes (FIFO); a leaf wins a count tie
+            // two-queue Huffman: leaves (sorted) against new nodes (FIFO); a leaf wins a count tie.
+            // The heads of both queues and the entries behind them sit in registers (an empty slot
+            // holds kNone, above every count), so the next shared-memory load is one pop ahead of
+            // its use and the serial chain is compares and adds.
+            constexpr uint64_t kNone = ~0ull;
             int li = 0, ii = 0;
+            uint64_t l0 = leaf_cnt[0], l1 = m > 1 ? leaf_cnt[1] : kNone;
+            uint64_t i0 = kNone, i1 = kNone;
             for (int k = 0; k < m - 1; ++k) {
                 uint64_t sum = 0;
+#pragma unroll
                 for (int pick = 0; pick < 2; ++pick) {
-                    const bool take_leaf = li < m && (ii >= k || leaf_cnt[li] <= int_cnt[ii]);
-                    if (take_leaf) {
+                    if (l0 <= i0) {  // l0 < kNone here: at least two nodes are left in all
                         leaf_parent[li] = static_cast<uint16_t>(k);
-                        sum += leaf_cnt[li++];
+                        sum += l0;
+                        ++li;
+                        l0 = l1;
+                        l1 = li + 1 < m ? leaf_cnt[li + 1] : kNone;
                     } else {
                         int_parent[ii] = static_cast<uint16_t>(k);
-                        sum += int_cnt[ii++];
+                        sum += i0;
+                        ++ii;
+                        i0 = i1;
+                        i1 = ii + 1 < k ? int_cnt[ii + 1] : kNone;
                     }
                 }
                 int_cnt[k] = sum;
+                // the new node joins the queue: as its head or right behind it
+                if (ii == k) i0 = sum;
+                else if (ii + 1 == k) i1 = sum;
             }
         }
         __syncthreads();

@@ -200,6 +200,8 @@ int launch_split(const uint16_t *w, size_t n, uint8_t *hi, uint8_t *lo, cudaStre
 int launch_merge(const uint8_t *hi, const uint8_t *lo, size_t n, uint16_t *w, cudaStream_t s);
 int launch_xor(const uint16_t *a, const uint16_t *b, size_t n, uint16_t *out, cudaStream_t s);
 int launch_split_w(const uint8_t *in, size_t n, int width, uint8_t *planes, size_t ps, cudaStream_t s);
+int launch_stream_copy(const uint8_t *src, size_t src_bytes, const uint64_t *off, size_t n_chunks, uint8_t *dst,
+                       size_t dst_cap, uint64_t *dst_off, int32_t *status, cudaStream_t s);
 int launch_merge_w(const uint8_t *planes, size_t n, int width, size_t ps, uint8_t *out, cudaStream_t s);
 
 inline int launch_status() {

@@ -22,6 +22,11 @@ which are not available):
 * ``sweep_segment``     -- int8 segment k (256 MiB) of a 16 GiB stream; the
   distribution cycles N(0,4), N(0,16), N(0,48), Laplace(b=8), uniform
   [-128, 127]; seed 5000 + k.
+* ``tensor_type_shard`` -- int8 shards of three tensor types for a codebook
+  bank: "weight" clamp(round(N(0, 12))); "activation" 0 with probability 0.5,
+  else clamp(round(Exp(mean 16))) (non-negative, like ReLU outputs);
+  "gradient" clamp(round(Laplace(b = 3))).  Warm-up shard k of type t uses
+  seed 7000 + 100 t + k, test shard k seed 7050 + 100 t + k.
 """
 from __future__ import annotations
 
@@ -38,6 +43,9 @@ SNAPSHOT_SHAPE = (65536, 30518)
 SWEEP_SEGMENTS = 64
 SWEEP_SEGMENT_BYTES = 256 << 20
 SWEEP_KINDS = ("gauss4", "gauss16", "gauss48", "laplace8", "uniform")
+TENSOR_TYPES = ("weight", "activation", "gradient")
+TYPE_WARMUP_SHAPE = (1024, 2048)
+TYPE_TEST_SHAPE = (4096, 2048)
 
 _BLOCK = 1 << 26  # elements drawn per block, bounds temporary memory
 
@@ -138,3 +146,27 @@ def sweep_segment(k: int, device="cpu", nbytes: int = SWEEP_SEGMENT_BYTES) -> to
         else:
             out[s:e] = torch.randint(-128, 128, (m,), generator=g, device=device, dtype=torch.int32).to(torch.int8)
     return out
+
+
+def tensor_type_shard(kind: str, k: int, warmup: bool, device="cpu", shape=None) -> torch.Tensor:
+    """Warm-up or test shard k of a tensor type (int8)."""
+    t = TENSOR_TYPES.index(kind)
+    if shape is None:
+        shape = TYPE_WARMUP_SHAPE if warmup else TYPE_TEST_SHAPE
+    n = int(math.prod(shape))
+    g = _gen(7000 + 100 * t + (0 if warmup else 50) + k, device)
+    out = torch.empty(n, dtype=torch.int8, device=device)
+    for s in range(0, n, _BLOCK):
+        e = min(n, s + _BLOCK)
+        m = e - s
+        if kind == "weight":
+            out[s:e] = _clamp_round_int8(torch.randn(m, generator=g, device=device).mul_(12.0))
+        elif kind == "activation":
+            u = torch.rand(m, generator=g, device=device, dtype=torch.float64)
+            x = -16.0 * torch.log1p(-torch.rand(m, generator=g, device=device, dtype=torch.float64))
+            out[s:e] = _clamp_round_int8(torch.where(u < 0.5, torch.zeros_like(x), x).float())
+        else:
+            u = torch.rand(m, generator=g, device=device, dtype=torch.float64) - 0.5
+            x = -3.0 * torch.sign(u) * torch.log1p(-2.0 * u.abs())
+            out[s:e] = _clamp_round_int8(x.float())
+    return out.view(shape)
