@@ -645,78 +645,128 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restric
 // scan gives each segment's offset before the encode starts.  The encode then
 // reads its input once (no counting pass) and no CTA waits for another.
 
-// Bits of each segment per plane: one warp per segment.
-__global__ void k_seg_bits(const uint32_t *__restrict__ seg_counts, uint32_t n_seg, const huff_codebook *cb_hi,
-                           const huff_codebook *cb_lo, uint64_t *__restrict__ bits, int32_t *status) {
+// Bits of each segment per plane (sum of count x length over its recorded
+// counts, a warp per segment, one wave of CTAs) and their inclusive prefix.  The last CTA to
+// finish its segments (a ticket counter) scans all segments' bits: thread t
+// of its 1024 sums a run of consecutive segments, a block scan combines the
+// runs, and each thread writes its run's prefixes as the descriptors.
+constexpr int kSegScanThreads = 1024;
+
+__global__ void __launch_bounds__(kSegScanThreads) k_seg_bits_scan(const uint32_t *__restrict__ seg_counts,
+                                                                   uint32_t n_seg, const huff_codebook *cb_hi,
+                                                                   const huff_codebook *cb_lo, uint32_t *bits,
+                                                                   uint64_t *desc_hi, uint64_t *desc_lo,
+                                                                   unsigned *done, int32_t *status) {
     __shared__ uint8_t len[kSegCountWords];
-    for (int i = threadIdx.x; i < kSegCountWords; i += blockDim.x) {
+    __shared__ uint64_t wsum[2][kSegScanThreads / 32];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kSegCountWords; i += blockDim.x) {
         const huff_codebook *cb = i < 256 ? cb_hi : cb_lo;
         len[i] = cb->magic == HUFF_CODEBOOK_MAGIC ? cb->len[i & 255] : 0;
     }
     __syncthreads();
-    const uint32_t seg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (seg >= n_seg) return;
-    const uint32_t *h = seg_counts + static_cast<size_t>(seg) * kSegCountWords;
-    uint64_t b0 = 0, b1 = 0;
-    bool missing = false;
+    for (uint32_t seg = blockIdx.x * (kSegScanThreads / 32) + warp; seg < n_seg;
+         seg += gridDim.x * (kSegScanThreads / 32)) {
+        const uint32_t *h = seg_counts + static_cast<size_t>(seg) * kSegCountWords;
+        uint64_t b0 = 0, b1 = 0;
+        bool missing = false;
 #pragma unroll
-    for (int j = lane; j < 256; j += 32) {
-        const uint32_t c0 = h[j], c1 = h[256 + j];
-        const uint32_t l0 = len[j], l1 = len[256 + j];
-        b0 += static_cast<uint64_t>(c0) * l0;
-        b1 += static_cast<uint64_t>(c1) * l1;
-        missing |= (c0 && !l0) || (c1 && !l1);
+        for (int j = lane; j < 256; j += 32) {
+            const uint32_t c0 = h[j], c1 = h[256 + j];
+            const uint32_t l0 = len[j], l1 = len[256 + j];
+            b0 += static_cast<uint64_t>(c0) * l0;
+            b1 += static_cast<uint64_t>(c1) * l1;
+            missing |= (c0 && !l0) || (c1 && !l1);
+        }
+        b0 = warp_sum_u64(b0);
+        b1 = warp_sum_u64(b1);
+        if (__any_sync(0xffffffffu, missing) && lane == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
+        if (lane == 0) {  // a segment has at most 131 072 * 24 bits per plane: 32-bit counts
+            bits[seg] = static_cast<uint32_t>(b0);
+            bits[n_seg + seg] = static_cast<uint32_t>(b1);
+        }
     }
-    b0 = warp_sum_u64(b0);
-    b1 = warp_sum_u64(b1);
-    if (__any_sync(0xffffffffu, missing) && lane == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
-    if (lane == 0) {
-        bits[seg] = b0;
-        bits[n_seg + seg] = b1;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // the last CTA: thread tid sums segments [lo, hi) of both planes (up to kRun of them held in
+    // registers, their loads all in flight at once; longer runs are read twice)
+    constexpr uint32_t kRun = 16;
+    const uint32_t K = (n_seg + kSegScanThreads - 1) / kSegScanThreads;
+    const uint32_t lo = tid * K < n_seg ? tid * K : n_seg;
+    const uint32_t hi = lo + K < n_seg ? lo + K : n_seg;
+    uint32_t v0[kRun], v1[kRun];
+    uint64_t s0 = 0, s1 = 0;
+    if (K <= kRun) {
+#pragma unroll
+        for (uint32_t j = 0; j < kRun; ++j) {
+            const bool in = lo + j < hi;
+            v0[j] = in ? __ldcg(&bits[lo + j]) : 0u;
+            v1[j] = in ? __ldcg(&bits[n_seg + lo + j]) : 0u;
+        }
+#pragma unroll
+        for (uint32_t j = 0; j < kRun; ++j) {
+            s0 += v0[j];
+            s1 += v1[j];
+        }
+    } else {
+        for (uint32_t i = lo; i < hi; ++i) {
+            s0 += __ldcg(&bits[i]);
+            s1 += __ldcg(&bits[n_seg + i]);
+        }
     }
-}
-
-// Inclusive prefix of the segment bit counts, as the lookback descriptors the
-// fix-up kernel reads (flag: inclusive prefix).  One CTA, rounds of 1024 x 8.
-__global__ void __launch_bounds__(1024) k_seg_scan(const uint64_t *__restrict__ bits, uint32_t n_seg,
-                                                   uint64_t *__restrict__ desc_hi, uint64_t *__restrict__ desc_lo) {
-    __shared__ uint64_t wsum[2][32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint64_t carry[2] = {0, 0};
-    for (uint32_t base = 0; base < n_seg; base += 1024 * 8) {
+    uint64_t i0 = s0, i1 = s1;  // inclusive scan across the block
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            uint64_t v[8], t = 0;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y0 = __shfl_up_sync(0xffffffffu, i0, o);
+        const uint64_t y1 = __shfl_up_sync(0xffffffffu, i1, o);
+        if (lane >= o) {
+            i0 += y0;
+            i1 += y1;
+        }
+    }
+    if (lane == 31) {
+        wsum[0][warp] = i0;
+        wsum[1][warp] = i1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t u0 = wsum[0][lane], u1 = wsum[1][lane];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t i = base + tid * 8 + j;
-                v[j] = i < n_seg ? bits[p * size_t(n_seg) + i] : 0;
-                t += v[j];
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y0 = __shfl_up_sync(0xffffffffu, u0, o);
+            const uint64_t y1 = __shfl_up_sync(0xffffffffu, u1, o);
+            if (lane >= o) {
+                u0 += y0;
+                u1 += y1;
             }
-            uint64_t incl = t;
+        }
+        wsum[0][lane] = u0;
+        wsum[1][lane] = u1;
+    }
+    __syncthreads();
+    uint64_t r0 = i0 - s0 + (warp ? wsum[0][warp - 1] : 0);  // exclusive prefix of this run
+    uint64_t r1 = i1 - s1 + (warp ? wsum[1][warp - 1] : 0);
+    if (K <= kRun) {
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+        for (uint32_t j = 0; j < kRun; ++j) {
+            if (lo + j < hi) {
+                r0 += v0[j];
+                r1 += v1[j];
+                desc_hi[lo + j] = kFlagPrefix | r0;
+                desc_lo[lo + j] = kFlagPrefix | r1;
             }
-            if (lane == 31) wsum[p][warp] = incl;
-            __syncthreads();
-            uint64_t before = carry[p], all = carry[p];
-            for (int w = 0; w < 32; ++w) {
-                before += w < warp ? wsum[p][w] : 0;
-                all += wsum[p][w];
-            }
-            uint64_t run = before + incl - t;
-            uint64_t *desc = p == 0 ? desc_hi : desc_lo;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t i = base + tid * 8 + j;
-                run += v[j];
-                if (i < n_seg) desc[i] = kFlagPrefix | run;
-            }
-            carry[p] = all;
-            __syncthreads();
+        }
+    } else {
+        for (uint32_t i = lo; i < hi; ++i) {
+            r0 += __ldcg(&bits[i]);
+            r1 += __ldcg(&bits[n_seg + i]);
+            desc_hi[i] = kFlagPrefix | r0;
+            desc_lo[i] = kFlagPrefix | r1;
         }
     }
 }
@@ -756,13 +806,11 @@ constexpr size_t kTableBytes = 256 * 256;
 constexpr size_t kRingBytes = size_t(kWarps) * kStages * kStageBytes;
 constexpr size_t kBufBytes = size_t(kWarps) * 2 * kBufWords * 4;
 constexpr size_t kBarBytes = size_t(kWarps) * kStages * 8;
-constexpr size_t kProdBytes = size_t(kWarps) * 32;                     // lane 0's copy-job cursor per warp
-constexpr size_t kSmem = kTableBytes + kRingBytes + kBufBytes + kBarBytes + kProdBytes;
+constexpr size_t kSmem = kTableBytes + kRingBytes + kBufBytes + kBarBytes;
 static_assert(kDirSegElems % kTile == 0, "segments of whole tiles");
 static_assert((kBufWords - 1) * 32 >= 31 + kTile * HUFF_MAX_LEN + 32 && kBufWords % 4 == 0,
               "tile buffer, and a last slot no tile uses");
 static_assert(kSmem <= 227 * 1024, "one CTA per SM");
-static_assert(kProdBytes % 16 == 0, "cursor slots");
 }  // namespace wenc
 
 // Table entry at byte address a (row = byte value, slot from the permute).
@@ -894,32 +942,30 @@ __device__ __forceinline__ void wpack(WPacker &pk, uint32_t *buf, const uint32_t
     }
 }
 
-// Lane 0's copy jobs: this warp's tiles in order, into the ring stages in turn.
-struct WProducer {
-    uint32_t seg, left, stage, last_bytes;
-    size_t first;  // the next tile's first element
-    template <bool XOR>
-    __device__ __forceinline__ void issue(uint8_t *ring, uint64_t *bar, uint32_t nw, uint32_t n_seg, uint32_t n_tiles,
-                                          const uint8_t *in, const uint8_t *in2, uint64_t pol) {
-        if (seg >= n_seg) return;  // no tiles left: the consumer stops before this job
-        // every tile is whole but the input's last one
-        const uint32_t bytes = (left == 1 && seg == n_seg - 1) ? last_bytes : uint32_t(wenc::kTile * 2);
-        uint8_t *dst = ring + stage * wenc::kStageBytes;
-        mbar_arrive_expect_tx(&bar[stage], bytes * (XOR ? 2u : 1u));
-        if (bytes) {
-            bulk_g2s_hint(dst, in + first * 2, bytes, &bar[stage], pol);
-            if (XOR) bulk_g2s_hint(dst + wenc::kTile * 2, in2 + first * 2, bytes, &bar[stage], pol);
-        }
-        stage = stage + 1 == uint32_t(wenc::kStages) ? 0u : stage + 1;
-        first += wenc::kTile;
-        if (--left == 0) {
-            seg += nw;
-            first = static_cast<size_t>(seg) * kDirSegElems;
-            const uint32_t rest = n_tiles - seg * wenc::kTilesPerSeg;
-            left = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
-        }
+// Lane 0's copy job for tile kk of this warp's sequence counted from segment
+// seg (which has `tiles` tiles); kk may run past that segment's end into the
+// warp's next one.  No job when the sequence ends first.
+template <bool XOR>
+__device__ __forceinline__ void wissue(uint8_t *ring, uint64_t *bar, uint32_t stage, uint32_t seg, uint32_t kk,
+                                       uint32_t tiles, uint32_t nw, uint32_t n_seg, uint32_t n_tiles,
+                                       uint32_t last_bytes, const uint8_t *in, const uint8_t *in2, uint64_t pol) {
+    if (kk >= tiles) {
+        kk -= tiles;
+        seg += nw;
+        if (seg >= n_seg) return;
+        const uint32_t rest = n_tiles - seg * wenc::kTilesPerSeg;
+        if (kk >= (rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg)) return;
     }
-};
+    const uint32_t t = seg * wenc::kTilesPerSeg + kk;
+    const uint32_t bytes = t == n_tiles - 1 ? last_bytes : uint32_t(wenc::kTile * 2);  // every tile whole but the last
+    const size_t src = static_cast<size_t>(t) * (wenc::kTile * 2);
+    uint8_t *dst = ring + stage * wenc::kStageBytes;
+    mbar_arrive_expect_tx(&bar[stage], bytes * (XOR ? 2u : 1u));
+    if (bytes) {
+        bulk_g2s_hint(dst, in + src, bytes, &bar[stage], pol);
+        if (XOR) bulk_g2s_hint(dst + wenc::kTile * 2, in2 + src, bytes, &bar[stage], pol);
+    }
+}
 
 // Complete words [skip, nfull) of a tile's buffer to dst (byte-swapped: the
 // stream is a byte sequence, most significant bit first).
@@ -963,22 +1009,12 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
     const uint32_t gw = static_cast<uint32_t>(warp) * gridDim.x + blockIdx.x;  // round r: segment r nw + gw
     const uint64_t pol = l2_policy_evict_first();
     const uint32_t last_n = static_cast<uint32_t>(n - static_cast<size_t>(n_tiles - 1) * wenc::kTile);  // 1..512
-    // lane 0's copy-job cursor lives in shared memory: registers are the scarce resource here
-    WProducer *prod = reinterpret_cast<WProducer *>(smem + wenc::kTableBytes + wenc::kRingBytes + wenc::kBufBytes +
-                                                    wenc::kBarBytes) + warp;
-    if (lane == 0) {
-        WProducer pc;
-        pc.seg = gw;
-        pc.stage = 0;
-        pc.last_bytes = (last_n * 2) & ~15u;
-        pc.first = static_cast<size_t>(gw) * kDirSegElems;
-        pc.left = 0;
-        if (gw < n_seg) {
-            const uint32_t rest = n_tiles - gw * wenc::kTilesPerSeg;
-            pc.left = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
-        }
-        for (int s = 0; s < wenc::kStages; ++s) pc.issue<XOR>(ring, bar, nw, n_seg, n_tiles, in, in2, pol);
-        *prod = pc;
+    const uint32_t last_bytes = (last_n * 2) & ~15u;
+    if (lane == 0 && gw < n_seg) {  // the first kStages tiles of the warp's sequence
+        const uint32_t rest = n_tiles - gw * wenc::kTilesPerSeg;
+        const uint32_t tiles0 = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
+        for (int j = 0; j < wenc::kStages; ++j)
+            wissue<XOR>(ring, bar, j, gw, j, tiles0, nw, n_seg, n_tiles, last_bytes, in, in2, pol);
     }
     const uint32_t kbh = static_cast<uint32_t>(lane & 15) << 3;
     const uint32_t kbl = kbh + 128u;
@@ -1045,11 +1081,10 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
                 }
             }
             __syncwarp();  // every lane has read the stage
-            if (lane == 0) {
-                WProducer pc = *prod;
-                pc.issue<XOR>(ring, bar, nw, n_seg, n_tiles, in, in2, pol);
-                *prod = pc;
-            }
+            // the stage is free again: lane 0 refills it with the tile kStages further on
+            if (lane == 0)
+                wissue<XOR>(ring, bar, cstage, seg, k + wenc::kStages, tiles, nw, n_seg, n_tiles, last_bytes, in, in2,
+                            pol);
             cstage = cstage + 1 == uint32_t(wenc::kStages) ? 0u : cstage + 1;
             cphase ^= cstage == 0 ? 1u : 0u;
 
@@ -1286,18 +1321,23 @@ int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n
     const size_t tiles = enc_bf16_tiles(n);
     const size_t segs = (tiles + kDirSegTiles - 1) / kDirSegTiles;
     uint64_t *w = static_cast<uint64_t *>(ws);
-    // layout: desc_hi, desc_lo, edge_hi, edge_lo, bits (2 x segs)
+    // layout: desc_hi, desc_lo, edge_hi, edge_lo, 32-bit bits (2 x segs), ticket counter (zeroed)
     EncPlane p0{cb_hi, reinterpret_cast<uint32_t *>(pay_hi), cap_hi / 4, off_hi, w, w + 2 * segs};
     EncPlane p1{cb_lo, reinterpret_cast<uint32_t *>(pay_lo), cap_lo / 4, off_lo, w + segs, w + 3 * segs};
-    uint64_t *bits = w + 4 * segs;
-    const unsigned nb = static_cast<unsigned>((segs * 32 + 255) / 256);
-    k_seg_bits<<<nb, 256, 0, s>>>(seg_counts, static_cast<uint32_t>(segs), cb_hi, cb_lo, bits, status);
-    if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
-    k_seg_scan<<<1, 1024, 0, s>>>(bits, static_cast<uint32_t>(segs), p0.desc, p1.desc);
-    if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
+    uint32_t *bits = reinterpret_cast<uint32_t *>(w + 4 * segs);
+    unsigned *ticket = reinterpret_cast<unsigned *>(w + 6 * segs);
+    int zst = launch_zero_u64(w + 6 * segs, 1, s);
+    if (zst != HUFF_OK) return zst;
+    const DevInfo d = dev_info();
+    {
+        size_t blocks = (segs + kSegScanThreads / 32 - 1) / (kSegScanThreads / 32);
+        if (blocks > static_cast<size_t>(d.sms)) blocks = static_cast<size_t>(d.sms);  // one wave
+        k_seg_bits_scan<<<static_cast<unsigned>(blocks), kSegScanThreads, 0, s>>>(seg_counts, static_cast<uint32_t>(segs), cb_hi, cb_lo,
+                                                            bits, p0.desc, p1.desc, ticket, status);
+        if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
+    }
     const uint8_t *a = reinterpret_cast<const uint8_t *>(w16);
     const uint8_t *b = reinterpret_cast<const uint8_t *>(x0);
-    const DevInfo d = dev_info();
     const size_t wtiles = (n + wenc::kTile - 1) / wenc::kTile;
     auto run = [&](auto kern) -> int {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(wenc::kSmem)) !=

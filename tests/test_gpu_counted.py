@@ -213,3 +213,22 @@ def test_runs_of_a_nonzero_one_bit_symbol(run_byte):
         # the byte-stream decoder on the high plane alone
         cb, s = codec.compress(torch.from_numpy(hi).cuda(), chunk)
         assert torch.equal(codec.decode(s, cb).cpu(), torch.from_numpy(hi))
+
+
+def test_counted_more_segments_than_the_scan_holds_in_registers():
+    # 16 385 segments: the segment scan's threads take runs longer than they keep in registers
+    n = 16385 * SEG + 7
+    g = torch.Generator(device="cuda")
+    g.manual_seed(12)
+    x1 = (torch.randn(n, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    s = codec.compress_bf16(x1, None, 16384)  # counted path
+    hh = torch.zeros(256, dtype=torch.int64, device="cuda")
+    hl = torch.zeros(256, dtype=torch.int64, device="cuda")
+    two = codec.compress_bf16(x1, None, 16384, cb_hi=s.cb_hi, cb_lo=s.cb_lo)  # two-pass, same codebooks
+    for a, b in ((two.hi, s.hi), (two.lo, s.lo)):
+        assert torch.equal(a.off, b.off)
+        nb = (a.total_bits() + 7) // 8
+        assert torch.equal(a.payload[:nb], b.payload[:nb])
+    del two, hh, hl
+    back = codec.decompress_bf16(s, None)
+    assert torch.equal(back.view(torch.int16), x1.view(torch.int16))
