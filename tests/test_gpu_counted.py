@@ -232,3 +232,16 @@ def test_counted_more_segments_than_the_scan_holds_in_registers():
     del two, hh, hl
     back = codec.decompress_bf16(s, None)
     assert torch.equal(back.view(torch.int16), x1.view(torch.int16))
+
+
+@pytest.mark.parametrize("chunk,n", [(256, 70_001 * 256 + 77), (256, 152 * 448 * 2 * 256 + 3), (1024, 300_000 * 1024 - 5)])
+@pytest.mark.parametrize("delta", [False, True])
+def test_decode_more_chunk_pairs_than_one_wave(chunk, n, delta):
+    # more chunk pairs than the SMs hold lanes at once: the decode runs in several waves
+    g = torch.Generator(device="cuda")
+    g.manual_seed(n % 1000 + delta)
+    x0 = (torch.randn(n, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    x1 = (x0.float() + torch.randn(n, generator=g, device="cuda") * 3e-4).to(torch.bfloat16)
+    s = codec.compress_bf16(x1, x0 if delta else None, chunk)
+    back = codec.decompress_bf16(s, x0 if delta else None)
+    assert torch.equal(back.view(torch.int16), x1.view(torch.int16))
