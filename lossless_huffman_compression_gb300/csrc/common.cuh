@@ -27,7 +27,6 @@ constexpr int kSegCountWords = 512;                                   // [hi 256
 constexpr int kLutRep = 8;                       // copies of the encode table (bank spreading)
 constexpr int kHistThreads = 512;
 constexpr int kHistCopies = 32;                  // one histogram copy per lane
-constexpr int kHistPitch = 257;                  // padded copy pitch: copy c of bin b sits in bank (c+b)%32
 constexpr unsigned kSpinLimit = 1u << 20;        // bounded waits (polls) before HUFF_ERR_TIMEOUT
 
 // lookback descriptor: flag in the top two bits, value in the low 62

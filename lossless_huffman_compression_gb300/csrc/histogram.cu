@@ -6,20 +6,29 @@
 // stage 2 (frequency statistics of the byte groups).
 //
 // Design: every CTA keeps 32 privatised copies of the 256 counters in shared
-// memory, one per lane index, with a pitch of 257 words so that the 32 copies
-// of one bin fall in 32 different banks.  A warp whose lanes all see the same
-// symbol (the usual case for the high byte plane of bf16, and for the XOR
-// delta, where one symbol dominates) therefore updates 32 distinct addresses
-// in 32 distinct banks: no address serialisation and no bank conflict.  Input
-// is read as 16-byte vectors, four per thread in flight.  At the end each CTA
-// folds its copies and adds one uint64 per non-zero bin to global memory.
+// memory, one per lane index, interleaved bin-major: copy c of bin b is word
+// 32 b + c, so lane c only ever touches bank c.  Whatever symbols the lanes of
+// a warp see, their 32 updates hit 32 distinct banks: no bank conflict and no
+// address serialisation.  The fold sums a bin's 32 copies in an order rotated
+// by the bin (thread b reads copy (k + b) mod 32 at step k), so the threads of
+// a warp read 32 distinct banks too.  Input is read as 16-byte vectors, four
+// per thread in flight.  At the end each CTA folds its copies and adds one
+// uint64 per non-zero bin to global memory.
 #include "common.cuh"
 
 namespace huffk {
 
 namespace {
 
-__device__ __forceinline__ void count_word(uint32_t *my, uint32_t w) {
+constexpr int kHistPlaneWords = 256 * kHistCopies;  // one plane's 32 copies
+
+// A lane's copy of the counters: bin b at word 32 b of the lane's column.
+struct LaneCopy {
+    uint32_t *p;
+    __device__ __forceinline__ uint32_t &operator[](uint32_t b) const { return p[b << 5]; }
+};
+
+__device__ __forceinline__ void count_word(LaneCopy my, uint32_t w) {
     atomicAdd(&my[w & 0xffu], 1u);
     atomicAdd(&my[(w >> 8) & 0xffu], 1u);
     atomicAdd(&my[(w >> 16) & 0xffu], 1u);
@@ -27,14 +36,14 @@ __device__ __forceinline__ void count_word(uint32_t *my, uint32_t w) {
 }
 
 // bytes 0 and 2 (par = 0) or 1 and 3 (par = 1) of a word
-__device__ __forceinline__ void count_word_half(uint32_t *my, uint32_t w, int par) {
+__device__ __forceinline__ void count_word_half(LaneCopy my, uint32_t w, int par) {
     w >>= 8 * par;
     atomicAdd(&my[w & 0xffu], 1u);
     atomicAdd(&my[(w >> 16) & 0xffu], 1u);
 }
 
 template <int STRIDE>
-__device__ __forceinline__ void count_vec(uint32_t *my, uint4 v, int par) {
+__device__ __forceinline__ void count_vec(LaneCopy my, uint4 v, int par) {
     if (STRIDE == 1) {
         count_word(my, v.x);
         count_word(my, v.y);
@@ -52,7 +61,7 @@ __device__ __forceinline__ void flush_copies(const uint32_t *sh, uint64_t *hist)
     for (int b = threadIdx.x; b < 256; b += blockDim.x) {
         uint64_t s = 0;
 #pragma unroll 8
-        for (int c = 0; c < kHistCopies; ++c) s += sh[c * kHistPitch + b];
+        for (int c = 0; c < kHistCopies; ++c) s += sh[b * kHistCopies + ((c + b) & (kHistCopies - 1))];
         if (s) atomicAdd(reinterpret_cast<unsigned long long *>(&hist[b]), static_cast<unsigned long long>(s));
     }
 }
@@ -61,9 +70,9 @@ template <int STRIDE>
 __global__ void __launch_bounds__(kHistThreads) k_histogram(const uint8_t *__restrict__ in, size_t n,
                                                             uint64_t *__restrict__ hist) {
     extern __shared__ uint32_t sh[];
-    for (int i = threadIdx.x; i < kHistCopies * kHistPitch; i += blockDim.x) sh[i] = 0;
+    for (int i = threadIdx.x; i < kHistPlaneWords; i += blockDim.x) sh[i] = 0;
     __syncthreads();
-    uint32_t *my = sh + (threadIdx.x & 31) * kHistPitch;
+    const LaneCopy my{sh + (threadIdx.x & 31)};
 
     const size_t gtid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -103,7 +112,7 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram(const uint8_t *__res
 }
 
 // Both byte planes of 16-bit words, optionally of (w ^ x0).
-__device__ __forceinline__ void count_pair(uint32_t *hi, uint32_t *lo, uint32_t w) {
+__device__ __forceinline__ void count_pair(LaneCopy hi, LaneCopy lo, uint32_t w) {
     atomicAdd(&lo[w & 0xffu], 1u);
     atomicAdd(&hi[(w >> 8) & 0xffu], 1u);
     atomicAdd(&lo[(w >> 16) & 0xffu], 1u);
@@ -116,10 +125,10 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16(const uint16_t 
                                                                  uint64_t *__restrict__ hist_hi,
                                                                  uint64_t *__restrict__ hist_lo) {
     extern __shared__ uint32_t sh[];
-    for (int i = threadIdx.x; i < 2 * kHistCopies * kHistPitch; i += blockDim.x) sh[i] = 0;
+    for (int i = threadIdx.x; i < 2 * kHistPlaneWords; i += blockDim.x) sh[i] = 0;
     __syncthreads();
-    uint32_t *hi = sh + (threadIdx.x & 31) * kHistPitch;
-    uint32_t *lo = hi + kHistCopies * kHistPitch;
+    const LaneCopy hi{sh + (threadIdx.x & 31)};
+    const LaneCopy lo{sh + kHistPlaneWords + (threadIdx.x & 31)};
 
     const size_t gtid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -166,7 +175,7 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16(const uint16_t 
     }
     __syncthreads();
     flush_copies(sh, hist_hi);
-    flush_copies(sh + kHistCopies * kHistPitch, hist_lo);
+    flush_copies(sh + kHistPlaneWords, hist_lo);
 }
 
 // Both byte planes, per segment of kDirSegElems elements: each CTA takes whole
@@ -184,11 +193,12 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16_counted(const u
     static_assert(kHistThreads == kSegCountWords, "one thread per (plane, bin)");
     extern __shared__ uint32_t sh[];
     const int tid = threadIdx.x;
-    for (int i = tid; i < 2 * kHistCopies * kHistPitch; i += blockDim.x) sh[i] = 0;
+    for (int i = tid; i < 2 * kHistPlaneWords; i += blockDim.x) sh[i] = 0;
     __syncthreads();
-    uint32_t *hi = sh + (tid & 31) * kHistPitch;
-    uint32_t *lo = hi + kHistCopies * kHistPitch;
-    uint32_t *fold = sh + (tid >> 8) * kHistCopies * kHistPitch + (tid & 255);  // this thread's bin, copy 0
+    const LaneCopy hi{sh + (tid & 31)};
+    const LaneCopy lo{sh + kHistPlaneWords + (tid & 31)};
+    const int fb = tid & 255;
+    uint32_t *fold = sh + (tid >> 8) * kHistPlaneWords + fb * kHistCopies;  // this thread's bin, its 32 copies
     uint64_t total = 0;
     for (uint32_t seg = blockIdx.x; seg < n_seg; seg += gridDim.x) {
         const size_t first = static_cast<size_t>(seg) * kDirSegElems;
@@ -231,8 +241,8 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16_counted(const u
         uint32_t s = 0;
 #pragma unroll 8
         for (int c = 0; c < kHistCopies; ++c) {
-            s += fold[c * kHistPitch];
-            fold[c * kHistPitch] = 0;
+            s += fold[(c + fb) & (kHistCopies - 1)];
+            fold[(c + fb) & (kHistCopies - 1)] = 0;
         }
         seg_counts[static_cast<size_t>(seg) * kSegCountWords + tid] = s;
         total += s;
@@ -292,7 +302,7 @@ int launch_zero_u64(uint64_t *p, size_t count, cudaStream_t s) {
 }
 
 int launch_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist, cudaStream_t s) {
-    const size_t smem = kHistCopies * kHistPitch * sizeof(uint32_t);
+    const size_t smem = kHistPlaneWords * sizeof(uint32_t);
     int grid = 1, st;
     if (stride == 1) {
         if ((st = hist_grid(k_histogram<1>, smem, n / 64 + 1, &grid)) != HUFF_OK) return st;
@@ -306,7 +316,7 @@ int launch_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist,
 
 int launch_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
                           uint64_t *hist_lo, cudaStream_t s) {
-    const size_t smem = 2 * kHistCopies * kHistPitch * sizeof(uint32_t);
+    const size_t smem = 2 * kHistPlaneWords * sizeof(uint32_t);
     int grid = 1, st;
     if (x0 != nullptr) {
         if ((st = hist_grid(k_histogram_bf16<true>, smem, n / 16 + 1, &grid)) != HUFF_OK) return st;
@@ -320,7 +330,7 @@ int launch_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint6
 
 int launch_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
                                   uint64_t *hist_lo, uint32_t *seg_counts, cudaStream_t s) {
-    const size_t smem = 2 * kHistCopies * kHistPitch * sizeof(uint32_t);
+    const size_t smem = 2 * kHistPlaneWords * sizeof(uint32_t);
     const size_t n_seg = (n + kDirSegElems - 1) / kDirSegElems;
     int grid = 1, st;
     if (x0 != nullptr) {
