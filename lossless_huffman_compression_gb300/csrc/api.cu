@@ -59,7 +59,7 @@ size_t huff_encode_bound(size_t n, int max_len) {
 
 size_t huff_workspace_size(size_t n, size_t chunk_bytes) {
     (void)chunk_bytes;
-    return (2 * enc_u8_tiles(n) + 2) * sizeof(uint64_t);
+    return enc_u8_workspace_words(n) * sizeof(uint64_t);
 }
 
 size_t lmc_workspace_size(size_t n, size_t chunk_bytes) {

@@ -83,6 +83,13 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// The 8 words have arrived in registers: the shared-memory loads that produced
+// them are complete (an empty instruction that consumes them), so a bulk copy
+// issued after a barrier cannot overwrite the stage under a pending load.
+__device__ __forceinline__ void consumed(const uint32_t (&v)[8]) {
+    asm volatile("" ::"r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -173,6 +180,8 @@ int launch_drift_check(const uint64_t *hist, const huff_codebook *cb, double thr
 int launch_codebook_from_lengths(int max_len, huff_codebook *cb, int32_t *status, cudaStream_t s);
 
 size_t enc_u8_tiles(size_t n);
+size_t enc_u8_seg_tiles(size_t n);
+size_t enc_u8_workspace_words(size_t n);
 size_t enc_bf16_tiles(size_t n);
 int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk,
                      uint8_t *payload, size_t cap, uint64_t *off, void *ws, int32_t *status,

@@ -848,7 +848,9 @@ __device__ __forceinline__ void wlookup(const uint8_t *tab, const uint32_t (&wv)
 
 // A lane's bits of one plane in one tile.  Pending bits: the low nb bits of
 // hi:lo (nb < 32 between appends); append(code, len) takes len <= 31.
-struct WPacker {
+// BUFWORDS: the tile buffer's size; its last slot is never part of a tile.
+template <int BUFWORDS>
+struct WPackerT {
     uint32_t hi, lo, nb, w;
     // A word that is not complete yet goes to the buffer's last slot, which no
     // tile uses: a plain store instead of a branch.
@@ -858,7 +860,7 @@ struct WPacker {
         nb += len;
         const bool full = nb >= 32;
         nb &= 31u;
-        buf[full ? w : uint32_t(wenc::kBufWords - 1)] = __funnelshift_r(lo, hi, nb);
+        buf[full ? w : uint32_t(BUFWORDS - 1)] = __funnelshift_r(lo, hi, nb);
         w += full ? 1u : 0u;
     }
     // The last, partial word (an OR of zero when there is none).
@@ -866,6 +868,7 @@ struct WPacker {
         atomicOr(&buf[w], nb ? lo << (32u - nb) : 0u);
     }
 };
+using WPacker = WPackerT<wenc::kBufWords>;
 
 // A lane's 16 elements (32 bytes, XOR x0 for the delta) straight from global
 // memory; bytes at or past tile_n elements read as zero.
@@ -1080,7 +1083,9 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
                     wv[kk >> 2] = (wv[kk >> 2] & ~(0xffu << (8 * (kk & 3)))) | (v << (8 * (kk & 3)));
                 }
             }
+            consumed(wv);
             __syncwarp();  // every lane has read the stage
+            if (lane == 0) fence_proxy_async_smem();  // the reads before the bulk copy that refills the stage
             // the stage is free again: lane 0 refills it with the tile kStages further on
             if (lane == 0)
                 wissue<XOR>(ring, bar, cstage, seg, k + wenc::kStages, tiles, nw, n_seg, n_tiles, last_bytes, in, in2,
@@ -1182,6 +1187,353 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ byte streams, one warp per segment
+//
+// With a given codebook (the fixed one, or a shard's own), a segment's bit
+// count is not known before its symbols are read, so a warp makes two passes
+// over each segment of seg_tiles tiles (16; down to 4 for small inputs, so
+// that there are segments for every warp): it streams the tiles in (L2 policy
+// evict_last) and counts their bits, publishes the count and looks back over
+// the earlier segments' descriptors for its offset (decoupled lookback), then
+// streams the same tiles again from L2 (evict_first) and packs them as the
+// counted bf16 encode does, one plane of 32 symbols per lane.  Segments are
+// claimed in order from a counter, and a warp claims its next segment only
+// three tiles before the end of its current one (its copy jobs run three
+// tiles ahead): a claimed segment is started right away, so the segments a
+// lookback waits on are being counted at the same time, not queued behind
+// another segment.  A symbol without a code has the table length 0x1000, so a
+// tile's count shows it; such a segment sets the status and is not packed.
+namespace wenc8 {
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kLaneSyms = 32;
+constexpr int kTile = 32 * kLaneSyms;  // 1024 symbols
+constexpr int kSegTilesMax = 16;       // 16 384 symbols per segment for large inputs
+constexpr int kSegTilesMin = 4;        // at least kStages + 1 tiles, for the claim three tiles before the end
+constexpr int kStages = 3;
+constexpr int kStageBytes = kTile;
+constexpr int kBufWords = 776;
+constexpr uint32_t kNoCode = 0x1000;   // table length of a symbol without a code
+constexpr size_t kTableBytes = 256 * 256;
+constexpr size_t kRingBytes = size_t(kWarps) * kStages * kStageBytes;
+constexpr size_t kBufBytes = size_t(kWarps) * kBufWords * 4;
+constexpr size_t kBarBytes = size_t(kWarps) * kStages * 8;
+constexpr size_t kSmem = kTableBytes + kRingBytes + kBufBytes + kBarBytes;
+static_assert((kBufWords - 1) * 32 >= 31 + kTile * HUFF_MAX_LEN + 32 && kBufWords % 4 == 0, "tile buffer");
+static_assert(kLaneSyms * HUFF_MAX_LEN < int(kNoCode), "a lane's count stays below the no-code mark");
+static_assert(kSegTilesMin > kStages, "a full segment claims its successor three tiles before its end");
+}  // namespace wenc8
+
+using WPacker8 = WPackerT<wenc8::kBufWords>;
+
+// Lane 0's copy-job cursor: pass p (0 count, 1 pack) of tile k of segment
+// seg; p == 2 once the segment's jobs are all issued (the next segment is
+// taken from the claim when its first job is due).
+struct Job8 {
+    uint32_t seg, k, pass;
+};
+
+__device__ __forceinline__ uint32_t seg_tiles8(uint32_t seg, uint32_t n_tiles, uint32_t st) {
+    const uint32_t rest = n_tiles - seg * st;
+    return rest < st ? rest : st;
+}
+
+// Issue the cursor's job into `stage` and advance it; seg_next is the warp's
+// claim of its next segment (0xffffffff until made), taken when the current
+// segment's jobs are done.
+__device__ __forceinline__ void wissue8(uint8_t *ring, uint64_t *bar, uint32_t stage, Job8 &j, uint32_t &seg_next,
+                                        uint32_t n_seg, uint32_t n_tiles, uint32_t st, uint32_t last_bytes,
+                                        const uint8_t *in, uint64_t pol_keep, uint64_t pol_drop) {
+    if (j.pass == 2) {
+        j.seg = seg_next;
+        j.pass = 0;
+        j.k = 0;
+        seg_next = 0xffffffffu;  // taken: the next claim replaces it
+    }
+    if (j.seg >= n_seg) return;
+    const uint32_t t = j.seg * st + j.k;
+    const uint32_t bytes = t == n_tiles - 1 ? last_bytes : uint32_t(wenc8::kTile);
+    mbar_arrive_expect_tx(&bar[stage], bytes);
+    if (bytes)
+        bulk_g2s_hint(ring + stage * wenc8::kStageBytes, in + static_cast<size_t>(t) * wenc8::kTile, bytes, &bar[stage],
+                      j.pass ? pol_drop : pol_keep);
+    if (++j.k == seg_tiles8(j.seg, n_tiles, st)) {
+        j.k = 0;
+        ++j.pass;
+    }
+}
+
+// A lane's 32 symbols: pairs of consecutive symbols as (code, length).
+template <bool RAGGED>
+__device__ __forceinline__ void wlookup8(const uint8_t *tab, const uint32_t (&wv)[8], uint32_t kb, int nvalid,
+                                         uint32_t (&m)[16], uint32_t (&L)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t word = wv[j >> 1];
+        const uint32_t sa = (j & 1) ? 0x5524u : 0x5504u, sb = (j & 1) ? 0x5534u : 0x5514u;
+        uint2 a = wtab(tab, __byte_perm(word, kb, sa));
+        uint2 b = wtab(tab, __byte_perm(word, kb, sb));
+        if (RAGGED) {
+            if (2 * j >= nvalid) a = make_uint2(0u, 0u);
+            if (2 * j + 1 >= nvalid) b = make_uint2(0u, 0u);
+        }
+        m[j] = (a.x << b.y) | b.x;
+        L[j] = a.y + b.y;
+    }
+}
+
+// A lane's 32 bytes of a tile from global memory (bytes at or past tile_n read as zero).
+__device__ __forceinline__ void wload8(const uint8_t *in, size_t first, int lane, int tile_n, uint32_t (&wv)[8]) {
+    const size_t b0 = first + static_cast<size_t>(lane) * wenc8::kLaneSyms;
+    if (tile_n == wenc8::kTile) {  // in is 16-byte aligned and first a multiple of 1024
+        const uint4 a = *reinterpret_cast<const uint4 *>(in + b0);
+        const uint4 c = *reinterpret_cast<const uint4 *>(in + b0 + 16);
+        wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+        wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) wv[j] = 0;
+    for (int k = 0; k < wenc8::kLaneSyms; ++k) {
+        const int bb = lane * wenc8::kLaneSyms + k;
+        if (bb >= tile_n) break;
+        wv[k >> 2] |= static_cast<uint32_t>(in[b0 + k]) << (8 * (k & 3));
+    }
+}
+
+// Appends a lane's 32 symbols in the largest group size that fits 31 bits for every lane.
+__device__ __forceinline__ void wpack8(WPacker8 &pk, uint32_t *buf, const uint32_t (&m)[16], const uint32_t (&L)[16],
+                                       const uint8_t *tab, uint32_t kb, const uint8_t *in, size_t first, int lane,
+                                       int tile_n, int nvalid) {
+    uint32_t Q[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) Q[q] = L[2 * q] + L[2 * q + 1];
+    uint32_t O[4];
+#pragma unroll
+    for (int o = 0; o < 4; ++o) O[o] = Q[2 * o] + Q[2 * o + 1];
+    if (!__any_sync(0xffffffffu, max(max(O[0], O[1]), max(O[2], O[3])) > 31u)) {
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const uint32_t qa = (m[4 * o] << L[4 * o + 1]) | m[4 * o + 1];
+            const uint32_t qb = (m[4 * o + 2] << L[4 * o + 3]) | m[4 * o + 3];
+            pk.append(buf, (qa << Q[2 * o + 1]) | qb, O[o]);
+        }
+    } else {
+        uint32_t qmax = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) qmax = max(qmax, Q[q]);
+        if (!__any_sync(0xffffffffu, qmax > 31u)) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pk.append(buf, (m[2 * q] << L[2 * q + 1]) | m[2 * q + 1], Q[q]);
+        } else {
+            uint32_t lmax = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) lmax = max(lmax, L[j]);
+            if (!__any_sync(0xffffffffu, lmax > 31u)) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk.append(buf, m[j], L[j]);
+            } else {
+                // some pair is longer than 31 bits: one symbol at a time, read and looked up again
+                uint32_t wv[8];
+                wload8(in, first, lane, tile_n, wv);
+#pragma unroll
+                for (int k = 0; k < wenc8::kLaneSyms; ++k) {
+                    uint2 e = wtab(tab, __byte_perm(wv[k >> 2], kb, 0x5504u + 0x10u * (k & 3)));
+                    if (k >= nvalid) e = make_uint2(0u, 0u);
+                    pk.append(buf, e.x, e.y);
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(wenc8::kThreads, 1)
+    k_encode_u8w(const uint8_t *__restrict__ in, size_t n, EncPlane P, uint32_t chunk, uint32_t n_tiles,
+                 uint32_t st, uint32_t n_seg, unsigned *seg_ctr, int32_t *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint8_t *tab = smem;
+    uint8_t *ring = smem + wenc8::kTableBytes + size_t(warp) * wenc8::kStages * wenc8::kStageBytes;
+    uint32_t *buf = reinterpret_cast<uint32_t *>(smem + wenc8::kTableBytes + wenc8::kRingBytes) + warp * wenc8::kBufWords;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + wenc8::kTableBytes + wenc8::kRingBytes + wenc8::kBufBytes) +
+                    warp * wenc8::kStages;
+
+    // code table: row = byte value, slot = lane; entry (code, length); no code: (0, kNoCode)
+    const bool ok = P.cb->magic == HUFF_CODEBOOK_MAGIC;
+    for (int i = tid; i < 256 * 32; i += wenc8::kThreads) {
+        const int sym = i >> 5;
+        const uint32_t len = ok ? P.cb->len[sym] : 0u;
+        const bool has = len >= 1 && len <= HUFF_MAX_LEN;
+        reinterpret_cast<uint2 *>(smem)[i] = make_uint2(has ? P.cb->code[sym] : 0u, has ? len : wenc8::kNoCode);
+    }
+    if (tid == 0 && !ok) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+    if (lane == 0) {
+        for (int s = 0; s < wenc8::kStages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint64_t pol_keep = l2_policy_evict_last(), pol_drop = l2_policy_evict_first();
+    const uint32_t last_n = static_cast<uint32_t>(n - static_cast<size_t>(n_tiles - 1) * wenc8::kTile);  // 1..1024
+    const uint32_t last_bytes = last_n & ~15u;
+    const uint32_t kb = static_cast<uint32_t>(lane) << 3;
+    // the warp's segment (claimed in order), lane 0's copy-job cursor
+    uint32_t seg = 0;
+    if (lane == 0) seg = atomicAdd(seg_ctr, 1u);
+    seg = __shfl_sync(0xffffffffu, seg, 0);
+    Job8 job{seg, 0, 0};
+    uint32_t job_next = 0xffffffffu;  // lane 0: the next segment, once claimed
+    if (lane == 0)
+        for (int s = 0; s < wenc8::kStages; ++s)
+            wissue8(ring, bar, s, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep, pol_drop);
+    uint32_t cstage = 0, cphase = 0;
+
+    auto next_stage = [&]() {
+        cstage = cstage + 1 == uint32_t(wenc8::kStages) ? 0u : cstage + 1;
+        cphase ^= cstage == 0 ? 1u : 0u;
+    };
+    // a lane's 32 bytes of the tile in the current stage (global memory for bytes past the bulk copy)
+    auto read_stage = [&](size_t first, int tile_n, uint32_t (&wv)[8]) {
+        if (!mbar_wait(&bar[cstage], cphase) && lane == 0) set_status(status, HUFF_ERR_TIMEOUT);
+        const uint8_t *st = ring + cstage * wenc8::kStageBytes;
+        const uint4 a = *reinterpret_cast<const uint4 *>(st + lane * 32);
+        const uint4 c = *reinterpret_cast<const uint4 *>(st + lane * 32 + 16);
+        wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+        wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+        if (tile_n < wenc8::kTile) {
+            const int tma = tile_n & ~15;
+            for (int k = 0; k < 32; ++k) {
+                const int bb = lane * 32 + k;
+                if (bb < tma) continue;
+                const uint32_t v = bb < tile_n ? in[first + bb] : 0u;
+                wv[k >> 2] = (wv[k >> 2] & ~(0xffu << (8 * (k & 3)))) | (v << (8 * (k & 3)));
+            }
+        }
+        consumed(wv);
+        __syncwarp();  // every lane has read the stage
+        if (lane == 0) fence_proxy_async_smem();  // the reads before the bulk copy that refills the stage
+    };
+
+    while (seg < n_seg) {
+        const uint32_t tiles = seg_tiles8(seg, n_tiles, st);
+        const size_t seg_first = static_cast<size_t>(seg) * st * wenc8::kTile;
+        // ---------------- pass 1: the segment's bits
+        uint32_t bits = 0;
+        bool no_code = false;
+        for (uint32_t k = 0; k < tiles; ++k) {
+            const size_t first = seg_first + static_cast<size_t>(k) * wenc8::kTile;
+            const int tile_n = seg * st + k == n_tiles - 1 ? static_cast<int>(last_n) : wenc8::kTile;
+            uint32_t wv[8];
+            read_stage(first, tile_n, wv);
+            if (lane == 0) wissue8(ring, bar, cstage, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep,
+                                    pol_drop);
+            next_stage();
+            const int nvalid = tile_n - lane * 32 < 0 ? 0 : (tile_n - lane * 32 > 32 ? 32 : tile_n - lane * 32);
+            uint32_t b = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t y = wtab(tab, __byte_perm(wv[j >> 2], kb, 0x5504u + 0x10u * (j & 3))).y;
+                b += j < nvalid ? y : 0u;
+            }
+            no_code |= b >= wenc8::kNoCode;  // a lane's tile counts at most 32 * 24 bits
+            bits += b;
+        }
+        // a symbol without a code shows as a tile count of 0x1000 or more in some lane
+        const bool missing = __any_sync(0xffffffffu, no_code);
+        uint64_t seg_bits = static_cast<uint64_t>(missing ? 0u : bits);
+        seg_bits = warp_sum_u64(seg_bits);
+        if (missing && lane == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
+        // publish, look back
+        if (lane == 0) st_relaxed(&P.desc[seg], (seg == 0 ? kFlagPrefix : kFlagAggregate) | seg_bits);
+        uint64_t start = 0;
+        if (seg != 0) {
+            uint64_t wnd[kLookbackPerLane];
+            load_window(P.desc, static_cast<int64_t>(seg) - 1, lane, wnd);
+            start = lookback(P.desc, seg, lane, status, wnd);
+            if (lane == 0) st_relaxed(&P.desc[seg], kFlagPrefix | (start + seg_bits));
+        }
+        // ---------------- pass 2: pack, tile after tile
+        uint32_t *const dst = P.payload + (start >> 5);
+        const uint64_t room = start >> 5 < P.cap_words ? (P.cap_words - (start >> 5)) * 32 : 0;
+        const uint32_t lim = room < 0xffffffffull ? static_cast<uint32_t>(room) : 0xffffffffu;
+        uint32_t pos = static_cast<uint32_t>(start & 31u);
+        uint32_t carry = 0, head = 0;
+        const uint32_t cr = static_cast<uint32_t>(seg_first % chunk);
+        uint64_t next_q = seg_first / chunk + (cr ? 1u : 0u);
+        uint32_t to_next = cr ? chunk - cr : 0u;
+        uint32_t seg_next = 0xffffffffu;
+        for (uint32_t k = 0; k < tiles; ++k) {
+            const size_t first = seg_first + static_cast<size_t>(k) * wenc8::kTile;
+            const int tile_n = seg * st + k == n_tiles - 1 ? static_cast<int>(last_n) : wenc8::kTile;
+            if (k + wenc8::kStages == tiles) {  // the copy job about to be issued is the next segment's first
+                uint32_t claim = 0;
+                if (lane == 0) job_next = claim = atomicAdd(seg_ctr, 1u);
+                seg_next = __shfl_sync(0xffffffffu, claim, 0);
+            }
+            uint32_t wv[8];
+            read_stage(first, tile_n, wv);
+            if (lane == 0) wissue8(ring, bar, cstage, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep,
+                                    pol_drop);
+            next_stage();
+            if (missing) continue;  // the status is set; this segment's stream is not written
+            const int nvalid = tile_n - lane * 32 < 0 ? 0 : (tile_n - lane * 32 > 32 ? 32 : tile_n - lane * 32);
+            uint32_t m[16], L[16];
+            if (tile_n == wenc8::kTile)
+                wlookup8<false>(tab, wv, kb, 32, m, L);
+            else
+                wlookup8<true>(tab, wv, kb, nvalid, m, L);
+            uint32_t b = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) b += L[j];
+            uint32_t incl = b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            const uint32_t excl = incl - b;
+            if (to_next < uint32_t(wenc8::kTile)) {
+                do {
+                    if (static_cast<uint32_t>(lane) * wenc8::kLaneSyms == to_next && to_next < uint32_t(tile_n))
+                        P.off[next_q] = start + (pos - (start & 31u)) + excl;
+                    to_next += chunk;
+                    ++next_q;
+                } while (to_next < uint32_t(wenc8::kTile));
+            }
+            to_next -= wenc8::kTile;
+            const uint32_t ph = pos & 31u, end = ph + tot;
+            buf[end >> 5] = 0;  // the word the tile ends in: no lane completes it
+            WPacker8 q;
+            {
+                const uint32_t s0 = ph + excl;
+                q.hi = 0;
+                q.nb = s0 & 31u;
+                q.w = s0 >> 5;
+                q.lo = lane == 0 ? __funnelshift_rc(carry, 0u, 32u - ph) : 0u;
+            }
+            wpack8(q, buf, m, L, tab, kb, in, first, lane, tile_n, nvalid);
+            __syncwarp();
+            q.tail(buf);
+            __syncwarp();
+            const uint32_t nf = end >> 5;
+            const uint32_t sk = (k == 0 && ph) ? 1u : 0u;
+            if (pos + tot <= lim) {
+                wwrite(dst + (pos >> 5), buf, sk, nf, lane);
+            } else if (lane == 0) {
+                set_status(status, HUFF_ERR_BUFFER_TOO_SMALL);
+            }
+            if (k == 0) head = ph ? buf[0] : 0u;
+            carry = buf[nf];
+            pos += tot;
+            __syncwarp();
+        }
+        if (lane == 0) P.edge[seg] = (static_cast<uint64_t>(head) << 32) | carry;
+        // a segment of fewer than kStages tiles is the last one: no next segment then
+        seg = seg_next;
+    }
+}
+
 // Boundary words: the word where segment t-1 ends and segment t begins holds
 // bits of both; the stream's last, partial word holds the end of the last
 // segment.
@@ -1241,6 +1593,24 @@ __global__ void k_encode_empty(uint64_t *off0, uint64_t *off1) {
 }  // namespace
 
 size_t enc_u8_tiles(size_t n) { return (n + kEncU8Tile - 1) / kEncU8Tile; }
+
+// Tiles per segment of the byte-stream encode: 16 when there are at least 8192
+// tiles per 16 of them (two segments and more for every warp of a large GPU),
+// fewer down to 4 for smaller inputs, so that small inputs still fill the GPU.
+size_t enc_u8_seg_tiles(size_t n) {
+    const size_t tiles = (n + wenc8::kTile - 1) / wenc8::kTile;
+    size_t st = tiles / 8192;
+    if (st < size_t(wenc8::kSegTilesMin)) st = wenc8::kSegTilesMin;
+    if (st > size_t(wenc8::kSegTilesMax)) st = wenc8::kSegTilesMax;
+    return st;
+}
+
+// Workspace words of the byte-stream encode: descriptor and edge word per segment, and a counter.
+size_t enc_u8_workspace_words(size_t n) {
+    const size_t tiles = (n + wenc8::kTile - 1) / wenc8::kTile;
+    const size_t st = enc_u8_seg_tiles(n);
+    return 2 * ((tiles + st - 1) / st) + 2;
+}
 size_t enc_bf16_tiles(size_t n) { return (n + kEncBf16Tile - 1) / kEncBf16Tile; }
 
 int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk, uint8_t *payload,
@@ -1249,16 +1619,31 @@ int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_
         k_encode_empty<<<1, 1, 0, s>>>(off, nullptr);
         return launch_status();
     }
-    const size_t tiles = enc_u8_tiles(n);
-    const size_t segs = (tiles + kSegTiles - 1) / kSegTiles;
+    const size_t tiles = (n + wenc8::kTile - 1) / wenc8::kTile;
+    const size_t seg_tiles = enc_u8_seg_tiles(n);
+    const size_t segs = (tiles + seg_tiles - 1) / seg_tiles;
     uint64_t *w = static_cast<uint64_t *>(ws);
-    // layout: segment descriptors, segment counter (zeroed), edge words (always written before they are read)
+    // layout: segment descriptors, segment counter (both zeroed), edge words (written before they are read);
+    // 2 segs + 1 words, within huff_workspace_size
     int st = launch_zero_u64(w, segs + 1, s);
     if (st != HUFF_OK) return st;
     EncPlane p0{cb, reinterpret_cast<uint32_t *>(payload), cap / 4, off, w, w + segs + 1};
-    EncPlane p1 = p0;
     unsigned *ctr = reinterpret_cast<unsigned *>(w + segs);
-    return run_encode<false, false>(in, nullptr, n, p0, p1, chunk, static_cast<uint32_t>(tiles), ctr, status, s);
+    if (cudaFuncSetAttribute(k_encode_u8w, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(wenc8::kSmem)) != cudaSuccess)
+        return HUFF_ERR_CUDA;
+    // one CTA of 16 warps per SM, fewer when there are fewer segments than warps
+    const size_t sms = static_cast<size_t>(dev_info().sms);
+    size_t grid = (segs + wenc8::kWarps - 1) / wenc8::kWarps;
+    if (grid > sms) grid = sms;
+    k_encode_u8w<<<static_cast<unsigned>(grid), wenc8::kThreads, wenc8::kSmem, s>>>(
+        in, n, p0, static_cast<uint32_t>(chunk), static_cast<uint32_t>(tiles), static_cast<uint32_t>(seg_tiles),
+        static_cast<uint32_t>(segs), ctr, status);
+    if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
+    const size_t n_chunks = (n + chunk - 1) / chunk;
+    k_encode_fixup<<<static_cast<unsigned>((segs + 255) / 256), 256, 0, s>>>(p0, p0, 1, static_cast<uint32_t>(segs),
+                                                                              n_chunks, status);
+    return launch_status();
 }
 
 // Device address of g_noalloc_scratch on the current device, looked up once per
@@ -1279,7 +1664,7 @@ static uint64_t *noalloc_scratch_address() {
 
 int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk, uint8_t *payload,
                              size_t cap, uint64_t *off, int32_t *status, cudaStream_t s) {
-    if (2 * enc_u8_tiles(n) + 2 > kNoAllocScratchWords) return HUFF_ERR_BUFFER_TOO_SMALL;
+    if (enc_u8_workspace_words(n) > kNoAllocScratchWords) return HUFF_ERR_BUFFER_TOO_SMALL;
     uint64_t *ws = noalloc_scratch_address();
     if (ws == nullptr) return HUFF_ERR_CUDA;
     // the same path as huff_encode; it zeroes what must start at zero before the encode kernel runs
