@@ -225,7 +225,7 @@ class SnapshotPath:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty(n, dtype=torch.int16, device=dev)
         # kernels launched per step: hist (1 zero of both adjacent histograms + 1), build (1 for both planes),
-        # encode (segment bits + scan + main + fix-up), decode (1)
+        # encode (1 zero of the scan ticket + segment bits and scan + main + fix-up), decode (1)
         self.launches_per_step = 8
 
     def compress(self, w=None, x0=None):
@@ -623,11 +623,13 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
 
     Every step copies that step's x1 and x0 from pinned host memory, compresses, copies the streams
     to the host and back (the stored form), decompresses with the x0 already on the device, and
-    copies the result to the host.  Copies in each direction run on their own streams, so one
-    step's results go to the host while the next step's inputs come in (the links are full duplex);
-    inputs and outputs are double-buffered on the device."""
-    L = path.L
+    copies the result to the host.  The step is a pipeline over six streams: input copies (x1, x0),
+    compress, the streams' round trip, decompress, output copy; inputs and outputs have three device
+    buffers each and consecutive steps alternate between two sets of stream buffers, codebooks and
+    workspaces, so no stage waits for a later stage of the step before it and the host-to-device
+    link, the narrower direction, stays busy."""
     n = path.n
+    paths = [path, SnapshotPath(x0, x1, path.chunk, path.max_len)]
     h_x1 = torch.empty(n, dtype=torch.int16, pin_memory=True)
     h_x0 = torch.empty(n, dtype=torch.int16, pin_memory=True)
     h_x1.copy_(path.x1)
@@ -635,25 +637,28 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
     T_hi, T_lo = path.sizes()
     cap_hi = ((T_hi + 31) // 32) * 4
     cap_lo = ((T_lo + 31) // 32) * 4
-    h_p_hi = torch.empty(path.p_hi.numel(), dtype=torch.uint8, pin_memory=True)
-    h_p_lo = torch.empty(path.p_lo.numel(), dtype=torch.uint8, pin_memory=True)
+    h_p_hi = torch.empty(cap_hi, dtype=torch.uint8, pin_memory=True)
+    h_p_lo = torch.empty(cap_lo, dtype=torch.uint8, pin_memory=True)
     h_o_hi = torch.empty(path.nc + 1, dtype=torch.int64, pin_memory=True)
     h_o_lo = torch.empty(path.nc + 1, dtype=torch.int64, pin_memory=True)
     h_out = torch.empty(n, dtype=torch.int16, pin_memory=True)
-    d_x1 = [torch.empty_like(path.x1) for _ in range(2)]
-    d_x0 = [torch.empty_like(path.x0) for _ in range(2)]
-    d_out = [torch.empty_like(path.out) for _ in range(2)]
-    s_in, s_in2, s_main, s_out = (torch.cuda.Stream() for _ in range(4))
-    steps = max(2, min(args.steps, 5))
-    free_in = [torch.cuda.Event() for _ in range(2)]   # buffer k % 2's inputs may be overwritten
-    free_out = [torch.cuda.Event() for _ in range(2)]  # buffer k % 2's output has reached the host
-    for e in free_in + free_out:
+    nbuf = 3
+    d_x1 = [torch.empty_like(path.x1) for _ in range(nbuf)]
+    d_x0 = [torch.empty_like(path.x0) for _ in range(nbuf)]
+    d_out = [torch.empty_like(path.out) for _ in range(nbuf)]
+    s_in, s_in2, s_comp, s_rt, s_dec, s_out = (torch.cuda.Stream() for _ in range(6))
+    steps = max(3, min(args.steps, 12))
+    free_in = [torch.cuda.Event() for _ in range(nbuf)]   # buffer k % nbuf's inputs may be overwritten
+    free_out = [torch.cuda.Event() for _ in range(nbuf)]  # buffer k % nbuf's output has reached the host
+    free_path = [torch.cuda.Event() for _ in paths]       # path k % 2's streams and codebooks are done with
+    for e in free_in + free_out + free_path:
         e.record(torch.cuda.current_stream())
 
     def one(k):
-        i = k % 2
-        arrived, decoded = torch.cuda.Event(), torch.cuda.Event()
-        arrived2 = torch.cuda.Event()
+        i = k % nbuf
+        j = k % len(paths)
+        P = paths[j]
+        arrived, arrived2, compressed, restored, decoded = (torch.cuda.Event() for _ in range(5))
         with torch.cuda.stream(s_in):  # the two inputs on two streams: two copy engines at once
             s_in.wait_event(free_in[i])
             d_x1[i].copy_(h_x1, non_blocking=True)
@@ -662,23 +667,30 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
             s_in2.wait_event(free_in[i])
             d_x0[i].copy_(h_x0, non_blocking=True)
             arrived2.record(s_in2)
-        with torch.cuda.stream(s_main):
-            s_main.wait_event(arrived)
-            s_main.wait_event(arrived2)
-            path.compress(d_x1[i], d_x0[i])
-            h_p_hi[:cap_hi].copy_(path.p_hi[:cap_hi], non_blocking=True)
-            h_p_lo[:cap_lo].copy_(path.p_lo[:cap_lo], non_blocking=True)
-            h_o_hi.copy_(path.o_hi, non_blocking=True)
-            h_o_lo.copy_(path.o_lo, non_blocking=True)
-            # decompress from the host-held streams
-            path.p_hi[:cap_hi].copy_(h_p_hi[:cap_hi], non_blocking=True)
-            path.p_lo[:cap_lo].copy_(h_p_lo[:cap_lo], non_blocking=True)
-            path.o_hi.copy_(h_o_hi, non_blocking=True)
-            path.o_lo.copy_(h_o_lo, non_blocking=True)
-            s_main.wait_event(free_out[i])
-            path.decompress(d_x0[i], d_out[i])
-            decoded.record(s_main)
-            free_in[i].record(s_main)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(arrived)
+            s_comp.wait_event(arrived2)
+            s_comp.wait_event(free_path[j])
+            P.compress(d_x1[i], d_x0[i])
+            compressed.record(s_comp)
+        with torch.cuda.stream(s_rt):  # the stored form: to the host and back (in order on this stream)
+            s_rt.wait_event(compressed)
+            h_p_hi.copy_(P.p_hi[:cap_hi], non_blocking=True)
+            h_p_lo.copy_(P.p_lo[:cap_lo], non_blocking=True)
+            h_o_hi.copy_(P.o_hi, non_blocking=True)
+            h_o_lo.copy_(P.o_lo, non_blocking=True)
+            P.p_hi[:cap_hi].copy_(h_p_hi, non_blocking=True)
+            P.p_lo[:cap_lo].copy_(h_p_lo, non_blocking=True)
+            P.o_hi.copy_(h_o_hi, non_blocking=True)
+            P.o_lo.copy_(h_o_lo, non_blocking=True)
+            restored.record(s_rt)
+        with torch.cuda.stream(s_dec):
+            s_dec.wait_event(restored)
+            s_dec.wait_event(free_out[i])
+            P.decompress(d_x0[i], d_out[i])
+            decoded.record(s_dec)
+            free_in[i].record(s_dec)
+            free_path[j].record(s_dec)
         with torch.cuda.stream(s_out):
             s_out.wait_event(decoded)
             h_out.copy_(d_out[i], non_blocking=True)
@@ -692,23 +704,26 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
     a.record(s_in)
     for k in range(steps):
         one(k + 1)
-    s_in.wait_stream(s_out)
-    s_in.wait_stream(s_main)
-    s_in.wait_stream(s_in2)
+    for s in (s_in2, s_comp, s_rt, s_dec, s_out):
+        s_in.wait_stream(s)
     b.record(s_in)
     torch.cuda.synchronize()
     ms = max_over_ranks(dist, a.elapsed_time(b) / steps, dev)
+    for P in paths:
+        st = int(P.status.item())
+        if st != 0:
+            raise RuntimeError(f"e2e device status {st}: {P.L.status_string(st)}")
     if not torch.equal(h_out, h_x1):
         raise RuntimeError("e2e round trip differs")
     total = sum_over_ranks(dist, float(2 * n), dev)
     h2d = 2 * n * 2 + cap_hi + cap_lo + 2 * 8 * (path.nc + 1)
     d2h = 2 * n + cap_hi + cap_lo + 2 * 8 * (path.nc + 1)
-    del d_x1, d_x0, d_out
+    del d_x1, d_x0, d_out, paths
     return {"value": round(total / ms / 1e6, 2), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "api": "lmc_histogram_bf16_counted, huff_build_codebooks, lmc_encode_bf16_counted, lmc_decode_bf16 with pinned host "
-                   "inputs, streams copied to host and back; input and output copies on their own streams, overlapping "
-                   "the previous and next steps"}
+                   "inputs, streams copied to host and back; a pipeline over six streams (input copies, compress, "
+                   "round trip, decompress, output copy), consecutive steps on alternating buffer sets"}
 
 
 # ------------------------------------------------------------------ oracle timing
