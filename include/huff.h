@@ -70,6 +70,7 @@ typedef enum huff_status {
 #define HUFF_MIN_MAX_LEN 8       /* smallest length limit that fits 256 symbols */
 #define HUFF_COVER_ALL 1u        /* raise zero counts to 1 before building (fixed codebooks) */
 #define HUFF_CHUNK_ALIGN 256     /* chunk_bytes must be a positive multiple of this */
+#define HUFF_MAX_CHUNK (1u << 30) /* and at most this: a chunk's symbol count fits an int with room */
 #define HUFF_ALIGN 16            /* alignment (bytes) required of bulk device buffers */
 #define HUFF_LUT_BITS 12         /* first-level decode table index width */
 #define HUFF_LUT_SYMS 6          /* most symbols one decode-table entry holds */
@@ -232,7 +233,8 @@ int huff_codebook_from_lengths(const uint8_t *h_len, int max_len, huff_codebook 
  * framework stage 3 "Huffman coding", split into parallel tasks].
  *   in            n symbols, 16-byte aligned.
  *   cb            device codebook built or imported above.
- *   chunk_bytes   symbols per chunk, a positive multiple of HUFF_CHUNK_ALIGN.
+ *   chunk_bytes   symbols per chunk, a positive multiple of HUFF_CHUNK_ALIGN,
+ *                 at most HUFF_MAX_CHUNK (otherwise HUFF_ERR_INVALID_ARG).
  *   payload       16-byte aligned, payload_cap bytes; huff_encode_bound(n,
  *                 max_len) always suffices.  The stream needs ceil(T/32)*4
  *                 bytes; a shorter buffer gives HUFF_ERR_BUFFER_TOO_SMALL in

@@ -22,7 +22,7 @@ constexpr size_t kMaxCodebooks = 65535;     // one CTA per codebook in one launc
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline cudaStream_t cs(huff_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
-inline bool chunk_ok(size_t chunk) { return chunk > 0 && chunk % HUFF_CHUNK_ALIGN == 0 && chunk <= (size_t(1) << 31); }
+inline bool chunk_ok(size_t chunk) { return chunk > 0 && chunk % HUFF_CHUNK_ALIGN == 0 && chunk <= HUFF_MAX_CHUNK; }
 
 }  // namespace
 

@@ -20,7 +20,9 @@
 //   * a step is one predicated basic block: a table lookup plus a second,
 //     dependent one when both fit 8 symbols, or, on a plane with a 1-bit
 //     code, a run of that code as long as the zero bits on top of the window
-//     (up to 32);
+//     (up to 32); on a plane without one, while every lane of the warp has
+//     room for two full steps in its chunk and its ring, two steps run
+//     without the per-step checks;
 //   * decoded bytes go to per-lane shared rings in segments; the warp steps
 //     until every lane has its segment (a lane that is ahead decodes into
 //     the ring's free part), then merges 8 lanes' segments per pass into
@@ -205,6 +207,7 @@ __device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecT
 constexpr int kSeg = 32;       // symbols per lane per segment (multiple of 16)
 constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
 constexpr int kStepMax = 8;    // symbols a table step may add (a run step: up to 32, within the ring's room)
+constexpr int kFastSteps = 2;  // steps per unchecked block on a plane without runs
 constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
 static_assert(kRing >= kSeg + 7 + 2 * kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
 static_assert(HUFF_LUT_SYMS <= kStepMax, "a table entry must fit one step");
@@ -306,15 +309,17 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
 // the zero bits on top of the window (up to 32, the chunk's rest and the
 // ring's room) when that beats a lookup; then up to four 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
-template <int RING, bool RUN, int W>
+template <int RING, bool RUN, int W, bool FAST = false>
 __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
+    static_assert(!(RUN && FAST), "a run step may add more symbols than a fast block reserves");
     // Predicated rather than branched: a lane with nothing to do (its chunk
     // is complete or its ring is full) takes a step of zero bits and zero
     // symbols, so the step stays one basic block.
-    const int rem = cnt - s.st - s.fill;
-    const int room = limit - s.st - s.fill;
-    const bool go = rem > 0 && room >= kStepMax;
+    // FAST: the caller has checked that the chunk and the ring have room for this step
+    const int rem = FAST ? (1 << 20) : cnt - s.st - s.fill;
+    const int room = FAST ? (1 << 20) : limit - s.st - s.fill;
+    const bool go = FAST || (rem > 0 && room >= kStepMax);
     s.refill(p, nbytes);
     const uint32_t win = s.bh >> (32 - W);
     const uint64_t e = T.lut[win];
@@ -384,6 +389,17 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
                                                uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
                                                bool &bad) {
     const uint64_t run = RUN ? T.run : 0ull;
+    if (!RUN) {
+        // while every lane's chunk and ring have room for kFastSteps full steps (a table step adds at
+        // most kStepMax symbols), take them without the per-step checks
+        while (__all_sync(0xffffffffu, limit - s.st - s.fill >= kFastSteps * kStepMax &&
+                                           cnt - s.st - s.fill >= kFastSteps * kStepMax) &&
+               __any_sync(0xffffffffu, s.st < need)) {
+#pragma unroll
+            for (int k = 0; k < kFastSteps; ++k)
+                step<RING, false, W, true>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+        }
+    }
     while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
         step<RING, RUN, W>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
     if (s.fill > 0 && s.st + s.fill == cnt) {

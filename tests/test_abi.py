@@ -73,3 +73,18 @@ def test_binding_fails_loudly_without_library(lib, tmp_path):
             mod.load(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
+
+
+def test_chunk_size_limits_rejected_before_any_device_work(lib):
+    """chunk_bytes must be a positive multiple of 256 and at most 2^30 (a chunk's symbol count
+    stays an int with room for the decoder's ring arithmetic).  Argument checks come before
+    any CUDA call, so rejected calls run here without a GPU; the pointers are aligned
+    placeholders that a rejected call never touches."""
+    L = lib.load()
+    fake = ctypes.c_void_p(1 << 20)
+    n = (1 << 31) + 512
+    for chunk in (0, 1000, (1 << 30) + 256, 1 << 31):
+        assert L.huff_decode(fake, 64, fake, n, chunk, fake, fake, fake, None) == lib.HUFF_ERR_INVALID_ARG
+        assert L.huff_encode(fake, n, fake, chunk, fake, 64, fake, fake, 64, fake, None) == lib.HUFF_ERR_INVALID_ARG
+        assert L.lmc_decode_bf16(fake, 64, fake, fake, 64, fake, n, chunk, fake, fake, fake, fake, fake,
+                                 None) == lib.HUFF_ERR_INVALID_ARG
