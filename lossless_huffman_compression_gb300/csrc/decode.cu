@@ -27,7 +27,9 @@
 //     until every lane has its segment (a lane that is ahead decodes into
 //     the ring's free part), then merges 8 lanes' segments per pass into
 //     16-bit words, XORs x0 (prefetched to L2 before the segments' decode;
-//     a merge's four loads issued together) and stores 16 bytes per lane.
+//     a merge's four loads issued together) and stores 16 bytes per lane;
+//     while every chunk of the warp has the same length (all warps but the
+//     last one of a ragged input), the merge skips the per-lane bounds.
 // Every chunk must end exactly at the next chunk's offset, otherwise
 // HUFF_ERR_CORRUPT_STREAM is reported.
 #include "common.cuh"
@@ -477,10 +479,24 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     plane_start(s, payload, nbytes, start, cnt);
     bool bad = false;
     const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
+    const bool whole = __all_sync(0xffffffffu, cnt == warp_cnt);  // every chunk of the warp has the same length
     for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSegU8) {
         fill_segment<kRingU8>(s, payload, nbytes, T, ring, swz, cnt, min(cnt, seg0 + kSegU8), seg0 + kRingU8, bad);
         __syncwarp();
         // copy-out: 8 lanes' segments per pass, 16 bytes per lane
+        if (whole && seg0 + kSegU8 <= warp_cnt) {  // every lane's segment is complete: no per-lane bounds
+            // pass i: source lane 8 i + lane / 4 (same parity as lane / 4), 8 i chunks further on
+            const int s0 = lane >> 2;
+            const int e0 = seg0 + 16 * (lane & 3);
+            const uint8_t *src = rings + s0 * kRingU8 + ((e0 & (kRingU8 - 1)) ^ ((s0 & 1) ? kRingU8 / 2 : 0));
+            uint8_t *dst = out + (c0 + s0) * chunk + e0;
+            const size_t ds = 8 * chunk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                __stcs(reinterpret_cast<uint4 *>(dst + i * ds), *reinterpret_cast<const uint4 *>(src + i * 8 * kRingU8));
+            __syncwarp();
+            continue;
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int sl = 8 * i + (lane >> 2);
@@ -554,6 +570,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
     plane_start(l, pay_lo, bytes_lo, sl, cnt);
     bool bad = false;
     const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
+    const bool whole = __all_sync(0xffffffffu, cnt == warp_cnt);  // every chunk of the warp has the same length
     for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSeg) {
         if (XOR && seg0 < cnt && (seg0 & 63) == 0) {  // one 128-byte line of x0 per two segments
             const uint16_t *xp = x0 + c * chunk + seg0;
@@ -563,44 +580,70 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
         fill_segment<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
         fill_segment<kRing>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
         __syncwarp();
-        // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane; the four passes'
-        // x0 loads are issued together, ahead of the shared-memory reads
-        uint4 xv[4];
+        if (whole && seg0 + kSeg <= warp_cnt) {
+            // every lane's segment is complete: no per-lane bounds
+            const size_t g0 = (c0 + (lane >> 2)) * chunk + seg0 + 8 * (lane & 3);  // pass i: + 8 i chunk
+            const size_t gs = 8 * chunk;
+            uint4 xv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = 8 * i + (lane >> 2);
-            const int e0 = seg0 + 8 * (lane & 3);
-            xv[i] = make_uint4(0, 0, 0, 0);
-            if (XOR && e0 + 8 <= __shfl_sync(0xffffffffu, cnt, q))
-                xv[i] = __ldcs(reinterpret_cast<const uint4 *>(x0 + (c0 + q) * chunk + e0));
-        }
+            for (int i = 0; i < 4; ++i)
+                xv[i] = XOR ? __ldcs(reinterpret_cast<const uint4 *>(x0 + g0 + i * gs)) : make_uint4(0, 0, 0, 0);
+            const int q0 = lane >> 2;
+            const uint32_t o = ((seg0 + 8 * (lane & 3)) & (kRing - 1)) ^ ((q0 & 2) ? kRing / 2 : 0);
+            const uint8_t *hr = rings + q0 * (2 * kRing) + ((q0 & 1) ? kRing : 0) + o;
+            const uint8_t *lr = rings + q0 * (2 * kRing) + ((q0 & 1) ? 0 : kRing) + o;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = 8 * i + (lane >> 2);  // source lane
-            const int e0 = seg0 + 8 * (lane & 3);
-            const int cs = __shfl_sync(0xffffffffu, cnt, q);
-            if (e0 < cs) {
-                const uint8_t *qr = rings + q * (2 * kRing);
-                const uint32_t o = (e0 & (kRing - 1)) ^ ((q & 2) ? kRing / 2 : 0);
-                const uint2 hv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? kRing : 0) + o);
-                const uint2 lv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? 0 : kRing) + o);
+            for (int i = 0; i < 4; ++i) {
+                const uint2 hv = *reinterpret_cast<const uint2 *>(hr + i * 8 * (2 * kRing));
+                const uint2 lv = *reinterpret_cast<const uint2 *>(lr + i * 8 * (2 * kRing));
                 uint4 v = make_uint4(__byte_perm(lv.x, hv.x, 0x5140), __byte_perm(lv.x, hv.x, 0x7362),
                                      __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
-                const size_t g = (c0 + q) * chunk + e0;  // first element of this group
-                if (e0 + 8 <= cs) {  // x0 and out are 16-byte aligned, chunk a multiple of 256
-                    v.x ^= xv[i].x;
-                    v.y ^= xv[i].y;
-                    v.z ^= xv[i].z;
-                    v.w ^= xv[i].w;
-                    __stcs(reinterpret_cast<uint4 *>(out + g), v);
-                } else {
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                v.x ^= xv[i].x;
+                v.y ^= xv[i].y;
+                v.z ^= xv[i].z;
+                v.w ^= xv[i].w;
+                __stcs(reinterpret_cast<uint4 *>(out + g0 + i * gs), v);
+            }
+        } else {
+            // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane; the four passes'
+            // x0 loads are issued together, ahead of the shared-memory reads
+            uint4 xv[4];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (e0 + k < cs) {
-                            uint16_t val = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
-                            if (XOR) val ^= x0[g + k];
-                            out[g + k] = val;
+            for (int i = 0; i < 4; ++i) {
+                const int q = 8 * i + (lane >> 2);
+                const int e0 = seg0 + 8 * (lane & 3);
+                xv[i] = make_uint4(0, 0, 0, 0);
+                if (XOR && e0 + 8 <= __shfl_sync(0xffffffffu, cnt, q))
+                    xv[i] = __ldcs(reinterpret_cast<const uint4 *>(x0 + (c0 + q) * chunk + e0));
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int q = 8 * i + (lane >> 2);  // source lane
+                const int e0 = seg0 + 8 * (lane & 3);
+                const int cs = __shfl_sync(0xffffffffu, cnt, q);
+                if (e0 < cs) {
+                    const uint8_t *qr = rings + q * (2 * kRing);
+                    const uint32_t o = (e0 & (kRing - 1)) ^ ((q & 2) ? kRing / 2 : 0);
+                    const uint2 hv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? kRing : 0) + o);
+                    const uint2 lv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? 0 : kRing) + o);
+                    uint4 v = make_uint4(__byte_perm(lv.x, hv.x, 0x5140), __byte_perm(lv.x, hv.x, 0x7362),
+                                         __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
+                    const size_t g = (c0 + q) * chunk + e0;  // first element of this group
+                    if (e0 + 8 <= cs) {  // x0 and out are 16-byte aligned, chunk a multiple of 256
+                        v.x ^= xv[i].x;
+                        v.y ^= xv[i].y;
+                        v.z ^= xv[i].z;
+                        v.w ^= xv[i].w;
+                        __stcs(reinterpret_cast<uint4 *>(out + g), v);
+                    } else {
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (e0 + k < cs) {
+                                uint16_t val = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+                                if (XOR) val ^= x0[g + k];
+                                out[g + k] = val;
+                            }
                         }
                     }
                 }
