@@ -307,14 +307,17 @@ int huff_stream_copy(const uint8_t *payload, size_t payload_bytes, const uint64_
  * huff_decode -- chunked decode [P2 framework: decompression reads the data,
  * Huffman-decodes it and restores it; lossless, so the output equals the
  * encoder's input].
- *   payload       payload_bytes bytes, 16-byte aligned; reads never pass
- *                 payload_bytes.
+ *   payload       payload_bytes bytes, 16-byte aligned.  It is read in whole
+ *                 16-byte units: the unit holding the last payload byte is
+ *                 read whole, and no unit after it is read.  The unit's bytes
+ *                 past payload_bytes never change the result.
  *   chunk_bit_off uint64[n_chunks + 1] as written by huff_encode.
  *   n, chunk_bytes the encoder's values.
  *   out           n bytes, 16-byte aligned.
  *   status        HUFF_ERR_CORRUPT_STREAM when a code is invalid, a chunk does
- *                 not end exactly at the next offset, or an offset lies outside
- *                 the payload; HUFF_ERR_INVALID_CODEBOOK.
+ *                 not end exactly at the next offset, an offset lies outside
+ *                 the payload, or a chunk holds fewer bits than symbols;
+ *                 HUFF_ERR_INVALID_CODEBOOK.
  */
 int huff_decode(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off,
                 size_t n, size_t chunk_bytes, const huff_codebook *cb, uint8_t *out,

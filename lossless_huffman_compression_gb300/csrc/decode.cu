@@ -15,8 +15,8 @@
 //     their count and total length), a secondary table for longer codes and
 //     the canonical arrays for a search when that table would not fit;
 //   * the bit reader keeps 64 bits in two registers and refills 32 at a time
-//     from a queue of the current 16-byte unit of the stream; reads never
-//     pass the payload's end;
+//     from a queue of the current 16-byte unit of the stream; units are read
+//     whole, the payload's last unit standing in for any unit past it;
 //   * a step is one predicated basic block: a table lookup plus a second,
 //     dependent one when both fit 8 symbols, or, on a plane with a 1-bit
 //     code, a run of that code as long as the zero bits on top of the window
@@ -143,34 +143,32 @@ __device__ void load_table_b(DecTables<W> &T, const huff_codebook *cb) {
     }
 }
 
-// Bytes of a 16-byte unit past the payload's end read as zero.
-__device__ __forceinline__ uint4 load_unit_tail(const uint8_t *p, size_t nbytes, size_t u) {
-    uint32_t w[4] = {0, 0, 0, 0};
-    for (int k = 0; k < 16; ++k) {
-        const size_t i = u * 16 + k;
-        if (i < nbytes) w[k >> 2] |= static_cast<uint32_t>(p[i]) << (8 * (k & 3));
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // Bit reader: 64 upcoming bits in (bh, bl), most significant first, and the
 // words of the current 16-byte unit of the stream not taken yet (a queue: the
 // next word is always cur.x).  The payload pointer and size are passed to
 // every call that may load, so they stay kernel parameters rather than
 // registers.
+//
+// Unit u of the payload, read whole; past the last unit that holds a payload
+// byte, that last unit again.  The payload is 16-byte aligned, so a unit that
+// holds one of its bytes lies in pages it occupies: every read is of mapped
+// memory, with no bounds branch.  Bytes past the payload's end (in its last
+// unit, or a repeated unit) only ever enter a lookup window beyond the end
+// of a valid stream, where the symbol count clamps every entry and no
+// decoded symbol depends on them.  Only lanes that decode load (nbytes >= 1:
+// a chunk of cnt symbols holds at least cnt bits).
 __device__ __forceinline__ uint4 load_unit(const uint8_t *p, size_t nbytes, size_t u) {
-    if (u * 16 + 16 <= nbytes) {
-        // a lane reads its chunk 16 bytes at a time over the whole kernel while x0 and the output
-        // stream past: keep the payload's lines in L2 ahead of them (x0 and out are evict-first)
-        uint64_t pol;
-        asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-        uint4 v;
-        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "l"(p + u * 16), "l"(pol));
-        return v;
-    }
-    return load_unit_tail(p, nbytes, u);
+    const size_t last = (nbytes - 1) >> 4;
+    const uint8_t *a = p + (u < last ? u : last) * 16;
+    // a lane reads its chunk 16 bytes at a time over the whole kernel while x0 and the output stream
+    // past: keep the payload's lines in L2 ahead of them (x0 and out are evict-first)
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(a), "l"(pol));
+    return v;
 }
 
 // Canonical search for a code longer than the table's W bits: returns
@@ -378,7 +376,15 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
 }
 
 __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, size_t nbytes, uint64_t start, int cnt) {
-    if (cnt > 0) s.start(pay, nbytes, start);
+    if (cnt > 0) {
+        s.start(pay, nbytes, start);
+    } else {  // no chunk: 64 valid bits, so the reader never refills and never loads
+        s.bh = s.bl = 0;
+        s.nb = 64;
+        s.qi = 0;
+        s.cur = make_uint4(0, 0, 0, 0);
+        s.ui = 0;
+    }
     s.a0 = 0;
     s.fill = 0;
     s.st = 0;
@@ -421,11 +427,12 @@ __device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size
         fill_segment_t<RING, false, W>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
-__device__ __forceinline__ bool chunk_bounds(const uint64_t *off, size_t c, size_t nbytes, uint64_t &start,
+// The chunk's bit range lies in the payload and holds at least one bit per symbol.
+__device__ __forceinline__ bool chunk_bounds(const uint64_t *off, size_t c, size_t nbytes, int cnt, uint64_t &start,
                                              uint64_t &end) {
     start = off[c];
     end = off[c + 1];
-    return start <= end && end <= static_cast<uint64_t>(nbytes) * 8;
+    return start <= end && end <= static_cast<uint64_t>(nbytes) * 8 && end - start >= static_cast<uint64_t>(cnt);
 }
 
 // Launch geometry: one lane per chunk (pair), blocks spread over every SM.
@@ -465,12 +472,12 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     uint64_t start = 0, end = 0;
     int cnt = 0;
     if (c < n_chunks) {
-        if (chunk_bounds(off, c, nbytes, start, end)) {
-            const size_t first = c * chunk;
-            cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
-        } else {
+        const size_t first = c * chunk;
+        const int want = static_cast<int>(n - first < chunk ? n - first : chunk);
+        if (chunk_bounds(off, c, nbytes, want, start, end))
+            cnt = want;
+        else
             set_status(status, HUFF_ERR_CORRUPT_STREAM);
-        }
     }
     uint8_t *rings = dsm + sizeof(DecTables<13>) + static_cast<size_t>(threadIdx.x - lane) * kRingU8;
     uint8_t *ring = rings + lane * kRingU8;
@@ -554,12 +561,12 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
     uint64_t sh = 0, eh = 0, sl = 0, el = 0;
     int cnt = 0;
     if (c < n_chunks) {
-        if (chunk_bounds(off_hi, c, bytes_hi, sh, eh) && chunk_bounds(off_lo, c, bytes_lo, sl, el)) {
-            const size_t first = c * chunk;
-            cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
-        } else {
+        const size_t first = c * chunk;
+        const int want = static_cast<int>(n - first < chunk ? n - first : chunk);
+        if (chunk_bounds(off_hi, c, bytes_hi, want, sh, eh) && chunk_bounds(off_lo, c, bytes_lo, want, sl, el))
+            cnt = want;
+        else
             set_status(status, HUFF_ERR_CORRUPT_STREAM);
-        }
     }
     uint8_t *rings = dsm + kBf16Tables + static_cast<size_t>(threadIdx.x - lane) * (2 * kRing);
     uint8_t *hring = rings + lane * (2 * kRing) + ((lane & 1) ? kRing : 0);

@@ -265,6 +265,27 @@ def test_corrupt_offsets_and_truncation_detected():
     assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
 
 
+def test_chunk_with_fewer_bits_than_symbols_and_empty_payload_are_corrupt():
+    """Every code is at least one bit long, so a chunk of c symbols spans at least c bits; the
+    decoder rejects a shorter chunk before it reads anything, which also covers an empty payload."""
+    x = _data("gauss", 40_000)
+    d = dev_u8(x)
+    cb = codec.build_codebook(codec.histogram(d))
+    s = codec.encode(d, cb, 4096)
+    off = s.off.clone()
+    off[2] = off[1] + 4095  # chunk 1: 4096 symbols in 4095 bits
+    out = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    st = codec.new_status()
+    _lib.huff_decode(s.payload, off, s.n, 4096, cb.buf, out, st, payload_bytes=s.nbytes())
+    torch.cuda.synchronize()
+    assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+    zero = torch.zeros_like(s.off)
+    st = codec.new_status()
+    _lib.huff_decode(s.payload, zero, s.n, 4096, cb.buf, out, st, payload_bytes=0)
+    torch.cuda.synchronize()
+    assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+
+
 def test_unbuilt_codebook_is_rejected():
     cb = codec.Codebook()
     with pytest.raises(_lib.HuffError) as e:
