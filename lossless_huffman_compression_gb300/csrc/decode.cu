@@ -51,6 +51,7 @@ struct __align__(16) DecTables {
     uint32_t bl_count[32];
     uint32_t first_code[32];
     uint32_t first_index[32];
+    uint32_t lim[32];       // 24-bit windows below lim[l] start with a code of at most l bits (all ones past the longest)
     uint8_t sorted[256];
     uint8_t len[256];
     int longest;
@@ -63,6 +64,16 @@ struct __align__(16) DecTables {
 static_assert(sizeof(DecTables<12>) % 16 == 0 && sizeof(DecTables<13>) % 16 == 0, "tables keep 16-byte alignment");
 
 constexpr size_t kBf16Tables = sizeof(DecTables<12>) + sizeof(DecTables<13>);
+
+// Canonical codes fill the code space in order of length, so the codes of at
+// most l bits are the 24-bit windows below (first_code[l] + bl_count[l]) <<
+// (24 - l), and a window's code length is one more than the number of lengths
+// whose limit it reaches.  All ones past the longest code.
+__device__ __forceinline__ uint32_t code_limit(const huff_codebook *cb, bool ok, int l) {
+    if (!ok || l > cb->longest) return 0xffffffffu;
+    if (l == 0) return 0;
+    return (cb->first_code[l] + cb->bl_count[l]) << (HUFF_MAX_LEN - l);
+}
 
 // Phase 1 of loading a codebook: the W-bit table, the canonical arrays and
 // the header.  For W = 13 an entry is the 12-bit entry of its first 12 bits
@@ -106,6 +117,7 @@ __device__ void load_table_a(DecTables<W> &T, const huff_codebook *cb) {
         T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
         T.first_code[tid] = ok ? cb->first_code[tid] : 0;
         T.first_index[tid] = ok ? cb->first_index[tid] : 0;
+        T.lim[tid] = code_limit(cb, ok, tid);
     }
     for (int i = tid; i < 256; i += blockDim.x) {
         T.sorted[i] = ok ? cb->sorted_symbols[i] : 0;
@@ -173,8 +185,32 @@ __device__ __forceinline__ uint4 load_unit(const uint8_t *p, size_t nbytes, size
 
 // Canonical search for a code longer than the table's W bits: returns
 // (length << 8) | symbol, length 0 if no code matches.
+// The window's code length counted against the limits (no loop-carried
+// search), then its symbol from the canonical arrays.  The caller knows the
+// first code is longer than W bits.
+template <int W, class Tab>
+__device__ __forceinline__ uint32_t long_code_lim(uint32_t top, const Tab &T, int longest) {
+    const uint32_t v = top >> (32 - HUFF_MAX_LEN);
+    uint32_t L = W + 1;
+#pragma unroll
+    for (int l = W + 1; l < HUFF_MAX_LEN; ++l) L += v >= T.lim[l] ? 1u : 0u;
+    const uint32_t d = (v >> (HUFF_MAX_LEN - L)) - T.first_code[L];
+    if (L > static_cast<uint32_t>(longest) || d >= T.bl_count[L]) return 0;
+    return (L << 8) | T.sorted[T.first_index[L] + d];
+}
+
 template <int W>
 __device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W> *T) {
+    return long_code_lim<W>(top, *T, T->longest);
+}
+
+// The same by a search over the lengths.  The fused bf16 decode uses this one:
+// its planes rarely have codes past the window, and the counting form
+// measured 1.2 % slower there (a different register allocation around the
+// call); the byte-stream decodes, whose fixed codebooks often meet data they
+// were not built for (codes of 17 to 24 bits), use the count.
+template <int W>
+__device__ __noinline__ uint32_t long_code_search(uint32_t top, const DecTables<W> *T) {
     const uint32_t v = top >> (32 - HUFF_MAX_LEN);
     for (int l = W + 1; l <= T->longest; ++l) {
         const uint32_t c = v >> (HUFF_MAX_LEN - l);
@@ -270,7 +306,7 @@ struct PlaneDec {
 // The rare cases of a step: a code longer than the table's window (or no
 // code at all: a corrupt stream), and an entry with more symbols than the
 // chunk has left.
-template <int W>
+template <int W, bool LIM>
 __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
                                        uint32_t &bits, uint64_t &v, bool &bad) {
     if (c == 0) {
@@ -285,7 +321,7 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
                 sym = e2 & 0xffu;
             }
         } else {
-            const uint32_t lc = long_code(top, &T);
+            const uint32_t lc = LIM ? long_code(top, &T) : long_code_search(top, &T);
             L = lc >> 8;
             sym = lc & 0xffu;
         }
@@ -309,7 +345,7 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
 // the zero bits on top of the window (up to 32, the chunk's rest and the
 // ring's room) when that beats a lookup; then up to four 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
-template <int RING, bool RUN, int W, bool FAST = false>
+template <int RING, bool RUN, int W, bool LIM, bool FAST = false>
 __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
     static_assert(!(RUN && FAST), "a run step may add more symbols than a fast block reserves");
@@ -339,7 +375,7 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
         v = is_run ? run : v;
     }
     const bool simple = c != 0 && static_cast<int>(c) <= rem;
-    if (go && !simple) step_rare(T, win, s.bh, rem, c, bits, v, bad);
+    if (go && !simple) step_rare<W, LIM>(T, win, s.bh, rem, c, bits, v, bad);
     if (!RUN) {
         // a second, dependent lookup on the bits after the first entry, taken when the first entry was
         // simple (at least 20 valid bits remain) and the two entries together are at most 8 symbols
@@ -392,7 +428,7 @@ __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, siz
 
 // Decode until every lane of the warp has stored symbols [.., need) into its
 // RING-byte ring (a lane whose chunk is complete stores its last partial word).
-template <int RING, bool RUN, int W>
+template <int RING, bool RUN, int W, bool LIM>
 __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                                uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
                                                bool &bad) {
@@ -405,11 +441,11 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
                __any_sync(0xffffffffu, s.st < need)) {
 #pragma unroll
             for (int k = 0; k < kFastSteps; ++k)
-                step<RING, false, W, true>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+                step<RING, false, W, LIM, true>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
         }
     }
     while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
-        step<RING, RUN, W>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+        step<RING, RUN, W, LIM>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
     if (s.fill > 0 && s.st + s.fill == cnt) {
         *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
         s.st = cnt;
@@ -418,13 +454,13 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
     }
 }
 
-template <int RING, int W>
+template <int RING, bool LIM, int W>
 __device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
                                              uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
     if (T.has_run)
-        fill_segment_t<RING, true, W>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, true, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
     else
-        fill_segment_t<RING, false, W>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, false, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
 // The chunk's bit range lies in the payload and holds at least one bit per symbol.
@@ -488,7 +524,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
     const bool whole = __all_sync(0xffffffffu, cnt == warp_cnt);  // every chunk of the warp has the same length
     for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSegU8) {
-        fill_segment<kRingU8>(s, payload, nbytes, T, ring, swz, cnt, min(cnt, seg0 + kSegU8), seg0 + kRingU8, bad);
+        fill_segment<kRingU8, true>(s, payload, nbytes, T, ring, swz, cnt, min(cnt, seg0 + kSegU8), seg0 + kRingU8, bad);
         __syncwarp();
         // copy-out: 8 lanes' segments per pass, 16 bytes per lane
         if (whole && seg0 + kSegU8 <= warp_cnt) {  // every lane's segment is complete: no per-lane bounds
@@ -525,6 +561,207 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
         __syncwarp();
     }
     if (cnt > 0 && (bad || s.pos() != off[c + 1])) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+}
+
+// ------------------------------------------------------------------ byte streams, few chunks
+//
+// With fewer chunks than the GPU has lanes to spare, one lane per chunk
+// leaves most of the GPU idle.  Then a CTA takes one chunk and splits its bit
+// range into S slices, one thread each (S = blockDim.x).  It relies on
+// Huffman codes being self-synchronising: a decode started at an arbitrary
+// bit usually falls onto the true code boundaries within a few codes (the
+// observation behind Klein and Wiseman's parallel decoding and the GPU
+// decoder of Weissenberger and Schmidt).  Three walks over the slice:
+//   1. from the slice's first bit (a true boundary for slice 0; slices start
+//      on multiples of the code lengths' greatest common divisor, so for a
+//      code of one length every slice does) to the first boundary of that
+//      walk at or after the slice's end: the exit;
+//   2. from the previous slice's exit, counting the codes that start in the
+//      slice, to a new exit; repeated while any exit changes.  Slice 0 starts
+//      at the chunk's offset, so after round r slices 0..r are exact and a
+//      round that changes nothing has every exit exact: at most S + 1 rounds,
+//      whatever the code (one that never resynchronises costs a round per
+//      slice);
+//   3. a block scan of the counts gives each slice its first output index;
+//      each slice decodes again from its entry and stores its symbols.
+// The chunk is valid when the counts add up to its symbol count and the last
+// slice's exit is the next chunk's offset.
+constexpr int kSplitMinSyms = 64;  // symbols per slice at least, where the chunk allows 32 slices
+
+// The split decode's copy of a codebook's canonical arrays (shared memory).
+struct SplitTab {
+    uint32_t lim[32];
+    uint32_t first_code[32];
+    uint32_t first_index[32];
+    uint32_t bl_count[32];
+    uint8_t sorted[256];
+};
+
+// The codes that start in [pos, lim): their count, and with WRITE the symbols
+// stored to out[0, room).  pos ends at the walk's first boundary at or after
+// lim.  Every iteration takes at least one bit, so a walk over corrupt data
+// ends as well; `bad` notes bits that are no code.
+template <bool WRITE>
+__device__ uint64_t split_walk(PlaneDec &s, const uint8_t *p, size_t nbytes, const huff_codebook *cb,
+                               const SplitTab &tab, int longest, uint64_t &pos, uint64_t lim, uint8_t *out,
+                               uint64_t room, bool &bad) {
+    uint64_t n = 0;
+    while (pos < lim) {
+        s.refill(p, nbytes);
+        const uint64_t e = __ldg(&cb->lut[s.bh >> (32 - HUFF_LUT_BITS)]);
+        uint32_t c = static_cast<uint32_t>(e >> 48) & 15u;
+        uint32_t bits = static_cast<uint32_t>(e >> 52) & 15u;
+        uint64_t v = e & 0xffffffffffffull;
+        if (c == 0) {  // the first code is longer than the table's window (or no code)
+            const uint32_t lc = long_code_lim<HUFF_LUT_BITS>(s.bh, tab, longest);
+            bits = lc >> 8;
+            v = lc & 0xffu;
+            c = 1;
+            if (bits == 0) {
+                bad = true;
+                bits = 1;
+            }
+        } else if (pos + bits > lim) {  // codes past lim in the entry: only the first starts before it
+            c = 1;
+            v &= 0xffu;
+            bits = __ldg(&cb->len[v]);
+        }
+        if (WRITE) {
+            for (uint32_t k = 0; k < c; ++k)
+                if (n + k < room) out[n + k] = static_cast<uint8_t>(v >> (8 * k));
+        }
+        n += c;
+        pos += bits;
+        s.consume(bits);
+    }
+    return n;
+}
+
+__global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restrict__ payload, size_t nbytes,
+                                                         const uint64_t *__restrict__ off, size_t n, size_t chunk,
+                                                         const huff_codebook *__restrict__ cb,
+                                                         uint8_t *__restrict__ out, int32_t *status) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    const int S = blockDim.x;
+    const int k = threadIdx.x;
+    uint64_t *ex = reinterpret_cast<uint64_t *>(dsm);          // slice exits, S
+    uint64_t *wsum = ex + S;                                    // per-warp count sums, 32
+    SplitTab &tab = *reinterpret_cast<SplitTab *>(wsum + 32);
+    const int longest = cb->longest;
+    if (cb->magic != HUFF_CODEBOOK_MAGIC || longest < 1 || longest > HUFF_MAX_LEN) {
+        if (k == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+        return;
+    }
+    const size_t c = blockIdx.x;
+    const size_t first = c * chunk;
+    const int cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
+    uint64_t start = 0, end = 0;
+    if (!chunk_bounds(off, c, nbytes, cnt, start, end)) {  // the same for the whole CTA
+        if (k == 0) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+        return;
+    }
+    // slice boundaries on multiples of g, the greatest common divisor of the code lengths, from the chunk's
+    // start: a code whose lengths share a divisor (all 8 bits, say) then starts every slice on a boundary
+    uint32_t g = 0;
+    for (int l = 1; l <= longest; ++l) {
+        if (__ldg(&cb->bl_count[l]) == 0) continue;
+        uint32_t a = static_cast<uint32_t>(l), b = g;
+        while (b) {
+            const uint32_t t = a % b;
+            a = b;
+            b = t;
+        }
+        g = a;
+    }
+    if (g == 0) g = 1;
+    if (k < 32) {
+        tab.lim[k] = code_limit(cb, true, k);
+        tab.first_code[k] = cb->first_code[k];
+        tab.first_index[k] = cb->first_index[k];
+        tab.bl_count[k] = cb->bl_count[k];
+    }
+    for (int i = k; i < 256; i += S) tab.sorted[i] = cb->sorted_symbols[i];
+    __syncthreads();
+    const uint64_t span = end - start;
+    const auto bound = [&](int j) -> uint64_t {
+        if (j >= S) return end;
+        const uint64_t b = span * static_cast<uint64_t>(j) / static_cast<uint64_t>(S);
+        return start + b / g * g;
+    };
+    const uint64_t lo = bound(k);
+    const uint64_t hi = bound(k + 1);
+    PlaneDec s;
+    bool unsynced = false;  // walks 1 and 2 may start off the code boundaries: bits that are no code mean nothing
+    bool bad = false;       // walk 3 starts on them
+    // 1. from the slice's first bit
+    uint64_t pos = lo;
+    if (pos < hi) {
+        s.start(payload, nbytes, pos);
+        split_walk<false>(s, payload, nbytes, cb, tab, longest, pos, hi, nullptr, 0, unsynced);
+    }
+    ex[k] = pos;
+    __syncthreads();
+    // 2. from the previous slice's exit until no exit changes
+    uint64_t entry = start, mine = 0;
+    for (int round = 0; round <= S; ++round) {
+        entry = k == 0 ? start : ex[k - 1];
+        pos = entry;
+        mine = 0;
+        if (pos < hi) {
+            s.start(payload, nbytes, pos);
+            mine = split_walk<false>(s, payload, nbytes, cb, tab, longest, pos, hi, nullptr, 0, unsynced);
+        }
+        const bool changed = pos != ex[k];
+        __syncthreads();  // every slice has read its entry
+        ex[k] = pos;
+        if (!__syncthreads_or(changed)) break;
+    }
+    // 3. output indices: exclusive scan of the counts over the block
+    const int lane = k & 31, warp = k >> 5;
+    uint64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = S >> 5;
+        uint64_t w = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nw) wsum[lane] = w;  // inclusive sums of whole warps
+    }
+    __syncthreads();
+    const uint64_t base = incl - mine + (warp ? wsum[warp - 1] : 0);
+    const uint64_t total = wsum[(S >> 5) - 1];
+    if (k == 0 && (total != static_cast<uint64_t>(cnt) || ex[S - 1] != end)) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+    pos = entry;
+    if (pos < hi && base < static_cast<uint64_t>(cnt)) {
+        s.start(payload, nbytes, pos);
+        split_walk<true>(s, payload, nbytes, cb, tab, longest, pos, hi, out + first + base,
+                         static_cast<uint64_t>(cnt) - base, bad);
+    }
+    if (bad) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+}
+
+// Threads per chunk for the split decode, or 0 when one lane per chunk fills the GPU.
+__host__ int split_threads(size_t n_chunks, size_t chunk, int sms) {
+    // the split decode walks every slice three times, so it pays where one lane per chunk would leave the
+    // SMs with fewer than about a third of the lanes they need to run at full rate (several hundred)
+    const size_t lanes = static_cast<size_t>(sms) * 256;
+    if (n_chunks >= lanes) return 0;
+    size_t t = (4 * lanes + n_chunks - 1) / n_chunks;     // about 1024 threads per SM in all
+    t = (t + 31) / 32 * 32;
+    const size_t by_syms = chunk / kSplitMinSyms / 32 * 32;  // slices of kSplitMinSyms symbols at least
+    if (t > by_syms) t = by_syms;
+    if (t > 1024) t = 1024;
+    if (t < 32) t = 32;
+    return static_cast<int>(t);
 }
 
 // ------------------------------------------------------------------ fused bf16
@@ -584,8 +821,8 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
             asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xp));
         }
         const int need = min(cnt, seg0 + kSeg);
-        fill_segment<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
-        fill_segment<kRing>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
+        fill_segment<kRing, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
+        fill_segment<kRing, false>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
         __syncwarp();
         if (whole && seg0 + kSeg <= warp_cnt) {
             // every lane's segment is complete: no per-lane bounds
@@ -668,6 +905,13 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
                      const huff_codebook *cb, uint8_t *out, int32_t *status, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
+    const int split = split_threads(n_chunks, chunk, dev_info().sms);
+    if (split > 0) {
+        const size_t smem = (static_cast<size_t>(split) + 32) * sizeof(uint64_t) + sizeof(SplitTab);
+        k_decode_u8_split<<<static_cast<unsigned>(n_chunks), split, smem, s>>>(payload, bytes, off, n, chunk, cb, out,
+                                                                              status);
+        return launch_status();
+    }
     const int block = decode_block(n_chunks, dev_info().sms);
     const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
     const size_t smem = sizeof(DecTables<13>) + static_cast<size_t>(block) * kRingU8;

@@ -1,0 +1,147 @@
+"""Both byte-stream decode paths, bit-exact.
+
+huff_decode gives every chunk one lane when there are enough chunks to fill
+the GPU (at least 512 per SM).  With fewer, it gives a chunk a CTA and each
+thread a slice of the chunk's bits, found by self-synchronisation (walks from
+arbitrary bits, then from the previous slice's exit until no exit changes).
+These tests size inputs on both sides of that threshold and give the split
+path the codes that make it work hardest:
+- codes of one length (slices start on the lengths' common divisor), and
+  codes that resynchronise only rarely;
+- a single 1-bit code;
+- long codes on data the codebook was not built for;
+- ragged last chunks;
+- corrupt offsets and payloads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_huffman_compression_gb300 import _lib, codec
+from gpu_util import dev_u8, host_u8, oracle_codebook
+
+pytestmark = pytest.mark.gpu
+
+RNG = np.random.default_rng(77)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    _lib.load()
+    assert torch.cuda.is_available()
+
+
+def _gauss(n, sigma, rng=RNG):
+    return np.clip(np.round(rng.normal(0, sigma, n)), -128, 127).astype(np.int8).view(np.uint8)
+
+
+def _round_trip(x: np.ndarray, cb: codec.Codebook, chunk: int) -> None:
+    d = dev_u8(x)
+    s = codec.encode(d, cb, chunk)
+    out = codec.decode(s, cb)
+    np.testing.assert_array_equal(host_u8(out), x)
+
+
+def _lanes_threshold() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count * 512
+
+
+@pytest.mark.parametrize("kind", ["gauss", "skew"])
+def test_one_lane_per_chunk_path(kind):
+    """Enough chunks for one lane each (the split path is not taken), ragged tail."""
+    chunk = 256
+    n = _lanes_threshold() * chunk + 77
+    if kind == "gauss":
+        x = _gauss(n, 8)
+    else:
+        x = RNG.choice(np.array([0, 1, 2, 255], dtype=np.uint8), n, p=[0.95, 0.03, 0.019, 0.001])
+    cb = codec.build_codebook(codec.histogram(dev_u8(x)))
+    _round_trip(x, cb, chunk)
+
+
+@pytest.mark.parametrize("n,chunk", [(1, 256), (1000, 256), (65_536, 65_536), (65_537, 65_536),
+                                     (1_000_003, 1 << 20), (3_000_001, 1 << 22), (200_017, 16_384)])
+def test_split_path_matches_oracle_payload(n, chunk):
+    """The oracle's payload (not the GPU encoder's) decoded by the split path."""
+    x = _gauss(n, 8)
+    ln, cd = oracle_codebook(oracle.histogram(x))
+    pay, off = oracle.encode(x, ln, cd, chunk)
+    cb = codec.codebook_from_lengths(ln)
+    pd = torch.from_numpy(np.concatenate([pay, np.zeros(16, np.uint8)])).cuda()
+    s = codec.Stream(pd, torch.from_numpy(off.astype(np.int64)).cuda(), n, chunk)
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
+    st = codec.new_status()
+    _lib.huff_decode(pd, s.off, n, chunk, cb.buf, out, st, payload_bytes=pay.size)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(host_u8(out), x)
+
+
+@pytest.mark.parametrize("n", [1_000_003, 777_777])
+def test_split_path_codes_of_one_length(n):
+    """256 codes of 8 bits: a walk that starts off the byte grid never meets it, so slices start on
+    multiples of the lengths' common divisor (and the chunk is not a multiple of the slice count)."""
+    cb = codec.build_codebook(torch.full((256,), 1000, dtype=torch.int64, device="cuda"))
+    assert (host_u8(cb.buf)[16:16 + 256] == 8).all()  # len[] follows the four 32-bit header fields
+    x = RNG.integers(0, 256, n, dtype=np.uint8)
+    _round_trip(x, cb, 1 << 20)
+
+
+@pytest.mark.parametrize("n", [1_000_003, 300_001])
+def test_split_path_slow_resynchronisation(n):
+    """Lengths 7, 8 and 9 (common divisor 1) on data of the 8-bit codes only: a walk off the byte
+    grid moves onto it only when it happens to read the 7- or 9-bit code, about once in a hundred
+    codes, so many slices stay off the grid after the first walk and the exit rounds place them."""
+    h = torch.full((256,), 1000, dtype=torch.int64, device="cuda")
+    h[0], h[254], h[255] = 2000, 1, 1
+    cb = codec.build_codebook(h)
+    ln = host_u8(cb.buf)[16:16 + 256]
+    assert sorted(set(ln.tolist())) == [7, 8, 9]
+    eight = np.flatnonzero(ln == 8).astype(np.uint8)
+    x = RNG.choice(eight, n)
+    _round_trip(x, cb, 1 << 20)
+
+
+def test_split_path_single_code_and_two_codes():
+    n = 2_000_001
+    x = np.full(n, 9, np.uint8)
+    _round_trip(x, codec.build_codebook(codec.histogram(dev_u8(x))), 1 << 20)
+    y = RNG.choice(np.array([3, 200], dtype=np.uint8), n, p=[0.5, 0.5])
+    _round_trip(y, codec.build_codebook(codec.histogram(dev_u8(y))), 1 << 20)
+
+
+def test_split_path_long_codes():
+    """A floor-at-1 codebook from narrow data, used on wide data: most codes are 17 to 24 bits."""
+    warm = _gauss(1 << 20, 4)
+    cb = codec.build_codebook(codec.histogram(dev_u8(warm)), flags=_lib.HUFF_COVER_ALL)
+    x = RNG.integers(0, 256, 1_500_007, dtype=np.uint8)
+    _round_trip(x, cb, 1 << 18)
+
+
+def test_split_path_corrupt_streams_detected():
+    n, chunk = 600_000, 1 << 17
+    x = _gauss(n, 8)
+    d = dev_u8(x)
+    cb = codec.build_codebook(codec.histogram(d))
+    s = codec.encode(d, cb, chunk)
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
+    for bump in (1, -1, 8):
+        off = s.off.clone()
+        off[2] += bump
+        st = codec.new_status()
+        _lib.huff_decode(s.payload, off, n, chunk, cb.buf, out, st, payload_bytes=s.nbytes())
+        torch.cuda.synchronize()
+        assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+    st = codec.new_status()
+    _lib.huff_decode(s.payload, s.off, n, chunk, cb.buf, out, st, payload_bytes=s.nbytes() - 1)
+    torch.cuda.synchronize()
+    assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+    # a count that is not the stream's: more symbols than the last chunk holds
+    st = codec.new_status()
+    _lib.huff_decode(s.payload, s.off, n + 5, chunk, cb.buf, torch.empty(n + 5, dtype=torch.uint8, device="cuda"),
+                     st, payload_bytes=s.nbytes())
+    torch.cuda.synchronize()
+    assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
