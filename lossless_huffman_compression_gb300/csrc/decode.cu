@@ -245,6 +245,7 @@ constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
 constexpr int kStepMax = 8;    // symbols a table step may add (a run step: up to 32, within the ring's room)
 constexpr int kFastSteps = 2;  // steps per unchecked block on a plane without runs
 constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
+constexpr int kPairBlock = 448;  // at most this many lanes per SM: the fused bf16 decode steps both planes in one loop
 static_assert(kRing >= kSeg + 7 + 2 * kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
 static_assert(HUFF_LUT_SYMS <= kStepMax, "a table entry must fit one step");
 
@@ -451,6 +452,51 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
         s.st = cnt;
         s.fill = 0;
         s.a0 = 0;
+    }
+}
+
+// Both planes of a lane in one loop, a step of each per pass, both steps
+// predicated in one block: two independent dependency chains per lane, for
+// launches with few lanes per SM (where issue slots are idle).  A plane that
+// is ahead keeps decoding into its ring's room or takes empty steps.
+template <int RING, bool RUN_H, bool RUN_L>
+__device__ __forceinline__ void fill_pair_t(PlaneDec &h, PlaneDec &l, const uint8_t *ph, size_t nh, const uint8_t *pl,
+                                            size_t nl, const DecTables<12> &Th, const DecTables<13> &Tl,
+                                            uint8_t *hring, uint8_t *lring, uint32_t swz, int cnt, int need,
+                                            int limit, bool &bad) {
+    const uint64_t run_h = RUN_H ? Th.run : 0ull, run_l = RUN_L ? Tl.run : 0ull;
+    while (__any_sync(0xffffffffu,
+                      (h.st < need && h.st + h.fill != cnt) || (l.st < need && l.st + l.fill != cnt))) {
+        step<RING, RUN_H, 12, false>(h, ph, nh, Th, hring, swz, cnt, limit, run_h, bad);
+        step<RING, RUN_L, 13, false>(l, pl, nl, Tl, lring, swz, cnt, limit, run_l, bad);
+    }
+    for (int q = 0; q < 2; ++q) {  // a chunk's last partial words
+        PlaneDec &s = q ? l : h;
+        uint8_t *ring = q ? lring : hring;
+        if (s.fill > 0 && s.st + s.fill == cnt) {
+            *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
+            s.st = cnt;
+            s.fill = 0;
+            s.a0 = 0;
+        }
+    }
+}
+
+template <int RING>
+__device__ __forceinline__ void fill_pair(PlaneDec &h, PlaneDec &l, const uint8_t *ph, size_t nh, const uint8_t *pl,
+                                          size_t nl, const DecTables<12> &Th, const DecTables<13> &Tl,
+                                          uint8_t *hring, uint8_t *lring, uint32_t swz, int cnt, int need, int limit,
+                                          bool &bad) {
+    if (Th.has_run) {
+        if (Tl.has_run)
+            fill_pair_t<RING, true, true>(h, l, ph, nh, pl, nl, Th, Tl, hring, lring, swz, cnt, need, limit, bad);
+        else
+            fill_pair_t<RING, true, false>(h, l, ph, nh, pl, nl, Th, Tl, hring, lring, swz, cnt, need, limit, bad);
+    } else {
+        if (Tl.has_run)
+            fill_pair_t<RING, false, true>(h, l, ph, nh, pl, nl, Th, Tl, hring, lring, swz, cnt, need, limit, bad);
+        else
+            fill_pair_t<RING, false, false>(h, l, ph, nh, pl, nl, Th, Tl, hring, lring, swz, cnt, need, limit, bad);
     }
 }
 
@@ -771,8 +817,8 @@ __host__ int split_threads(size_t n_chunks, size_t chunk, int sms) {
 // the other; each ring's two 32-byte halves swapped on every second lane
 // pair), then the warp merges 8 lanes' segments per pass: bytes to 16-bit
 // words, XOR x0, 16-byte streaming stores.
-template <bool XOR>
-__global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
+template <bool XOR, bool PAIR>
+__global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf16(
     const uint8_t *__restrict__ pay_hi, size_t bytes_hi, const uint64_t *__restrict__ off_hi,
     const uint8_t *__restrict__ pay_lo, size_t bytes_lo, const uint64_t *__restrict__ off_lo, size_t n,
     size_t chunk, const huff_codebook *__restrict__ cb_hi, const huff_codebook *__restrict__ cb_lo,
@@ -821,8 +867,13 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_bf16(
             asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xp));
         }
         const int need = min(cnt, seg0 + kSeg);
-        fill_segment<kRing, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
-        fill_segment<kRing, false>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
+        if (PAIR) {
+            fill_pair<kRing>(h, l, pay_hi, bytes_hi, pay_lo, bytes_lo, Th, Tl, hring, lring, swz, cnt, need, seg0 + kRing,
+                             bad);
+        } else {
+            fill_segment<kRing, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
+            fill_segment<kRing, false>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
+        }
         __syncwarp();
         if (whole && seg0 + kSeg <= warp_cnt) {
             // every lane's segment is complete: no per-lane bounds
@@ -931,19 +982,22 @@ int launch_decode_bf16(const uint8_t *pay_hi, size_t bytes_hi, const uint64_t *o
     const int block = decode_block(n_chunks, dev_info().sms);
     const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
     const size_t smem = kBf16Tables + static_cast<size_t>(block) * (2 * kRing);
-    if (x0 != nullptr) {
-        if (cudaFuncSetAttribute(k_decode_bf16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
+    const auto go = [&](auto kern, const uint16_t *x) -> int {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
             return HUFF_ERR_CUDA;
-        k_decode_bf16<true><<<grid, block, smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n, chunk,
-                                                      cb_hi, cb_lo, x0, out, status);
-    } else {
-        if (cudaFuncSetAttribute(k_decode_bf16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return HUFF_ERR_CUDA;
-        k_decode_bf16<false><<<grid, block, smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n,
-                                                       chunk, cb_hi, cb_lo, nullptr, out, status);
-    }
+        kern<<<grid, block, smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n, chunk, cb_hi, cb_lo, x,
+                                       out, status);
+        return HUFF_OK;
+    };
+    // few lanes per SM: both planes stepped in one loop
+    const bool pair = block <= kPairBlock;
+    int st;
+    if (x0 != nullptr)
+        st = pair ? go(k_decode_bf16<true, true>, x0) : go(k_decode_bf16<true, false>, x0);
+    else
+        st = pair ? go(k_decode_bf16<false, true>, nullptr) : go(k_decode_bf16<false, false>, nullptr);
+    if (st != HUFF_OK) return st;
     return launch_status();
 }
 
