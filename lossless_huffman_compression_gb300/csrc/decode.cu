@@ -647,11 +647,57 @@ struct SplitTab {
 // stored to out[0, room).  pos ends at the walk's first boundary at or after
 // lim.  Every iteration takes at least one bit, so a walk over corrupt data
 // ends as well; `bad` notes bits that are no code.
+// A slice's output bytes, stored as aligned 8-byte words.  Its first and
+// last words may hold other slices' bytes, so those two are written byte by
+// byte (the slice's own bytes only); every word between them in one store.
+struct WordOut {
+    uint8_t *w;     // the aligned word being filled
+    uint64_t acc;   // its bytes so far, byte k of the word in byte k
+    uint32_t f;     // position of the next byte in the word
+    uint32_t f0;    // the slice's first byte in the word (nonzero only in the slice's first word)
+    uint64_t left;  // bytes the slice may still write
+    __device__ __forceinline__ void init(uint8_t *o, uint64_t room) {
+        f0 = f = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(o) & 7u);
+        w = o - f;
+        acc = 0;
+        left = room;
+    }
+    __device__ __forceinline__ void bytes(uint32_t upto) {  // bytes [f0, upto) of the word
+        for (uint32_t k = f0; k < upto; ++k) w[k] = static_cast<uint8_t>(acc >> (8 * k));
+    }
+    __device__ __forceinline__ void put(uint64_t v, uint32_t c) {  // c <= 6 bytes, v's higher bytes zero
+        if (c > left) {  // only a corrupt chunk decodes more symbols than it holds
+            c = static_cast<uint32_t>(left);
+            v &= (1ull << (8 * c)) - 1ull;
+        }
+        left -= c;
+        acc |= v << (8 * f);
+        const uint32_t nf = f + c;
+        if (nf >= 8) {  // the word is complete (f >= 2 here, so the carry shift is 16..48)
+            if (f0 == 0)
+                *reinterpret_cast<uint64_t *>(w) = acc;
+            else
+                bytes(8);
+            w += 8;
+            f0 = 0;
+            acc = v >> (8 * (8 - f));
+            f = nf - 8;
+        } else {
+            f = nf;
+        }
+    }
+    __device__ __forceinline__ void finish() {
+        if (f > f0) bytes(f);
+    }
+};
+
 template <bool WRITE>
 __device__ uint64_t split_walk(PlaneDec &s, const uint8_t *p, size_t nbytes, const huff_codebook *cb,
                                const SplitTab &tab, int longest, uint64_t &pos, uint64_t lim, uint8_t *out,
                                uint64_t room, bool &bad) {
     uint64_t n = 0;
+    WordOut wo;
+    if (WRITE) wo.init(out, room);
     while (pos < lim) {
         s.refill(p, nbytes);
         const uint64_t e = __ldg(&cb->lut[s.bh >> (32 - HUFF_LUT_BITS)]);
@@ -672,14 +718,12 @@ __device__ uint64_t split_walk(PlaneDec &s, const uint8_t *p, size_t nbytes, con
             v &= 0xffu;
             bits = __ldg(&cb->len[v]);
         }
-        if (WRITE) {
-            for (uint32_t k = 0; k < c; ++k)
-                if (n + k < room) out[n + k] = static_cast<uint8_t>(v >> (8 * k));
-        }
+        if (WRITE) wo.put(v, c);
         n += c;
         pos += bits;
         s.consume(bits);
     }
+    if (WRITE) wo.finish();
     return n;
 }
 
