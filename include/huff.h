@@ -316,7 +316,8 @@ int huff_stream_copy(const uint8_t *payload, size_t payload_bytes, const uint64_
  *   out           n bytes, 16-byte aligned.
  *   status        HUFF_ERR_CORRUPT_STREAM when a code is invalid, a chunk does
  *                 not end exactly at the next offset, an offset lies outside
- *                 the payload, or a chunk holds fewer bits than symbols;
+ *                 the payload, or a chunk holds fewer than 1 or more than
+ *                 HUFF_MAX_LEN bits per symbol;
  *                 HUFF_ERR_INVALID_CODEBOOK.
  */
 int huff_decode(const uint8_t *payload, size_t payload_bytes, const uint64_t *chunk_bit_off,

@@ -509,12 +509,14 @@ __device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size
         fill_segment_t<RING, false, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
-// The chunk's bit range lies in the payload and holds at least one bit per symbol.
+// The chunk's bit range lies in the payload and holds between one and
+// HUFF_MAX_LEN bits per symbol.
 __device__ __forceinline__ bool chunk_bounds(const uint64_t *off, size_t c, size_t nbytes, int cnt, uint64_t &start,
                                              uint64_t &end) {
     start = off[c];
     end = off[c + 1];
-    return start <= end && end <= static_cast<uint64_t>(nbytes) * 8 && end - start >= static_cast<uint64_t>(cnt);
+    return start <= end && end <= static_cast<uint64_t>(nbytes) * 8 && end - start >= static_cast<uint64_t>(cnt) &&
+           end - start <= static_cast<uint64_t>(cnt) * HUFF_MAX_LEN;
 }
 
 // Launch geometry: one lane per chunk (pair), blocks spread over every SM.
@@ -691,11 +693,13 @@ struct WordOut {
     }
 };
 
+// Positions are relative to the slice's first bit (32 bits: a chunk holds at
+// most 2^30 * 24 bits and has at least 32 slices).
 template <bool WRITE>
-__device__ uint64_t split_walk(PlaneDec &s, const uint8_t *p, size_t nbytes, const huff_codebook *cb,
-                               const SplitTab &tab, int longest, uint64_t &pos, uint64_t lim, uint8_t *out,
+__device__ uint32_t split_walk(PlaneDec &s, const uint8_t *p, size_t nbytes, const huff_codebook *cb,
+                               const SplitTab &tab, int longest, uint32_t &pos, uint32_t lim, uint8_t *out,
                                uint64_t room, bool &bad) {
-    uint64_t n = 0;
+    uint32_t n = 0;
     WordOut wo;
     if (WRITE) wo.init(out, room);
     while (pos < lim) {
@@ -784,10 +788,14 @@ __global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restr
     bool unsynced = false;  // walks 1 and 2 may start off the code boundaries: bits that are no code mean nothing
     bool bad = false;       // walk 3 starts on them
     // 1. from the slice's first bit
+    // (every entry and exit of slice k is at or after lo: an exit is at or after its own slice's end)
+    const uint32_t rl = static_cast<uint32_t>(hi - lo);
     uint64_t pos = lo;
-    if (pos < hi) {
-        s.start(payload, nbytes, pos);
-        split_walk<false>(s, payload, nbytes, cb, tab, longest, pos, hi, nullptr, 0, unsynced);
+    if (lo < hi) {
+        s.start(payload, nbytes, lo);
+        uint32_t rp = 0;
+        split_walk<false>(s, payload, nbytes, cb, tab, longest, rp, rl, nullptr, 0, unsynced);
+        pos = lo + rp;
     }
     ex[k] = pos;
     __syncthreads();
@@ -797,9 +805,11 @@ __global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restr
         entry = k == 0 ? start : ex[k - 1];
         pos = entry;
         mine = 0;
-        if (pos < hi) {
-            s.start(payload, nbytes, pos);
-            mine = split_walk<false>(s, payload, nbytes, cb, tab, longest, pos, hi, nullptr, 0, unsynced);
+        if (entry < hi) {
+            s.start(payload, nbytes, entry);
+            uint32_t rp = static_cast<uint32_t>(entry - lo);
+            mine = split_walk<false>(s, payload, nbytes, cb, tab, longest, rp, rl, nullptr, 0, unsynced);
+            pos = lo + rp;
         }
         const bool changed = pos != ex[k];
         __syncthreads();  // every slice has read its entry
@@ -830,10 +840,10 @@ __global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restr
     const uint64_t base = incl - mine + (warp ? wsum[warp - 1] : 0);
     const uint64_t total = wsum[(S >> 5) - 1];
     if (k == 0 && (total != static_cast<uint64_t>(cnt) || ex[S - 1] != end)) set_status(status, HUFF_ERR_CORRUPT_STREAM);
-    pos = entry;
-    if (pos < hi && base < static_cast<uint64_t>(cnt)) {
-        s.start(payload, nbytes, pos);
-        split_walk<true>(s, payload, nbytes, cb, tab, longest, pos, hi, out + first + base,
+    if (entry < hi && base < static_cast<uint64_t>(cnt)) {
+        s.start(payload, nbytes, entry);
+        uint32_t rp = static_cast<uint32_t>(entry - lo);
+        split_walk<true>(s, payload, nbytes, cb, tab, longest, rp, rl, out + first + base,
                          static_cast<uint64_t>(cnt) - base, bad);
     }
     if (bad) set_status(status, HUFF_ERR_CORRUPT_STREAM);

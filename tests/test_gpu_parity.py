@@ -265,20 +265,22 @@ def test_corrupt_offsets_and_truncation_detected():
     assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
 
 
-def test_chunk_with_fewer_bits_than_symbols_and_empty_payload_are_corrupt():
-    """Every code is at least one bit long, so a chunk of c symbols spans at least c bits; the
-    decoder rejects a shorter chunk before it reads anything, which also covers an empty payload."""
+def test_chunk_bit_counts_out_of_range_and_empty_payload_are_corrupt():
+    """Codes are 1 to 24 bits long, so a chunk of c symbols spans c to 24 c bits; the decoder
+    rejects any other chunk before it reads anything, which also covers an empty payload."""
     x = _data("gauss", 40_000)
     d = dev_u8(x)
     cb = codec.build_codebook(codec.histogram(d))
     s = codec.encode(d, cb, 4096)
-    off = s.off.clone()
-    off[2] = off[1] + 4095  # chunk 1: 4096 symbols in 4095 bits
     out = torch.empty(x.size, dtype=torch.uint8, device="cuda")
-    st = codec.new_status()
-    _lib.huff_decode(s.payload, off, s.n, 4096, cb.buf, out, st, payload_bytes=s.nbytes())
-    torch.cuda.synchronize()
-    assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+    for span in (4095, 24 * 4096 + 1):  # chunk 1: 4096 symbols in fewer than 1 or more than 24 bits each
+        off = s.off.clone()
+        off[2] = off[1] + span
+        assert int(off[2]) <= 8 * s.nbytes()
+        st = codec.new_status()
+        _lib.huff_decode(s.payload, off, s.n, 4096, cb.buf, out, st, payload_bytes=s.nbytes())
+        torch.cuda.synchronize()
+        assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
     zero = torch.zeros_like(s.off)
     st = codec.new_status()
     _lib.huff_decode(s.payload, zero, s.n, 4096, cb.buf, out, st, payload_bytes=0)
