@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -95,9 +96,15 @@ def hbm_peak():
 
 
 def kernel_hash(name: str) -> str:
+    """Hash of the kernel's source file without its comments and blank space, so that a comment edit
+    keeps a traffic record that the code it was measured on still matches."""
     src = os.path.join(ROOT, "lossless_huffman_compression_gb300", "csrc", KERNEL_SOURCES[name])
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(src, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
 def recorded_traffic(name: str, units: float):

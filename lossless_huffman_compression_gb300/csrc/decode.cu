@@ -8,12 +8,17 @@
 //
 // GPU design:
 //   * one lane per chunk (per chunk pair for bf16), every lane of the grid
-//     resident at once; the block size follows the chunk count;
+//     resident at once; the block size follows the chunk count.  With fewer
+//     than 256 chunks per SM, byte streams instead split each chunk over a
+//     CTA by self-synchronisation (the section on few chunks below), and
+//     with at most 448 lanes per SM the fused bf16 decode steps both planes
+//     of a lane in one loop;
 //   * shared tables per plane: a window table of 2^W 64-bit entries (W = 12
 //     for the high plane, 13 for the low plane and byte streams), each
 //     listing the codes wholly inside the next W bits (up to six symbols,
 //     their count and total length), a secondary table for longer codes and
-//     the canonical arrays for a search when that table would not fit;
+//     the canonical arrays for when that table would not fit (byte streams
+//     count the length limits a window reaches; the bf16 planes search);
 //   * the bit reader keeps 64 bits in two registers and refills 32 at a time
 //     from a queue of the current 16-byte unit of the stream; units are read
 //     whole, the payload's last unit standing in for any unit past it;
