@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
 //      each slice decodes again from its entry and stores its symbols.
 // The chunk is valid when the counts add up to its symbol count and the last
 // slice's exit is the next chunk's offset.
-constexpr int kSplitMinSyms = 64;  // symbols per slice at least, where the chunk allows 32 slices
+constexpr int kSplitMinSyms = 16;  // symbols per slice at least, where the chunk allows 32 slices
 
 // The split decode's copy of a codebook's canonical arrays (shared memory).
 struct SplitTab {
