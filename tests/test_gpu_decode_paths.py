@@ -1,7 +1,7 @@
 """Both byte-stream decode paths, bit-exact.
 
 huff_decode gives every chunk one lane when there are enough chunks to fill
-the GPU (at least 512 per SM).  With fewer, it gives a chunk a CTA and each
+the GPU (at least 256 per SM).  With fewer, it gives a chunk a CTA and each
 thread a slice of the chunk's bits, found by self-synchronisation (walks from
 arbitrary bits, then from the previous slice's exit until no exit changes).
 These tests size inputs on both sides of that threshold and give the split
@@ -46,6 +46,7 @@ def _round_trip(x: np.ndarray, cb: codec.Codebook, chunk: int) -> None:
 
 
 def _lanes_threshold() -> int:
+    # twice the chunk count below which the split decode is taken
     return torch.cuda.get_device_properties(0).multi_processor_count * 512
 
 
