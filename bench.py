@@ -654,7 +654,7 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
     d_x0 = [torch.empty_like(path.x0) for _ in range(nbuf)]
     d_out = [torch.empty_like(path.out) for _ in range(nbuf)]
     s_in, s_in2, s_comp, s_rt, s_dec, s_out = (torch.cuda.Stream() for _ in range(6))
-    steps = max(3, min(args.steps, 12))
+    steps = max(3, min(args.steps, 24))  # the pipeline fills and drains over about one step
     free_in = [torch.cuda.Event() for _ in range(nbuf)]   # buffer k % nbuf's inputs may be overwritten
     free_out = [torch.cuda.Event() for _ in range(nbuf)]  # buffer k % nbuf's output has reached the host
     free_path = [torch.cuda.Event() for _ in paths]       # path k % 2's streams and codebooks are done with
