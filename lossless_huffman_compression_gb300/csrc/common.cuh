@@ -179,7 +179,6 @@ int launch_drift_check(const uint64_t *hist, const huff_codebook *cb, double thr
                        double *gap, cudaStream_t s);
 int launch_codebook_from_lengths(int max_len, huff_codebook *cb, int32_t *status, cudaStream_t s);
 
-size_t enc_u8_tiles(size_t n);
 size_t enc_u8_seg_tiles(size_t n);
 size_t enc_u8_workspace_words(size_t n);
 size_t enc_bf16_tiles(size_t n);

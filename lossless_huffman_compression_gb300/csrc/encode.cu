@@ -1592,8 +1592,6 @@ __global__ void k_encode_empty(uint64_t *off0, uint64_t *off1) {
 
 }  // namespace
 
-size_t enc_u8_tiles(size_t n) { return (n + kEncU8Tile - 1) / kEncU8Tile; }
-
 // Tiles per segment of the byte-stream encode: 16 when there are at least 8192
 // tiles per 16 of them (two segments and more for every warp of a large GPU),
 // fewer down to 4 for smaller inputs, so that small inputs still fill the GPU.
