@@ -466,6 +466,67 @@ int lmc_decode_bf16(const uint8_t *payload_hi, size_t bytes_hi, const uint64_t *
  */
 int huff_code_stats(const uint64_t *h_hist, const uint8_t *h_len, huff_stats *out);
 
+/*
+ * Serialised stream (a container) [P1 Methodology: with a fixed codebook the
+ * per-message codebook is neither recomputed nor transmitted; P2 framework:
+ * the compressed data and what decompression needs].  All fields little-endian,
+ * on HOST memory, no padding:
+ *   offset  0  uint32 magic HUFF_CONTAINER_MAGIC ("HUFC")
+ *           4  uint16 version (1)
+ *           6  uint16 flags: bit 0 set when the 256 code lengths follow the
+ *                    header (per-shard mode); clear for a fixed codebook,
+ *                    which the receiver already holds
+ *           8  uint32 max_len the codebook was built with
+ *          12  uint32 zero
+ *          16  uint64 n (symbols)
+ *          24  uint64 chunk_bytes
+ *          32  uint64 n_chunks = huff_num_chunks(n, chunk_bytes)
+ *          40  uint64 T (total bits) = chunk_bit_off[n_chunks]
+ *          48  [uint8 len[256] when flag bit 0]
+ *          then uint64 chunk_bit_off[n_chunks + 1], then the payload's first
+ *          ceil(T / 8) bytes.
+ */
+#define HUFF_CONTAINER_MAGIC 0x43465548u
+#define HUFF_CONTAINER_HEADER 48
+#define HUFF_CONTAINER_LENGTHS 1u
+
+/* Bytes of a container for n symbols, chunk_bytes, T bits; with_lengths: flag bit 0. */
+size_t huff_container_size(size_t n, size_t chunk_bytes, uint64_t total_bits, int with_lengths);
+
+/*
+ * huff_container_write -- serialise a stream (HOST buffers; no device work).
+ *   h_len     HOST uint8[256] code lengths, or NULL for a fixed codebook.
+ *   h_off     HOST uint64[n_chunks + 1] chunk bit offsets; h_off[n_chunks] = T.
+ *   h_payload HOST payload, at least ceil(T / 8) bytes.
+ *   h_dst     HOST buffer of cap bytes; *written gets the container's size.
+ * Returns HUFF_ERR_INVALID_ARG for a bad chunk size, offsets that are not
+ * non-decreasing from 0, or lengths above max_len; HUFF_ERR_BUFFER_TOO_SMALL
+ * when cap < huff_container_size(...).
+ */
+int huff_container_write(uint8_t *h_dst, size_t cap, size_t n, size_t chunk_bytes, int max_len,
+                         const uint8_t *h_len, const uint64_t *h_off, const uint8_t *h_payload,
+                         size_t *written);
+
+/* A parsed container: the fields, and pointers into the parsed buffer. */
+typedef struct huff_container_view {
+    uint64_t n, chunk_bytes, n_chunks, total_bits;
+    int32_t max_len;
+    int32_t has_lengths;
+    const uint8_t *len;       /* 256 lengths, or NULL */
+    const uint8_t *off;       /* (n_chunks + 1) little-endian uint64, unaligned in general */
+    const uint8_t *payload;   /* ceil(T / 8) bytes */
+    uint64_t payload_bytes;
+} huff_container_view;
+
+/*
+ * huff_container_parse -- check and view a container of size bytes (HOST; no
+ * copy).  Returns HUFF_ERR_CORRUPT_STREAM when the magic, version, reserved
+ * field or sizes do not agree, n_chunks is not huff_num_chunks(n,
+ * chunk_bytes), the offsets do not rise from 0 to T, or a length exceeds
+ * max_len; HUFF_ERR_INVALID_ARG for NULL pointers.
+ */
+int huff_container_parse(const uint8_t *h_src, size_t size, huff_container_view *view);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,6 +35,9 @@ HUFF_CODEBOOK_MAGIC = 0x48554642
 HUFF_NOALLOC_MAX_SYMBOLS = 1 << 30
 HUFF_COUNT_SEGMENT = 131072
 CODEBOOK_LEN_OFFSET = 16  # byte offset of len[256] inside huff_codebook
+HUFF_CONTAINER_MAGIC = 0x43465548
+HUFF_CONTAINER_HEADER = 48
+HUFF_CONTAINER_LENGTHS = 1
 
 EXPORTS = (
     "huff_version", "huff_status_string", "huff_codebook_size", "huff_encode_bound", "huff_workspace_size",
@@ -43,7 +46,7 @@ EXPORTS = (
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
     "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
     "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if", "huff_build_codebooks",
-    "huff_stream_copy",
+    "huff_stream_copy", "huff_container_size", "huff_container_write", "huff_container_parse",
 )
 
 
@@ -56,6 +59,13 @@ class HuffError(RuntimeError):
 class HuffStats(ctypes.Structure):
     _fields_ = [("n", ctypes.c_uint64), ("total_bits", ctypes.c_uint64), ("entropy_bits", ctypes.c_double),
                 ("mean_len", ctypes.c_double), ("shannon_gap", ctypes.c_double)]
+
+
+class HuffContainerView(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_uint64), ("chunk_bytes", ctypes.c_uint64), ("n_chunks", ctypes.c_uint64),
+                ("total_bits", ctypes.c_uint64), ("max_len", ctypes.c_int32), ("has_lengths", ctypes.c_int32),
+                ("len", ctypes.c_void_p), ("off", ctypes.c_void_p), ("payload", ctypes.c_void_p),
+                ("payload_bytes", ctypes.c_uint64)]
 
 
 _lib = None
@@ -96,6 +106,9 @@ def load(path: str = LIB_PATH):
         "lmc_encode_bf16": (I, [P, P, S, P, P, S, P, S, P, P, S, P, P, S, P, P]),
         "lmc_decode_bf16": (I, [P, S, P, P, S, P, S, S, P, P, P, P, P, P]),
         "huff_code_stats": (I, [P, P, ctypes.POINTER(HuffStats)]),
+        "huff_container_size": (S, [S, S, ctypes.c_uint64, I]),
+        "huff_container_write": (I, [P, S, S, S, I, P, P, P, ctypes.POINTER(S)]),
+        "huff_container_parse": (I, [P, S, ctypes.POINTER(HuffContainerView)]),
         "lmc_segment_counts_size": (S, [S]),
         "huff_drift_check": (I, [P, P, ctypes.c_double, P, P, P]),
         "huff_build_codebook_if": (I, [P, P, I, ctypes.c_uint, P, P, P]),
@@ -369,3 +382,41 @@ def huff_code_stats(hist, lengths) -> dict:
     _check("huff_code_stats", st)
     return {"n": int(out.n), "total_bits": int(out.total_bits), "entropy_bits": out.entropy_bits,
             "mean_len": out.mean_len, "shannon_gap": out.shannon_gap}
+
+
+def huff_container_size(n: int, chunk_bytes: int, total_bits: int, with_lengths: bool) -> int:
+    return int(load().huff_container_size(n, chunk_bytes, total_bits, 1 if with_lengths else 0))
+
+
+def huff_container_write(n: int, chunk_bytes: int, max_len: int, lengths, off, payload) -> bytes:
+    """Host helper: the container bytes of a stream (lengths None for a fixed codebook)."""
+    o = np.ascontiguousarray(np.asarray(off, dtype=np.uint64))
+    pay = np.ascontiguousarray(np.asarray(payload, dtype=np.uint8))
+    ln = None if lengths is None else np.ascontiguousarray(np.asarray(lengths, dtype=np.uint8).reshape(256))
+    T = int(o[-1]) if o.size else 0
+    size = huff_container_size(n, chunk_bytes, T, ln is not None)
+    dst = np.empty(size, dtype=np.uint8)
+    written = ctypes.c_size_t(0)
+    st = load().huff_container_write(dst.ctypes.data, size, n, chunk_bytes, max_len,
+                                     None if ln is None else ln.ctypes.data, o.ctypes.data, pay.ctypes.data,
+                                     ctypes.byref(written))
+    _check("huff_container_write", st)
+    return dst[: written.value].tobytes()
+
+
+def huff_container_parse(buf) -> dict:
+    """Host helper: the fields of a container, with copies of its lengths, offsets and payload."""
+    src = np.frombuffer(buf, dtype=np.uint8)
+    v = HuffContainerView()
+    st = load().huff_container_parse(src.ctypes.data, src.size, ctypes.byref(v))
+    _check("huff_container_parse", st)
+    base = src.ctypes.data
+
+    def view(ptr, count):
+        return src[ptr - base: ptr - base + count]
+
+    off = view(v.off, 8 * (v.n_chunks + 1)).copy().view("<u8").astype(np.uint64)
+    return {"n": int(v.n), "chunk_bytes": int(v.chunk_bytes), "n_chunks": int(v.n_chunks),
+            "total_bits": int(v.total_bits), "max_len": int(v.max_len),
+            "lengths": view(v.len, 256).copy() if v.has_lengths else None,
+            "off": off, "payload": view(v.payload, int(v.payload_bytes)).copy()}

@@ -195,6 +195,32 @@ def compress(x: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, max_len: int = 2
     return cb, encode(x, cb, chunk_bytes, max_len)
 
 
+def to_container(s: Stream, cb: Codebook | None = None, max_len: int = 24) -> bytes:
+    """The stream as container bytes (huff_container_write).  With cb (per-shard mode) the container
+    carries cb's 256 code lengths; without (a fixed codebook the receiver holds) it does not."""
+    T = s.total_bits()
+    off = s.off.cpu().numpy().astype(np.uint64)
+    payload = s.payload[: (T + 7) // 8].cpu().numpy()
+    return _lib.huff_container_write(s.n, s.chunk_bytes, max_len, None if cb is None else cb.lengths(), off,
+                                     payload)
+
+
+def from_container(buf, cb: Codebook | None = None, device=None) -> tuple[Stream, Codebook]:
+    """A container's stream on the device and its codebook: imported from the carried lengths, or the
+    fixed codebook cb the caller holds."""
+    f = _lib.huff_container_parse(buf)
+    device = torch.device("cuda") if device is None else torch.device(device)
+    pb = f["payload"].size
+    payload = torch.zeros(((pb + 15) // 16) * 16 + 16, dtype=torch.uint8, device=device)
+    payload[:pb] = torch.from_numpy(f["payload"]).to(device)
+    off = torch.from_numpy(f["off"].astype(np.int64)).to(device)
+    if f["lengths"] is not None:
+        cb = codebook_from_lengths(f["lengths"], f["max_len"], device)
+    elif cb is None:
+        raise ValueError("a fixed-codebook container carries no lengths: pass the codebook")
+    return Stream(payload, off, f["n"], f["chunk_bytes"]), cb
+
+
 @dataclass
 class Bf16Streams:
     cb_hi: Codebook

@@ -328,4 +328,103 @@ int huff_code_stats(const uint64_t *h_hist, const uint8_t *h_len, huff_stats *ou
     return st;
 }
 
+
+// ---------------------------------------------------------------- container (host only)
+
+static void le_put(uint8_t *p, uint64_t v, int bytes) {
+    for (int k = 0; k < bytes; ++k) p[k] = static_cast<uint8_t>(v >> (8 * k));
+}
+static uint64_t le_get(const uint8_t *p, int bytes) {
+    uint64_t v = 0;
+    for (int k = 0; k < bytes; ++k) v |= static_cast<uint64_t>(p[k]) << (8 * k);
+    return v;
+}
+
+size_t huff_container_size(size_t n, size_t chunk_bytes, uint64_t total_bits, int with_lengths) {
+    return HUFF_CONTAINER_HEADER + (with_lengths ? 256 : 0) + 8 * (huff_num_chunks(n, chunk_bytes) + 1) +
+           static_cast<size_t>((total_bits + 7) / 8);
+}
+
+int huff_container_write(uint8_t *h_dst, size_t cap, size_t n, size_t chunk_bytes, int max_len,
+                         const uint8_t *h_len, const uint64_t *h_off, const uint8_t *h_payload,
+                         size_t *written) {
+    if (h_dst == nullptr || h_off == nullptr || written == nullptr || !chunk_ok(chunk_bytes) || n > kMaxN ||
+        max_len < 1 || max_len > HUFF_MAX_LEN)
+        return HUFF_ERR_INVALID_ARG;
+    const size_t nc = huff_num_chunks(n, chunk_bytes);
+    if (h_off[0] != 0) return HUFF_ERR_INVALID_ARG;
+    for (size_t c = 0; c < nc; ++c)
+        if (h_off[c + 1] < h_off[c]) return HUFF_ERR_INVALID_ARG;
+    const uint64_t T = h_off[nc];
+    if (T > 0 && h_payload == nullptr) return HUFF_ERR_INVALID_ARG;
+    if (h_len != nullptr)
+        for (int s = 0; s < 256; ++s)
+            if (h_len[s] > max_len) return HUFF_ERR_INVALID_ARG;
+    const size_t size = huff_container_size(n, chunk_bytes, T, h_len != nullptr);
+    if (cap < size) return HUFF_ERR_BUFFER_TOO_SMALL;
+    uint8_t *p = h_dst;
+    le_put(p, HUFF_CONTAINER_MAGIC, 4);
+    le_put(p + 4, 1, 2);
+    le_put(p + 6, h_len != nullptr ? HUFF_CONTAINER_LENGTHS : 0u, 2);
+    le_put(p + 8, static_cast<uint64_t>(max_len), 4);
+    le_put(p + 12, 0, 4);
+    le_put(p + 16, n, 8);
+    le_put(p + 24, chunk_bytes, 8);
+    le_put(p + 32, nc, 8);
+    le_put(p + 40, T, 8);
+    p += HUFF_CONTAINER_HEADER;
+    if (h_len != nullptr) {
+        for (int s = 0; s < 256; ++s) p[s] = h_len[s];
+        p += 256;
+    }
+    for (size_t c = 0; c <= nc; ++c, p += 8) le_put(p, h_off[c], 8);
+    const size_t pb = static_cast<size_t>((T + 7) / 8);
+    for (size_t i = 0; i < pb; ++i) p[i] = h_payload[i];
+    *written = size;
+    return HUFF_OK;
+}
+
+int huff_container_parse(const uint8_t *h_src, size_t size, huff_container_view *view) {
+    if (h_src == nullptr || view == nullptr) return HUFF_ERR_INVALID_ARG;
+    if (size < HUFF_CONTAINER_HEADER) return HUFF_ERR_CORRUPT_STREAM;
+    if (le_get(h_src, 4) != HUFF_CONTAINER_MAGIC || le_get(h_src + 4, 2) != 1 || le_get(h_src + 12, 4) != 0)
+        return HUFF_ERR_CORRUPT_STREAM;
+    const uint64_t flags = le_get(h_src + 6, 2);
+    const uint64_t max_len = le_get(h_src + 8, 4);
+    const uint64_t n = le_get(h_src + 16, 8), chunk = le_get(h_src + 24, 8);
+    const uint64_t nc = le_get(h_src + 32, 8), T = le_get(h_src + 40, 8);
+    if ((flags & ~static_cast<uint64_t>(HUFF_CONTAINER_LENGTHS)) != 0 || max_len < 1 || max_len > HUFF_MAX_LEN ||
+        !chunk_ok(chunk) || n > kMaxN || nc != huff_num_chunks(n, chunk) || T > static_cast<uint64_t>(n) * max_len)
+        return HUFF_ERR_CORRUPT_STREAM;
+    const bool has_len = (flags & HUFF_CONTAINER_LENGTHS) != 0;
+    if (size != huff_container_size(n, chunk, T, has_len)) return HUFF_ERR_CORRUPT_STREAM;
+    const uint8_t *p = h_src + HUFF_CONTAINER_HEADER;
+    const uint8_t *len = nullptr;
+    if (has_len) {
+        len = p;
+        for (int s = 0; s < 256; ++s)
+            if (len[s] > max_len) return HUFF_ERR_CORRUPT_STREAM;
+        p += 256;
+    }
+    const uint8_t *off = p;
+    uint64_t prev = 0;
+    for (uint64_t c = 0; c <= nc; ++c) {
+        const uint64_t o = le_get(off + 8 * c, 8);
+        if ((c == 0 && o != 0) || o < prev) return HUFF_ERR_CORRUPT_STREAM;
+        prev = o;
+    }
+    if (prev != T) return HUFF_ERR_CORRUPT_STREAM;
+    view->n = n;
+    view->chunk_bytes = chunk;
+    view->n_chunks = nc;
+    view->total_bits = T;
+    view->max_len = static_cast<int32_t>(max_len);
+    view->has_lengths = has_len ? 1 : 0;
+    view->len = len;
+    view->off = off;
+    view->payload = off + 8 * (nc + 1);
+    view->payload_bytes = (T + 7) / 8;
+    return HUFF_OK;
+}
+
 }  // extern "C"

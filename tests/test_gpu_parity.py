@@ -288,6 +288,24 @@ def test_chunk_bit_counts_out_of_range_and_empty_payload_are_corrupt():
     assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
 
 
+@pytest.mark.parametrize("fixed", [False, True])
+def test_container_round_trip(fixed):
+    """Encode on the GPU, serialise to host bytes, parse, upload and decode: per-shard mode carries
+    the lengths (the codebook is imported from them), fixed mode relies on the receiver's codebook."""
+    x = _data("gauss", 300_001)
+    d = dev_u8(x)
+    cb = codec.build_codebook(codec.histogram(d), flags=_lib.HUFF_COVER_ALL if fixed else 0)
+    s = codec.encode(d, cb, 16384)
+    buf = codec.to_container(s, None if fixed else cb)
+    s2, cb2 = codec.from_container(buf, cb if fixed else None)
+    if not fixed:
+        np.testing.assert_array_equal(cb2.lengths(), cb.lengths())
+    assert torch.equal(s2.off, s.off)
+    np.testing.assert_array_equal(host_u8(codec.decode(s2, cb2)), x)
+    with pytest.raises(ValueError):
+        codec.from_container(codec.to_container(s, None))
+
+
 def test_unbuilt_codebook_is_rejected():
     cb = codec.Codebook()
     with pytest.raises(_lib.HuffError) as e:
