@@ -147,3 +147,10 @@ def test_split_path_corrupt_streams_detected():
                      st, payload_bytes=s.nbytes())
     torch.cuda.synchronize()
     assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+
+
+def test_largest_chunk_gpu_round_trip():
+    """Encode and decode on the GPU with one chunk of the largest accepted size."""
+    x = _gauss(3_000_017, 8)
+    cb = codec.build_codebook(codec.histogram(dev_u8(x)))
+    _round_trip(x, cb, 1 << 30)
