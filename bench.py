@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -93,6 +94,11 @@ def hbm_peak():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_info() -> dict:
+    """The machine the numbers come from (the GPU host may be Arm or x86)."""
+    return {"machine": platform.machine(), "cpus": os.cpu_count()}
 
 
 def kernel_hash(name: str) -> str:
@@ -383,6 +389,9 @@ def run_ours(args, dist, rank, ws):
         "drift_adaptive": drift, "loopback": loopback, "codebook_bank": bank,
         "quality": quality,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": path.launches_per_step * args.steps, "clocks": clk,
+        # both planes' histograms of the input delta, hashed: the same seeds give the same inputs everywhere
+        "input_hist_sha256_16": hashlib.sha256(path.hists.cpu().numpy().tobytes()).hexdigest()[:16],
+        "host": host_info(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -798,6 +807,7 @@ def run_reference(args, dist, rank, ws):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"first {elems} elements of x0/x1 per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "host": host_info(),
     }
     print(json.dumps(line), flush=True)
 
@@ -826,9 +836,13 @@ def run_workload(args):
     peak, peak_kind = hbm_peak()
     reps = max(3, args.steps)
     out = {"metric": METRIC, "workload": args.workload, "n_gpus": 1, "data": "synthetic", "peak_gbs": peak,
-           "peak_source": peak_kind}
+           "peak_source": peak_kind, "host": host_info()}
+    def hist_sha(t):  # the byte histogram of an input, hashed: the same seeds give the same inputs everywhere
+        return hashlib.sha256(codec.histogram(t.reshape(-1).view(torch.uint8)).cpu().numpy().tobytes()).hexdigest()[:16]
+
     if args.workload == "per_shard":
         x = workloads.per_shard_int8(device="cuda").view(torch.uint8)
+        out["input_hist_sha256_16"] = hist_sha(x)
         n = x.numel()
         cb, s = codec.compress(x, args.chunk)
         comp = _timed(lambda: codec.compress(x, args.chunk), reps)
@@ -846,6 +860,7 @@ def run_workload(args):
         cb = codec.build_codebook(hist, 24, _lib.HUFF_COVER_ALL)
         shards = [workloads.fixed_codebook_shard(k, warmup=False, device="cuda").view(torch.uint8).reshape(-1)
                   for k in range(workloads.TEST_SHARDS)]
+        out["input_hist_sha256_16"] = hashlib.sha256(hist.cpu().numpy().tobytes()).hexdigest()[:16]  # warm-up
         n = sum(x.numel() for x in shards)
         streams = [codec.encode(x, cb, args.chunk) for x in shards]
         enc = _timed(lambda: [codec.encode(x, cb, args.chunk) for x in shards], 3)
@@ -886,6 +901,7 @@ def run_workload(args):
     elif args.workload == "bf16_weights":
         x = workloads.bf16_weights(device="cuda")
         n = x.numel()
+        out["input_hist_sha256_16"] = hist_sha(x)
         s = codec.compress_bf16(x, None, args.chunk)
         comp = _timed(lambda: codec.compress_bf16(x, None, args.chunk), reps)
         dec = _timed(lambda: codec.decompress_bf16(s), reps)
@@ -902,6 +918,7 @@ def run_workload(args):
         for k in range(workloads.SWEEP_SEGMENTS):
             x[k * seg:(k + 1) * seg] = workloads.sweep_segment(k, device="cuda").view(torch.uint8)
         cb = codec.build_codebook(codec.histogram(x[: 64 << 20]), 24, _lib.HUFF_COVER_ALL)
+        out["input_hist_sha256_16"] = hist_sha(x)
         res = {}
         dst = torch.empty_like(x)
         for chunk in (16 << 10, 64 << 10, 256 << 10, 1 << 20):
