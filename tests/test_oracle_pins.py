@@ -10,6 +10,7 @@ patterns, and a library routine (numpy.bincount) for the histogram.
 """
 import json
 import math
+from fractions import Fraction
 import os
 
 import numpy as np
@@ -277,6 +278,98 @@ def test_fibonacci_counts_force_the_length_limit():
     # the most frequent symbols keep the shortest codes
     order = np.argsort(-h[:30].astype(np.int64), kind="stable")
     assert all(limited[order[i]] <= limited[order[i + 1]] for i in range(29))
+
+
+def _adjust_bits_cases(golden_dir):
+    with open(os.path.join(golden_dir, "adjust_bits.json")) as f:
+        return json.load(f)["cases"]
+
+
+def _case_counts(case) -> np.ndarray:
+    h = np.zeros(256, dtype=np.uint64)
+    if "counts" in case:
+        for k, v in case["counts"].items():
+            h[int(k)] = v
+    else:
+        fib = [1, 1]
+        while len(fib) < case["counts_fibonacci_symbols"]:
+            fib.append(fib[-1] + fib[-2])
+        h[: len(fib)] = fib
+    return h
+
+
+def test_adjust_bits_golden_moves_follow_the_procedure(golden_dir):
+    """Each recorded move of the hand derivation is the one T.81 Annex K.3 prescribes (the fixture
+    is checked against the rule itself, independently of either oracle)."""
+    for case in _adjust_bits_cases(golden_dir):
+        if "bits_window" in case:  # BITS(lo..hi) shown; BITS(1..lo-1) stay 1 throughout
+            lo = case["bits_window"][0]
+            bits = [0] + [1] * (lo - 1) + case["bits_before_window"]
+            moves = [(i, j, [1] * (lo - 1) + b) for i, j, b in case["moves_window"]]
+        else:
+            bits = [0] + case["bits_before"]
+            moves = case["moves"]
+        L = case["max_len"]
+        for i, j, after in moves:
+            over = [k for k in range(L + 1, len(bits)) if bits[k] > 0]
+            assert i == max(over), case["name"]
+            jj = i - 2
+            while bits[jj] == 0:
+                jj -= 1
+            assert j == jj, case["name"]
+            bits[i] -= 2
+            bits[i - 1] += 1
+            bits[j + 1] += 2
+            bits[j] -= 1
+            assert bits[1:] == after, (case["name"], i, j)
+            assert sum(Fraction(b, 2 ** k) for k, b in enumerate(bits) if k) == 1
+        assert not any(bits[L + 1:]), case["name"]
+        if "bits_after" in case:
+            assert bits[1:] == case["bits_after"]
+
+
+def test_adjust_bits_golden_lengths(golden_dir):
+    """Both oracles end at the hand-derived lengths; their unlimited depths are the derivation's start."""
+    for case in _adjust_bits_cases(golden_dir):
+        h = _case_counts(case)
+        L = case["max_len"]
+        if "lengths" in case:
+            want = np.zeros(256, dtype=np.uint8)
+            for k, v in case["lengths"].items():
+                want[int(k)] = v
+            start = case["bits_before"]
+        else:
+            want = np.zeros(256, dtype=np.uint8)
+            want[: len(case["lengths_by_symbol"])] = case["lengths_by_symbol"]
+            lo = case["bits_window"][0]
+            start = [1] * (lo - 1) + case["bits_before_window"]
+        unlimited = oracle.code_lengths(h, 63)
+        bl = np.bincount(unlimited[unlimited > 0], minlength=len(start) + 1)[1:]
+        assert list(bl[: len(start)]) == start[: len(bl)] and not bl[len(start):].any(), case["name"]
+        got = oracle.code_lengths(h, L)
+        np.testing.assert_array_equal(got, want, err_msg=case["name"])
+        assert tiny.code_lengths([int(v) for v in h], L) == [int(v) for v in want], case["name"]
+
+
+@pytest.mark.parametrize("max_len", [8, 9, 10, 12])
+def test_c_and_python_oracles_agree_when_the_limit_triggers(max_len):
+    """Skewed histograms whose Huffman depths exceed max_len: the two restatements of the repair agree."""
+    rng = np.random.default_rng(100 + max_len)
+    hit = 0
+    for trial in range(40):
+        m = int(rng.integers(max_len + 2, 257))
+        h = np.zeros(256, dtype=np.uint64)
+        syms = rng.choice(256, size=m, replace=False)
+        ratio = 1.3 + rng.random() * 0.9  # geometric counts give deep trees
+        h[syms] = np.maximum(1, (ratio ** rng.uniform(0, 40, m)).astype(np.uint64))
+        unlimited = oracle.code_lengths(h, 63)
+        ln = oracle.code_lengths(h, max_len)
+        if int(unlimited.max()) > max_len:
+            hit += 1
+        assert int(ln.max()) <= max_len
+        _kraft_equal(ln)
+        assert [int(v) for v in ln] == tiny.code_lengths([int(v) for v in h], max_len)
+    assert hit >= 20  # the repair ran in most trials
 
 
 # --------------------------------------------------------------------- C6 + C7 closed forms
