@@ -55,3 +55,29 @@ def check_sampled_chunks(payload: np.ndarray, off: np.ndarray, symbols: np.ndarr
         want = bits_of(ref_pay, 0, int(ref_off[-1]))
         assert got.size == want.size, f"chunk {c}: {got.size} bits, oracle {want.size}"
         np.testing.assert_array_equal(got, want, err_msg=f"chunk {c}")
+
+
+def assert_offsets_match_lengths(off: torch.Tensor, symbols, n: int, ln, chunk: int, block: int = 1 << 27):
+    """Every chunk's bit count off[c+1] - off[c] equals the sum of len[x] over its symbols, and off[0] = 0.
+
+    ``symbols(lo, hi)`` returns the device uint8 symbols [lo, hi).  Lengths are gathered with torch on
+    the device, block by block, so the check covers every chunk of a multi-GB stream without the
+    decoder or the oracle's encoder."""
+    offs = off.to(torch.int64)
+    assert int(offs[0].item()) == 0
+    diff = offs[1:] - offs[:-1]
+    lens = torch.as_tensor(np.asarray(ln, dtype=np.int64), device=off.device)
+    per = max(1, block // chunk)  # chunks per block
+    n_chunks = (n + chunk - 1) // chunk
+    assert diff.numel() == n_chunks
+    for c0 in range(0, n_chunks, per):
+        c1 = min(n_chunks, c0 + per)
+        lo, hi = c0 * chunk, min(n, c1 * chunk)
+        L = lens.gather(0, symbols(lo, hi).to(torch.int64))
+        pad = (c1 - c0) * chunk - (hi - lo)  # the ragged last chunk
+        if pad:
+            L = torch.cat([L, torch.zeros(pad, dtype=torch.int64, device=L.device)])
+        want = L.view(c1 - c0, chunk).sum(1)
+        bad = torch.nonzero(want != diff[c0:c1])
+        assert bad.numel() == 0, f"chunk {c0 + int(bad[0, 0])}: offsets differ from the summed code lengths"
+        del L, want

@@ -9,6 +9,9 @@ checks are:
 - sampled chunks (first, second, middle, last and random ones) equal the
   oracle's encoding of that chunk's symbols alone, bit for bit;
 - the total bit count equals sum(hist * len) (true at any size);
+- every chunk's offset difference equals the sum of its symbols' code
+  lengths, gathered with torch over the whole stream (independent of the
+  decoder);
 - decode returns the input exactly;
 - the small workloads (1 MiB) are compared whole.
 """
@@ -18,7 +21,7 @@ import torch
 
 import oracle
 from lossless_huffman_compression_gb300 import _lib, codec, workloads
-from gpu_util import assert_stream_equal, check_sampled_chunks, host, host_u8
+from gpu_util import assert_offsets_match_lengths, assert_stream_equal, check_sampled_chunks, host, host_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -124,6 +127,7 @@ def test_fixed_codebook_shards():
         else:
             chunks = _sample_chunks(s.n_chunks(), k, 2)
             _check_stream_samples(s.payload, s.off, _chunk_symbols(xb, chunks, CHUNK), ln, cd, CHUNK)
+            assert_offsets_match_lengths(s.off, lambda a, b: xb[a:b], xb.numel(), ln, CHUNK)
         assert torch.equal(codec.decode(s, cb), xb)
 
 
@@ -145,6 +149,8 @@ def _bf16_config(w: torch.Tensor, x0):
             plane[c] = host(((seg >> shift) & 0xFF).to(torch.uint8))
         _check_stream_samples(st.payload, st.off, plane, ln, cd, CHUNK)
         del plane
+        assert_offsets_match_lengths(
+            st.off, lambda a, b, sh=shift: ((d16[a:b].to(torch.int32) >> sh) & 0xFF).to(torch.uint8), s.n, ln, CHUNK)
     back = codec.decompress_bf16(s, x0)
     assert torch.equal(back.view(torch.int16), w16)
 
@@ -181,6 +187,7 @@ def test_chunk_size_sweep_16gib():
         assert s.total_bits() == T  # the payload does not depend on the chunk size
         chunks = _sample_chunks(s.n_chunks(), chunk, 3)
         _check_stream_samples(s.payload, s.off, _chunk_symbols(xb, chunks, chunk), ln, cd, chunk)
+        assert_offsets_match_lengths(s.off, lambda a, b: xb[a:b], n, ln, chunk)
         codec.decode(s, cb, out=out)
         assert torch.equal(out, xb)
         del s
