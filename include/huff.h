@@ -270,9 +270,11 @@ int huff_encode(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chu
  *                 returns HUFF_ERR_BUFFER_TOO_SMALL and enqueues nothing.
  *   other arguments as in huff_encode; the output is identical to its output.
  * The array lives in every GPU that loads the library, until the process
- * exits.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, once per device, with that device current); make
- * that first call before any stream capture.  All calls share the one array:
+ * exits.  Every call looks up the array's address on the current device
+ * (cudaGetSymbolAddress: a host-side query that allocates nothing), so the
+ * address stays right after cudaDeviceReset.  The first call on a device may
+ * load the library's device code; make that first call before any stream
+ * capture.  All calls share the one array:
  * calls whose work can overlap on the GPU (different streams, or several host
  * threads) race and corrupt each other's output; serialise them, or use
  * huff_encode with one workspace per stream.
@@ -378,15 +380,24 @@ int lmc_bytegroup_merge_w(const uint8_t *planes, size_t n, int width, size_t pla
 int lmc_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
                        uint64_t *hist_lo, int accumulate, huff_stream_t stream);
 
-/* Workspace bytes lmc_encode_bf16 needs for n elements. */
+/* Workspace bytes lmc_encode_bf16 needs for n elements: the per-segment
+ * counts (lmc_segment_counts_size), the counted encode's workspace
+ * (lmc_counted_workspace_size), each rounded up to 256 bytes, and 4 KiB for
+ * the two histograms the counting pass also produces (about 32 MB for 2e9
+ * elements). */
 size_t lmc_workspace_size(size_t n, size_t chunk_bytes);
 
 /*
  * lmc_encode_bf16 -- encode both byte planes of a bf16 tensor (optionally of
  * its XOR delta against x0) straight from the 16-bit words, each plane with
- * its own codebook (P2 framework stages 1 and 3 fused).  The outputs are
- * byte-identical to split + huff_encode per plane: plane streams (payload_hi,
- * off_hi) and (payload_lo, off_lo) with chunk_bytes elements per chunk.
+ * its own given codebook (P2 framework stages 1 and 3 fused; P1 Methodology
+ * step 4, a codebook fixed in advance).  The outputs are byte-identical to
+ * split + huff_encode per plane: plane streams (payload_hi, off_hi) and
+ * (payload_lo, off_lo) with chunk_bytes elements per chunk.  Runs as two
+ * passes over the input: lmc_histogram_bf16_counted's counting pass into the
+ * workspace, then lmc_encode_bf16_counted under the given codebooks.  A
+ * symbol present in the data without a code in its plane's codebook sets
+ * HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK (the stream is then not usable).
  *   w, x0     16-byte aligned; x0 may be NULL.
  *   other arguments as in huff_encode, once per plane.
  */
@@ -526,6 +537,34 @@ typedef struct huff_container_view {
  * max_len; HUFF_ERR_INVALID_ARG for NULL pointers.
  */
 int huff_container_parse(const uint8_t *h_src, size_t size, huff_container_view *view);
+
+/* ---------------------------------------------------------------- test hook */
+
+/*
+ * huff_debug_wait -- runs one of the library's bounded device waits on its
+ * own, so that a test can watch it run out without any fault: the waits of
+ * the encode kernels (the decoupled lookback over segment descriptors, after
+ * Merrill & Garland's single-pass scan, and the bulk-copy mbarrier waits)
+ * give up after a poll limit and report HUFF_ERR_TIMEOUT instead of hanging.
+ * (Failure handling around the method; the pages have no step for it.)
+ *   kind 0   one warp looks back from segment seg over desc[0 .. seg) (device
+ *            uint64 descriptors: flag in bits 62-63, 1 = aggregate, 2 =
+ *            inclusive prefix, 0 = not yet published; bit count in bits
+ *            0-61), n_desc >= seg >= 1.  A descriptor left at 0 makes the
+ *            wait run out after `limit` polls, or at the first poll count
+ *            divisible by 256 when *status already holds an error.
+ *   kind 1   one warp waits on a fresh mbarrier that nothing arrives on and
+ *            no copy targets, at most `limit` polls; desc is ignored.
+ *   limit    1 .. 2^20 polls.
+ *   out      device uint64[2]: the lookback's exclusive prefix (kind 0) and
+ *            the number of polls made.
+ *   status   device int32, caller-zeroed: HUFF_ERR_TIMEOUT when the wait ran
+ *            out (the first error recorded stays).
+ * Returns HUFF_ERR_INVALID_ARG for other arguments.  One launch of 32 threads
+ * on `stream`; no allocation, no synchronisation.
+ */
+int huff_debug_wait(int kind, const uint64_t *desc, size_t n_desc, uint32_t seg, uint32_t limit, uint64_t *out,
+                    int32_t *status, huff_stream_t stream);
 
 #ifdef __cplusplus
 }

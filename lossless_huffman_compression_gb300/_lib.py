@@ -46,7 +46,7 @@ EXPORTS = (
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
     "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
     "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if", "huff_build_codebooks",
-    "huff_stream_copy", "huff_container_size", "huff_container_write", "huff_container_parse",
+    "huff_stream_copy", "huff_container_size", "huff_container_write", "huff_container_parse", "huff_debug_wait",
 )
 
 
@@ -117,6 +117,7 @@ def load(path: str = LIB_PATH):
         "lmc_counted_workspace_size": (S, [S]),
         "lmc_histogram_bf16_counted": (I, [P, P, S, P, P, P, S, P]),
         "lmc_encode_bf16_counted": (I, [P, P, S, P, P, S, P, S, P, S, P, P, S, P, P, S, P, P]),
+        "huff_debug_wait": (I, [I, P, S, ctypes.c_uint32, ctypes.c_uint32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -266,6 +267,13 @@ def huff_encode_noalloc(inp: torch.Tensor, cb: torch.Tensor, chunk_bytes: int, p
     _check("huff_encode_noalloc", load().huff_encode_noalloc(
         _dev(inp, "inp"), n, _dev(cb, "cb"), chunk_bytes, _dev(payload, "payload"),
         payload.numel() * payload.element_size(), _dev(off, "off"), _dev(status, "status"), _stream(stream)))
+
+
+def huff_debug_wait(kind: int, desc, seg: int, limit: int, out: torch.Tensor, status: torch.Tensor, stream=None):
+    """Test hook: one bounded device wait run on its own (kind 0: lookback over desc, kind 1: an mbarrier)."""
+    _check("huff_debug_wait", load().huff_debug_wait(
+        kind, None if desc is None else _dev(desc, "desc"), 0 if desc is None else desc.numel(), seg, limit,
+        _dev(out, "out"), _dev(status, "status"), _stream(stream)))
 
 
 def huff_decode(payload: torch.Tensor, off: torch.Tensor, n: int, chunk_bytes: int, cb: torch.Tensor,

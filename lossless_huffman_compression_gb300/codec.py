@@ -259,7 +259,7 @@ def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: 
                                      st)
         raise_on_status(st, "lmc_encode_bf16_counted")
     else:
-        # fixed codebooks: the encode counts each segment's bits itself
+        # given codebooks: a counting pass over the input, then the one-pass encode
         ws = torch.empty(max(_lib.lmc_workspace_size(n, chunk_bytes), 16) // 8, dtype=torch.int64, device=dev)
         st = new_status(dev)
         _lib.lmc_encode_bf16(w16, x16, cb_hi.buf, cb_lo.buf, chunk_bytes, p_hi, o_hi, p_lo, o_lo, ws, st)

@@ -64,7 +64,7 @@ size_t huff_workspace_size(size_t n, size_t chunk_bytes) {
 
 size_t lmc_workspace_size(size_t n, size_t chunk_bytes) {
     (void)chunk_bytes;
-    return (4 * enc_bf16_tiles(n) + 2) * sizeof(uint64_t);
+    return enc_bf16_given_ws_parts(n, nullptr, nullptr);
 }
 
 int huff_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist, int accumulate,
@@ -425,6 +425,16 @@ int huff_container_parse(const uint8_t *h_src, size_t size, huff_container_view 
     view->payload = off + 8 * (nc + 1);
     view->payload_bytes = (T + 7) / 8;
     return HUFF_OK;
+}
+
+int huff_debug_wait(int kind, const uint64_t *desc, size_t n_desc, uint32_t seg, uint32_t limit, uint64_t *out,
+                    int32_t *status, huff_stream_t stream) {
+    if ((kind != 0 && kind != 1) || out == nullptr || status == nullptr || !aligned(out, 8) || limit == 0 ||
+        limit > kSpinLimit)
+        return HUFF_ERR_INVALID_ARG;
+    if (kind == 0 && (desc == nullptr || !aligned(desc, 8) || seg == 0 || seg > n_desc))
+        return HUFF_ERR_INVALID_ARG;
+    return launch_wait_probe(kind, desc, seg, limit, out, status, cs(stream));
 }
 
 }  // extern "C"

@@ -12,19 +12,11 @@
 namespace huffk {
 
 // ----------------------------------------------------------------- tuning constants
-constexpr int kEncThreads = 256;                 // encode CTA size (8 warps)
-constexpr int kEncU8SymsPerThread = 32;          // two 16-byte vectors per thread
-constexpr int kEncU8Tile = kEncThreads * kEncU8SymsPerThread;     // 8192 symbols
-constexpr int kEncBf16ElemsPerThread = 16;       // two 16-byte vectors of bf16
-constexpr int kEncBf16Tile = kEncThreads * kEncBf16ElemsPerThread; // 4096 elements
-constexpr int kEncStages = 3;                    // TMA ring depth
 // Counted (per-shard) bf16 path: the histogram pass records each plane's
-// counts per segment of kDirSegTiles encode tiles, so the encode knows every
+// counts per segment of kDirSegElems elements, so the encode knows every
 // segment's bit offset before it starts and reads its input once.
-constexpr int kDirSegTiles = 32;
-constexpr size_t kDirSegElems = size_t(kDirSegTiles) * kEncBf16Tile;  // 131072 bf16 elements
-constexpr int kSegCountWords = 512;                                   // [hi 256 | lo 256] per segment
-constexpr int kLutRep = 8;                       // copies of the encode table (bank spreading)
+constexpr size_t kDirSegElems = 131072;          // bf16 elements per counted segment
+constexpr int kSegCountWords = 512;              // [hi 256 | lo 256] per segment
 constexpr int kHistThreads = 512;
 constexpr int kHistCopies = 32;                  // one histogram copy per lane
 constexpr unsigned kSpinLimit = 1u << 20;        // bounded waits (polls) before HUFF_ERR_TIMEOUT
@@ -150,13 +142,25 @@ __device__ __forceinline__ bool error_recorded(const int32_t *status) {
     return status != nullptr && *reinterpret_cast<const volatile int32_t *>(status) != 0;
 }
 
-// Bounded wait on an mbarrier phase; false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (unsigned i = 0; i < kSpinLimit; ++i) {
+// Bounded wait on an mbarrier phase: at most `limit` polls; false when the
+// limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned limit = kSpinLimit) {
+    for (unsigned i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i > 64) __nanosleep(32);
     }
     return false;
+}
+
+// A warp's copy ring after one of its waits ran out: every lane waits once
+// more (bounded) on each stage whose copy may still be in flight (bit s of
+// `inflight`), so that the warp does not leave while a bulk copy is still
+// writing its shared memory.  Stages before `cstage` in the ring complete in
+// the next lap (parity cphase ^ 1), the others in this one.
+__device__ __forceinline__ void drain_ring(uint64_t *bar, int stages, uint32_t inflight, uint32_t cstage,
+                                           uint32_t cphase) {
+    for (int s = 0; s < stages; ++s)
+        if (inflight & (1u << s)) mbar_wait(&bar[s], static_cast<uint32_t>(s) < cstage ? cphase ^ 1u : cphase);
 }
 
 // ----------------------------------------------------------------- launchers (host)
@@ -181,7 +185,7 @@ int launch_codebook_from_lengths(int max_len, huff_codebook *cb, int32_t *status
 
 size_t enc_u8_seg_tiles(size_t n);
 size_t enc_u8_workspace_words(size_t n);
-size_t enc_bf16_tiles(size_t n);
+size_t enc_bf16_given_ws_parts(size_t n, size_t *counted_off, size_t *hist_off);
 int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk,
                      uint8_t *payload, size_t cap, uint64_t *off, void *ws, int32_t *status,
                      cudaStream_t s);
@@ -210,6 +214,8 @@ int launch_split_w(const uint8_t *in, size_t n, int width, uint8_t *planes, size
 int launch_stream_copy(const uint8_t *src, size_t src_bytes, const uint64_t *off, size_t n_chunks, uint8_t *dst,
                        size_t dst_cap, uint64_t *dst_off, int32_t *status, cudaStream_t s);
 int launch_merge_w(const uint8_t *planes, size_t n, int width, size_t ps, uint8_t *out, cudaStream_t s);
+int launch_wait_probe(int kind, const uint64_t *desc, uint32_t seg, unsigned limit, uint64_t *out, int32_t *status,
+                      cudaStream_t s);
 
 inline int launch_status() {
     cudaError_t e = cudaGetLastError();

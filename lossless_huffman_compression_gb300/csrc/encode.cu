@@ -10,35 +10,21 @@
 // Output format: codes appended MSB first into one contiguous stream; the bit
 // offset of every chunk start is recorded so chunks decode independently.
 //
-// GPU design (two passes over each segment, the second from L2):
-//   * the input is cut into 8 KiB tiles and segments of kSegTiles tiles;
-//     persistent CTAs take segments from an atomic counter;
-//   * pass 1 streams a segment's tiles from HBM into a shared-memory ring with
-//     1-D bulk copies (cp.async.bulk on mbarriers, L2 policy evict_last), looks
-//     up each symbol's code length and keeps every thread's bit count;
-//   * the CTA publishes the segment's bit count, claims its next segment, and
-//     one warp resolves the segment's global bit offset with a decoupled
-//     lookback (Merrill & Garland, "Single-pass Parallel Prefix Scan with
-//     Decoupled Look-back", 2016) over windows of 320 segment descriptors;
-//     one lookback per segment, so its latency is amortised over 8 tiles;
-//   * pass 2 streams the same tiles again (now from L2, evict_first), looks
-//     up (code << 8 | len) in a shared-memory table replicated kLutRep times
-//     (lanes with different symbols spread over more banks), scans the stored
-//     per-thread counts, packs the codes into a tile-local bit buffer with
-//     32-bit funnel shifts (each thread's symbols as two independent halves
-//     per plane, so two to four packing chains interleave), and writes whole
-//     32-bit words shifted to the tile's bit phase
-//     with coalesced stores; the CTA carries each tile's last partial word
-//     into the next tile of the segment itself;
-//   * the two partial words at each segment boundary are left in the
-//     workspace and written by a small fix-up kernel, so no CTA ever waits for
-//     another CTA's output.
-//   The fused bf16 variant reads 16-bit words (and optionally x0, for the XOR
-//   delta) and encodes the high and low byte planes as two streams in one
-//   pass.  All waits are bounded; a wait that runs out sets HUFF_ERR_TIMEOUT
-//   and the kernel carries on to completion.
-#include <mutex>
-
+// GPU design: one warp encodes a whole segment, with its own ring of 1-D
+// bulk copies (cp.async.bulk on mbarriers) that stages the segment's tiles in
+// shared memory, a conflict-free code table, and warp-level scans and packing
+// (no block barrier on the path).  A segment's bit offset comes either from
+// counts recorded before the encode (the counted bf16 encode: per-segment
+// plane counts from the histogram pass give sum(count x length) and one scan
+// over all segments) or from a decoupled lookback over the segments before it
+// (the byte-stream encode, which counts a segment's bits in a first pass over
+// its tiles and packs them in a second pass, from L2: Merrill & Garland,
+// "Single-pass Parallel Prefix Scan with Decoupled Look-back", 2016).  The
+// two partial words at each segment boundary are left in the workspace and
+// written by a small fix-up kernel, so no warp ever waits for another warp's
+// output.  All waits are bounded: a wait that runs out sets HUFF_ERR_TIMEOUT;
+// a warp whose copy wait ran out issues no further copies, gives each copy it
+// has in flight one more bounded wait, and stops.
 #include "common.cuh"
 
 namespace huffk {
@@ -46,14 +32,13 @@ namespace huffk {
 // Workspace for huff_encode_noalloc, sized like huff_workspace_size for
 // HUFF_NOALLOC_MAX_SYMBOLS symbols.  Every GPU that loads the library keeps
 // these 2 MiB until the process exits; all calls share them.
-constexpr size_t kNoAllocScratchWords = 2 * (HUFF_NOALLOC_MAX_SYMBOLS / kEncU8Tile) + 2;
+// (2 MiB: twice the byte-stream encode's need at that size, 2 words per
+// segment of 16 tiles of 1024 symbols plus the counter.)
+constexpr size_t kNoAllocScratchWords = 2 * (HUFF_NOALLOC_MAX_SYMBOLS / 8192) + 2;
 static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocScratchWords];
 
 namespace {
 
-constexpr int kThreads = kEncThreads;  // 8 warps
-constexpr int kSegTiles = 8;           // tiles per segment
-constexpr int kStages = 3;             // bulk-copy ring depth
 constexpr int kLookbackPerLane = 10;   // descriptors per lane per lookback step (window 320)
 
 struct EncPlane {
@@ -64,38 +49,6 @@ struct EncPlane {
     uint64_t *desc;     // per-segment lookback descriptors (zeroed before the launch)
     uint64_t *edge;     // per-segment boundary words: head bits << 32 | tail bits
 };
-
-template <bool BF16, bool XOR>
-struct EncCfg {
-    static constexpr int kPlanes = BF16 ? 2 : 1;
-    static constexpr int kSyms = BF16 ? kEncBf16ElemsPerThread : kEncU8SymsPerThread;  // per plane, per thread
-    static constexpr int kTileSyms = kThreads * kSyms;
-    static constexpr int kTileBytes = 8192;  // per input array
-    static constexpr int kInputs = XOR ? 2 : 1;
-    static constexpr int kBufWords = kTileSyms * HUFF_MAX_LEN / 32 + 4;
-    static constexpr int kLutWords = 256 * kLutRep;
-    static constexpr size_t kMiscBytes = 512;
-    static constexpr size_t kRingBytes = size_t(kStages) * kInputs * kTileBytes;
-    static constexpr size_t kLutBytes = size_t(kPlanes) * kLutWords * 4;
-    static constexpr size_t kBufBytes = size_t(kPlanes) * kBufWords * 4;
-    static constexpr size_t kCntBytes = size_t(kSegTiles) * kThreads * 4;
-    static constexpr size_t kSmem = kMiscBytes + kRingBytes + kLutBytes + kBufBytes + kCntBytes;
-    static_assert(kTileSyms * (BF16 ? 2 : 1) == kTileBytes && kTileSyms <= 8192, "tile geometry");
-};
-
-struct Misc {
-    uint64_t full[kStages];
-    uint64_t warp_sum[kThreads / 32];
-    uint64_t prefix[2];      // [plane] segment bit counts, handed to the lookback warp
-    uint64_t run[2];         // [plane] bit offset of the current tile
-    uint32_t carry[2];       // [plane] bits of the previous tile in the word the current tile starts in
-    uint32_t seg_head[2];    // [plane] the segment's bits in its first, partial word
-    uint32_t segq[2];        // segment of round r at [r & 1]
-    int32_t bad_codebook;
-    uint64_t chunk_q;        // the current tile's first element is element chunk_r of chunk chunk_q
-    uint32_t chunk_r;
-};
-static_assert(sizeof(Misc) <= 512, "misc area");
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
@@ -116,12 +69,17 @@ __device__ __forceinline__ void load_window(const uint64_t *desc, int64_t base, 
 // windows of 32 * kLookbackPerLane predecessors; returns the exclusive bit
 // offset.  The segment's own aggregate is already published.  d holds the
 // first window, already loaded (two streams' first windows fly together).
+// At most `limit` polls of an unpublished window (the spin count is left in
+// `polls`); the wait also stops at a poll count divisible by 256 once any
+// error is recorded, so one failure does not hold every later segment for
+// the full limit.
 __device__ uint64_t lookback(const uint64_t *desc, uint32_t t, int lane, int32_t *status,
-                             uint64_t (&d)[kLookbackPerLane]) {
+                             uint64_t (&d)[kLookbackPerLane], unsigned limit, unsigned &polls) {
+    unsigned spins = 0;
+    polls = 0;
     if (t == 0) return 0;
     uint64_t excl = 0;
     int64_t base = static_cast<int64_t>(t) - 1;
-    unsigned spins = 0;
     for (bool first = true;; first = false) {
         if (!first) load_window(desc, base, lane, d);
         // nearest inclusive prefix in the window (distance q = 32 j + lane)
@@ -154,114 +112,27 @@ __device__ uint64_t lookback(const uint64_t *desc, uint32_t t, int lane, int32_t
             base -= 32 * kLookbackPerLane;
         } else {
             ++spins;
-            const bool give_up = spins > kSpinLimit || ((spins & 255u) == 0 && error_recorded(status));
+            const bool give_up = spins > limit || ((spins & 255u) == 0 && error_recorded(status));
             if (__any_sync(0xffffffffu, give_up)) {
-                if (lane == 0 && spins > kSpinLimit) set_status(status, HUFF_ERR_TIMEOUT);
+                if (lane == 0 && spins > limit) set_status(status, HUFF_ERR_TIMEOUT);
                 break;
             }
             __nanosleep(64);
         }
     }
+    polls = spins;
     return excl;
 }
 
-// Packs (code << 8 | len) entries, len <= 24 in the low 5 bits, into a
-// tile-local bit buffer from bit `start` on.  The pending bits sit in the
-// 64-bit pair (hi, lo); since len < 32, 32-bit funnel shifts move them, and
-// the entry itself serves as the shift count (funnel shifts use its low 5
-// bits).  A word wholly inside this thread's bits is stored under a
-// predicate (no branch, no atomic); the first word, which may hold bits of
-// earlier threads, is kept in a register and OR-ed in by finish() together
-// with the last, partial word (the buffer is zero before packing).
-struct Packer {
-    uint32_t *buf;
-    uint32_t hi, lo;  // pending bits: the low `nb` bits of hi:lo
-    uint32_t nb;
-    uint32_t w;       // next buffer word
-    uint32_t w0;      // the first word
-    uint32_t head;    // the first word's bits, once complete
-    bool first;       // the first word is not complete yet
 
-    __device__ __forceinline__ void begin(uint32_t *b, uint32_t start) {
-        buf = b;
-        hi = lo = 0;
-        nb = start & 31u;
-        w = w0 = start >> 5;
-        head = 0;
-        first = true;
-    }
-    __device__ __forceinline__ void push(uint32_t e) {
-        hi = __funnelshift_l(lo, hi, e);
-        lo = __funnelshift_l(0u, lo, e) | (e >> 8);
-        nb += e & 31u;
-        const bool full = nb >= 32;
-        nb -= full ? 32u : 0u;
-        const uint32_t word = __funnelshift_r(lo, hi, nb);
-        if (full && !first) buf[w] = word;
-        head = (full && first) ? word : head;
-        first = first && !full;
-        w += full ? 1u : 0u;
-    }
-    // Two codes at once when together they are at most 31 bits.
-    __device__ __forceinline__ void push2(uint32_t ea, uint32_t eb, uint32_t L) {  // L = both lengths
-        const uint32_t code = ((ea >> 8) << (eb & 31u)) | (eb >> 8);
-        hi = __funnelshift_l(lo, hi, L);
-        lo = (lo << L) | code;
-        nb += L;
-        const bool full = nb >= 32;
-        nb -= full ? 32u : 0u;
-        const uint32_t word = __funnelshift_r(lo, hi, nb);
-        if (full && !first) buf[w] = word;
-        head = (full && first) ? word : head;
-        first = first && !full;
-        w += full ? 1u : 0u;
-    }
-    __device__ __forceinline__ void finish() {
-        if (!first) atomicOr(&buf[w0], head);
-        if (nb > 0) atomicOr(&buf[w], lo << (32 - nb));
-    }
-};
-
-// Chunk starts among a tile's per-thread groups.  Chunks are multiples of 256
-// elements and a thread's group is 16 or 32, so a group starts a chunk or lies
-// inside one.  With the tile's position in its chunk (q, r) kept by thread 0,
-// a thread's distance d = r + first-of-group < chunk + 8192 (a tile is at
-// most 8192 symbols) is divided exactly by a multiply-high when chunk < 8192
-// (magic = ceil(2^32 / chunk); exact since d * chunk < 2^32) or by one
-// compare when chunk >= 8192 (then d < 2 chunk).
+// The chunk size, as the encode kernels take it (chunks are multiples of 256
+// elements, so a chunk starts at the first symbol of some lane's group).
 struct ChunkDiv {
     uint32_t chunk;  // < 2^31
-    uint32_t magic;  // 0 when chunk >= 8192
-    __device__ __forceinline__ uint32_t div(uint32_t d) const {
-        return magic ? __umulhi(d, magic) : (d >= chunk ? 1u : 0u);
-    }
 };
 
 __host__ inline ChunkDiv make_chunk_div(size_t chunk) {
-    const uint32_t c = static_cast<uint32_t>(chunk);
-    return ChunkDiv{c, c < 8192 ? static_cast<uint32_t>(((1ull << 32) + c - 1) / c) : 0u};
-}
-
-// Thread 0, before a tile: its first element's chunk and offset in it
-// (incrementally from the previous tile of the same segment).
-__device__ __forceinline__ void chunk_position(Misc *ms, const ChunkDiv &cd, size_t first, bool seg_start,
-                                               uint32_t tile_syms) {
-    if (seg_start) {
-        ms->chunk_q = first / cd.chunk;
-        ms->chunk_r = static_cast<uint32_t>(first % cd.chunk);
-    } else {
-        const uint32_t d = ms->chunk_r + tile_syms;
-        const uint32_t k = cd.div(d);
-        ms->chunk_q += k;
-        ms->chunk_r = d - k * cd.chunk;
-    }
-}
-
-// Global word i of a tile whose bits start at phase ph, from the tile-local buffer.
-__device__ __forceinline__ uint32_t shifted_word(const uint32_t *buf, uint32_t i, uint32_t ph) {
-    if (ph == 0) return buf[i];
-    const uint32_t lo = buf[i] >> ph;
-    return i == 0 ? lo : (lo | (buf[i - 1] << (32 - ph)));
+    return ChunkDiv{static_cast<uint32_t>(chunk)};
 }
 
 __device__ __forceinline__ void put_word(uint32_t *payload, size_t cap_words, uint64_t gw, uint32_t v,
@@ -272,384 +143,6 @@ __device__ __forceinline__ void put_word(uint32_t *payload, size_t cap_words, ui
         set_status(status, HUFF_ERR_BUFFER_TOO_SMALL);
 }
 
-// Job q of a CTA: round r = q / (2 kSegTiles) works on segment segq[r & 1];
-// its first kSegTiles jobs are pass 1, the next kSegTiles pass 2.
-template <bool BF16, bool XOR>
-__device__ __forceinline__ void issue_job(uint8_t *ring, Misc *ms, uint32_t q, uint32_t n_seg, uint32_t n_tiles,
-                                          const uint8_t *in, const uint8_t *in2, size_t n) {
-    using C = EncCfg<BF16, XOR>;
-    const uint32_t r = q / (2 * kSegTiles);
-    const uint32_t w = q % (2 * kSegTiles);
-    const uint32_t seg = ms->segq[r & 1];
-    if (seg >= n_seg) return;  // the consumers stop before this job
-    const int s = static_cast<int>(q % kStages);
-    const uint32_t t = seg * kSegTiles + (w % kSegTiles);
-    uint32_t bytes = 0;
-    size_t first = 0;
-    if (t < n_tiles) {
-        first = static_cast<size_t>(t) * C::kTileSyms;
-        const size_t cnt = n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms);
-        bytes = static_cast<uint32_t>(cnt * (BF16 ? 2 : 1)) & ~15u;
-    }
-    mbar_arrive_expect_tx(&ms->full[s], bytes * C::kInputs);
-    if (bytes) {
-        const uint64_t pol = w < kSegTiles ? l2_policy_evict_last() : l2_policy_evict_first();
-        const size_t src = first * (BF16 ? 2 : 1);
-        uint8_t *dst = ring + size_t(s) * C::kInputs * C::kTileBytes;
-        bulk_g2s_hint(dst, in + src, bytes, &ms->full[s], pol);
-        if (XOR) bulk_g2s_hint(dst + C::kTileBytes, in2 + src, bytes, &ms->full[s], pol);
-    }
-}
-
-// This thread's 32 input bytes (16-bit words XOR x0 for the fused delta) of the tile in a stage.
-template <bool BF16, bool XOR>
-__device__ __forceinline__ void read_tile(const uint8_t *stage, int tid, size_t first, int tile_n,
-                                          const uint8_t *in, const uint8_t *in2, uint32_t (&wv)[8]) {
-    using C = EncCfg<BF16, XOR>;
-    const uint4 a = *reinterpret_cast<const uint4 *>(stage + tid * 32);
-    const uint4 c = *reinterpret_cast<const uint4 *>(stage + tid * 32 + 16);
-    wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
-    wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
-    if (XOR) {
-        const uint4 d = *reinterpret_cast<const uint4 *>(stage + C::kTileBytes + tid * 32);
-        const uint4 e = *reinterpret_cast<const uint4 *>(stage + C::kTileBytes + tid * 32 + 16);
-        wv[0] ^= d.x; wv[1] ^= d.y; wv[2] ^= d.z; wv[3] ^= d.w;
-        wv[4] ^= e.x; wv[5] ^= e.y; wv[6] ^= e.z; wv[7] ^= e.w;
-    }
-    const int es = BF16 ? 2 : 1;
-    const int tile_bytes = tile_n * es;
-    const int tma_bytes = tile_bytes & ~15;
-    if (tid * 32 + 32 > tma_bytes && tid * 32 < tile_bytes) {
-        // ragged end of the last tile: bytes the bulk copy did not cover come from global memory
-        for (int k = 0; k < 32; ++k) {
-            const int bb = tid * 32 + k;
-            if (bb < tma_bytes) continue;
-            uint32_t v = 0;
-            if (bb < tile_bytes) {
-                v = in[first * es + bb];
-                if (XOR) v ^= in2[first * es + bb];
-            }
-            wv[k >> 2] = (wv[k >> 2] & ~(0xffu << (8 * (k & 3)))) | (v << (8 * (k & 3)));
-        }
-    }
-}
-
-// (code << 8 | len) of this thread's symbols; symbols past the tile's end get 0.
-// mn ends at 0 when a valid symbol has no code.
-template <bool BF16, bool XOR, bool COUNT>
-__device__ __forceinline__ void lookup(const uint32_t *lut_r, const uint32_t (&wv)[8], bool full, int nvalid,
-                                       uint32_t (&e0)[EncCfg<BF16, XOR>::kSyms],
-                                       uint32_t (&e1)[BF16 ? EncCfg<BF16, XOR>::kSyms : 1], uint32_t &bits0,
-                                       uint32_t &bits1, uint32_t &mn) {
-    using C = EncCfg<BF16, XOR>;
-    bits0 = bits1 = 0;
-    mn = 0xffffffffu;
-    if (full) {
-#pragma unroll
-        for (int k = 0; k < C::kSyms; ++k) {
-            if (BF16) {
-                const uint32_t w2 = wv[k >> 1];
-                const uint32_t hi = lut_r[__byte_perm(w2, 0, 0x4441 + 2 * (k & 1)) * kLutRep];
-                const uint32_t lo = lut_r[C::kLutWords + __byte_perm(w2, 0, 0x4440 + 2 * (k & 1)) * kLutRep];
-                mn = min(mn, min(hi, lo));
-                e0[k] = hi;
-                e1[BF16 ? k : 0] = lo;
-                if (COUNT) {
-                    bits0 += hi & 31u;
-                    bits1 += lo & 31u;
-                }
-            } else {
-                const uint32_t v = lut_r[__byte_perm(wv[k >> 2], 0, 0x4440 + (k & 3)) * kLutRep];
-                mn = min(mn, v);
-                e0[k] = v;
-                if (COUNT) bits0 += v & 31u;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < C::kSyms; ++k) {
-            if (BF16) {
-                const uint32_t v = (wv[k >> 1] >> (16 * (k & 1))) & 0xffffu;
-                uint32_t hi = lut_r[(v >> 8) * kLutRep];
-                uint32_t lo = lut_r[C::kLutWords + (v & 0xffu) * kLutRep];
-                if (k >= nvalid) hi = lo = 0;
-                else mn = min(mn, min(hi, lo));
-                e0[k] = hi;
-                e1[BF16 ? k : 0] = lo;
-                if (COUNT) {
-                    bits0 += hi & 31u;
-                    bits1 += lo & 31u;
-                }
-            } else {
-                const uint32_t sym = (wv[k >> 2] >> (8 * (k & 3))) & 0xffu;
-                uint32_t v = lut_r[sym * kLutRep];
-                if (k >= nvalid) v = 0;
-                else mn = min(mn, v);
-                e0[k] = v;
-                if (COUNT) bits0 += v & 31u;
-            }
-        }
-    }
-}
-
-template <bool BF16, bool XOR>
-__global__ void __launch_bounds__(kThreads, 2) k_encode(const uint8_t *__restrict__ in, const uint8_t *__restrict__ in2,
-                                                     size_t n, EncPlane p0, EncPlane p1, ChunkDiv cdiv,
-                                                     uint32_t n_tiles, unsigned *seg_ctr, int32_t *status) {
-    using C = EncCfg<BF16, XOR>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    Misc *ms = reinterpret_cast<Misc *>(smem);
-    uint8_t *ring = smem + C::kMiscBytes;
-    uint32_t *lut = reinterpret_cast<uint32_t *>(ring + C::kRingBytes);
-    uint32_t *bufs = lut + C::kPlanes * C::kLutWords;
-    uint32_t *cnt = bufs + C::kPlanes * C::kBufWords;  // [kSegTiles][kThreads] hi << 16 | lo
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const uint32_t n_seg = (n_tiles + kSegTiles - 1) / kSegTiles;
-
-    // code table: entry (s * kLutRep + r) = (code << 8) | len, 0 when the symbol has no code
-    if (tid == 0) ms->bad_codebook = 0;
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < C::kPlanes; ++p) {
-        const huff_codebook *cb = p == 0 ? p0.cb : p1.cb;
-        const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
-        if (!ok && tid == 0) ms->bad_codebook = 1;
-        for (int i = tid; i < C::kLutWords; i += kThreads) {
-            const int s = i / kLutRep;
-            const uint32_t L = ok ? cb->len[s] : 0u;
-            lut[p * C::kLutWords + i] = (L >= 1 && L <= HUFF_MAX_LEN) ? ((cb->code[s] << 8) | L) : 0u;
-        }
-    }
-    for (int i = tid; i < C::kPlanes * C::kBufWords; i += kThreads) bufs[i] = 0;
-    uint32_t issued = 0;  // next job to issue (thread 0 only)
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&ms->full[s], 1);
-        fence_mbar_init();
-        ms->segq[0] = atomicAdd(seg_ctr, 1u);
-        ms->segq[1] = 0xffffffffu;
-        for (; issued < uint32_t(kStages); ++issued) issue_job<BF16, XOR>(ring, ms, issued, n_seg, n_tiles, in, in2, n);
-    }
-    __syncthreads();
-    if (ms->bad_codebook && tid == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
-    const uint32_t *lut_r = lut + (lane & (kLutRep - 1));
-
-    for (uint32_t r = 0;; ++r) {
-        const uint32_t seg = ms->segq[r & 1];
-        if (seg >= n_seg) break;
-        const uint32_t t_first = seg * kSegTiles;
-        const int seg_tiles = static_cast<int>(n_tiles - t_first < uint32_t(kSegTiles) ? n_tiles - t_first : kSegTiles);
-        const uint32_t q0 = r * 2 * kSegTiles;
-
-        // ---------------- pass 1: bit counts per thread and per tile
-        uint32_t sum0 = 0, sum1 = 0, mn_all = 0xffffffffu;
-        for (int k = 0; k < kSegTiles; ++k) {
-            const uint32_t q = q0 + k;
-            const int s = static_cast<int>(q % kStages);
-            if (!mbar_wait(&ms->full[s], (q / kStages) & 1u) && tid == 0) set_status(status, HUFF_ERR_TIMEOUT);
-            if (k < seg_tiles) {
-                const uint32_t t = t_first + k;
-                const size_t first = static_cast<size_t>(t) * C::kTileSyms;
-                const int tile_n = static_cast<int>(n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms));
-                uint32_t wv[8];
-                read_tile<BF16, XOR>(ring + size_t(s) * C::kInputs * C::kTileBytes, tid, first, tile_n, in, in2, wv);
-                const int nvalid = tile_n - tid * C::kSyms < 0
-                                       ? 0
-                                       : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
-                uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
-                lookup<BF16, XOR, true>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
-                if (nvalid > 0) mn_all = min(mn_all, mn);
-                cnt[k * kThreads + tid] = (b0 << 16) | b1;
-                sum0 += b0;
-                sum1 += b1;
-            }
-            __syncthreads();  // stage s consumed
-            if (tid == 0) issue_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
-        }
-        if (mn_all == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
-
-        // ---------------- segment bit count, publish, claim the next segment
-        const uint64_t v = warp_sum_u64((static_cast<uint64_t>(sum0) << 32) | sum1);
-        if (lane == 0) ms->warp_sum[warp] = v;
-        __syncthreads();
-        if (tid == 0) {
-            uint64_t tot = 0;
-            for (int w = 0; w < kThreads / 32; ++w) tot += ms->warp_sum[w];
-            const uint64_t tot0 = tot >> 32;
-            const uint64_t tot1 = tot & 0xffffffffull;
-            const uint64_t f = seg == 0 ? kFlagPrefix : kFlagAggregate;
-            st_relaxed(&p0.desc[seg], f | tot0);
-            if (BF16) st_relaxed(&p1.desc[seg], f | tot1);
-            ms->segq[(r + 1) & 1] = atomicAdd(seg_ctr, 1u);
-            ms->prefix[0] = tot0;  // the totals, handed to warp 0
-            ms->prefix[1] = tot1;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const uint64_t tot0 = ms->prefix[0], tot1 = ms->prefix[1];
-            uint64_t w0[kLookbackPerLane], w1[kLookbackPerLane];
-            load_window(p0.desc, static_cast<int64_t>(seg) - 1, lane, w0);
-            if (BF16) load_window(p1.desc, static_cast<int64_t>(seg) - 1, lane, w1);
-            const uint64_t pre0 = lookback(p0.desc, seg, lane, status, w0);
-            const uint64_t pre1 = BF16 ? lookback(p1.desc, seg, lane, status, w1) : 0;
-            if (lane == 0) {
-                if (seg != 0) {
-                    st_relaxed(&p0.desc[seg], kFlagPrefix | (pre0 + tot0));
-                    if (BF16) st_relaxed(&p1.desc[seg], kFlagPrefix | (pre1 + tot1));
-                }
-                ms->run[0] = pre0;
-                ms->run[1] = pre1;
-                ms->carry[0] = ms->carry[1] = 0;
-                ms->seg_head[0] = ms->seg_head[1] = 0;
-            }
-        }
-        __syncthreads();
-
-        // ---------------- pass 2: pack and write, tile after tile
-        for (int k = 0; k < kSegTiles; ++k) {
-            const uint32_t q = q0 + kSegTiles + k;
-            const int s = static_cast<int>(q % kStages);
-            if (!mbar_wait(&ms->full[s], (q / kStages) & 1u) && tid == 0) set_status(status, HUFF_ERR_TIMEOUT);
-            if (k < seg_tiles) {
-                const uint32_t t = t_first + k;
-                const size_t first = static_cast<size_t>(t) * C::kTileSyms;
-                const int tile_n = static_cast<int>(n - first < size_t(C::kTileSyms) ? n - first : size_t(C::kTileSyms));
-                uint32_t wv[8];
-                read_tile<BF16, XOR>(ring + size_t(s) * C::kInputs * C::kTileBytes, tid, first, tile_n, in, in2, wv);
-                const int nvalid = tile_n - tid * C::kSyms < 0
-                                       ? 0
-                                       : (tile_n - tid * C::kSyms > C::kSyms ? C::kSyms : tile_n - tid * C::kSyms);
-                uint32_t e0[C::kSyms], e1[BF16 ? C::kSyms : 1], b0, b1, mn;
-                lookup<BF16, XOR, false>(lut_r, wv, tile_n == C::kTileSyms, nvalid, e0, e1, b0, b1, mn);
-                // each pair's total length, once: the bit counts, the pair check and the packing use it
-                uint32_t L0[C::kSyms / 2], L1[BF16 ? C::kSyms / 2 : 1], longest_pair = 0;
-#pragma unroll
-                for (int j = 0; j < C::kSyms / 2; ++j) {
-                    L0[j] = (e0[2 * j] & 31u) + (e0[2 * j + 1] & 31u);
-                    b0 += L0[j];
-                    longest_pair = max(longest_pair, L0[j]);
-                    if (BF16) {
-                        L1[BF16 ? j : 0] = (e1[BF16 ? 2 * j : 0] & 31u) + (e1[BF16 ? 2 * j + 1 : 0] & 31u);
-                        b1 += L1[BF16 ? j : 0];
-                        longest_pair = max(longest_pair, L1[BF16 ? j : 0]);
-                    }
-                }
-                // block scan of the counts kept from pass 1
-                const uint32_t c = cnt[k * kThreads + tid];
-                const uint64_t mine = (static_cast<uint64_t>(c >> 16) << 32) | (c & 0xffffu);
-                uint64_t incl = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                if (lane == 31) ms->warp_sum[warp] = incl;
-                if (tid == 0) chunk_position(ms, cdiv, first, k == 0, C::kTileSyms);
-                __syncthreads();  // stage s consumed; warp sums ready
-                if (tid == 0) issue_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
-                uint64_t before = 0, total = 0;
-#pragma unroll
-                for (int w = 0; w < kThreads / 32; ++w) {
-                    const uint64_t ws = ms->warp_sum[w];
-                    before += w < warp ? ws : 0;
-                    total += ws;
-                }
-                const uint64_t excl = before + incl - mine;
-                const uint32_t excl0 = uint32_t(excl >> 32);
-                const uint32_t excl1 = uint32_t(excl);
-                const uint32_t tot0 = uint32_t(total >> 32);
-                const uint32_t tot1 = uint32_t(total);
-                Packer pk0, pk1;
-                pk0.begin(bufs, excl0);
-                if (BF16) pk1.begin(bufs + C::kBufWords, excl1);
-                // pairs of codes at most 31 bits long go in one step; a warp with a longer pair
-                // anywhere packs its codes one by one
-                if (__any_sync(0xffffffffu, longest_pair > 31u)) {
-#pragma unroll
-                    for (int j = 0; j < C::kSyms; ++j) {
-                        pk0.push(e0[j]);
-                        if (BF16) pk1.push(e1[BF16 ? j : 0]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < C::kSyms; j += 2) {
-                        pk0.push2(e0[j], e0[j + 1], L0[j / 2]);
-                        if (BF16) pk1.push2(e1[BF16 ? j : 0], e1[BF16 ? j + 1 : 0], L1[BF16 ? j / 2 : 0]);
-                    }
-                }
-                pk0.finish();
-                if (BF16) pk1.finish();
-                __syncthreads();  // buffers packed
-                // write the tile's words at its global bit offset
-                uint64_t next_run = 0;  // thread 32 p: plane p's offset after this tile
-#pragma unroll
-                for (int p = 0; p < C::kPlanes; ++p) {
-                    const EncPlane &P = p == 0 ? p0 : p1;
-                    const uint32_t *buf = bufs + p * C::kBufWords;
-                    const uint64_t pre = ms->run[p];
-                    const uint32_t ph = static_cast<uint32_t>(pre & 31u);
-                    const uint64_t g0 = pre >> 5;
-                    const uint32_t tot = p == 0 ? tot0 : tot1;
-                    const uint32_t nfull = (ph + tot) >> 5;
-                    for (uint32_t i = (ph ? 1u : 0u) + tid; i < nfull; i += kThreads)
-                        put_word(P.payload, P.cap_words, g0 + i, shifted_word(buf, i, ph), status);
-                    const size_t g = first + size_t(tid) * C::kSyms;
-                    if (nvalid > 0) {
-                        const uint32_t d = ms->chunk_r + static_cast<uint32_t>(tid) * C::kSyms;
-                        const uint32_t kq = cdiv.div(d);
-                        if (kq * cdiv.chunk == d) P.off[ms->chunk_q + kq] = pre + (p == 0 ? excl0 : excl1);
-                    }
-                    if (tid == 32 * p) {
-                        // the word this tile starts in, and the one it ends in
-                        const uint32_t head = ph ? shifted_word(buf, 0, ph) : 0u;
-                        uint32_t combined = head;
-                        if (ph) {
-                            if (k == 0) {
-                                ms->seg_head[p] = head;  // the segment's first word: the fix-up kernel's
-                            } else {
-                                combined |= ms->carry[p];
-                                if (nfull >= 1) put_word(P.payload, P.cap_words, g0, combined, status);
-                            }
-                        }
-                        uint32_t tail = 0;
-                        if ((ph + tot) & 31u) tail = nfull == 0 ? (ph ? combined : buf[0]) : shifted_word(buf, nfull, ph);
-                        ms->carry[p] = tail;  // read only by this thread
-                        next_run = pre + tot;
-                        if (k == seg_tiles - 1)
-                            P.edge[seg] = (static_cast<uint64_t>(ms->seg_head[p]) << 32) | tail;
-                    }
-                }
-                __syncthreads();  // everyone has read the buffers and the running offsets
-                if (tid == 0) ms->run[0] = next_run;
-                if (BF16 && tid == 32) ms->run[1] = next_run;
-#pragma unroll
-                for (int p = 0; p < C::kPlanes; ++p) {
-                    uint32_t *buf = bufs + p * C::kBufWords;
-                    const uint32_t used = ((p == 0 ? tot0 : tot1) + 31u) / 32u + 1u;
-                    for (uint32_t i = tid; i < used; i += kThreads) buf[i] = 0;
-                }
-            } else {
-                __syncthreads();  // stage s consumed (an empty job)
-                if (tid == 0) issue_job<BF16, XOR>(ring, ms, issued++, n_seg, n_tiles, in, in2, n);
-            }
-        }
-    }
-}
-
-// ------------------------------------------------------------------ counted path (bf16, per shard)
-//
-// When the histogram pass has recorded each plane's counts per segment of
-// kDirSegTiles tiles, every segment's bit count is sum(count * length): a
-// scan gives each segment's offset before the encode starts.  The encode then
-// reads its input once (no counting pass) and no CTA waits for another.
-
-// Bits of each segment per plane (sum of count x length over its recorded
-// counts, a warp per segment, one wave of CTAs) and their inclusive prefix.  The last CTA to
-// finish its segments (a ticket counter) scans all segments' bits: thread t
-// of its 1024 sums a run of consecutive segments, a block scan combines the
-// runs, and each thread writes its run's prefixes as the descriptors.
 constexpr int kSegScanThreads = 1024;
 
 __global__ void __launch_bounds__(kSegScanThreads) k_seg_bits_scan(const uint32_t *__restrict__ seg_counts,
@@ -948,16 +441,17 @@ __device__ __forceinline__ void wpack(WPacker &pk, uint32_t *buf, const uint32_t
 // Lane 0's copy job for tile kk of this warp's sequence counted from segment
 // seg (which has `tiles` tiles); kk may run past that segment's end into the
 // warp's next one.  No job when the sequence ends first.
+// Returns whether a job was issued on the stage.
 template <bool XOR>
-__device__ __forceinline__ void wissue(uint8_t *ring, uint64_t *bar, uint32_t stage, uint32_t seg, uint32_t kk,
+__device__ __forceinline__ bool wissue(uint8_t *ring, uint64_t *bar, uint32_t stage, uint32_t seg, uint32_t kk,
                                        uint32_t tiles, uint32_t nw, uint32_t n_seg, uint32_t n_tiles,
                                        uint32_t last_bytes, const uint8_t *in, const uint8_t *in2, uint64_t pol) {
     if (kk >= tiles) {
         kk -= tiles;
         seg += nw;
-        if (seg >= n_seg) return;
+        if (seg >= n_seg) return false;
         const uint32_t rest = n_tiles - seg * wenc::kTilesPerSeg;
-        if (kk >= (rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg)) return;
+        if (kk >= (rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg)) return false;
     }
     const uint32_t t = seg * wenc::kTilesPerSeg + kk;
     const uint32_t bytes = t == n_tiles - 1 ? last_bytes : uint32_t(wenc::kTile * 2);  // every tile whole but the last
@@ -968,6 +462,7 @@ __device__ __forceinline__ void wissue(uint8_t *ring, uint64_t *bar, uint32_t st
         bulk_g2s_hint(dst, in + src, bytes, &bar[stage], pol);
         if (XOR) bulk_g2s_hint(dst + wenc::kTile * 2, in2 + src, bytes, &bar[stage], pol);
     }
+    return true;
 }
 
 // Complete words [skip, nfull) of a tile's buffer to dst (byte-swapped: the
@@ -1013,11 +508,13 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
     const uint64_t pol = l2_policy_evict_first();
     const uint32_t last_n = static_cast<uint32_t>(n - static_cast<size_t>(n_tiles - 1) * wenc::kTile);  // 1..512
     const uint32_t last_bytes = (last_n * 2) & ~15u;
+    uint32_t inflight = 0;  // lane 0: stages with a job issued and not yet waited for
     if (lane == 0 && gw < n_seg) {  // the first kStages tiles of the warp's sequence
         const uint32_t rest = n_tiles - gw * wenc::kTilesPerSeg;
         const uint32_t tiles0 = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
         for (int j = 0; j < wenc::kStages; ++j)
-            wissue<XOR>(ring, bar, j, gw, j, tiles0, nw, n_seg, n_tiles, last_bytes, in, in2, pol);
+            if (wissue<XOR>(ring, bar, j, gw, j, tiles0, nw, n_seg, n_tiles, last_bytes, in, in2, pol))
+                inflight |= 1u << j;
     }
     const uint32_t kbh = static_cast<uint32_t>(lane & 15) << 3;
     const uint32_t kbl = kbh + 128u;
@@ -1049,7 +546,13 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
         uint32_t to_next = cr ? cdiv.chunk - cr : 0u;
         for (uint32_t k = 0; k < tiles; ++k) {
             const int tile_n = t0 + k == n_tiles - 1 ? static_cast<int>(last_n) : wenc::kTile;
-            if (!mbar_wait(&bar[cstage], cphase) && lane == 0) set_status(status, HUFF_ERR_TIMEOUT);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar[cstage], cphase))) {
+                // the copy never arrived: no further copies; wait for those in flight, then stop
+                if (lane == 0) set_status(status, HUFF_ERR_TIMEOUT);
+                drain_ring(bar, wenc::kStages, __shfl_sync(0xffffffffu, inflight, 0), cstage, cphase);
+                return;
+            }
+            inflight &= ~(1u << cstage);
             const uint8_t *st = ring + cstage * wenc::kStageBytes;
             uint32_t wv[8];
             {
@@ -1087,9 +590,9 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
             __syncwarp();  // every lane has read the stage
             if (lane == 0) fence_proxy_async_smem();  // the reads before the bulk copy that refills the stage
             // the stage is free again: lane 0 refills it with the tile kStages further on
-            if (lane == 0)
-                wissue<XOR>(ring, bar, cstage, seg, k + wenc::kStages, tiles, nw, n_seg, n_tiles, last_bytes, in, in2,
-                            pol);
+            if (lane == 0 && wissue<XOR>(ring, bar, cstage, seg, k + wenc::kStages, tiles, nw, n_seg, n_tiles,
+                                         last_bytes, in, in2, pol))
+                inflight |= 1u << cstage;
             cstage = cstage + 1 == uint32_t(wenc::kStages) ? 0u : cstage + 1;
             cphase ^= cstage == 0 ? 1u : 0u;
 
@@ -1241,7 +744,8 @@ __device__ __forceinline__ uint32_t seg_tiles8(uint32_t seg, uint32_t n_tiles, u
 // Issue the cursor's job into `stage` and advance it; seg_next is the warp's
 // claim of its next segment (0xffffffff until made), taken when the current
 // segment's jobs are done.
-__device__ __forceinline__ void wissue8(uint8_t *ring, uint64_t *bar, uint32_t stage, Job8 &j, uint32_t &seg_next,
+// Returns whether a job was issued on the stage.
+__device__ __forceinline__ bool wissue8(uint8_t *ring, uint64_t *bar, uint32_t stage, Job8 &j, uint32_t &seg_next,
                                         uint32_t n_seg, uint32_t n_tiles, uint32_t st, uint32_t last_bytes,
                                         const uint8_t *in, uint64_t pol_keep, uint64_t pol_drop) {
     if (j.pass == 2) {
@@ -1250,7 +754,7 @@ __device__ __forceinline__ void wissue8(uint8_t *ring, uint64_t *bar, uint32_t s
         j.k = 0;
         seg_next = 0xffffffffu;  // taken: the next claim replaces it
     }
-    if (j.seg >= n_seg) return;
+    if (j.seg >= n_seg) return false;
     const uint32_t t = j.seg * st + j.k;
     const uint32_t bytes = t == n_tiles - 1 ? last_bytes : uint32_t(wenc8::kTile);
     mbar_arrive_expect_tx(&bar[stage], bytes);
@@ -1261,6 +765,7 @@ __device__ __forceinline__ void wissue8(uint8_t *ring, uint64_t *bar, uint32_t s
         j.k = 0;
         ++j.pass;
     }
+    return true;
 }
 
 // A lane's 32 symbols: pairs of consecutive symbols as (code, length).
@@ -1383,18 +888,26 @@ __global__ void __launch_bounds__(wenc8::kThreads, 1)
     seg = __shfl_sync(0xffffffffu, seg, 0);
     Job8 job{seg, 0, 0};
     uint32_t job_next = 0xffffffffu;  // lane 0: the next segment, once claimed
+    uint32_t inflight = 0;  // lane 0: stages with a job issued and not yet waited for
     if (lane == 0)
         for (int s = 0; s < wenc8::kStages; ++s)
-            wissue8(ring, bar, s, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep, pol_drop);
+            if (wissue8(ring, bar, s, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep, pol_drop))
+                inflight |= 1u << s;
     uint32_t cstage = 0, cphase = 0;
 
     auto next_stage = [&]() {
         cstage = cstage + 1 == uint32_t(wenc8::kStages) ? 0u : cstage + 1;
         cphase ^= cstage == 0 ? 1u : 0u;
     };
-    // a lane's 32 bytes of the tile in the current stage (global memory for bytes past the bulk copy)
-    auto read_stage = [&](size_t first, int tile_n, uint32_t (&wv)[8]) {
-        if (!mbar_wait(&bar[cstage], cphase) && lane == 0) set_status(status, HUFF_ERR_TIMEOUT);
+    // a lane's 32 bytes of the tile in the current stage (global memory for bytes past the bulk copy);
+    // false when the stage's copy never arrived (the warp must then stop: see the callers)
+    auto read_stage = [&](size_t first, int tile_n, uint32_t (&wv)[8]) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar[cstage], cphase))) {
+            if (lane == 0) set_status(status, HUFF_ERR_TIMEOUT);
+            drain_ring(bar, wenc8::kStages, __shfl_sync(0xffffffffu, inflight, 0), cstage, cphase);
+            return false;
+        }
+        inflight &= ~(1u << cstage);
         const uint8_t *st = ring + cstage * wenc8::kStageBytes;
         const uint4 a = *reinterpret_cast<const uint4 *>(st + lane * 32);
         const uint4 c = *reinterpret_cast<const uint4 *>(st + lane * 32 + 16);
@@ -1412,6 +925,7 @@ __global__ void __launch_bounds__(wenc8::kThreads, 1)
         consumed(wv);
         __syncwarp();  // every lane has read the stage
         if (lane == 0) fence_proxy_async_smem();  // the reads before the bulk copy that refills the stage
+        return true;
     };
 
     while (seg < n_seg) {
@@ -1424,9 +938,10 @@ __global__ void __launch_bounds__(wenc8::kThreads, 1)
             const size_t first = seg_first + static_cast<size_t>(k) * wenc8::kTile;
             const int tile_n = seg * st + k == n_tiles - 1 ? static_cast<int>(last_n) : wenc8::kTile;
             uint32_t wv[8];
-            read_stage(first, tile_n, wv);
-            if (lane == 0) wissue8(ring, bar, cstage, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep,
-                                    pol_drop);
+            if (!read_stage(first, tile_n, wv)) return;
+            if (lane == 0 && wissue8(ring, bar, cstage, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep,
+                                     pol_drop))
+                inflight |= 1u << cstage;
             next_stage();
             const int nvalid = tile_n - lane * 32 < 0 ? 0 : (tile_n - lane * 32 > 32 ? 32 : tile_n - lane * 32);
             uint32_t b = 0;
@@ -1449,7 +964,8 @@ __global__ void __launch_bounds__(wenc8::kThreads, 1)
         if (seg != 0) {
             uint64_t wnd[kLookbackPerLane];
             load_window(P.desc, static_cast<int64_t>(seg) - 1, lane, wnd);
-            start = lookback(P.desc, seg, lane, status, wnd);
+            unsigned polls;
+            start = lookback(P.desc, seg, lane, status, wnd, kSpinLimit, polls);
             if (lane == 0) st_relaxed(&P.desc[seg], kFlagPrefix | (start + seg_bits));
         }
         // ---------------- pass 2: pack, tile after tile
@@ -1471,9 +987,10 @@ __global__ void __launch_bounds__(wenc8::kThreads, 1)
                 seg_next = __shfl_sync(0xffffffffu, claim, 0);
             }
             uint32_t wv[8];
-            read_stage(first, tile_n, wv);
-            if (lane == 0) wissue8(ring, bar, cstage, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep,
-                                    pol_drop);
+            if (!read_stage(first, tile_n, wv)) return;
+            if (lane == 0 && wissue8(ring, bar, cstage, job, job_next, n_seg, n_tiles, st, last_bytes, in, pol_keep,
+                                     pol_drop))
+                inflight |= 1u << cstage;
             next_stage();
             if (missing) continue;  // the status is set; this segment's stream is not written
             const int nvalid = tile_n - lane * 32 < 0 ? 0 : (tile_n - lane * 32 > 32 ? 32 : tile_n - lane * 32);
@@ -1559,30 +1076,42 @@ __global__ void k_encode_fixup(EncPlane p0, EncPlane p1, int planes, uint32_t n_
     }
 }
 
-template <bool BF16, bool XOR>
-int run_encode(const uint8_t *in, const uint8_t *in2, size_t n, EncPlane p0, EncPlane p1, size_t chunk,
-               uint32_t n_tiles, unsigned *seg_ctr, int32_t *status, cudaStream_t s) {
-    using C = EncCfg<BF16, XOR>;
-    auto kern = k_encode<BF16, XOR>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) !=
-        cudaSuccess)
-        return HUFF_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::kSmem) != cudaSuccess)
-        return HUFF_ERR_CUDA;
-    if (per_sm < 1) return HUFF_ERR_CUDA;
-    const uint32_t n_seg = (n_tiles + kSegTiles - 1) / kSegTiles;
-    const DevInfo d = dev_info();
-    size_t grid = static_cast<size_t>(d.sms) * per_sm;
-    if (grid > n_seg) grid = n_seg;
-    // segments are claimed in order by CTAs that are already running, so every segment a
-    // lookback waits for belongs to a resident CTA and the grid needs no co-residency
-    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(in, in2, n, p0, p1, make_chunk_div(chunk), n_tiles,
-                                                                  seg_ctr, status);
-    if (cudaGetLastError() != cudaSuccess) return HUFF_ERR_CUDA;
-    const size_t n_chunks = (n + chunk - 1) / chunk;
-    k_encode_fixup<<<(n_seg + 255) / 256, 256, 0, s>>>(p0, p1, C::kPlanes, n_seg, n_chunks, status);
-    return launch_status();
+// The bounded waits on their own (huff_debug_wait): one warp runs the
+// lookback of segment `seg` over desc[0 .. seg) (kind 0), or waits on an
+// mbarrier that nothing arrives on and no copy targets (kind 1), with at most
+// `limit` polls; out[0] = the lookback's exclusive prefix, out[1] = the polls
+// made.
+__global__ void k_wait_probe(int kind, const uint64_t *desc, uint32_t seg, unsigned limit, uint64_t *out,
+                             int32_t *status) {
+    __shared__ uint64_t bar;
+    const int lane = threadIdx.x & 31;
+    if (kind == 0) {
+        uint64_t wnd[kLookbackPerLane];
+        load_window(desc, static_cast<int64_t>(seg) - 1, lane, wnd);
+        unsigned polls = 0;
+        const uint64_t excl = lookback(desc, seg, lane, status, wnd, limit, polls);
+        if (lane == 0) {
+            out[0] = excl;
+            out[1] = polls;
+        }
+        return;
+    }
+    if (lane == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    unsigned polls = 0;
+    bool ok = false;
+    while (!ok && polls < limit) {  // the same bounded wait, one poll per round, counted
+        ok = mbar_wait(&bar, 0, 1);
+        ++polls;
+    }
+    if (lane == 0) {
+        if (!ok) set_status(status, HUFF_ERR_TIMEOUT);
+        out[0] = 0;
+        out[1] = polls;
+    }
 }
 
 __global__ void k_encode_empty(uint64_t *off0, uint64_t *off1) {
@@ -1591,6 +1120,12 @@ __global__ void k_encode_empty(uint64_t *off0, uint64_t *off1) {
 }
 
 }  // namespace
+
+int launch_wait_probe(int kind, const uint64_t *desc, uint32_t seg, unsigned limit, uint64_t *out, int32_t *status,
+                      cudaStream_t s) {
+    k_wait_probe<<<1, 32, 0, s>>>(kind, desc, seg, limit, out, status);
+    return launch_status();
+}
 
 // Tiles per segment of the byte-stream encode: 16 when there are at least 8192
 // tiles per 16 of them (two segments and more for every warp of a large GPU),
@@ -1609,7 +1144,6 @@ size_t enc_u8_workspace_words(size_t n) {
     const size_t st = enc_u8_seg_tiles(n);
     return 2 * ((tiles + st - 1) / st) + 2;
 }
-size_t enc_bf16_tiles(size_t n) { return (n + kEncBf16Tile - 1) / kEncBf16Tile; }
 
 int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk, uint8_t *payload,
                      size_t cap, uint64_t *off, void *ws, int32_t *status, cudaStream_t s) {
@@ -1644,20 +1178,14 @@ int launch_encode_u8(const uint8_t *in, size_t n, const huff_codebook *cb, size_
     return launch_status();
 }
 
-// Device address of g_noalloc_scratch on the current device, looked up once per
-// device (host code only sees a host-side stand-in under the array's name).
+// Device address of g_noalloc_scratch on the current device (host code only
+// sees a host-side stand-in under the array's name).  Looked up on every call:
+// the query allocates nothing, and a cached address would go stale when the
+// device's context is torn down and made again (cudaDeviceReset).
 static uint64_t *noalloc_scratch_address() {
-    static std::mutex mu;
-    static uint64_t *addr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<uint64_t *>(p);
-    }
-    return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    return static_cast<uint64_t *>(p);
 }
 
 int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *cb, size_t chunk, uint8_t *payload,
@@ -1669,6 +1197,21 @@ int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *c
     return launch_encode_u8(in, n, cb, chunk, payload, cap, off, ws, status, s);
 }
 
+// bf16 with given codebooks (the fixed-codebook mode): the counted histogram pass records both planes'
+// counts per segment, and the one-pass counted encode then gives every segment its bit offset from
+// sum(count x length) under the given codebooks (a symbol present without a code is reported by that
+// sum).  The input is read twice from HBM (it is larger than L2), by two kernels that each run near
+// their own bound.  Workspace (lmc_workspace_size): segment counts, the counted encode's workspace,
+// then the two histograms the counting pass also produces.
+size_t enc_bf16_given_ws_parts(size_t n, size_t *counted_off, size_t *hist_off) {
+    const size_t segs = (n + kDirSegElems - 1) / kDirSegElems;
+    const size_t counts = (static_cast<size_t>(kSegCountWords) * 4 * segs + 255) / 256 * 256;
+    const size_t counted = (48 * segs + 16 + 255) / 256 * 256;
+    if (counted_off) *counted_off = counts;
+    if (hist_off) *hist_off = counts + counted;
+    return counts + counted + 512 * sizeof(uint64_t);
+}
+
 int launch_encode_bf16(const uint16_t *w16, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
                        const huff_codebook *cb_lo, size_t chunk, uint8_t *pay_hi, size_t cap_hi, uint64_t *off_hi,
                        uint8_t *pay_lo, size_t cap_lo, uint64_t *off_lo, void *ws, int32_t *status,
@@ -1677,20 +1220,17 @@ int launch_encode_bf16(const uint16_t *w16, const uint16_t *x0, size_t n, const 
         k_encode_empty<<<1, 1, 0, s>>>(off_hi, off_lo);
         return launch_status();
     }
-    const size_t tiles = enc_bf16_tiles(n);
-    const size_t segs = (tiles + kSegTiles - 1) / kSegTiles;
-    uint64_t *w = static_cast<uint64_t *>(ws);
-    // layout: desc_hi, desc_lo, segment counter (zeroed), edge_hi, edge_lo
-    int st = launch_zero_u64(w, 2 * segs + 1, s);
+    size_t counted_off = 0, hist_off = 0;
+    enc_bf16_given_ws_parts(n, &counted_off, &hist_off);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *seg_counts = reinterpret_cast<uint32_t *>(w);
+    uint64_t *hist = reinterpret_cast<uint64_t *>(w + hist_off);
+    int st = launch_zero_u64(hist, 512, s);
     if (st != HUFF_OK) return st;
-    EncPlane p0{cb_hi, reinterpret_cast<uint32_t *>(pay_hi), cap_hi / 4, off_hi, w, w + 2 * segs + 1};
-    EncPlane p1{cb_lo, reinterpret_cast<uint32_t *>(pay_lo), cap_lo / 4, off_lo, w + segs, w + 3 * segs + 1};
-    unsigned *ctr = reinterpret_cast<unsigned *>(w + 2 * segs);
-    const uint8_t *a = reinterpret_cast<const uint8_t *>(w16);
-    if (x0 != nullptr)
-        return run_encode<true, true>(a, reinterpret_cast<const uint8_t *>(x0), n, p0, p1, chunk,
-                                      static_cast<uint32_t>(tiles), ctr, status, s);
-    return run_encode<true, false>(a, nullptr, n, p0, p1, chunk, static_cast<uint32_t>(tiles), ctr, status, s);
+    st = launch_histogram_bf16_counted(w16, x0, n, hist, hist + 256, seg_counts, s);
+    if (st != HUFF_OK) return st;
+    return launch_encode_bf16_counted(w16, x0, n, cb_hi, cb_lo, chunk, seg_counts, pay_hi, cap_hi, off_hi, pay_lo,
+                                      cap_lo, off_lo, w + counted_off, status, s);
 }
 
 int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n, const huff_codebook *cb_hi,
@@ -1701,8 +1241,7 @@ int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n
         k_encode_empty<<<1, 1, 0, s>>>(off_hi, off_lo);
         return launch_status();
     }
-    const size_t tiles = enc_bf16_tiles(n);
-    const size_t segs = (tiles + kDirSegTiles - 1) / kDirSegTiles;
+    const size_t segs = (n + kDirSegElems - 1) / kDirSegElems;
     uint64_t *w = static_cast<uint64_t *>(ws);
     // layout: desc_hi, desc_lo, edge_hi, edge_lo, 32-bit bits (2 x segs), ticket counter (zeroed)
     EncPlane p0{cb_hi, reinterpret_cast<uint32_t *>(pay_hi), cap_hi / 4, off_hi, w, w + 2 * segs};

@@ -245,3 +245,61 @@ def test_decode_more_chunk_pairs_than_one_wave(chunk, n, delta):
     s = codec.compress_bf16(x1, x0 if delta else None, chunk)
     back = codec.decompress_bf16(s, x0 if delta else None)
     assert torch.equal(back.view(torch.int16), x1.view(torch.int16))
+
+
+# ------------------------------------------------------------------ given codebooks (the fixed-codebook mode)
+@pytest.mark.parametrize("n", [1, 4097, SEG + 1, 3 * SEG + 4097])
+@pytest.mark.parametrize("delta", [False, True])
+def test_given_codebooks_match_oracle(n, delta):
+    """lmc_encode_bf16 with codebooks fixed in advance (built, every symbol covered, from a warm-up
+    pair) encodes another pair exactly as the oracle does with those lengths."""
+    rng = np.random.default_rng(1000 + n + delta)
+    w0, w1 = _pair(50_000, rng)  # warm-up
+    x0, x1 = _pair(n, rng)
+    def planes(a, b):
+        w = a.view(torch.int16).numpy().view(np.uint16)
+        if delta:
+            w = oracle.delta_xor(w, b.view(torch.int16).numpy().view(np.uint16))
+        return oracle.bytegroup_split(w)
+    whi, wlo = planes(w1, w0)
+    hi, lo = planes(x1, x0)
+    cbs, lens = [], []
+    for p in (whi, wlo):
+        h = torch.from_numpy(oracle.histogram(p).astype(np.int64)).cuda()
+        cbs.append(codec.build_codebook(h, 24, _lib.HUFF_COVER_ALL))
+        lens.append(oracle.code_lengths(oracle.histogram(p), 24, oracle.REF_COVER_ALL))
+        np.testing.assert_array_equal(cbs[-1].lengths(), lens[-1])
+    dx0 = x0.cuda() if delta else None
+    s = codec.compress_bf16(x1.cuda(), dx0, 4096, cb_hi=cbs[0], cb_lo=cbs[1])
+    for plane, ln, stream in ((hi, lens[0], s.hi), (lo, lens[1], s.lo)):
+        pay, off = oracle.encode(plane, ln, oracle.canonical_codes(ln), 4096)
+        assert_stream_equal(stream, pay, off)
+    back = codec.decompress_bf16(s, dx0)
+    assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
+
+
+def test_given_codebook_without_a_symbol_sets_status():
+    rng = np.random.default_rng(12)
+    x0, x1 = _pair(SEG + 77, rng)
+    h = torch.zeros(256, dtype=torch.int64, device="cuda")
+    h[0] = 10
+    h[1] = 3
+    cb = codec.build_codebook(h)
+    with pytest.raises(_lib.HuffError) as e:
+        codec.compress_bf16(x1.cuda(), x0.cuda(), 4096, cb_hi=cb, cb_lo=cb)
+    assert e.value.status == _lib.HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK
+
+
+def test_given_codebooks_workspace_size_is_checked():
+    n = SEG + 1
+    w = torch.zeros(n, dtype=torch.int16, device="cuda")
+    cb = codec.build_codebook(torch.ones(256, dtype=torch.int64, device="cuda"))
+    cap = _lib.huff_encode_bound(n, 24)
+    p = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    o = torch.empty(_lib.huff_num_chunks(n, 4096) + 1, dtype=torch.int64, device="cuda")
+    need = _lib.lmc_workspace_size(n, 4096)
+    assert need >= _lib.lmc_segment_counts_size(n) + _lib.lmc_counted_workspace_size(n)
+    ws = torch.empty(need // 8 - 1, dtype=torch.int64, device="cuda")
+    with pytest.raises(_lib.HuffError) as e:
+        _lib.lmc_encode_bf16(w, None, cb.buf, cb.buf, 4096, p, o, p.clone(), o.clone(), ws, codec.new_status())
+    assert e.value.status == _lib.HUFF_ERR_BUFFER_TOO_SMALL

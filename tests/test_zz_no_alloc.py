@@ -62,3 +62,23 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
         _lib.huff_encode_noalloc(x, cb.buf, 1 << 20, payload, off, codec.new_status(),
                                  n=_lib.HUFF_NOALLOC_MAX_SYMBOLS + 1)
     assert e.value.status == _lib.HUFF_ERR_BUFFER_TOO_SMALL
+
+
+def test_noalloc_at_its_largest_size_equals_workspace_encode():
+    """n at HUFF_NOALLOC_MAX_SYMBOLS (and just below it, ragged), where the byte-stream encode uses the
+    most segments of 16 tiles and so the most of the scratch: the same stream as huff_encode."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(123)
+    top = _lib.HUFF_NOALLOC_MAX_SYMBOLS
+    for n, chunk in ((top, 1 << 20), (top - 4097, 16384)):
+        x = torch.randn(n, device="cuda", generator=g).mul_(12).round_().clamp_(-128, 127).to(torch.int8)
+        x = x.view(torch.uint8)
+        cb = codec.build_codebook(codec.histogram(x))
+        ref = codec.encode(x, cb, chunk)
+        payload, off = _encode_noalloc(x, cb, chunk)
+        assert torch.equal(off, ref.off)
+        T = int(ref.off[-1].item())
+        used = ((T + 31) // 32) * 4
+        assert torch.equal(payload[:used], ref.payload[:used])
+        del x, ref, payload, off
+        torch.cuda.empty_cache()
