@@ -28,13 +28,19 @@
 //     (up to 32); on a plane without one, while every lane of the warp has
 //     room for two full steps in its chunk and its ring, two steps run
 //     without the per-step checks;
+//   * the fused bf16 decode of a high plane with a 1-bit code (a snapshot
+//     delta's, about 98 % one symbol) takes at most one other code per step
+//     and then the whole run of the 1-bit code after it, into a ring that
+//     already holds that code's symbol (no stores for runs); it has its own
+//     kernel, which also stages x0 in shared memory a segment ahead;
 //   * decoded bytes go to per-lane shared rings in segments; the warp steps
 //     until every lane has its segment (a lane that is ahead decodes into
 //     the ring's free part), then merges 8 lanes' segments per pass into
-//     16-bit words, XORs x0 (prefetched to L2 before the segments' decode;
-//     a merge's four loads issued together) and stores 16 bytes per lane;
-//     while every chunk of the warp has the same length (all warps but the
-//     last one of a ragged input), the merge skips the per-lane bounds.
+//     16-bit words, XORs x0 (staged, or prefetched to L2 before the segments'
+//     decode with a merge's four loads issued together) and stores 16 bytes
+//     per lane; while every chunk of the warp has the same length (all warps
+//     but the last one of a ragged input), the merge skips the per-lane
+//     bounds.
 // Every chunk must end exactly at the next chunk's offset, otherwise
 // HUFF_ERR_CORRUPT_STREAM is reported.
 #include "common.cuh"
@@ -48,10 +54,10 @@ constexpr int kSecMax = 2048;  // secondary-table entries per plane
 // Shared decode tables of one codebook for a W-bit window (W = 12: the
 // codebook's own table; W = 13: built from it in the prologue).  16-byte
 // aligned and sized, so tables placed back to back stay aligned.
-template <int W>
+template <int W, int SEC = kSecMax>
 struct __align__(16) DecTables {
     uint64_t lut[1u << W];  // syms (48 bits) | count << 48 | total bits << 52; 0: first code > W bits
-    uint16_t sec[kSecMax];  // codes longer than W bits: symbol | length << 8 (0: no code)
+    uint16_t sec[SEC];      // codes longer than W bits: symbol | length << 8 (0: no code)
     uint64_t run;           // the 1-bit code's symbol in all 8 bytes (when there is one)
     uint32_t bl_count[32];
     uint32_t first_code[32];
@@ -68,7 +74,30 @@ struct __align__(16) DecTables {
 };
 static_assert(sizeof(DecTables<12>) % 16 == 0 && sizeof(DecTables<13>) % 16 == 0, "tables keep 16-byte alignment");
 
-constexpr size_t kBf16Tables = sizeof(DecTables<12>) + sizeof(DecTables<13>);
+// Tables of a plane with a 1-bit code, for the run decode below: the
+// canonical arrays and, for each 10-bit window, the first code's symbol and
+// length (symbol | length << 8; 0 when that code is longer than 10 bits,
+// which the canonical search then decodes).
+constexpr int kZWin = 10;
+struct __align__(16) RunTables {
+    uint64_t run;  // the 1-bit code's symbol in all 8 bytes
+    uint32_t bl_count[32];
+    uint32_t first_code[32];
+    uint32_t first_index[32];
+    uint8_t sorted[256];
+    int longest;
+    int ok;
+    uint16_t zf[1u << kZWin];
+};
+
+// Secondary-table entries of the low plane next to a run-decoded high plane
+// (less than the default, so that x0 can be staged in the shared memory).
+constexpr int kSecRun = 1024;
+using LoTables = DecTables<13>;
+using LoTablesRun = DecTables<13, kSecRun>;
+static_assert(sizeof(RunTables) % 16 == 0 && sizeof(LoTablesRun) % 16 == 0, "tables keep 16-byte alignment");
+constexpr size_t kBf16Tables = sizeof(DecTables<12>) + sizeof(LoTables);
+constexpr size_t kBf16RunTables = sizeof(RunTables) + sizeof(LoTablesRun);
 
 // Canonical codes fill the code space in order of length, so the codes of at
 // most l bits are the 24-bit windows below (first_code[l] + bl_count[l]) <<
@@ -85,8 +114,8 @@ __device__ __forceinline__ uint32_t code_limit(const huff_codebook *cb, bool ok,
 // plus, when it holds fewer than the maximum number of symbols, the one code
 // that ends exactly at the 13th bit (a code ending earlier would already be
 // in the 12-bit entry, and no code is shorter than 1 bit).
-template <int W>
-__device__ void load_table_a(DecTables<W> &T, const huff_codebook *cb) {
+template <int W, int SEC>
+__device__ void load_table_a(DecTables<W, SEC> &T, const huff_codebook *cb) {
     static_assert(W == HUFF_LUT_BITS || W == HUFF_LUT_BITS + 1, "12- or 13-bit window");
     const int tid = threadIdx.x;
     const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
@@ -117,7 +146,7 @@ __device__ void load_table_a(DecTables<W> &T, const huff_codebook *cb) {
         }
     }
     uint4 *sz = reinterpret_cast<uint4 *>(T.sec);
-    for (int i = tid; i < kSecMax / 8; i += blockDim.x) sz[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < SEC / 8; i += blockDim.x) sz[i] = make_uint4(0, 0, 0, 0);
     if (tid < 32) {
         T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
         T.first_code[tid] = ok ? cb->first_code[tid] : 0;
@@ -138,7 +167,7 @@ __device__ void load_table_a(DecTables<W> &T, const huff_codebook *cb) {
         const int first = k ? static_cast<int>(cb->first_code[W + 1] >> 1) : (1 << W);
         T.sec_k = k;
         T.sec_first = first;
-        T.sec_ok = k == 0 || (first <= (1 << W) && (static_cast<long long>((1 << W) - first) << k) <= kSecMax);
+        T.sec_ok = k == 0 || (first <= (1 << W) && (static_cast<long long>((1 << W) - first) << k) <= SEC);
     }
 }
 
@@ -147,8 +176,8 @@ __device__ void load_table_a(DecTables<W> &T, const huff_codebook *cb) {
 // shorter ones, so their W-bit prefixes are the contiguous range
 // [first_code[W + 1] / 2, 2^W); sec holds, per prefix, 2^k entries
 // (k = longest - W) indexed by the next k bits.
-template <int W>
-__device__ void load_table_b(DecTables<W> &T, const huff_codebook *cb) {
+template <int W, int SEC>
+__device__ void load_table_b(DecTables<W, SEC> &T, const huff_codebook *cb) {
     if (!T.ok || T.sec_k == 0 || !T.sec_ok) return;
     const int k = T.sec_k;
     for (int sym = threadIdx.x; sym < 256; sym += blockDim.x) {
@@ -204,8 +233,8 @@ __device__ __forceinline__ uint32_t long_code_lim(uint32_t top, const Tab &T, in
     return (L << 8) | T.sorted[T.first_index[L] + d];
 }
 
-template <int W>
-__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W> *T) {
+template <int W, int SEC>
+__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W, SEC> *T) {
     return long_code_lim<W>(top, *T, T->longest);
 }
 
@@ -214,8 +243,8 @@ __device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W> *T) 
 // measured 1.2 % slower there (a different register allocation around the
 // call); the byte-stream decodes, whose fixed codebooks often meet data they
 // were not built for (codes of 17 to 24 bits), use the count.
-template <int W>
-__device__ __noinline__ uint32_t long_code_search(uint32_t top, const DecTables<W> *T) {
+template <int W, class Tab>
+__device__ __noinline__ uint32_t long_code_search(uint32_t top, const Tab *T) {
     const uint32_t v = top >> (32 - HUFF_MAX_LEN);
     for (int l = W + 1; l <= T->longest; ++l) {
         const uint32_t c = v >> (HUFF_MAX_LEN - l);
@@ -227,8 +256,8 @@ __device__ __noinline__ uint32_t long_code_search(uint32_t top, const DecTables<
 
 // The rare case where a table entry holds more symbols than the chunk has
 // left: the total length of its first c symbols.
-template <int W>
-__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables<W> *T) {
+template <int W, int SEC>
+__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables<W, SEC> *T) {
     uint32_t bits = 0;
     for (uint32_t k = 0; k < c; ++k) bits += T->len[(v >> (8 * k)) & 0xffu];
     return bits;
@@ -312,8 +341,8 @@ struct PlaneDec {
 // The rare cases of a step: a code longer than the table's window (or no
 // code at all: a corrupt stream), and an entry with more symbols than the
 // chunk has left.
-template <int W, bool LIM>
-__device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
+template <int W, bool LIM, int SEC>
+__device__ __forceinline__ void step_rare(const DecTables<W, SEC> &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
                                        uint32_t &bits, uint64_t &v, bool &bad) {
     if (c == 0) {
         uint32_t L = 0, sym = 0;
@@ -327,7 +356,7 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
                 sym = e2 & 0xffu;
             }
         } else {
-            const uint32_t lc = LIM ? long_code(top, &T) : long_code_search(top, &T);
+            const uint32_t lc = LIM ? long_code(top, &T) : long_code_search<W>(top, &T);
             L = lc >> 8;
             sym = lc & 0xffu;
         }
@@ -351,8 +380,8 @@ __device__ __forceinline__ void step_rare(const DecTables<W> &T, uint32_t win, u
 // the zero bits on top of the window (up to 32, the chunk's rest and the
 // ring's room) when that beats a lookup; then up to four 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
-template <int RING, bool RUN, int W, bool LIM, bool FAST = false>
-__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
+template <int RING, bool RUN, int W, bool LIM, bool FAST = false, int SEC = kSecMax>
+__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
     static_assert(!(RUN && FAST), "a run step may add more symbols than a fast block reserves");
     // Predicated rather than branched: a lane with nothing to do (its chunk
@@ -434,8 +463,8 @@ __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, siz
 
 // Decode until every lane of the warp has stored symbols [.., need) into its
 // RING-byte ring (a lane whose chunk is complete stores its last partial word).
-template <int RING, bool RUN, int W, bool LIM>
-__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
+template <int RING, bool RUN, int W, bool LIM, int SEC>
+__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
                                                uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
                                                bool &bad) {
     const uint64_t run = RUN ? T.run : 0ull;
@@ -505,13 +534,109 @@ __device__ __forceinline__ void fill_pair(PlaneDec &h, PlaneDec &l, const uint8_
     }
 }
 
-template <int RING, bool LIM, int W>
-__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W> &T,
+template <int RING, bool LIM, int W, int SEC>
+__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
                                              uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
     if (T.has_run)
         fill_segment_t<RING, true, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
     else
         fill_segment_t<RING, false, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+}
+
+// ------------------------------------------------------------------ planes with a 1-bit code
+//
+// A plane whose most frequent symbol has a 1-bit code (the high plane of a
+// snapshot delta: that symbol is 0 for about 98 % of elements) is decoded as
+// runs.  The lane's ring holds that symbol in every slot not yet decoded
+// (filled at the start, and again by the merge after it reads a segment), so
+// a run costs no store at all.  One step takes at most one other code (it
+// starts with a 1 bit: the 1-bit code is 0; its symbol is stored as one byte)
+// and then the run of 1-bit codes after it: as many as the zero bits on top of
+// the buffer, up to the valid bits, the chunk's rest and the ring's room.  No
+// symbols are ever pending: st counts the symbols placed.
+
+// The run tables of a codebook with a 1-bit code (every thread of the block
+// takes part).
+__device__ void load_run_tables(RunTables &T, const huff_codebook *cb) {
+    const int tid = threadIdx.x;
+    const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC && cb->longest <= HUFF_MAX_LEN;
+    if (tid < 32) {
+        T.bl_count[tid] = ok ? cb->bl_count[tid] : 0;
+        T.first_code[tid] = ok ? cb->first_code[tid] : 0;
+        T.first_index[tid] = ok ? cb->first_index[tid] : 0;
+    }
+    for (int i = tid; i < 256; i += blockDim.x) T.sorted[i] = ok ? cb->sorted_symbols[i] : 0;
+    // the codebook's 12-bit table gives each window's first symbol; its code is taken when it is at most
+    // kZWin bits long
+    for (int i = tid; i < (1 << kZWin); i += blockDim.x) {
+        uint32_t v = 0;
+        if (ok) {
+            const uint64_t e = cb->lut[static_cast<size_t>(i) << (HUFF_LUT_BITS - kZWin)];
+            const uint32_t sym = static_cast<uint32_t>(e & 0xffu);
+            const uint32_t L = cb->len[sym];
+            if (((e >> 48) & 15u) != 0 && L <= static_cast<uint32_t>(kZWin)) v = sym | (L << 8);
+        }
+        T.zf[i] = static_cast<uint16_t>(v);
+    }
+    if (tid == 0) {
+        T.longest = ok ? cb->longest : 0;
+        T.ok = ok;
+        T.run = (ok ? static_cast<uint64_t>(cb->sorted_symbols[0]) : 0ull) * 0x0101010101010101ull;
+    }
+}
+
+// Shift the 64-bit buffer (bh, bl) left by r bits, 0 <= r <= 64.
+__device__ __forceinline__ void consume64(PlaneDec &s, uint32_t r) {
+    const uint32_t r1 = r < 32 ? r : 32u;  // first up to 32 bits, then the rest
+    const uint32_t r2 = r - r1;
+    uint32_t bh = __funnelshift_lc(s.bl, s.bh, r1);
+    uint32_t bl = __funnelshift_lc(0u, s.bl, r1);
+    bh = __funnelshift_lc(bl, bh, r2);
+    bl = __funnelshift_lc(0u, bl, r2);
+    s.bh = bh;
+    s.bl = bl;
+    s.nb -= static_cast<int>(r);
+}
+
+template <int RING>
+__device__ __forceinline__ void step_zrun(PlaneDec &s, const uint8_t *p, size_t nbytes, const RunTables &T,
+                                          uint8_t *ring, uint32_t swz, int cnt, int limit, bool &bad) {
+    const int rem = cnt - s.st;
+    const int room = limit - s.st;
+    const bool go = rem > 0 && room > 0;
+    s.refill(p, nbytes);
+    // another code first, when the top bit is 1
+    const bool nz = go && static_cast<int32_t>(s.bh) < 0;
+    const uint32_t f = T.zf[s.bh >> (32 - kZWin)];
+    uint32_t L = f >> 8, sym = f & 0xffu;
+    if (__any_sync(0xffffffffu, nz && L == 0)) {  // a code longer than the window (or none: corrupt)
+        if (nz && L == 0) {
+            const uint32_t lc = long_code_search<kZWin>(s.bh, &T);
+            L = lc >> 8;
+            sym = lc & 0xffu;
+            if (L == 0) {
+                bad = true;
+                L = 1;
+            }
+        }
+    }
+    if (nz) ring[(s.st & (RING - 1)) ^ swz] = static_cast<uint8_t>(sym);
+    const int one = nz ? 1 : 0;
+    s.consume(nz ? L : 0u);
+    // then the run: the zero bits on top, within the valid bits, the chunk and the ring
+    const uint32_t z = s.bh != 0 ? __clz(s.bh) : 32u + __clz(s.bl);  // 64 when the buffer is all zeros
+    int r = min(min(static_cast<int>(z), s.nb), min(rem, room) - one);
+    r = go ? r : 0;
+    consume64(s, static_cast<uint32_t>(r));
+    s.st += one + r;
+}
+
+// Steps until every lane of the warp has placed symbols [.., need).
+template <int RING>
+__device__ __forceinline__ void fill_zrun(PlaneDec &s, const uint8_t *p, size_t nbytes, const RunTables &T,
+                                          uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
+    while (__any_sync(0xffffffffu, s.st < need && s.st != cnt))
+        step_zrun<RING>(s, p, nbytes, T, ring, swz, cnt, limit, bad);
 }
 
 // The chunk's bit range lies in the payload and holds between one and
@@ -876,26 +1001,30 @@ __host__ int split_threads(size_t n_chunks, size_t chunk, int sms) {
 // the other; each ring's two 32-byte halves swapped on every second lane
 // pair), then the warp merges 8 lanes' segments per pass: bytes to 16-bit
 // words, XOR x0, 16-byte streaming stores.
-template <bool XOR, bool PAIR>
-__global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf16(
-    const uint8_t *__restrict__ pay_hi, size_t bytes_hi, const uint64_t *__restrict__ off_hi,
-    const uint8_t *__restrict__ pay_lo, size_t bytes_lo, const uint64_t *__restrict__ off_lo, size_t n,
-    size_t chunk, const huff_codebook *__restrict__ cb_hi, const huff_codebook *__restrict__ cb_lo,
-    const uint16_t *__restrict__ x0, uint16_t *__restrict__ out, int32_t *status) {
-    extern __shared__ __align__(16) uint8_t dsm[];
-    // high plane: the codebook's 12-bit table; low plane: a 13-bit table
-    DecTables<12> &Th = *reinterpret_cast<DecTables<12> *>(dsm);
-    DecTables<13> &Tl = *reinterpret_cast<DecTables<13> *>(dsm + sizeof(DecTables<12>));
-    load_table_a(Th, cb_hi);
-    load_table_a(Tl, cb_lo);
-    __syncthreads();
-    load_table_b(Th, cb_hi);
-    load_table_b(Tl, cb_lo);
-    __syncthreads();
-    if (!Th.ok || !Tl.ok) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
-        return;
-    }
+//
+// Three cases, each its own kernel (ZR), so that each keeps its own register
+// allocation: 0, the high plane decoded by table lookups (or both planes
+// stepped together, PAIR); 1, the high plane has a 1-bit code and is decoded
+// as runs; 2, the same with x0 staged in shared memory: each lane copies its
+// chunk's next 64 bytes of x0 (one segment) with four asynchronous 16-byte
+// copies (cp.async, no registers held) right after the merge that used the
+// previous ones, so the merge finds x0 waiting instead of waiting for it (it
+// is read a segment's decode after its copies were issued).  The run-decoded
+// cases carry the high plane's run tables (no window table) and a smaller
+// secondary table for the low plane, which is what leaves room for the
+// staging area.
+constexpr int kStageLane = kSeg * 2;  // bytes of x0 per lane per segment
+
+template <bool XOR, bool PAIR, int ZR, class TH, class TL>
+__device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uint8_t *rings_base, uint8_t *stage_base,
+                                                 const uint8_t *__restrict__ pay_hi,
+                                                 size_t bytes_hi, const uint64_t *__restrict__ off_hi,
+                                                 const uint8_t *__restrict__ pay_lo, size_t bytes_lo,
+                                                 const uint64_t *__restrict__ off_lo, size_t n, size_t chunk,
+                                                 const uint16_t *__restrict__ x0, uint16_t *__restrict__ out,
+                                                 int32_t *status) {
+    constexpr bool zrun = ZR >= 1;
+    constexpr bool stage = ZR == 2 && XOR;
     const int lane = threadIdx.x & 31;
     const size_t n_chunks = (n + chunk - 1) / chunk;
     const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -910,7 +1039,7 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
         else
             set_status(status, HUFF_ERR_CORRUPT_STREAM);
     }
-    uint8_t *rings = dsm + kBf16Tables + static_cast<size_t>(threadIdx.x - lane) * (2 * kRing);
+    uint8_t *rings = rings_base + static_cast<size_t>(threadIdx.x - lane) * (2 * kRing);
     uint8_t *hring = rings + lane * (2 * kRing) + ((lane & 1) ? kRing : 0);
     uint8_t *lring = rings + lane * (2 * kRing) + ((lane & 1) ? 0 : kRing);
     const uint32_t swz = (lane & 2) ? kRing / 2 : 0;
@@ -920,17 +1049,40 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
     bool bad = false;
     const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
     const bool whole = __all_sync(0xffffffffu, cnt == warp_cnt);  // every chunk of the warp has the same length
+    // a high plane with a 1-bit code is decoded as runs into a ring that holds that code's symbol
+    const uint2 run2 = make_uint2(static_cast<uint32_t>(Th.run), static_cast<uint32_t>(Th.run >> 32));
+    if (zrun) {
+#pragma unroll
+        for (int k = 0; k < kRing; k += 8) *reinterpret_cast<uint2 *>(hring + k) = run2;
+    }
+    // x0 staging (warp-uniform): the warp's 2 KiB area, lane q's chunk at 64 q (32-bit shared addresses),
+    // filled by each lane's own asynchronous 16-byte copies; xf: staging in use
+    const uint32_t xst = stage ? smem_u32(stage_base) + (threadIdx.x - lane) * kStageLane : 0u;
+    bool xf = stage && whole && warp_cnt >= kSeg;
+    const auto stage_issue = [&](int seg) {  // x0 of segment [seg, seg + kSeg) of this lane's chunk
+        const uint16_t *src = x0 + c * chunk + seg;
+#pragma unroll
+        for (int k = 0; k < kStageLane / 16; ++k)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(xst + lane * kStageLane + 16 * k),
+                         "l"(src + 8 * k)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (xf) stage_issue(0);
     for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSeg) {
-        if (XOR && seg0 < cnt && (seg0 & 63) == 0) {  // one 128-byte line of x0 per two segments
+        if (XOR && !xf && seg0 < cnt && (seg0 & 63) == 0) {  // one 128-byte line of x0 per two segments
             const uint16_t *xp = x0 + c * chunk + seg0;
             asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xp));
         }
         const int need = min(cnt, seg0 + kSeg);
-        if (PAIR) {
+        if constexpr (PAIR) {
             fill_pair<kRing>(h, l, pay_hi, bytes_hi, pay_lo, bytes_lo, Th, Tl, hring, lring, swz, cnt, need, seg0 + kRing,
                              bad);
         } else {
-            fill_segment<kRing, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
+            if constexpr (zrun)
+                fill_zrun<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
+            else
+                fill_segment<kRing, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
             fill_segment<kRing, false>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
         }
         __syncwarp();
@@ -938,18 +1090,33 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
             // every lane's segment is complete: no per-lane bounds
             const size_t g0 = (c0 + (lane >> 2)) * chunk + seg0 + 8 * (lane & 3);  // pass i: + 8 i chunk
             const size_t gs = 8 * chunk;
-            uint4 xv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                xv[i] = XOR ? __ldcs(reinterpret_cast<const uint4 *>(x0 + g0 + i * gs)) : make_uint4(0, 0, 0, 0);
             const int q0 = lane >> 2;
+            uint4 xv[4];
+            bool staged = false;
+            if (stage && xf) {
+                // this lane's copies have landed (issued a segment's decode ago); then every lane's
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                __syncwarp();
+                staged = true;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (staged)
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(xv[i].x), "=r"(xv[i].y), "=r"(xv[i].z), "=r"(xv[i].w)
+                                 : "r"(xst + (8 * i + q0) * kStageLane + 16 * (lane & 3))
+                                 : "memory");
+                else
+                    xv[i] = XOR ? __ldcs(reinterpret_cast<const uint4 *>(x0 + g0 + i * gs)) : make_uint4(0, 0, 0, 0);
+            }
             const uint32_t o = ((seg0 + 8 * (lane & 3)) & (kRing - 1)) ^ ((q0 & 2) ? kRing / 2 : 0);
-            const uint8_t *hr = rings + q0 * (2 * kRing) + ((q0 & 1) ? kRing : 0) + o;
+            uint8_t *hr = rings + q0 * (2 * kRing) + ((q0 & 1) ? kRing : 0) + o;
             const uint8_t *lr = rings + q0 * (2 * kRing) + ((q0 & 1) ? 0 : kRing) + o;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint2 hv = *reinterpret_cast<const uint2 *>(hr + i * 8 * (2 * kRing));
                 const uint2 lv = *reinterpret_cast<const uint2 *>(lr + i * 8 * (2 * kRing));
+                if (zrun) *reinterpret_cast<uint2 *>(hr + i * 8 * (2 * kRing)) = run2;
                 uint4 v = make_uint4(__byte_perm(lv.x, hv.x, 0x5140), __byte_perm(lv.x, hv.x, 0x7362),
                                      __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
                 v.x ^= xv[i].x;
@@ -957,6 +1124,11 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
                 v.z ^= xv[i].z;
                 v.w ^= xv[i].w;
                 __stcs(reinterpret_cast<uint4 *>(out + g0 + i * gs), v);
+            }
+            if (stage && xf && seg0 + 2 * kSeg <= warp_cnt) {
+                // every lane has read its staged x0 (the values fed the stores above): refill the area
+                __syncwarp();
+                stage_issue(seg0 + kSeg);
             }
         } else {
             // merge: 8 lanes' segments per pass, 8 elements (16 output bytes) per lane; the four passes'
@@ -976,10 +1148,11 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
                 const int e0 = seg0 + 8 * (lane & 3);
                 const int cs = __shfl_sync(0xffffffffu, cnt, q);
                 if (e0 < cs) {
-                    const uint8_t *qr = rings + q * (2 * kRing);
+                    uint8_t *qr = rings + q * (2 * kRing);
                     const uint32_t o = (e0 & (kRing - 1)) ^ ((q & 2) ? kRing / 2 : 0);
                     const uint2 hv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? kRing : 0) + o);
                     const uint2 lv = *reinterpret_cast<const uint2 *>(qr + ((q & 1) ? 0 : kRing) + o);
+                    if (zrun) *reinterpret_cast<uint2 *>(qr + ((q & 1) ? kRing : 0) + o) = run2;
                     uint4 v = make_uint4(__byte_perm(lv.x, hv.x, 0x5140), __byte_perm(lv.x, hv.x, 0x7362),
                                          __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
                     const size_t g = (c0 + q) * chunk + e0;  // first element of this group
@@ -1007,6 +1180,66 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
     }
     if (cnt > 0 && (bad || h.pos() != off_hi[c + 1] || l.pos() != off_lo[c + 1]))
         set_status(status, HUFF_ERR_CORRUPT_STREAM);
+}
+
+// Shared memory of each case for a block of `block` lanes.
+__host__ size_t bf16_smem(int zr, int block) {
+    const size_t b = static_cast<size_t>(block);
+    if (zr == 0) return kBf16Tables + b * (2 * kRing);
+    const size_t s = kBf16RunTables + b * (2 * kRing);
+    return zr == 1 ? s : s + b * kStageLane;
+}
+
+// ZR (with one lane per chunk pair): 1 and 2 decode streams whose high plane
+// has a 1-bit code (as runs; 2 stages x0), 0 those without.  Two kernels are
+// launched, one after the other (0 and 1 or 2); the one whose case does not
+// hold returns at once (the host cannot read the codebook).
+template <bool XOR, bool PAIR, int ZR>
+__global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf16(
+    const uint8_t *__restrict__ pay_hi, size_t bytes_hi, const uint64_t *__restrict__ off_hi,
+    const uint8_t *__restrict__ pay_lo, size_t bytes_lo, const uint64_t *__restrict__ off_lo, size_t n,
+    size_t chunk, const huff_codebook *__restrict__ cb_hi, const huff_codebook *__restrict__ cb_lo,
+    const uint16_t *__restrict__ x0, uint16_t *__restrict__ out, int32_t *status) {
+    if (!PAIR) {
+        const bool has_run = cb_hi->magic == HUFF_CODEBOOK_MAGIC && cb_hi->longest <= HUFF_MAX_LEN &&
+                             cb_hi->bl_count[1] > 0;
+        if (has_run != (ZR >= 1)) return;  // the other kernel's case
+    }
+    extern __shared__ __align__(16) uint8_t dsm[];
+    if constexpr (ZR >= 1) {
+        // high plane: run tables; low plane: a 13-bit table with a smaller secondary table
+        RunTables &Th = *reinterpret_cast<RunTables *>(dsm);
+        LoTablesRun &Tl = *reinterpret_cast<LoTablesRun *>(dsm + sizeof(RunTables));
+        load_run_tables(Th, cb_hi);
+        load_table_a(Tl, cb_lo);
+        __syncthreads();
+        load_table_b(Tl, cb_lo);
+        __syncthreads();
+        if (!Th.ok || !Tl.ok) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+            return;
+        }
+        uint8_t *rings = dsm + kBf16RunTables;
+        uint8_t *stage = rings + static_cast<size_t>(blockDim.x) * (2 * kRing);
+        decode_bf16_body<XOR, PAIR, ZR>(Th, Tl, rings, stage, pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo,
+                                        n, chunk, x0, out, status);
+    } else {
+        // high plane: the codebook's 12-bit table; low plane: a 13-bit table
+        DecTables<12> &Th = *reinterpret_cast<DecTables<12> *>(dsm);
+        LoTables &Tl = *reinterpret_cast<LoTables *>(dsm + sizeof(DecTables<12>));
+        load_table_a(Th, cb_hi);
+        load_table_a(Tl, cb_lo);
+        __syncthreads();
+        load_table_b(Th, cb_hi);
+        load_table_b(Tl, cb_lo);
+        __syncthreads();
+        if (!Th.ok || !Tl.ok) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+            return;
+        }
+        decode_bf16_body<XOR, PAIR, 0>(Th, Tl, dsm + kBf16Tables, nullptr, pay_hi, bytes_hi, off_hi, pay_lo,
+                                       bytes_lo, off_lo, n, chunk, x0, out, status);
+    }
 }
 
 }  // namespace
@@ -1038,26 +1271,40 @@ int launch_decode_bf16(const uint8_t *pay_hi, size_t bytes_hi, const uint64_t *o
                        uint16_t *out, int32_t *status, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    const int block = decode_block(n_chunks, dev_info().sms);
+    const DevInfo d = dev_info();
+    const int block = decode_block(n_chunks, d.sms);
     const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
-    const size_t smem = kBf16Tables + static_cast<size_t>(block) * (2 * kRing);
-    const auto go = [&](auto kern, const uint16_t *x) -> int {
+    const auto go = [&](auto kern, int zr, const uint16_t *x) -> int {
+        const size_t smem = bf16_smem(zr, block);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
             return HUFF_ERR_CUDA;
         kern<<<grid, block, smem, s>>>(pay_hi, bytes_hi, off_hi, pay_lo, bytes_lo, off_lo, n, chunk, cb_hi, cb_lo, x,
                                        out, status);
-        return HUFF_OK;
+        return cudaGetLastError() == cudaSuccess ? HUFF_OK : HUFF_ERR_CUDA;
     };
-    // few lanes per SM: both planes stepped in one loop
+    // few lanes per SM: both planes stepped in one loop; otherwise the kernels of the high plane's two
+    // cases (with and without a 1-bit code), of which one returns at once; with x0, the run case stages
+    // x0 in shared memory when the block's staging area fits
     const bool pair = block <= kPairBlock;
     int st;
-    if (x0 != nullptr)
-        st = pair ? go(k_decode_bf16<true, true>, x0) : go(k_decode_bf16<true, false>, x0);
-    else
-        st = pair ? go(k_decode_bf16<false, true>, nullptr) : go(k_decode_bf16<false, false>, nullptr);
-    if (st != HUFF_OK) return st;
-    return launch_status();
+    if (x0 != nullptr) {
+        if (pair) {
+            st = go(k_decode_bf16<true, true, 0>, 0, x0);
+        } else {
+            const bool fits = bf16_smem(2, block) <= static_cast<size_t>(d.max_smem_optin);
+            st = fits ? go(k_decode_bf16<true, false, 2>, 2, x0) : go(k_decode_bf16<true, false, 1>, 1, x0);
+            if (st == HUFF_OK) st = go(k_decode_bf16<true, false, 0>, 0, x0);
+        }
+    } else {
+        if (pair) {
+            st = go(k_decode_bf16<false, true, 0>, 0, nullptr);
+        } else {
+            st = go(k_decode_bf16<false, false, 1>, 1, nullptr);
+            if (st == HUFF_OK) st = go(k_decode_bf16<false, false, 0>, 0, nullptr);
+        }
+    }
+    return st;
 }
 
 }  // namespace huffk
