@@ -238,8 +238,9 @@ class SnapshotPath:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty(n, dtype=torch.int16, device=dev)
         # kernels launched per step: hist (1 zero of both adjacent histograms + 1), build (1 for both planes),
-        # encode (1 zero of the scan ticket + segment bits and scan + main + fix-up), decode (1)
-        self.launches_per_step = 8
+        # encode (1 zero of the scan ticket + segment bits and scan + main + fix-up), decode (2: the kernels of
+        # the high plane's two cases, of which one returns at once)
+        self.launches_per_step = 9
 
     def compress(self, w=None, x0=None):
         L = self.L
@@ -597,14 +598,18 @@ def bank_stage(args):
 
 
 def materialised_delta_stages(path, args, peak):
-    """Encode and decode of the byte-grouped delta d = x1 ^ x0 held in HBM (codebooks given)."""
+    """Encode and decode with the codebooks given (the fixed-codebook single stage): the snapshot delta
+    straight from (x1, x0) and the byte-grouped delta d = x1 ^ x0 already held in HBM."""
     L = path.L
     n = path.n
     d = torch.empty_like(path.x1)
     L.lmc_delta_xor(path.x1, path.x0, d)
     reps = max(3, min(args.steps, 10))
     out = {}
-    for nm, fn in (("encode_bf16", lambda: L.lmc_encode_bf16(d, None, path.cb_hi.buf, path.cb_lo.buf, path.chunk,
+    for nm, fn in (("encode_bf16_xor_given", lambda: L.lmc_encode_bf16(path.x1, path.x0, path.cb_hi.buf, path.cb_lo.buf,
+                                                                       path.chunk, path.p_hi, path.o_hi, path.p_lo,
+                                                                       path.o_lo, path.ws, path.status)),
+                   ("encode_bf16", lambda: L.lmc_encode_bf16(d, None, path.cb_hi.buf, path.cb_lo.buf, path.chunk,
                                                              path.p_hi, path.o_hi, path.p_lo, path.o_lo, path.ws,
                                                              path.status)),
                    ("decode_bf16", lambda: L.lmc_decode_bf16(path.p_hi, path.o_hi, path.p_lo, path.o_lo, n,
@@ -622,7 +627,7 @@ def materialised_delta_stages(path, args, peak):
         ms = a.elapsed_time(b) / reps
         T_hi, T_lo = path.sizes()
         C = (T_hi + 7) // 8 + (T_lo + 7) // 8 + 2 * 8 * (path.nc + 1)
-        alg = 2 * n + C
+        alg = (4 * n if nm.endswith("xor_given") else 2 * n) + C
         out[nm] = {"ms": round(ms, 4), "gbs_uncompressed": round(2 * n / ms / 1e6, 1), "alg_bytes": alg,
                    "hbm_frac": round(alg / ms / 1e6 / peak, 4)}
     torch.cuda.synchronize()
@@ -630,6 +635,8 @@ def materialised_delta_stages(path, args, peak):
         raise RuntimeError("materialised-delta decode differs")
     if int(path.status.item()) != 0:
         raise RuntimeError("materialised-delta status")
+    out["note"] = ("codebooks given (the step's): encode_bf16_xor_given reads x1 and x0 (counting pass, then the "
+                   "one-pass encode); encode_bf16 / decode_bf16 work on the byte-grouped delta already in HBM")
     del d
     return out
 
@@ -765,22 +772,54 @@ def snapshot_sample(x0, x1, elems):
     return a, b
 
 
+PAGES_16CORE = {"compress_gibs": 2.78, "decompress_gibs": 3.76,
+                "source": "Lossless Compression for LLM Tensor Incremental Snapshots, English abstract / "
+                          "experiment highlights (16-core CPU)"}
+
+
+def _thread_counts():
+    n = os.cpu_count() or 1
+    return sorted({t for t in (1, 16, n) if t <= n})
+
+
 def cpu_baseline_snapshot(x0, x1, args):
+    """The oracle on the host's cores: the sequential oracle on one thread, and its per-chunk steps over
+    16 and all host threads (oracle/huff_oracle_mt.c, payload byte-identical to the sequential oracle's),
+    each on the first elements of the snapshot pair; compress and decompress timed apart, as the pages
+    report them."""
+    import oracle
+    from oracle import mt
+    oracle.build()
     elems = args.cpu_sample
     a, b = snapshot_sample(x0, x1, elems)
-    t = time.perf_counter()
-    oracle_snapshot_step(a, b, args.chunk)
-    dt = time.perf_counter() - t
-    return {"value": round(2 * elems / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {elems} elements of x0/x1 (the snapshot's own distribution); one sequential pass of "
-                      f"delta, split, histograms, codebooks, encode, decode, merge, re-apply; {dt:.1f} s"}
+    rows = {}
+    for t in _thread_counts():
+        if t == 1:  # the sequential oracle as it stands, on a quarter of the sample
+            e1 = max(1, elems // 4)
+            t0 = time.perf_counter()
+            oracle_snapshot_step(a[:e1], b[:e1], args.chunk)
+            dt = time.perf_counter() - t0
+            rows["1"] = {"elements": e1, "round_trip_gbs": round(2 * e1 / dt / 1e9, 4), "seconds": round(dt, 2),
+                         "how": "sequential oracle (delta, planes, histograms, codebooks, encode, decode, merge)"}
+            continue
+        size, tc, td = mt.snapshot_round_trip(a, b, args.chunk, t)
+        rows[str(t)] = {"elements": elems, "compress_gibs": round(2 * elems / tc / 2 ** 30, 3),
+                        "decompress_gibs": round(2 * elems / td / 2 ** 30, 3),
+                        "round_trip_gbs": round(2 * elems / (tc + td) / 1e9, 4), "seconds": round(tc + td, 2)}
+    top = str(max(_thread_counts()))
+    return {"value": rows[top]["round_trip_gbs"], "unit": "GB/s", "cores": int(top), "kind": "oracle",
+            "sample": f"first {elems} elements of x0/x1 (the snapshot's own distribution), compress + decompress "
+                      f"round trip; one thread: the sequential oracle on {rows['1']['elements']} elements",
+            "by_threads": rows, "pages_16core": PAGES_16CORE, "host": host_info()}
 
 
 def run_reference(args, dist, rank, ws):
-    """The oracle, as it stands, on a bounded sample per step (rank 0 only)."""
+    """The oracle on the host's cores (its per-chunk steps over every host thread), on a bounded sample
+    per step; rank 0 only."""
     if rank != 0:
         return
     import oracle
+    from oracle import mt
     oracle.build()
     from lossless_huffman_compression_gb300 import workloads
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -789,13 +828,13 @@ def run_reference(args, dist, rank, ws):
     elems = min(args.ref_sample, x0.numel())
     a, b = snapshot_sample(x0, x1, elems)
     del x0, x1
+    threads = os.cpu_count() or 1
     for _ in range(args.warmup):
-        oracle_snapshot_step(a[: elems // 8], b[: elems // 8], args.chunk)
+        mt.snapshot_round_trip(a[: max(1, elems // 8)], b[: max(1, elems // 8)], args.chunk, threads)
     times = []
     for _ in range(args.steps):
-        t = time.perf_counter()
-        oracle_snapshot_step(a, b, args.chunk)
-        times.append(time.perf_counter() - t)
+        _, tc, td = mt.snapshot_round_trip(a, b, args.chunk, threads)
+        times.append(tc + td)
     ms = 1e3 * sum(times) / len(times)
     value = 2 * elems / (ms / 1e3) / 1e9
     line = {
@@ -804,8 +843,9 @@ def run_reference(args, dist, rank, ws):
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": f"snapshot_delta_bf16_{args.rows}x30518", "chunk_bytes": args.chunk,
                    "sample_elements": elems},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {elems} elements of x0/x1 per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {elems} elements of x0/x1 per step, compress + decompress round trip "
+                                   f"over {threads} host threads"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "host": host_info(),
     }
@@ -934,6 +974,18 @@ def run_workload(args):
     print(json.dumps(out), flush=True)
 
 
+def relaunch_ranks(n: int) -> int:
+    """--gpus N > 1 outside a torchrun job: run this same command as N ranks (one per GPU, rendezvous on
+    127.0.0.1) under torch.distributed.run and return its exit status."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -950,10 +1002,12 @@ def main():
                     default="snapshot", help="snapshot = the default benchmark line; the others print their own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=256 << 20, help="elements for the oracle baseline (about 10 s)")
-    ap.add_argument("--ref-sample", type=int, default=16 << 20, help="elements per reference step")
+    ap.add_argument("--ref-sample", type=int, default=64 << 20, help="elements per reference step")
     args = ap.parse_args()
     if args.small:
         args.rows = 4096
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.workload == "snapshot":
+        sys.exit(relaunch_ranks(args.gpus))
     ws, rank, local = dist_env()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -963,6 +1017,8 @@ def main():
     if args.impl == "reference":
         dist = init_dist(ws, "gloo")
         run_reference(args, dist, rank, ws)
+        if dist is not None:
+            dist.destroy_process_group()
         return
     dist = init_dist(ws, "nccl")
     run_ours(args, dist, rank, ws)

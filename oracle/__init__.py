@@ -50,6 +50,8 @@ def build(force: bool = False) -> str:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
+    from . import mt
+    mt.build(force)
     return _LIB_PATH
 
 

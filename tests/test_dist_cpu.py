@@ -53,3 +53,21 @@ def test_single_rank_needs_no_process_group():
     import bench
     value, ms = bench.whole_job(None, 8.0e9, 20.0, torch.device("cpu"))
     assert ms == 20.0 and value == pytest.approx(4.0e11)
+
+
+def test_gpus_flag_launches_that_many_ranks():
+    """bench.py --gpus 2 (outside torchrun) re-runs itself as two ranks under torch.distributed.run;
+    the reference arm (CPU only: the oracle on host threads) prints one line, from rank 0, with n_gpus 2."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--rows", "2", "--ref-sample", "8192", "--steps", "1", "--warmup", "0", "--chunk", "4096"],
+                       capture_output=True, text=True, timeout=300, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
