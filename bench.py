@@ -942,15 +942,22 @@ def run_workload(args):
         x = workloads.bf16_weights(device="cuda")
         n = x.numel()
         out["input_hist_sha256_16"] = hist_sha(x)
-        s = codec.compress_bf16(x, None, args.chunk)
-        comp = _timed(lambda: codec.compress_bf16(x, None, args.chunk), reps)
-        dec = _timed(lambda: codec.decompress_bf16(s), reps)
-        C = s.hi.nbytes() + s.lo.nbytes()
-        out.update({"elements": n, "chunk_bytes": args.chunk, "compress_gbs": round(2 * n / comp / 1e6, 1),
-                    "decode_gbs": round(2 * n / dec / 1e6, 1),
-                    "decode_hbm_frac": round((C + 4 * n) / (dec / 1e3) / 1e9 / peak, 4),
-                    "ratio": round(2 * n / C, 4),
-                    "bits_per_symbol": [round(s.hi.total_bits() / n, 4), round(s.lo.total_bits() / n, 4)]})
+        res = {}
+        # the bench's chunk size, and the one huff_pick_chunk gives for this size (one wave of 448 to 896
+        # decode lanes per SM)
+        for chunk in dict.fromkeys((args.chunk, _lib.huff_pick_chunk(n))):
+            s = codec.compress_bf16(x, None, chunk)
+            comp = _timed(lambda: codec.compress_bf16(x, None, chunk), reps)
+            dec = _timed(lambda: codec.decompress_bf16(s), reps)
+            C = s.hi.nbytes() + s.lo.nbytes()
+            offs = 2 * 8 * (s.hi.n_chunks() + 1)
+            res[str(chunk)] = {"compress_gbs": round(2 * n / comp / 1e6, 1), "decode_gbs": round(2 * n / dec / 1e6, 1),
+                               "compress_hbm_frac": round((C + offs + 2 * n) / (comp / 1e3) / 1e9 / peak, 4),
+                               "decode_hbm_frac": round((C + offs + 2 * n) / (dec / 1e3) / 1e9 / peak, 4),
+                               "ratio": round(2 * n / C, 4), "container_ratio": round(2 * n / (C + offs + 512), 4),
+                               "bits_per_symbol": [round(s.hi.total_bits() / n, 4), round(s.lo.total_bits() / n, 4)]}
+            del s
+        out.update({"elements": n, "picked_chunk": _lib.huff_pick_chunk(n), "per_chunk_size": res})
     elif args.workload == "sweep":
         seg = workloads.SWEEP_SEGMENT_BYTES
         n = workloads.SWEEP_SEGMENTS * seg

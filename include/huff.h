@@ -124,13 +124,26 @@ size_t huff_codebook_size(void);
  * rounded up to whole 32-bit words, plus 16 bytes of slack. */
 size_t huff_encode_bound(size_t n, int max_len);
 
-/* Workspace bytes huff_encode needs for n symbols (per 8 KiB tile: a lookback
- * descriptor and the tile's two boundary words).  chunk_bytes does not change it today; it is an argument so
- * the format can change without an ABI break. */
+/* Workspace bytes huff_encode needs for n symbols (per segment of 4 to 16
+ * tiles of 1024 symbols: a lookback descriptor and the segment's boundary-word
+ * pair, plus a segment counter).  chunk_bytes does not change it today; it is
+ * an argument so the format can change without an ABI break. */
 size_t huff_workspace_size(size_t n, size_t chunk_bytes);
 
 /* Number of chunks: ceil(n / chunk_bytes); 0 when n == 0. */
 size_t huff_num_chunks(size_t n, size_t chunk_bytes);
+
+/*
+ * huff_pick_chunk -- a chunk size for n symbols (elements, for the fused bf16
+ * calls) on the current device.  The decode runs one lane per chunk, all lanes
+ * resident, up to 896 per SM: this returns the power of two from 256 to 16384
+ * that gives each SM more than 448 and at most 896 chunks, so one wave of
+ * lanes covers the input with as many lanes as fit; 256 when even that gives
+ * at most 448 per SM, 16384 when even that gives more than 896.  (The chunk
+ * size is the caller's choice on the pages' format; each chunk costs 8 bytes
+ * of offset per stream.)  Returns 0 when the device cannot be queried.
+ */
+size_t huff_pick_chunk(size_t n);
 
 /* ---------------------------------------------------------------- histogram */
 

@@ -47,6 +47,7 @@ EXPORTS = (
     "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
     "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if", "huff_build_codebooks",
     "huff_stream_copy", "huff_container_size", "huff_container_write", "huff_container_parse", "huff_debug_wait",
+    "huff_pick_chunk",
 )
 
 
@@ -118,6 +119,7 @@ def load(path: str = LIB_PATH):
         "lmc_histogram_bf16_counted": (I, [P, P, S, P, P, P, S, P]),
         "lmc_encode_bf16_counted": (I, [P, P, S, P, P, S, P, S, P, S, P, P, S, P, P, S, P, P]),
         "huff_debug_wait": (I, [I, P, S, ctypes.c_uint32, ctypes.c_uint32, P, P, P]),
+        "huff_pick_chunk": (S, [S]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -176,6 +178,14 @@ def huff_encode_bound(n: int, max_len: int = HUFF_MAX_LEN) -> int:
 
 def huff_workspace_size(n: int, chunk_bytes: int) -> int:
     return int(load().huff_workspace_size(n, chunk_bytes))
+
+
+def huff_pick_chunk(n: int) -> int:
+    """A chunk size that gives the decode one wave of 448 to 896 lanes per SM (see include/huff.h)."""
+    c = int(load().huff_pick_chunk(n))
+    if c == 0:
+        raise HuffError("huff_pick_chunk", HUFF_ERR_CUDA)
+    return c
 
 
 def lmc_workspace_size(n: int, chunk_bytes: int) -> int:

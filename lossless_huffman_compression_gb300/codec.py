@@ -164,10 +164,13 @@ def codebook_from_lengths(lengths, max_len: int = 24, device=None) -> Codebook:
     return cb
 
 
-def encode(x: torch.Tensor, cb: Codebook, chunk_bytes: int = DEFAULT_CHUNK, max_len: int = 24,
+def encode(x: torch.Tensor, cb: Codebook, chunk_bytes: int | None = DEFAULT_CHUNK, max_len: int = 24,
            status: torch.Tensor | None = None) -> Stream:
+    """Encode x's bytes with a given codebook; chunk_bytes=None picks the size (huff_pick_chunk)."""
     flat = x.reshape(-1)
     n = flat.numel() * flat.element_size()
+    if chunk_bytes is None:
+        chunk_bytes = _lib.huff_pick_chunk(n)
     payload = torch.empty(_lib.huff_encode_bound(n, max_len), dtype=torch.uint8, device=x.device)
     off = torch.empty(_lib.huff_num_chunks(n, chunk_bytes) + 1, dtype=torch.int64, device=x.device)
     ws = torch.empty(max(_lib.huff_workspace_size(n, chunk_bytes), 16) // 8, dtype=torch.int64, device=x.device)
@@ -230,13 +233,16 @@ class Bf16Streams:
     n: int
 
 
-def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: int = DEFAULT_CHUNK,
+def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: int | None = DEFAULT_CHUNK,
                   max_len: int = 24, flags: int = 0, cb_hi: Codebook | None = None,
                   cb_lo: Codebook | None = None) -> Bf16Streams:
-    """LMC snapshot compress: optional XOR delta, byte planes, one codebook per plane."""
+    """LMC snapshot compress: optional XOR delta, byte planes, one codebook per plane.
+    chunk_bytes=None picks the chunk size for the device (huff_pick_chunk)."""
     w16 = w.reshape(-1).view(torch.int16)
     x16 = None if x0 is None else x0.reshape(-1).view(torch.int16)
     n = w16.numel()
+    if chunk_bytes is None:
+        chunk_bytes = _lib.huff_pick_chunk(n)
     dev = w.device
     cap = _lib.huff_encode_bound(n, max_len)
     p_hi = torch.empty(cap, dtype=torch.uint8, device=dev)

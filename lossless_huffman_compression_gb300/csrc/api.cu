@@ -51,6 +51,17 @@ size_t huff_num_chunks(size_t n, size_t chunk_bytes) {
     return (n + chunk_bytes - 1) / chunk_bytes;
 }
 
+size_t huff_pick_chunk(size_t n) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess || sms <= 0)
+        return 0;
+    const size_t lanes = static_cast<size_t>(sms) * 896;  // one wave of the decode's lanes
+    size_t c = 16384;                                     // halving c doubles the chunks: stop at the first
+    while (c > 256 && (n + c - 1) / c <= lanes / 2) c >>= 1;  // size with more than 448 per SM
+    return c;
+}
+
 size_t huff_encode_bound(size_t n, int max_len) {
     if (max_len < 1 || max_len > HUFF_MAX_LEN) max_len = HUFF_MAX_LEN;
     const size_t words = (n * static_cast<size_t>(max_len) + 31) / 32;

@@ -661,6 +661,12 @@ __host__ int decode_block(size_t n_chunks, int sms) {
 // Lane ring: 2 * kRing bytes (one plane, twice the slack); swizzled by lane
 // parity so that the copy-out's reads of 8 lanes' segments spread over the banks.
 constexpr int kRingU8 = 2 * kRing;
+// Byte streams often meet data their (fixed) codebook was not built for, where
+// most symbols have codes of 17 to 24 bits: a secondary table of 16 Ki entries
+// (32 KiB; the block's rings leave room for it) holds all of them when their
+// 13-bit prefixes are few, so such a code costs one lookup.
+constexpr int kSecU8 = 16384;
+using U8Tables = DecTables<13, kSecU8>;
 constexpr int kSegU8 = 2 * kSeg;
 static_assert(kRingU8 >= kSegU8 + 7 + 2 * kStepMax && (kRingU8 & (kRingU8 - 1)) == 0 && kSegU8 % 16 == 0,
               "byte-stream ring geometry");
@@ -670,7 +676,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
                                                            const huff_codebook *__restrict__ cb,
                                                            uint8_t *__restrict__ out, int32_t *status) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    DecTables<13> &T = *reinterpret_cast<DecTables<13> *>(dsm);
+    U8Tables &T = *reinterpret_cast<U8Tables *>(dsm);
     load_table_a(T, cb);
     __syncthreads();
     load_table_b(T, cb);
@@ -693,7 +699,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
         else
             set_status(status, HUFF_ERR_CORRUPT_STREAM);
     }
-    uint8_t *rings = dsm + sizeof(DecTables<13>) + static_cast<size_t>(threadIdx.x - lane) * kRingU8;
+    uint8_t *rings = dsm + sizeof(U8Tables) + static_cast<size_t>(threadIdx.x - lane) * kRingU8;
     uint8_t *ring = rings + lane * kRingU8;
     const uint32_t swz = (lane & 1) ? kRingU8 / 2 : 0;
     PlaneDec s;
@@ -1257,7 +1263,7 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
     }
     const int block = decode_block(n_chunks, dev_info().sms);
     const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
-    const size_t smem = sizeof(DecTables<13>) + static_cast<size_t>(block) * kRingU8;
+    const size_t smem = sizeof(U8Tables) + static_cast<size_t>(block) * kRingU8;
     if (cudaFuncSetAttribute(k_decode_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return HUFF_ERR_CUDA;

@@ -131,3 +131,20 @@ def test_corrupt_stream_is_reported_by_the_run_kernels():
                          x0.view(torch.int16), out, st)
     torch.cuda.synchronize()
     assert int(st.item()) == _lib.HUFF_ERR_CORRUPT_STREAM
+
+
+@pytest.mark.parametrize("n", [1, 1 << 20, 1 << 26, 536_870_912, 2_000_027_648, 1 << 36])
+def test_pick_chunk_gives_one_wave_of_lanes(n):
+    """huff_pick_chunk: a power of two in [256, 16384] with more than 448 and at most 896 chunks per SM,
+    unless an end of that range is reached."""
+    c = _lib.huff_pick_chunk(n)
+    assert c & (c - 1) == 0 and 256 <= c <= 16384
+    per_sm = -(-n // c) / _sms()
+    if c == 256:
+        assert per_sm <= 896 or n <= 0
+    elif c == 16384:
+        assert per_sm > 448
+    else:
+        assert 448 < per_sm <= 896 + 1
+    if n == 2_000_027_648:
+        assert c == 16384  # the snapshot: about 803 chunk pairs per SM on 152 SMs
