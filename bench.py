@@ -960,15 +960,17 @@ def run_workload(args):
         out.update({"elements": n, "picked_chunk": _lib.huff_pick_chunk(n), "per_chunk_size": res})
     elif args.workload == "sweep":
         seg = workloads.SWEEP_SEGMENT_BYTES
-        n = workloads.SWEEP_SEGMENTS * seg
+        nseg = args.segments or workloads.SWEEP_SEGMENTS
+        n = nseg * seg
         x = torch.empty(n, dtype=torch.uint8, device="cuda")
-        for k in range(workloads.SWEEP_SEGMENTS):
+        for k in range(nseg):
             x[k * seg:(k + 1) * seg] = workloads.sweep_segment(k, device="cuda").view(torch.uint8)
         cb = codec.build_codebook(codec.histogram(x[: 64 << 20]), 24, _lib.HUFF_COVER_ALL)
         out["input_hist_sha256_16"] = hist_sha(x)
         res = {}
         dst = torch.empty_like(x)
-        for chunk in (16 << 10, 64 << 10, 256 << 10, 1 << 20):
+        chunks = [int(c) for c in args.chunks.split(",")] if args.chunks else [16 << 10, 64 << 10, 256 << 10, 1 << 20]
+        for chunk in chunks:
             st = codec.encode(x, cb, chunk)
             enc = _timed(lambda: codec.encode(x, cb, chunk), 2)
             dec = _timed(lambda: codec.decode(st, cb, out=dst), 2)
@@ -977,7 +979,7 @@ def run_workload(args):
                                "decode_hbm_frac": round((C + n) / (dec / 1e3) / 1e9 / peak, 4),
                                "ratio": round(n / C, 4)}
             del st
-        out.update({"elements": n, "per_chunk_size": res})
+        out.update({"elements": n, "segments": nseg, "per_chunk_size": res})
     print(json.dumps(out), flush=True)
 
 
@@ -1008,6 +1010,9 @@ def main():
     ap.add_argument("--workload", choices=["snapshot", "per_shard", "fixed_codebook", "bf16_weights", "sweep"],
                     default="snapshot", help="snapshot = the default benchmark line; the others print their own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="sweep: 256 MiB segments (0 = all 64, the 16 GiB workload; fewer for profiling runs)")
+    ap.add_argument("--chunks", default="", help="sweep: comma-separated chunk sizes (default 16K,64K,256K,1M)")
     ap.add_argument("--cpu-sample", type=int, default=256 << 20, help="elements for the oracle baseline (about 10 s)")
     ap.add_argument("--ref-sample", type=int, default=64 << 20, help="elements per reference step")
     args = ap.parse_args()
