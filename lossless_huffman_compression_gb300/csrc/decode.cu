@@ -23,11 +23,13 @@
 //     from a queue of the current 16-byte unit of the stream; units are read
 //     whole, the payload's last unit standing in for any unit past it;
 //   * a step is one predicated basic block: a table lookup plus a second,
-//     dependent one when both fit 8 symbols, or, on a plane with a 1-bit
-//     code, a run of that code as long as the zero bits on top of the window
-//     (up to 32); on a plane without one, while every lane of the warp has
-//     room for two full steps in its chunk and its ring, two steps run
-//     without the per-step checks;
+//     dependent one when both fit 8 symbols, then (bf16 planes) a third on
+//     the bits after them when its codes lie within the buffer's valid bits
+//     (its symbols emitted as a second round of the pending-word logic; up
+//     to 14 symbols a step), or, on a plane with a 1-bit code, a run of that code as long
+//     as the zero bits on top of the window (up to 32); on a plane without
+//     one, while every lane of the warp has room for a full step in its
+//     chunk and its ring, steps run without the per-step checks;
 //   * the fused bf16 decode of a high plane with a 1-bit code (a snapshot
 //     delta's, about 98 % one symbol) takes at most one other code per step
 //     and then the whole run of the 1-bit code after it, into a ring that
@@ -278,6 +280,8 @@ constexpr int kSeg = 32;       // symbols per lane per segment (multiple of 16)
 constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
 constexpr int kStepMax = 8;    // symbols a table step may add (a run step: up to 32, within the ring's room)
 constexpr int kFastSteps = 2;  // steps per unchecked block on a plane without runs
+constexpr int kStepMax3 = 14;  // symbols a three-lookup step may add (8 from the first two, 6 from the third)
+static_assert(kRing >= kSeg + 7 + kStepMax3, "a three-lookup step fits the ring's slack");
 constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
 constexpr int kPairBlock = 448;  // at most this many lanes per SM: the fused bf16 decode steps both planes in one loop
 static_assert(kRing >= kSeg + 7 + 2 * kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
@@ -380,9 +384,10 @@ __device__ __forceinline__ void step_rare(const DecTables<W, SEC> &T, uint32_t w
 // the zero bits on top of the window (up to 32, the chunk's rest and the
 // ring's room) when that beats a lookup; then up to four 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
-template <int RING, bool RUN, int W, bool LIM, bool FAST = false, int SEC = kSecMax>
+template <int RING, bool RUN, int W, bool LIM, bool FAST = false, bool THIRD = false, int SEC = kSecMax>
 __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
+    static_assert(!(RUN && THIRD), "a third lookup is for planes without runs");
     static_assert(!(RUN && FAST), "a run step may add more symbols than a fast block reserves");
     // Predicated rather than branched: a lane with nothing to do (its chunk
     // is complete or its ring is full) takes a step of zero bits and zero
@@ -390,7 +395,7 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     // FAST: the caller has checked that the chunk and the ring have room for this step
     const int rem = FAST ? (1 << 20) : cnt - s.st - s.fill;
     const int room = FAST ? (1 << 20) : limit - s.st - s.fill;
-    const bool go = FAST || (rem > 0 && room >= kStepMax);
+    const bool go = FAST || (rem > 0 && room >= (THIRD ? kStepMax3 : kStepMax));
     s.refill(p, nbytes);
     const uint32_t win = s.bh >> (32 - W);
     const uint64_t e = T.lut[win];
@@ -444,6 +449,28 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     s.a0 = full ? (v >> 1) >> (63 - keep) : a;
     s.st += nf & ~7;
     s.fill = nf & 7;
+    if (THIRD) {
+        // a third lookup on the bits after the first two entries, taken when the step went the simple
+        // way and its codes lie within the valid bits and the chunk; its symbols are emitted as a
+        // second round of the same pending-word logic (at most 6 more, so at most one word is stored)
+        const uint64_t e3 = T.lut[s.bh >> (32 - W)];
+        const uint32_t eh3 = static_cast<uint32_t>(e3 >> 32);
+        const uint32_t c3 = (eh3 >> 16) & 15u;
+        const uint32_t b3 = eh3 >> 20;
+        const bool take3 = go && simple && c3 != 0 && static_cast<int>(b3) <= s.nb &&
+                           static_cast<int>(c + c3) <= rem;
+        const uint64_t v3 = take3 ? (e3 & 0xffffffffffffull) : 0ull;
+        const uint32_t n3 = take3 ? c3 : 0u;
+        s.consume(take3 ? b3 : 0u);
+        const int f3 = s.fill;
+        const uint64_t a3 = s.a0 | (v3 << (8 * f3));
+        const int nf3 = f3 + static_cast<int>(n3);
+        const bool full3 = nf3 >= 8;
+        if (full3) *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = a3;
+        s.a0 = full3 ? (v3 >> 1) >> (63 - 8 * f3) : a3;
+        s.st += nf3 & ~7;
+        s.fill = nf3 & 7;
+    }
 }
 
 __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, size_t nbytes, uint64_t start, int cnt) {
@@ -463,24 +490,25 @@ __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, siz
 
 // Decode until every lane of the warp has stored symbols [.., need) into its
 // RING-byte ring (a lane whose chunk is complete stores its last partial word).
-template <int RING, bool RUN, int W, bool LIM, int SEC>
+template <int RING, bool RUN, int W, bool LIM, int SEC, bool THIRD = false>
 __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
                                                uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
                                                bool &bad) {
     const uint64_t run = RUN ? T.run : 0ull;
     if (!RUN) {
-        // while every lane's chunk and ring have room for kFastSteps full steps (a table step adds at
-        // most kStepMax symbols), take them without the per-step checks
-        while (__all_sync(0xffffffffu, limit - s.st - s.fill >= kFastSteps * kStepMax &&
-                                           cnt - s.st - s.fill >= kFastSteps * kStepMax) &&
+        // while every lane's chunk and ring have room for the unchecked steps (a table step adds at
+        // most kStepMax symbols, a three-lookup step kStepMax3), take them without the per-step checks
+        constexpr int kFast = THIRD ? 1 : kFastSteps;
+        constexpr int kNeed = THIRD ? kStepMax3 : kFastSteps * kStepMax;
+        while (__all_sync(0xffffffffu, limit - s.st - s.fill >= kNeed && cnt - s.st - s.fill >= kNeed) &&
                __any_sync(0xffffffffu, s.st < need)) {
 #pragma unroll
-            for (int k = 0; k < kFastSteps; ++k)
-                step<RING, false, W, LIM, true>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+            for (int k = 0; k < kFast; ++k)
+                step<RING, false, W, LIM, true, THIRD>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
         }
     }
     while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
-        step<RING, RUN, W, LIM>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+        step<RING, RUN, W, LIM, false, THIRD && !RUN>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
     if (s.fill > 0 && s.st + s.fill == cnt) {
         *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
         s.st = cnt;
@@ -534,13 +562,13 @@ __device__ __forceinline__ void fill_pair(PlaneDec &h, PlaneDec &l, const uint8_
     }
 }
 
-template <int RING, bool LIM, int W, int SEC>
+template <int RING, bool LIM, bool THIRD = false, int W, int SEC>
 __device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
                                              uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
     if (T.has_run)
-        fill_segment_t<RING, true, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, true, W, LIM, SEC>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
     else
-        fill_segment_t<RING, false, W, LIM>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, false, W, LIM, SEC, THIRD>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
 // ------------------------------------------------------------------ planes with a 1-bit code
@@ -708,6 +736,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     const int warp_cnt = __reduce_max_sync(0xffffffffu, cnt);
     const bool whole = __all_sync(0xffffffffu, cnt == warp_cnt);  // every chunk of the warp has the same length
     for (int seg0 = 0; seg0 < warp_cnt; seg0 += kSegU8) {
+        // (no third lookup here: on the sweep's drifted data, where long codes dominate, it measured slower)
         fill_segment<kRingU8, true>(s, payload, nbytes, T, ring, swz, cnt, min(cnt, seg0 + kSegU8), seg0 + kRingU8, bad);
         __syncwarp();
         // copy-out: 8 lanes' segments per pass, 16 bytes per lane
@@ -1088,8 +1117,8 @@ __device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uin
             if constexpr (zrun)
                 fill_zrun<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
             else
-                fill_segment<kRing, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
-            fill_segment<kRing, false>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
+                fill_segment<kRing, false, true>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
+            fill_segment<kRing, false, true>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
         }
         __syncwarp();
         if (whole && seg0 + kSeg <= warp_cnt) {
