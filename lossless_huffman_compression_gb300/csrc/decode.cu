@@ -281,7 +281,7 @@ constexpr int kRing = 64;      // ring bytes per lane per plane (power of two)
 constexpr int kStepMax = 8;    // symbols a table step may add (a run step: up to 32, within the ring's room)
 constexpr int kFastSteps = 2;  // steps per unchecked block on a plane without runs
 constexpr int kStepMax3 = 14;  // symbols a three-lookup step may add (8 from the first two, 6 from the third)
-static_assert(kRing >= kSeg + 7 + kStepMax3, "a three-lookup step fits the ring's slack");
+static_assert(kRing >= kSeg + kFastSteps * kStepMax3, "a lane at its segment's start has room for a fast block");
 constexpr int kMaxBlock = 896;   // 72 registers per thread; 152 SMs x 896 lanes cover 16 KiB chunks of 2e9 elements in one wave
 constexpr int kPairBlock = 448;  // at most this many lanes per SM: the fused bf16 decode steps both planes in one loop
 static_assert(kRing >= kSeg + 7 + 2 * kStepMax && (kRing & (kRing - 1)) == 0 && kSeg % 16 == 0, "ring geometry");
@@ -496,10 +496,10 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
                                                bool &bad) {
     const uint64_t run = RUN ? T.run : 0ull;
     if (!RUN) {
-        // while every lane's chunk and ring have room for the unchecked steps (a table step adds at
-        // most kStepMax symbols, a three-lookup step kStepMax3), take them without the per-step checks
-        constexpr int kFast = THIRD ? 1 : kFastSteps;
-        constexpr int kNeed = THIRD ? kStepMax3 : kFastSteps * kStepMax;
+        // while every lane's chunk and ring have room for kFastSteps unchecked steps (a table step adds
+        // at most kStepMax symbols, a three-lookup step kStepMax3), take them without the per-step checks
+        constexpr int kFast = kFastSteps;
+        constexpr int kNeed = THIRD ? kFastSteps * kStepMax3 : kFastSteps * kStepMax;
         while (__all_sync(0xffffffffu, limit - s.st - s.fill >= kNeed && cnt - s.st - s.fill >= kNeed) &&
                __any_sync(0xffffffffu, s.st < need)) {
 #pragma unroll
