@@ -382,7 +382,8 @@ def run_ours(args, dist, rank, ws):
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": f"snapshot_delta_bf16_{args.rows}x{workloads.SNAPSHOT_SHAPE[1]}",
-                   "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk, "max_len": 24,
+                   "elements": n, "uncompressed_bytes": snap_bytes, "chunk_bytes": args.chunk,
+                   "picked_chunk": _lib.huff_pick_chunk(n, delta=True), "max_len": 24,
                    "step": "xor+split+hist with segment counts, both codebooks in one launch, one-pass fused encode, "
                            "fused decode+merge+xor",
                    "l2": "inputs (8 GB) larger than L2; no flush", "parallelism": f"replicas{ws}"},
@@ -943,8 +944,8 @@ def run_workload(args):
         n = x.numel()
         out["input_hist_sha256_16"] = hist_sha(x)
         res = {}
-        # the bench's chunk size, and the one huff_pick_chunk gives for this size (one wave of 448 to 896
-        # decode lanes per SM)
+        # the bench's chunk size, and the one huff_pick_chunk gives for this size without a delta (one
+        # wave of full decode blocks on every SM)
         for chunk in dict.fromkeys((args.chunk, _lib.huff_pick_chunk(n))):
             s = codec.compress_bf16(x, None, chunk)
             comp = _timed(lambda: codec.compress_bf16(x, None, chunk), reps)
@@ -995,13 +996,19 @@ def relaunch_ranks(n: int) -> int:
     return subprocess.call(cmd)
 
 
+# The snapshot's chunk: 2.0e9 elements in 126 010 chunk pairs, one 832-lane decode block (the widest whose
+# x0 staging fits in shared memory) on each of the 152 SMs; huff_pick_chunk's choice for this size with a delta.
+SNAPSHOT_CHUNK = 15872
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--chunk", type=int, default=16384)
+    ap.add_argument("--chunk", type=int, default=None,
+                    help=f"symbols per chunk (default {SNAPSHOT_CHUNK} for the snapshot, 16384 for the other workloads)")
     ap.add_argument("--rows", type=int, default=65536,
                     help="snapshot rows of 30518 bf16 (65536 = the 4.0 GB workload; fewer for quick checks)")
     ap.add_argument("--small", action="store_true", help="same as --rows 4096 (a 250 MB snapshot)")
@@ -1018,6 +1025,8 @@ def main():
     args = ap.parse_args()
     if args.small:
         args.rows = 4096
+    if args.chunk is None:
+        args.chunk = SNAPSHOT_CHUNK if args.workload == "snapshot" else 16384
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.workload == "snapshot":
         sys.exit(relaunch_ranks(args.gpus))
     ws, rank, local = dist_env()

@@ -119,7 +119,7 @@ def load(path: str = LIB_PATH):
         "lmc_histogram_bf16_counted": (I, [P, P, S, P, P, P, S, P]),
         "lmc_encode_bf16_counted": (I, [P, P, S, P, P, S, P, S, P, S, P, P, S, P, P, S, P, P]),
         "huff_debug_wait": (I, [I, P, S, ctypes.c_uint32, ctypes.c_uint32, P, P, P]),
-        "huff_pick_chunk": (S, [S]),
+        "huff_pick_chunk": (S, [S, I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -180,9 +180,10 @@ def huff_workspace_size(n: int, chunk_bytes: int) -> int:
     return int(load().huff_workspace_size(n, chunk_bytes))
 
 
-def huff_pick_chunk(n: int) -> int:
-    """A chunk size that gives the decode one wave of 448 to 896 lanes per SM (see include/huff.h)."""
-    c = int(load().huff_pick_chunk(n))
+def huff_pick_chunk(n: int, delta: bool = False) -> int:
+    """The smallest chunk size that gives the decode one wave of full blocks on every SM; delta: the
+    stream is decoded with an XOR delta (see include/huff.h)."""
+    c = int(load().huff_pick_chunk(n, 1 if delta else 0))
     if c == 0:
         raise HuffError("huff_pick_chunk", HUFF_ERR_CUDA)
     return c

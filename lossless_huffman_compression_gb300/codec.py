@@ -237,12 +237,12 @@ def compress_bf16(w: torch.Tensor, x0: torch.Tensor | None = None, chunk_bytes: 
                   max_len: int = 24, flags: int = 0, cb_hi: Codebook | None = None,
                   cb_lo: Codebook | None = None) -> Bf16Streams:
     """LMC snapshot compress: optional XOR delta, byte planes, one codebook per plane.
-    chunk_bytes=None picks the chunk size for the device (huff_pick_chunk)."""
+    chunk_bytes=None picks the chunk size for the device and for whether a delta is decoded (huff_pick_chunk)."""
     w16 = w.reshape(-1).view(torch.int16)
     x16 = None if x0 is None else x0.reshape(-1).view(torch.int16)
     n = w16.numel()
     if chunk_bytes is None:
-        chunk_bytes = _lib.huff_pick_chunk(n)
+        chunk_bytes = _lib.huff_pick_chunk(n, delta=x0 is not None)
     dev = w.device
     cap = _lib.huff_encode_bound(n, max_len)
     p_hi = torch.empty(cap, dtype=torch.uint8, device=dev)

@@ -51,15 +51,19 @@ size_t huff_num_chunks(size_t n, size_t chunk_bytes) {
     return (n + chunk_bytes - 1) / chunk_bytes;
 }
 
-size_t huff_pick_chunk(size_t n) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                   cudaSuccess || sms <= 0)
+size_t huff_pick_chunk(size_t n, int delta) {
+    int dev = 0, sms = 0, smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0 ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return 0;
-    const size_t lanes = static_cast<size_t>(sms) * 896;  // one wave of the decode's lanes
-    size_t c = 16384;                                     // halving c doubles the chunks: stop at the first
-    while (c > 256 && (n + c - 1) / c <= lanes / 2) c >>= 1;  // size with more than 448 per SM
-    return c;
+    // one full block of the decode's widest width on every SM: the smallest chunk size (in steps of
+    // HUFF_CHUNK_ALIGN) that gives at most that many chunks
+    const size_t lanes = static_cast<size_t>(sms) * static_cast<size_t>(decode_lanes(smem, delta != 0));
+    size_t c = (n + lanes - 1) / lanes;
+    c = (c + HUFF_CHUNK_ALIGN - 1) / HUFF_CHUNK_ALIGN * HUFF_CHUNK_ALIGN;
+    if (c < HUFF_CHUNK_ALIGN) c = HUFF_CHUNK_ALIGN;
+    return c > HUFF_MAX_CHUNK ? HUFF_MAX_CHUNK : c;
 }
 
 size_t huff_encode_bound(size_t n, int max_len) {

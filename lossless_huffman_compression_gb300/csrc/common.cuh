@@ -170,6 +170,8 @@ struct DevInfo {
     int max_smem_optin;
 };
 DevInfo dev_info();
+// Widest decode block that fits in max_smem bytes, with or without an XOR delta (decode.cu).
+int decode_lanes(int max_smem, bool delta);
 
 int launch_zero_u64(uint64_t *p, size_t count, cudaStream_t s);
 int launch_histogram(const uint8_t *in, size_t n, size_t stride, uint64_t *hist, cudaStream_t s);

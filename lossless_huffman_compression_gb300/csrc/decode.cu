@@ -45,6 +45,7 @@
 //     bounds.
 // Every chunk must end exactly at the next chunk's offset, otherwise
 // HUFF_ERR_CORRUPT_STREAM is reported.
+#include <algorithm>
 #include "common.cuh"
 
 namespace huffk {
@@ -294,8 +295,9 @@ struct PlaneDec {
     uint4 cur;        // the current unit's words not taken yet, from cur.x on (raw little-endian)
     size_t ui;        // index of the unit after cur
     uint64_t a0;      // pending decoded bytes: byte k of the stream order is byte k of a0
-    int fill;         // pending symbols, < 8 between steps
-    int st;           // symbols stored to the ring (a multiple of 8 until the chunk is complete)
+    int fill;         // pending symbols, < 8 between steps (< 4 on a plane stepped with three lookups)
+    int st;           // symbols stored to the ring (a multiple of 8, or of 4 with three lookups, until
+                      // the chunk is complete)
 
     __device__ __forceinline__ void refill(const uint8_t *p, size_t nbytes) {
         const bool rf = nb <= 32;
@@ -379,6 +381,24 @@ __device__ __forceinline__ void step_rare(const DecTables<W, SEC> &T, uint32_t w
     }
 }
 
+// Append c symbols (v's low c bytes, the rest zero) to the pending bytes of a
+// plane whose pending part is at most 3 bytes (the low word of a0), storing
+// every completed 4-byte word: only 32-bit shifts.
+template <int RING>
+__device__ __forceinline__ void put4(PlaneDec &s, uint8_t *ring, uint32_t swz, uint64_t v, uint32_t c) {
+    const uint32_t sh = 8u * static_cast<uint32_t>(s.fill);  // fill <= 3
+    const uint32_t vl = static_cast<uint32_t>(v), vh = static_cast<uint32_t>(v >> 32);
+    const uint32_t w0 = static_cast<uint32_t>(s.a0) | (vl << sh);
+    const uint32_t w1 = __funnelshift_l(vl, vh, sh);
+    const uint32_t w2 = __funnelshift_l(vh, 0u, sh);
+    const int nf = s.fill + static_cast<int>(c);
+    if (nf >= 4) *reinterpret_cast<uint32_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = w0;
+    if (nf >= 8) *reinterpret_cast<uint32_t *>(ring + (((s.st + 4) & (RING - 1)) ^ swz)) = w1;
+    s.a0 = nf >= 8 ? w2 : (nf >= 4 ? w1 : w0);
+    s.st += nf & ~3;
+    s.fill = nf & 3;
+}
+
 // One step: if the chunk has symbols left and the ring has room, one table
 // lookup, or, for a plane with a 1-bit code, a run of that code as long as
 // the zero bits on top of the window (up to 32, the chunk's rest and the
@@ -434,6 +454,21 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     bits = go ? bits : 0u;
     v = go ? v : 0ull;
     s.consume(bits);
+    if constexpr (THIRD) {
+        // pending bytes kept below a word, so both rounds' appends use 32-bit shifts only; then a third
+        // lookup on the bits after the first two entries, taken when the step went the simple way and
+        // its codes lie within the valid bits and the chunk, appended as a second round
+        put4<RING>(s, ring, swz, v, c);
+        const uint64_t e3 = T.lut[s.bh >> (32 - W)];
+        const uint32_t eh3 = static_cast<uint32_t>(e3 >> 32);
+        const uint32_t c3 = (eh3 >> 16) & 15u;
+        const uint32_t b3 = eh3 >> 20;
+        const bool take3 = go && simple && c3 != 0 && static_cast<int>(b3) <= s.nb &&
+                           static_cast<int>(c + c3) <= rem;
+        s.consume(take3 ? b3 : 0u);
+        put4<RING>(s, ring, swz, take3 ? (e3 & 0xffffffffffffull) : 0ull, take3 ? c3 : 0u);
+        return;
+    }
     const int f = s.fill;
     const uint64_t a = s.a0 | (v << (8 * f));
     const int nf = f + static_cast<int>(c);
@@ -449,28 +484,6 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     s.a0 = full ? (v >> 1) >> (63 - keep) : a;
     s.st += nf & ~7;
     s.fill = nf & 7;
-    if (THIRD) {
-        // a third lookup on the bits after the first two entries, taken when the step went the simple
-        // way and its codes lie within the valid bits and the chunk; its symbols are emitted as a
-        // second round of the same pending-word logic (at most 6 more, so at most one word is stored)
-        const uint64_t e3 = T.lut[s.bh >> (32 - W)];
-        const uint32_t eh3 = static_cast<uint32_t>(e3 >> 32);
-        const uint32_t c3 = (eh3 >> 16) & 15u;
-        const uint32_t b3 = eh3 >> 20;
-        const bool take3 = go && simple && c3 != 0 && static_cast<int>(b3) <= s.nb &&
-                           static_cast<int>(c + c3) <= rem;
-        const uint64_t v3 = take3 ? (e3 & 0xffffffffffffull) : 0ull;
-        const uint32_t n3 = take3 ? c3 : 0u;
-        s.consume(take3 ? b3 : 0u);
-        const int f3 = s.fill;
-        const uint64_t a3 = s.a0 | (v3 << (8 * f3));
-        const int nf3 = f3 + static_cast<int>(n3);
-        const bool full3 = nf3 >= 8;
-        if (full3) *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = a3;
-        s.a0 = full3 ? (v3 >> 1) >> (63 - 8 * f3) : a3;
-        s.st += nf3 & ~7;
-        s.fill = nf3 & 7;
-    }
 }
 
 __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, size_t nbytes, uint64_t start, int cnt) {
@@ -510,7 +523,10 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
     while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
         step<RING, RUN, W, LIM, false, THIRD && !RUN>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
     if (s.fill > 0 && s.st + s.fill == cnt) {
-        *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
+        if (THIRD && !RUN)  // pending part below a word, st a multiple of 4
+            *reinterpret_cast<uint32_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = static_cast<uint32_t>(s.a0);
+        else
+            *reinterpret_cast<uint64_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = s.a0;
         s.st = cnt;
         s.fill = 0;
         s.a0 = 0;
@@ -1278,6 +1294,20 @@ __global__ void __launch_bounds__(PAIR ? kPairBlock : kMaxBlock, 1) k_decode_bf1
 }
 
 }  // namespace
+
+// The most lanes per block (whole warps, at most kMaxBlock) whose decode fits
+// in max_smem bytes of shared memory: with an XOR delta, the fused bf16
+// decode's case with x0 staged; without, every other case.
+int decode_lanes(int max_smem, bool delta) {
+    const auto need = [delta](int b) {
+        if (delta) return bf16_smem(2, b);
+        const size_t u8 = sizeof(U8Tables) + static_cast<size_t>(b) * kRingU8;
+        return std::max(std::max(bf16_smem(0, b), bf16_smem(1, b)), u8);
+    };
+    int b = kMaxBlock;
+    while (b > 32 && need(b) > static_cast<size_t>(max_smem)) b -= 32;
+    return b;
+}
 
 int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, size_t n, size_t chunk,
                      const huff_codebook *cb, uint8_t *out, int32_t *status, cudaStream_t s) {

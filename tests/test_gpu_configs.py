@@ -1,5 +1,6 @@
 """The five workloads at their full sizes, through the C ABI, in the launch
-configuration the benchmark uses (16 KiB chunks, max length 24).
+configuration the benchmark uses (16 KiB chunks, 15 872-element chunks for the
+snapshot delta; max length 24).
 
 At these sizes the oracle cannot encode whole tensors in seconds, so the
 checks are:
@@ -26,6 +27,7 @@ from gpu_util import assert_offsets_match_lengths, assert_stream_equal, check_sa
 pytestmark = pytest.mark.gpu
 
 CHUNK = 16384
+SNAPSHOT_CHUNK = 15872  # the benchmark's snapshot chunk: one 832-lane decode block on each of 152 SMs
 BLOCK = 1 << 27
 
 
@@ -132,11 +134,11 @@ def test_fixed_codebook_shards():
 
 
 # ------------------------------------------------------------------ bf16 tensors: weights (1 GiB) and snapshot delta (4 GB)
-def _bf16_config(w: torch.Tensor, x0):
+def _bf16_config(w: torch.Tensor, x0, chunk: int = CHUNK):
     w16 = w.reshape(-1).view(torch.int16)
     d16 = w16 if x0 is None else (w16 ^ x0.reshape(-1).view(torch.int16))
     hh, hl = _bincount_planes(d16)
-    s = codec.compress_bf16(w, x0, CHUNK)
+    s = codec.compress_bf16(w, x0, chunk)
     for hist, cb, st, shift in ((hh, s.cb_hi, s.hi, 8), (hl, s.cb_lo, s.lo, 0)):
         ln = oracle.code_lengths(hist)
         cd = oracle.canonical_codes(ln)
@@ -145,12 +147,12 @@ def _bf16_config(w: torch.Tensor, x0):
         chunks = _sample_chunks(st.n_chunks(), shift + 17)
         plane = {}
         for c in chunks:
-            seg = d16[c * CHUNK: min(s.n, (c + 1) * CHUNK)].to(torch.int32) & 0xFFFF
+            seg = d16[c * chunk: min(s.n, (c + 1) * chunk)].to(torch.int32) & 0xFFFF
             plane[c] = host(((seg >> shift) & 0xFF).to(torch.uint8))
-        _check_stream_samples(st.payload, st.off, plane, ln, cd, CHUNK)
+        _check_stream_samples(st.payload, st.off, plane, ln, cd, chunk)
         del plane
         assert_offsets_match_lengths(
-            st.off, lambda a, b, sh=shift: ((d16[a:b].to(torch.int32) >> sh) & 0xFF).to(torch.uint8), s.n, ln, CHUNK)
+            st.off, lambda a, b, sh=shift: ((d16[a:b].to(torch.int32) >> sh) & 0xFF).to(torch.uint8), s.n, ln, chunk)
     back = codec.decompress_bf16(s, x0)
     assert torch.equal(back.view(torch.int16), w16)
 
@@ -161,7 +163,7 @@ def test_bf16_weights_full():
 
 def test_snapshot_delta_full():
     x0, x1 = workloads.snapshot_pair(device="cuda")
-    _bf16_config(x1, x0)
+    _bf16_config(x1, x0, SNAPSHOT_CHUNK)
 
 
 # ------------------------------------------------------------------ chunk-size sweep: 16 GiB int8, fixed codebook
