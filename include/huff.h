@@ -426,16 +426,27 @@ int lmc_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n,
 /*
  * Counted per-shard path.  When the codebooks are built from the tensor's own
  * histograms (per-shard mode, P2 framework stages 2-3), the histogram pass
- * can also record both planes' counts per segment of HUFF_COUNT_SEGMENT
+ * can also record both planes' counts per segment of S = lmc_count_segment(n)
  * elements.  lmc_encode_bf16_counted then derives every segment's bit offset
  * as sum(count * length) and encodes in one pass over the input, with no
  * counting pass and no waiting between CTAs.  Its outputs are byte-identical
  * to lmc_encode_bf16's.  (A GPU arrangement of the same method; the pages
  * have no separate step for it.)
  */
-#define HUFF_COUNT_SEGMENT 131072
+#define HUFF_COUNT_SEGMENT 131072 /* the least segment size S */
 
-/* Bytes of the per-segment counts for n elements: 2048 * ceil(n / HUFF_COUNT_SEGMENT). */
+/*
+ * lmc_count_segment -- S, the elements per counted segment for n elements on
+ * the current device: HUFF_COUNT_SEGMENT while the counted encode's warps (16
+ * per SM) outnumber segments of that size; otherwise the multiple of 512 in
+ * [HUFF_COUNT_SEGMENT, 2 * HUFF_COUNT_SEGMENT) that gives every warp the same
+ * number of segments.  lmc_histogram_bf16_counted and lmc_encode_bf16_counted
+ * both use it, so both must run on devices with the same SM count.
+ */
+size_t lmc_count_segment(size_t n);
+
+/* Bytes of the per-segment counts for n elements: 2048 * ceil(n / HUFF_COUNT_SEGMENT)
+ * (enough for any S). */
 size_t lmc_segment_counts_size(size_t n);
 
 /* Workspace bytes lmc_encode_bf16_counted needs: 48 * ceil(n / HUFF_COUNT_SEGMENT) + 16. */
@@ -444,7 +455,8 @@ size_t lmc_counted_workspace_size(size_t n);
 /*
  * lmc_histogram_bf16_counted -- lmc_histogram_bf16 that also writes
  * seg_counts[s][0][b] and seg_counts[s][1][b] (uint32): the counts of symbol
- * b in the high and low plane of elements [s * HUFF_COUNT_SEGMENT, ...).
+ * b in the high and low plane of elements [s * S, (s + 1) * S), S =
+ * lmc_count_segment(n).
  *   w, x0       16-byte aligned; x0 may be NULL (no delta).
  *   hist_hi, hist_lo  uint64[256] each, overwritten.
  *   seg_counts  uint32 array of seg_counts_bytes >= lmc_segment_counts_size(n), 4-byte aligned.

@@ -44,7 +44,7 @@ EXPORTS = (
     "huff_num_chunks", "huff_histogram", "huff_build_codebook", "huff_codebook_from_lengths", "huff_encode",
     "huff_decode", "huff_encode_noalloc", "lmc_bytegroup_split", "lmc_bytegroup_merge", "lmc_delta_xor", "lmc_histogram_bf16",
     "lmc_workspace_size", "lmc_encode_bf16", "lmc_decode_bf16", "huff_code_stats", "lmc_segment_counts_size",
-    "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
+    "lmc_count_segment", "lmc_counted_workspace_size", "lmc_histogram_bf16_counted", "lmc_encode_bf16_counted", "lmc_bytegroup_split_w",
     "lmc_bytegroup_merge_w", "huff_drift_check", "huff_build_codebook_if", "huff_build_codebooks",
     "huff_stream_copy", "huff_container_size", "huff_container_write", "huff_container_parse", "huff_debug_wait",
     "huff_pick_chunk",
@@ -111,6 +111,7 @@ def load(path: str = LIB_PATH):
         "huff_container_write": (I, [P, S, S, S, I, P, P, P, ctypes.POINTER(S)]),
         "huff_container_parse": (I, [P, S, ctypes.POINTER(HuffContainerView)]),
         "lmc_segment_counts_size": (S, [S]),
+        "lmc_count_segment": (S, [S]),
         "huff_drift_check": (I, [P, P, ctypes.c_double, P, P, P]),
         "huff_build_codebook_if": (I, [P, P, I, ctypes.c_uint, P, P, P]),
         "lmc_bytegroup_split_w": (I, [P, S, I, P, S, P]),
@@ -191,6 +192,11 @@ def huff_pick_chunk(n: int, delta: bool = False) -> int:
 
 def lmc_workspace_size(n: int, chunk_bytes: int) -> int:
     return int(load().lmc_workspace_size(n, chunk_bytes))
+
+
+def lmc_count_segment(n: int) -> int:
+    """Elements per counted segment for n elements on the current device (see include/huff.h)."""
+    return int(load().lmc_count_segment(n))
 
 
 def lmc_segment_counts_size(n: int) -> int:

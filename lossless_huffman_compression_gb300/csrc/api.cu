@@ -262,6 +262,8 @@ size_t lmc_segment_counts_size(size_t n) {
     return static_cast<size_t>(huffk::kSegCountWords) * 4 * ((n + HUFF_COUNT_SEGMENT - 1) / HUFF_COUNT_SEGMENT);
 }
 
+size_t lmc_count_segment(size_t n) { return huffk::count_seg_elems(n); }
+
 size_t lmc_counted_workspace_size(size_t n) { return 48 * ((n + HUFF_COUNT_SEGMENT - 1) / HUFF_COUNT_SEGMENT) + 16; }
 
 int lmc_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,

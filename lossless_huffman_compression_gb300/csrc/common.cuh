@@ -13,9 +13,10 @@ namespace huffk {
 
 // ----------------------------------------------------------------- tuning constants
 // Counted (per-shard) bf16 path: the histogram pass records each plane's
-// counts per segment of kDirSegElems elements, so the encode knows every
-// segment's bit offset before it starts and reads its input once.
-constexpr size_t kDirSegElems = 131072;          // bf16 elements per counted segment
+// counts per segment (at least kDirSegElems elements; count_seg_elems), so
+// the encode knows every segment's bit offset before it starts and reads its
+// input once.
+constexpr size_t kDirSegElems = 131072;          // least bf16 elements per counted segment
 constexpr int kSegCountWords = 512;              // [hi 256 | lo 256] per segment
 constexpr int kHistThreads = 512;
 constexpr int kHistCopies = 32;                  // one histogram copy per lane
@@ -170,6 +171,8 @@ struct DevInfo {
     int max_smem_optin;
 };
 DevInfo dev_info();
+// Elements per counted segment for n elements on the current device (encode.cu).
+size_t count_seg_elems(size_t n);
 // Widest decode block that fits in max_smem bytes, with or without an XOR delta (decode.cu).
 int decode_lanes(int max_smem, bool delta);
 

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kSegScanThreads) k_seg_bits_scan(const uint32_
         b0 = warp_sum_u64(b0);
         b1 = warp_sum_u64(b1);
         if (__any_sync(0xffffffffu, missing) && lane == 0) set_status(status, HUFF_ERR_SYMBOL_NOT_IN_CODEBOOK);
-        if (lane == 0) {  // a segment has at most 131 072 * 24 bits per plane: 32-bit counts
+        if (lane == 0) {  // a segment has fewer than 512 * 512 * 24 bits per plane: 32-bit counts
             bits[seg] = static_cast<uint32_t>(b0);
             bits[n_seg + seg] = static_cast<uint32_t>(b1);
         }
@@ -291,7 +291,7 @@ constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kLaneElems = 16;
 constexpr int kTile = 32 * kLaneElems;                                 // 512 elements
-constexpr uint32_t kTilesPerSeg = static_cast<uint32_t>(kDirSegElems / kTile);  // 256
+constexpr uint32_t kMinSegTiles = static_cast<uint32_t>(kDirSegElems / kTile);  // 256
 constexpr int kStages = 3;
 constexpr int kStageBytes = 2 * kTile * 2;                             // the tile of w, then of x0
 constexpr int kBufWords = 392;                                         // a tile's bits of one plane
@@ -445,15 +445,16 @@ __device__ __forceinline__ void wpack(WPacker &pk, uint32_t *buf, const uint32_t
 template <bool XOR>
 __device__ __forceinline__ bool wissue(uint8_t *ring, uint64_t *bar, uint32_t stage, uint32_t seg, uint32_t kk,
                                        uint32_t tiles, uint32_t nw, uint32_t n_seg, uint32_t n_tiles,
-                                       uint32_t last_bytes, const uint8_t *in, const uint8_t *in2, uint64_t pol) {
+                                       uint32_t seg_tiles, uint32_t last_bytes, const uint8_t *in,
+                                       const uint8_t *in2, uint64_t pol) {
     if (kk >= tiles) {
         kk -= tiles;
         seg += nw;
         if (seg >= n_seg) return false;
-        const uint32_t rest = n_tiles - seg * wenc::kTilesPerSeg;
-        if (kk >= (rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg)) return false;
+        const uint32_t rest = n_tiles - seg * seg_tiles;
+        if (kk >= (rest < seg_tiles ? rest : seg_tiles)) return false;
     }
-    const uint32_t t = seg * wenc::kTilesPerSeg + kk;
+    const uint32_t t = seg * seg_tiles + kk;
     const uint32_t bytes = t == n_tiles - 1 ? last_bytes : uint32_t(wenc::kTile * 2);  // every tile whole but the last
     const size_t src = static_cast<size_t>(t) * (wenc::kTile * 2);
     uint8_t *dst = ring + stage * wenc::kStageBytes;
@@ -475,7 +476,8 @@ __device__ __forceinline__ void wwrite(uint32_t *dst, const uint32_t *buf, uint3
 template <bool XOR>
 __global__ void __launch_bounds__(wenc::kThreads, 1)
     k_encode_counted(const uint8_t *__restrict__ in, const uint8_t *__restrict__ in2, size_t n, EncPlane p0,
-                     EncPlane p1, ChunkDiv cdiv, uint32_t n_tiles, uint32_t n_seg, int32_t *status) {
+                     EncPlane p1, ChunkDiv cdiv, uint32_t n_tiles, uint32_t seg_tiles, uint32_t n_seg,
+                     int32_t *status) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -510,10 +512,10 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
     const uint32_t last_bytes = (last_n * 2) & ~15u;
     uint32_t inflight = 0;  // lane 0: stages with a job issued and not yet waited for
     if (lane == 0 && gw < n_seg) {  // the first kStages tiles of the warp's sequence
-        const uint32_t rest = n_tiles - gw * wenc::kTilesPerSeg;
-        const uint32_t tiles0 = rest < wenc::kTilesPerSeg ? rest : wenc::kTilesPerSeg;
+        const uint32_t rest = n_tiles - gw * seg_tiles;
+        const uint32_t tiles0 = rest < seg_tiles ? rest : seg_tiles;
         for (int j = 0; j < wenc::kStages; ++j)
-            if (wissue<XOR>(ring, bar, j, gw, j, tiles0, nw, n_seg, n_tiles, last_bytes, in, in2, pol))
+            if (wissue<XOR>(ring, bar, j, gw, j, tiles0, nw, n_seg, n_tiles, seg_tiles, last_bytes, in, in2, pol))
                 inflight |= 1u << j;
     }
     const uint32_t kbh = static_cast<uint32_t>(lane & 15) << 3;
@@ -523,9 +525,10 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
     for (uint32_t r = 0;; ++r) {
         const uint32_t seg = r * nw + gw;
         if (seg >= n_seg) break;
-        const uint32_t t0 = seg * wenc::kTilesPerSeg;
-        const uint32_t tiles = n_tiles - t0 < wenc::kTilesPerSeg ? n_tiles - t0 : wenc::kTilesPerSeg;
-        // Bit positions inside the segment are 32-bit (a segment has at most 131072 * 24 bits): pos =
+        const uint32_t t0 = seg * seg_tiles;
+        const uint32_t tiles = n_tiles - t0 < seg_tiles ? n_tiles - t0 : seg_tiles;
+        // Bit positions inside the segment are 32-bit (a segment has fewer than 512 tiles, at most
+        // 511 * 512 * 24 bits): pos =
         // the segment's phase in its first word + bits so far; word pos >> 5 of the segment is global
         // word (start >> 5) + (pos >> 5).
         const uint64_t start0 = seg ? (p0.desc[seg - 1] & kValueMask) : 0;
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
             if (lane == 0) fence_proxy_async_smem();  // the reads before the bulk copy that refills the stage
             // the stage is free again: lane 0 refills it with the tile kStages further on
             if (lane == 0 && wissue<XOR>(ring, bar, cstage, seg, k + wenc::kStages, tiles, nw, n_seg, n_tiles,
-                                         last_bytes, in, in2, pol))
+                                         seg_tiles, last_bytes, in, in2, pol))
                 inflight |= 1u << cstage;
             cstage = cstage + 1 == uint32_t(wenc::kStages) ? 0u : cstage + 1;
             cphase ^= cstage == 0 ? 1u : 0u;
@@ -1197,6 +1200,19 @@ int launch_encode_u8_noalloc(const uint8_t *in, size_t n, const huff_codebook *c
     return launch_encode_u8(in, n, cb, chunk, payload, cap, off, ws, status, s);
 }
 
+// Elements per counted segment for n elements: kDirSegElems (256 tiles) while the counted encode's warps
+// (one CTA of 16 per SM) outnumber such segments; otherwise the whole number of tiles (at least 256,
+// fewer than 512) that gives every warp the same number of segments, so that no warp's last segment
+// runs while most of its SM's warps are done.
+size_t count_seg_elems(size_t n) {
+    const size_t tiles = (n + wenc::kTile - 1) / wenc::kTile;
+    const size_t warps = static_cast<size_t>(dev_info().sms) * wenc::kWarps;
+    const size_t rounds = tiles / (static_cast<size_t>(wenc::kMinSegTiles) * warps);
+    if (rounds == 0) return kDirSegElems;
+    const size_t st = (tiles + warps * rounds - 1) / (warps * rounds);
+    return st * wenc::kTile;
+}
+
 // bf16 with given codebooks (the fixed-codebook mode): the counted histogram pass records both planes'
 // counts per segment, and the one-pass counted encode then gives every segment its bit offset from
 // sum(count x length) under the given codebooks (a symbol present without a code is reported by that
@@ -1241,7 +1257,8 @@ int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n
         k_encode_empty<<<1, 1, 0, s>>>(off_hi, off_lo);
         return launch_status();
     }
-    const size_t segs = (n + kDirSegElems - 1) / kDirSegElems;
+    const size_t seg_elems = count_seg_elems(n);
+    const size_t segs = (n + seg_elems - 1) / seg_elems;  // at most ceil(n / kDirSegElems): the workspace's size
     uint64_t *w = static_cast<uint64_t *>(ws);
     // layout: desc_hi, desc_lo, edge_hi, edge_lo, 32-bit bits (2 x segs), ticket counter (zeroed)
     EncPlane p0{cb_hi, reinterpret_cast<uint32_t *>(pay_hi), cap_hi / 4, off_hi, w, w + 2 * segs};
@@ -1269,7 +1286,8 @@ int launch_encode_bf16_counted(const uint16_t *w16, const uint16_t *x0, size_t n
         size_t grid = static_cast<size_t>(d.sms);
         if (grid > segs) grid = segs;
         kern<<<static_cast<unsigned>(grid), wenc::kThreads, wenc::kSmem, s>>>(
-            a, b, n, p0, p1, make_chunk_div(chunk), static_cast<uint32_t>(wtiles), static_cast<uint32_t>(segs), status);
+            a, b, n, p0, p1, make_chunk_div(chunk), static_cast<uint32_t>(wtiles),
+            static_cast<uint32_t>(seg_elems / wenc::kTile), static_cast<uint32_t>(segs), status);
         return cudaGetLastError() == cudaSuccess ? HUFF_OK : HUFF_ERR_CUDA;
     };
     int st = x0 != nullptr ? run(k_encode_counted<true>) : run(k_encode_counted<false>);

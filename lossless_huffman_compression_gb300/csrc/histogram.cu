@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16(const uint16_t 
     flush_copies(sh + kHistPlaneWords, hist_lo);
 }
 
-// Both byte planes, per segment of kDirSegElems elements: each CTA takes whole
+// Both byte planes, per segment of seg_elems elements: each CTA takes whole
 // segments; after a segment it folds its 32 copies into the segment's 512
 // counts (high plane, then low plane), zeroes them, and keeps a running total
 // per bin for the whole-tensor histograms.  Folding costs 0.25 shared-memory
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16_counted(const u
                                                                          uint64_t *__restrict__ hist_hi,
                                                                          uint64_t *__restrict__ hist_lo,
                                                                          uint32_t *__restrict__ seg_counts,
-                                                                         uint32_t n_seg) {
+                                                                         size_t seg_elems, uint32_t n_seg) {
     static_assert(kHistThreads == kSegCountWords, "one thread per (plane, bin)");
     extern __shared__ uint32_t sh[];
     const int tid = threadIdx.x;
@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(kHistThreads) k_histogram_bf16_counted(const u
     uint32_t *fold = sh + (tid >> 8) * kHistPlaneWords + fb * kHistCopies;  // this thread's bin, its 32 copies
     uint64_t total = 0;
     for (uint32_t seg = blockIdx.x; seg < n_seg; seg += gridDim.x) {
-        const size_t first = static_cast<size_t>(seg) * kDirSegElems;
-        const size_t cnt = n - first < kDirSegElems ? n - first : kDirSegElems;
+        const size_t first = static_cast<size_t>(seg) * seg_elems;
+        const size_t cnt = n - first < seg_elems ? n - first : seg_elems;
         const size_t nv = cnt / 8;
         const uint4 *vw = reinterpret_cast<const uint4 *>(w + first);
         const uint4 *vx = reinterpret_cast<const uint4 *>(XOR ? x0 + first : w + first);
@@ -331,17 +331,19 @@ int launch_histogram_bf16(const uint16_t *w, const uint16_t *x0, size_t n, uint6
 int launch_histogram_bf16_counted(const uint16_t *w, const uint16_t *x0, size_t n, uint64_t *hist_hi,
                                   uint64_t *hist_lo, uint32_t *seg_counts, cudaStream_t s) {
     const size_t smem = 2 * kHistPlaneWords * sizeof(uint32_t);
-    const size_t n_seg = (n + kDirSegElems - 1) / kDirSegElems;
+    const size_t seg_elems = count_seg_elems(n);  // the counted encode's segments
+    const size_t n_seg = (n + seg_elems - 1) / seg_elems;
     int grid = 1, st;
     if (x0 != nullptr) {
         if ((st = hist_grid(k_histogram_bf16_counted<true>, smem, n_seg * kHistThreads, &grid)) != HUFF_OK) return st;
         k_histogram_bf16_counted<true><<<grid, kHistThreads, smem, s>>>(w, x0, n, hist_hi, hist_lo, seg_counts,
-                                                                         static_cast<uint32_t>(n_seg));
+                                                                         seg_elems, static_cast<uint32_t>(n_seg));
     } else {
         if ((st = hist_grid(k_histogram_bf16_counted<false>, smem, n_seg * kHistThreads, &grid)) != HUFF_OK)
             return st;
         k_histogram_bf16_counted<false><<<grid, kHistThreads, smem, s>>>(w, nullptr, n, hist_hi, hist_lo,
-                                                                          seg_counts, static_cast<uint32_t>(n_seg));
+                                                                          seg_counts, seg_elems,
+                                                                          static_cast<uint32_t>(n_seg));
     }
     return launch_status();
 }

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from lossless_huffman_compression_gb300 import _lib, codec
-from gpu_util import assert_stream_equal, host, oracle_codebook
+from gpu_util import assert_offsets_match_lengths, assert_stream_equal, check_sampled_chunks, host, oracle_codebook
 
 pytestmark = pytest.mark.gpu
 
@@ -69,12 +69,14 @@ def test_counted_matches_oracle_and_two_pass(n, delta, chunk):
     np.testing.assert_array_equal(host(hh).astype(np.uint64), oracle.histogram(hi))
     np.testing.assert_array_equal(host(hl).astype(np.uint64), oracle.histogram(lo))
     counts = host(seg).view(np.uint32)
-    n_seg = (n + SEG - 1) // SEG
+    S = _lib.lmc_count_segment(n)
+    assert S == SEG  # inputs this small keep the least segment size
+    n_seg = (n + S - 1) // S
     for s in range(n_seg):
         np.testing.assert_array_equal(counts[s * 512:s * 512 + 256].astype(np.uint64),
-                                      oracle.histogram(hi[s * SEG:(s + 1) * SEG]))
+                                      oracle.histogram(hi[s * S:(s + 1) * S]))
         np.testing.assert_array_equal(counts[s * 512 + 256:s * 512 + 512].astype(np.uint64),
-                                      oracle.histogram(lo[s * SEG:(s + 1) * SEG]))
+                                      oracle.histogram(lo[s * S:(s + 1) * S]))
     for plane, cb, stream in ((hi, cb_hi, s_hi), (lo, cb_lo, s_lo)):
         ln, cd = oracle_codebook(oracle.histogram(plane))
         np.testing.assert_array_equal(cb.lengths(), ln)
@@ -88,6 +90,69 @@ def test_counted_matches_oracle_and_two_pass(n, delta, chunk):
         assert torch.equal(a.payload[:nb], b.payload[:nb])
     back = codec.decompress_bf16(codec.Bf16Streams(cb_hi, cb_lo, s_hi, s_lo, n), dx0)
     assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
+
+
+def _enc_warps():
+    return torch.cuda.get_device_properties(0).multi_processor_count * 16
+
+
+@pytest.mark.parametrize("n", [0, 1, SEG, 318_767_103, 318_767_104, 400_000_003, 2_000_027_648, 1 << 34])
+def test_count_segment_gives_every_encode_warp_the_same_rounds(n):
+    """lmc_count_segment: SEG while the encode's warps outnumber SEG-element segments; otherwise the
+    smallest whole number of 512-element tiles that splits the input into at most warps x rounds
+    segments, rounds = floor(tiles / (256 warps))."""
+    S = _lib.lmc_count_segment(n)
+    warps = _enc_warps()
+    tiles = -(-n // 512)
+    rounds = tiles // (256 * warps)
+    if rounds == 0:
+        assert S == SEG
+        return
+    assert S % 512 == 0 and SEG <= S < 2 * SEG
+    st = S // 512
+    assert -(-tiles // st) <= warps * rounds < -(-tiles // (st - 1))
+    if n == 2_000_027_648 and warps == 152 * 16:
+        assert S == 268 * 512 and -(-n // S) == 14576  # 6 rounds of 2432 warps, 16 warps idle in the last
+
+
+def test_counted_segments_above_the_least_size():
+    """A 400 M-element delta, where segments are longer than SEG: sampled segments' counts equal
+    torch.bincount of their bytes, every chunk's offset difference equals its symbols' summed code
+    lengths, sampled chunks equal the oracle's encoding, and the decode is exact."""
+    n = 400_000_003
+    S = _lib.lmc_count_segment(n)
+    if S == SEG:
+        pytest.skip("this GPU keeps the least segment size at this n")
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x0 = (torch.randn(n, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    x1 = (x0.float() + torch.randn(n, device="cuda", generator=g) * 1e-4).to(torch.bfloat16)
+    chunk = 16384
+    hh, hl, seg, cb_hi, cb_lo, s_hi, s_lo, st = _counted(x1, x0, chunk)
+    assert st == 0
+    d16 = (x1.view(torch.int16) ^ x0.view(torch.int16)).to(torch.int32) & 0xFFFF
+    counts = seg.view(torch.int32)
+    n_seg = -(-n // S)
+    for s in sorted({0, 1, n_seg // 2, n_seg - 1}):
+        v = d16[s * S:min(n, (s + 1) * S)]
+        for plane, sh in ((0, 8), (1, 0)):
+            want = torch.bincount((v >> sh) & 0xFF, minlength=256)
+            got = counts[s * 512 + 256 * plane: s * 512 + 256 * plane + 256].to(torch.int64)
+            assert torch.equal(got, want), (s, plane)
+    for hist, cb, stream, sh in ((hh, cb_hi, s_hi, 8), (hl, cb_lo, s_lo, 0)):
+        ln, cd = oracle_codebook(host(hist).astype(np.uint64))
+        np.testing.assert_array_equal(cb.lengths(), ln)
+        sym = lambda a, b, sh=sh: ((d16[a:b] >> sh) & 0xFF).to(torch.uint8)
+        assert_offsets_match_lengths(stream.off, sym, n, ln, chunk)
+        offs = host(stream.off).astype(np.uint64)
+        nc = stream.n_chunks()
+        for c in sorted({0, nc // 3, nc - 1}):
+            lo, hi = int(offs[c]), int(offs[c + 1])
+            b0, b1 = lo // 8, (hi + 7) // 8
+            pay = host(stream.payload[b0:b1 + 1])
+            check_sampled_chunks(pay, np.array([lo - 8 * b0, hi - 8 * b0], dtype=np.uint64),
+                                 host(sym(c * chunk, min(n, (c + 1) * chunk))), ln, cd, chunk, [0])
+    back = codec.decompress_bf16(codec.Bf16Streams(cb_hi, cb_lo, s_hi, s_lo, n), x0)
+    assert torch.equal(back.view(torch.int16), x1.view(torch.int16))
 
 
 def test_counted_compress_bf16_round_trip_wide_noise():
