@@ -996,9 +996,10 @@ def relaunch_ranks(n: int) -> int:
     return subprocess.call(cmd)
 
 
-# The snapshot's chunk: 2.0e9 elements in 126 010 chunk pairs, one 832-lane decode block (the widest whose
-# x0 staging fits in shared memory) on each of the 152 SMs; huff_pick_chunk's choice for this size with a delta.
-SNAPSHOT_CHUNK = 15872
+# The snapshot's chunk: 2.0e9 elements in 134 699 chunk pairs, 896-lane decode blocks (the widest whose x0
+# staging fits in shared memory; 7 warps per scheduler) on 151 SMs; huff_pick_chunk's choice for this size
+# with a delta.
+SNAPSHOT_CHUNK = 14848
 
 
 def main():

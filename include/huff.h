@@ -136,15 +136,15 @@ size_t huff_num_chunks(size_t n, size_t chunk_bytes);
 /*
  * huff_pick_chunk -- a chunk size for n symbols (elements, for the fused bf16
  * calls) on the current device.  The decode runs one lane per chunk, all lanes
- * resident, at most L lanes per SM: L = 832 when the stream will be decoded
- * with an XOR delta (delta != 0: lmc_decode_bf16 with x0, whose x0 staging
- * takes shared memory), otherwise 896 (on a GPU with 227 KiB of shared memory
- * per block).  This returns the smallest multiple of HUFF_CHUNK_ALIGN that
- * gives at most L chunks per SM (at least HUFF_CHUNK_ALIGN, at most
- * HUFF_MAX_CHUNK), so that one wave of blocks of nearly L lanes covers the
- * input on every SM.  (The chunk size is the caller's choice on the pages'
- * format; each chunk costs 8 bytes of offset per stream.)  Returns 0 when the
- * device cannot be queried.
+ * resident, at most L lanes per SM: the widest block whose shared memory fits
+ * for the decode that will run (delta != 0: lmc_decode_bf16 with x0, whose x0
+ * staging takes shared memory; L = 896 either way on a GPU with 227 KiB of
+ * shared memory per block).  This returns the smallest multiple of
+ * HUFF_CHUNK_ALIGN that gives at most L chunks per SM (at least
+ * HUFF_CHUNK_ALIGN, at most HUFF_MAX_CHUNK), so that one wave of blocks of
+ * nearly L lanes covers the input on every SM.  (The chunk size is the
+ * caller's choice on the pages' format; each chunk costs 8 bytes of offset
+ * per stream.)  Returns 0 when the device cannot be queried.
  */
 size_t huff_pick_chunk(size_t n, int delta);
 

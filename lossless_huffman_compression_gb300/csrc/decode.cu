@@ -57,9 +57,22 @@ constexpr int kSecMax = 2048;  // secondary-table entries per plane
 // Shared decode tables of one codebook for a W-bit window (W = 12: the
 // codebook's own table; W = 13: built from it in the prologue).  16-byte
 // aligned and sized, so tables placed back to back stay aligned.
-template <int W, int SEC = kSecMax>
-struct __align__(16) DecTables {
-    uint64_t lut[1u << W];  // syms (48 bits) | count << 48 | total bits << 52; 0: first code > W bits
+// The W-bit table: one 64-bit entry per window (syms (48 bits) | count << 48 | total bits << 52; 0: the
+// first code is longer than W bits), or, split (SPLIT), at most 4 symbols per window in a 32-bit word
+// (first symbol in the low byte) and count | total bits << 3 in a byte: 5 bytes per window instead of 8.
+template <int W, bool SPLIT>
+struct LutStore {
+    uint64_t lut[1u << W];
+};
+template <int W>
+struct LutStore<W, true> {
+    uint32_t syms[1u << W];
+    uint8_t meta[1u << W];
+};
+constexpr int kSplitSyms = 4;  // symbols a split entry holds
+
+template <int W, int SEC = kSecMax, bool SPLIT = false>
+struct __align__(16) DecTables : LutStore<W, SPLIT> {
     uint16_t sec[SEC];      // codes longer than W bits: symbol | length << 8 (0: no code)
     uint64_t run;           // the 1-bit code's symbol in all 8 bytes (when there is one)
     uint32_t bl_count[32];
@@ -77,6 +90,25 @@ struct __align__(16) DecTables {
 };
 static_assert(sizeof(DecTables<12>) % 16 == 0 && sizeof(DecTables<13>) % 16 == 0, "tables keep 16-byte alignment");
 
+// Entry i of the W-bit table: its symbols (first in the low byte, the rest zero), their count and total
+// bits.
+template <int W, int SEC, bool SPLIT>
+__device__ __forceinline__ void lut_get(const DecTables<W, SEC, SPLIT> &T, uint32_t i, uint64_t &v, uint32_t &c,
+                                        uint32_t &bits) {
+    if constexpr (SPLIT) {
+        const uint32_t m = T.meta[i];
+        v = T.syms[i];
+        c = m & 7u;
+        bits = m >> 3;
+    } else {
+        const uint64_t e = T.lut[i];
+        const uint32_t eh = static_cast<uint32_t>(e >> 32);
+        c = (eh >> 16) & 15u;
+        bits = eh >> 20;
+        v = e & 0xffffffffffffull;
+    }
+}
+
 // Tables of a plane with a 1-bit code, for the run decode below: the
 // canonical arrays and, for each 10-bit window, the first code's symbol and
 // length (symbol | length << 8; 0 when that code is longer than 10 bits,
@@ -93,11 +125,14 @@ struct __align__(16) RunTables {
     uint16_t zf[1u << kZWin];
 };
 
-// Secondary-table entries of the low plane next to a run-decoded high plane
-// (less than the default, so that x0 can be staged in the shared memory).
+// The low plane next to a run-decoded high plane: a split 13-bit table (at
+// most 4 symbols per window, which changes the symbols a three-lookup step
+// takes by less than 0.1 % on a snapshot delta's low plane) and a smaller
+// secondary table, so that the rings and the x0 staging of 896 lanes fit next
+// to them (7 warps on each of the SM's 4 schedulers).
 constexpr int kSecRun = 1024;
 using LoTables = DecTables<13>;
-using LoTablesRun = DecTables<13, kSecRun>;
+using LoTablesRun = DecTables<13, kSecRun, true>;
 static_assert(sizeof(RunTables) % 16 == 0 && sizeof(LoTablesRun) % 16 == 0, "tables keep 16-byte alignment");
 constexpr size_t kBf16Tables = sizeof(DecTables<12>) + sizeof(LoTables);
 constexpr size_t kBf16RunTables = sizeof(RunTables) + sizeof(LoTablesRun);
@@ -117,12 +152,13 @@ __device__ __forceinline__ uint32_t code_limit(const huff_codebook *cb, bool ok,
 // plus, when it holds fewer than the maximum number of symbols, the one code
 // that ends exactly at the 13th bit (a code ending earlier would already be
 // in the 12-bit entry, and no code is shorter than 1 bit).
-template <int W, int SEC>
-__device__ void load_table_a(DecTables<W, SEC> &T, const huff_codebook *cb) {
+template <int W, int SEC, bool SPLIT>
+__device__ void load_table_a(DecTables<W, SEC, SPLIT> &T, const huff_codebook *cb) {
     static_assert(W == HUFF_LUT_BITS || W == HUFF_LUT_BITS + 1, "12- or 13-bit window");
+    static_assert(!SPLIT || W == HUFF_LUT_BITS + 1, "split tables have 13-bit windows");
     const int tid = threadIdx.x;
     const bool ok = cb->magic == HUFF_CODEBOOK_MAGIC;
-    if (W == HUFF_LUT_BITS) {
+    if constexpr (W == HUFF_LUT_BITS && !SPLIT) {
         const uint4 *src = reinterpret_cast<const uint4 *>(cb->lut);
         uint4 *dst = reinterpret_cast<uint4 *>(T.lut);
         for (int i = tid; i < (1 << W) / 2; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
@@ -145,7 +181,20 @@ __device__ void load_table_a(DecTables<W, SEC> &T, const huff_codebook *cb) {
                     }
                 }
             }
-            T.lut[i] = e;
+            if constexpr (SPLIT) {
+                // the first kSplitSyms symbols and their bits
+                uint32_t c = static_cast<uint32_t>(e >> 48) & 15u;
+                uint32_t bits = static_cast<uint32_t>(e >> 52) & 15u;
+                if (c > static_cast<uint32_t>(kSplitSyms)) {
+                    c = kSplitSyms;
+                    bits = 0;
+                    for (int k = 0; k < kSplitSyms; ++k) bits += cb->len[(e >> (8 * k)) & 0xffu];
+                }
+                T.syms[i] = static_cast<uint32_t>(e);
+                T.meta[i] = static_cast<uint8_t>(c | (bits << 3));
+            } else {
+                T.lut[i] = e;
+            }
         }
     }
     uint4 *sz = reinterpret_cast<uint4 *>(T.sec);
@@ -179,8 +228,8 @@ __device__ void load_table_a(DecTables<W, SEC> &T, const huff_codebook *cb) {
 // shorter ones, so their W-bit prefixes are the contiguous range
 // [first_code[W + 1] / 2, 2^W); sec holds, per prefix, 2^k entries
 // (k = longest - W) indexed by the next k bits.
-template <int W, int SEC>
-__device__ void load_table_b(DecTables<W, SEC> &T, const huff_codebook *cb) {
+template <int W, int SEC, bool SPLIT>
+__device__ void load_table_b(DecTables<W, SEC, SPLIT> &T, const huff_codebook *cb) {
     if (!T.ok || T.sec_k == 0 || !T.sec_ok) return;
     const int k = T.sec_k;
     for (int sym = threadIdx.x; sym < 256; sym += blockDim.x) {
@@ -236,8 +285,8 @@ __device__ __forceinline__ uint32_t long_code_lim(uint32_t top, const Tab &T, in
     return (L << 8) | T.sorted[T.first_index[L] + d];
 }
 
-template <int W, int SEC>
-__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W, SEC> *T) {
+template <int W, int SEC, bool SPLIT>
+__device__ __noinline__ uint32_t long_code(uint32_t top, const DecTables<W, SEC, SPLIT> *T) {
     return long_code_lim<W>(top, *T, T->longest);
 }
 
@@ -259,8 +308,8 @@ __device__ __noinline__ uint32_t long_code_search(uint32_t top, const Tab *T) {
 
 // The rare case where a table entry holds more symbols than the chunk has
 // left: the total length of its first c symbols.
-template <int W, int SEC>
-__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables<W, SEC> *T) {
+template <int W, int SEC, bool SPLIT>
+__device__ __noinline__ uint32_t clamped_bits(uint64_t v, uint32_t c, const DecTables<W, SEC, SPLIT> *T) {
     uint32_t bits = 0;
     for (uint32_t k = 0; k < c; ++k) bits += T->len[(v >> (8 * k)) & 0xffu];
     return bits;
@@ -347,8 +396,8 @@ struct PlaneDec {
 // The rare cases of a step: a code longer than the table's window (or no
 // code at all: a corrupt stream), and an entry with more symbols than the
 // chunk has left.
-template <int W, bool LIM, int SEC>
-__device__ __forceinline__ void step_rare(const DecTables<W, SEC> &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
+template <int W, bool LIM, int SEC, bool SPLIT>
+__device__ __forceinline__ void step_rare(const DecTables<W, SEC, SPLIT> &T, uint32_t win, uint32_t top, int rem, uint32_t &c,
                                        uint32_t &bits, uint64_t &v, bool &bad) {
     if (c == 0) {
         uint32_t L = 0, sym = 0;
@@ -404,8 +453,8 @@ __device__ __forceinline__ void put4(PlaneDec &s, uint8_t *ring, uint32_t swz, u
 // the zero bits on top of the window (up to 32, the chunk's rest and the
 // ring's room) when that beats a lookup; then up to four 8-byte stores.
 // `limit` = the first symbol position whose slot still holds unmerged data.
-template <int RING, bool RUN, int W, bool LIM, bool FAST = false, bool THIRD = false, int SEC = kSecMax>
-__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
+template <int RING, bool RUN, int W, bool LIM, bool FAST = false, bool THIRD = false, int SEC = kSecMax, bool SPLIT = false>
+__device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC, SPLIT> &T,
                                      uint8_t *ring, uint32_t swz, int cnt, int limit, uint64_t run, bool &bad) {
     static_assert(!(RUN && THIRD), "a third lookup is for planes without runs");
     static_assert(!(RUN && FAST), "a run step may add more symbols than a fast block reserves");
@@ -418,11 +467,9 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
     const bool go = FAST || (rem > 0 && room >= (THIRD ? kStepMax3 : kStepMax));
     s.refill(p, nbytes);
     const uint32_t win = s.bh >> (32 - W);
-    const uint64_t e = T.lut[win];
-    const uint32_t eh = static_cast<uint32_t>(e >> 32);
-    uint32_t c = (eh >> 16) & 15u;
-    uint32_t bits = eh >> 20;
-    uint64_t v = e & 0xffffffffffffull;
+    uint32_t c, bits;
+    uint64_t v;
+    lut_get(T, win, v, c, bits);
     bool is_run = false;
     if (RUN) {
         // the 1-bit code is all zeros: clz(bh) symbols of it are next (bh holds >= 33 valid bits)
@@ -441,13 +488,13 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
         // simple (at least 20 valid bits remain) and the two entries together are at most 8 symbols
         // within the chunk; otherwise those bits wait for the next step
         const uint32_t top2 = __funnelshift_l(s.bl, s.bh, bits);
-        const uint64_t e2 = T.lut[top2 >> (32 - W)];
-        const uint32_t eh2 = static_cast<uint32_t>(e2 >> 32);
-        const uint32_t c2 = (eh2 >> 16) & 15u;
+        uint32_t c2, b2;
+        uint64_t v2;
+        lut_get(T, top2 >> (32 - W), v2, c2, b2);
         const bool take2 = simple && c2 != 0 && c + c2 <= static_cast<uint32_t>(kStepMax) &&
                            static_cast<int>(c + c2) <= rem;
-        v |= take2 ? (e2 & 0xffffffffffffull) << (8 * c) : 0ull;
-        bits += take2 ? (eh2 >> 20) : 0u;
+        v |= take2 ? v2 << (8 * c) : 0ull;
+        bits += take2 ? b2 : 0u;
         c += take2 ? c2 : 0u;
     }
     c = go ? c : 0u;
@@ -459,14 +506,13 @@ __device__ __forceinline__ void step(PlaneDec &s, const uint8_t *p, size_t nbyte
         // lookup on the bits after the first two entries, taken when the step went the simple way and
         // its codes lie within the valid bits and the chunk, appended as a second round
         put4<RING>(s, ring, swz, v, c);
-        const uint64_t e3 = T.lut[s.bh >> (32 - W)];
-        const uint32_t eh3 = static_cast<uint32_t>(e3 >> 32);
-        const uint32_t c3 = (eh3 >> 16) & 15u;
-        const uint32_t b3 = eh3 >> 20;
+        uint32_t c3, b3;
+        uint64_t v3;
+        lut_get(T, s.bh >> (32 - W), v3, c3, b3);
         const bool take3 = go && simple && c3 != 0 && static_cast<int>(b3) <= s.nb &&
                            static_cast<int>(c + c3) <= rem;
         s.consume(take3 ? b3 : 0u);
-        put4<RING>(s, ring, swz, take3 ? (e3 & 0xffffffffffffull) : 0ull, take3 ? c3 : 0u);
+        put4<RING>(s, ring, swz, take3 ? v3 : 0ull, take3 ? c3 : 0u);
         return;
     }
     const int f = s.fill;
@@ -503,8 +549,8 @@ __device__ __forceinline__ void plane_start(PlaneDec &s, const uint8_t *pay, siz
 
 // Decode until every lane of the warp has stored symbols [.., need) into its
 // RING-byte ring (a lane whose chunk is complete stores its last partial word).
-template <int RING, bool RUN, int W, bool LIM, int SEC, bool THIRD = false>
-__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
+template <int RING, bool RUN, int W, bool LIM, int SEC, bool THIRD = false, bool SPLIT = false>
+__device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC, SPLIT> &T,
                                                uint8_t *ring, uint32_t swz, int cnt, int need, int limit,
                                                bool &bad) {
     const uint64_t run = RUN ? T.run : 0ull;
@@ -517,11 +563,11 @@ __device__ __forceinline__ void fill_segment_t(PlaneDec &s, const uint8_t *p, si
                __any_sync(0xffffffffu, s.st < need)) {
 #pragma unroll
             for (int k = 0; k < kFast; ++k)
-                step<RING, false, W, LIM, true, THIRD>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+                step<RING, false, W, LIM, true, THIRD, SEC, SPLIT>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
         }
     }
     while (__any_sync(0xffffffffu, s.st < need && s.st + s.fill != cnt))
-        step<RING, RUN, W, LIM, false, THIRD && !RUN>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
+        step<RING, RUN, W, LIM, false, THIRD && !RUN, SEC, SPLIT>(s, p, nbytes, T, ring, swz, cnt, limit, run, bad);
     if (s.fill > 0 && s.st + s.fill == cnt) {
         if (THIRD && !RUN)  // pending part below a word, st a multiple of 4
             *reinterpret_cast<uint32_t *>(ring + ((s.st & (RING - 1)) ^ swz)) = static_cast<uint32_t>(s.a0);
@@ -578,13 +624,13 @@ __device__ __forceinline__ void fill_pair(PlaneDec &h, PlaneDec &l, const uint8_
     }
 }
 
-template <int RING, bool LIM, bool THIRD = false, int W, int SEC>
-__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC> &T,
+template <int RING, bool LIM, bool THIRD = false, int W, int SEC, bool SPLIT>
+__device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size_t nbytes, const DecTables<W, SEC, SPLIT> &T,
                                              uint8_t *ring, uint32_t swz, int cnt, int need, int limit, bool &bad) {
     if (T.has_run)
-        fill_segment_t<RING, true, W, LIM, SEC>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, true, W, LIM, SEC, false, SPLIT>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
     else
-        fill_segment_t<RING, false, W, LIM, SEC, THIRD>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
+        fill_segment_t<RING, false, W, LIM, SEC, THIRD, SPLIT>(s, p, nbytes, T, ring, swz, cnt, need, limit, bad);
 }
 
 // ------------------------------------------------------------------ planes with a 1-bit code
@@ -1061,9 +1107,9 @@ __host__ int split_threads(size_t n_chunks, size_t chunk, int sms) {
 // copies (cp.async, no registers held) right after the merge that used the
 // previous ones, so the merge finds x0 waiting instead of waiting for it (it
 // is read a segment's decode after its copies were issued).  The run-decoded
-// cases carry the high plane's run tables (no window table) and a smaller
-// secondary table for the low plane, which is what leaves room for the
-// staging area.
+// cases carry the high plane's run tables (no window table) and the low
+// plane's split table with a smaller secondary table, which is what leaves
+// room for the staging area of up to 896 lanes.
 constexpr int kStageLane = kSeg * 2;  // bytes of x0 per lane per segment
 
 template <bool XOR, bool PAIR, int ZR, class TH, class TL>
