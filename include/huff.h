@@ -124,10 +124,12 @@ size_t huff_codebook_size(void);
  * rounded up to whole 32-bit words, plus 16 bytes of slack. */
 size_t huff_encode_bound(size_t n, int max_len);
 
-/* Workspace bytes huff_encode needs for n symbols (per segment of 4 to 16
- * tiles of 1024 symbols: a lookback descriptor and the segment's boundary-word
- * pair, plus a segment counter).  chunk_bytes does not change it today; it is
- * an argument so the format can change without an ABI break. */
+/* Workspace bytes huff_encode needs for n symbols on the current device (per
+ * segment of 4 to 16 tiles of 1024 symbols, the size chosen from n and the SM
+ * count: a lookback descriptor and the segment's boundary-word pair, plus a
+ * segment counter; at most 16 bytes per 4096 symbols + 16).  chunk_bytes does
+ * not change it today; it is an argument so the format can change without an
+ * ABI break. */
 size_t huff_workspace_size(size_t n, size_t chunk_bytes);
 
 /* Number of chunks: ceil(n / chunk_bytes); 0 when n == 0. */

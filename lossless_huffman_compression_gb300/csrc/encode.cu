@@ -1130,12 +1130,17 @@ int launch_wait_probe(int kind, const uint64_t *desc, uint32_t seg, unsigned lim
     return launch_status();
 }
 
-// Tiles per segment of the byte-stream encode: 16 when there are at least 8192
-// tiles per 16 of them (two segments and more for every warp of a large GPU),
-// fewer down to 4 for smaller inputs, so that small inputs still fill the GPU.
+// Tiles per segment of the byte-stream encode: the fewest rounds of segments
+// over the GPU's encode warps (one CTA of 16 per SM) that segments of at most
+// 16 tiles allow, and then the fewest tiles per segment that keep to those
+// rounds, so that the last round has (nearly) every warp busy; at least 4
+// tiles.  A 16 MiB input: 7-tile segments in one round of 2341 of the 2432
+// warps (4-tile segments made 1.68 rounds); large inputs: 16.
 size_t enc_u8_seg_tiles(size_t n) {
     const size_t tiles = (n + wenc8::kTile - 1) / wenc8::kTile;
-    size_t st = tiles / 8192;
+    const size_t warps = static_cast<size_t>(dev_info().sms) * wenc8::kWarps;
+    const size_t rounds = (tiles + size_t(wenc8::kSegTilesMax) * warps - 1) / (size_t(wenc8::kSegTilesMax) * warps);
+    size_t st = rounds ? (tiles + rounds * warps - 1) / (rounds * warps) : 0;
     if (st < size_t(wenc8::kSegTilesMin)) st = wenc8::kSegTilesMin;
     if (st > size_t(wenc8::kSegTilesMax)) st = wenc8::kSegTilesMax;
     return st;
