@@ -872,7 +872,6 @@ def run_workload(args):
     2 planes), sweep (16 GiB int8, chunk sizes 16 KiB .. 1 MiB).  GB/s of uncompressed bytes; codec API
     calls (status checked per call)."""
     from lossless_huffman_compression_gb300 import _lib, codec, workloads
-    import oracle
     torch.cuda.set_device(0)
     peak, peak_kind = hbm_peak()
     reps = max(3, args.steps)
@@ -888,11 +887,11 @@ def run_workload(args):
         cb, s = codec.compress(x, args.chunk)
         comp = _timed(lambda: codec.compress(x, args.chunk), reps)
         dec = _timed(lambda: codec.decode(s, cb), reps)
-        h = oracle.histogram(x.cpu().numpy())
+        stats = _lib.huff_code_stats(codec.histogram(x).cpu().numpy(), cb.lengths())
         out.update({"elements": n, "chunk_bytes": args.chunk, "l2": "1 MiB: L2-resident, latency-bound",
                     "compress_us": round(comp * 1e3, 1), "decode_us": round(dec * 1e3, 1),
                     "compress_gbs": round(n / comp / 1e6, 2), "decode_gbs": round(n / dec / 1e6, 2),
-                    "ratio": round(8 * n / s.total_bits(), 4), "entropy_bits": round(oracle.entropy(h), 4),
+                    "ratio": round(8 * n / s.total_bits(), 4), "entropy_bits": round(stats["entropy_bits"], 4),
                     "mean_len": round(s.total_bits() / n, 4)})
     elif args.workload == "fixed_codebook":
         hist = torch.zeros(256, dtype=torch.int64, device="cuda")
@@ -903,39 +902,54 @@ def run_workload(args):
                   for k in range(workloads.TEST_SHARDS)]
         out["input_hist_sha256_16"] = hashlib.sha256(hist.cpu().numpy().tobytes()).hexdigest()[:16]  # warm-up
         n = sum(x.numel() for x in shards)
-        streams = [codec.encode(x, cb, args.chunk) for x in shards]
-        enc = _timed(lambda: [codec.encode(x, cb, args.chunk) for x in shards], 3)
-        dec = _timed(lambda: [codec.decode(st, cb) for st in streams], 3)
-        # the same calls back to back, each with its own status, all statuses read once at the end
-        sts = [codec.new_status() for _ in shards]
-        outs = [torch.empty_like(x) for x in shards]
+        res = {}
+        fixed_bits = 0
+        # the bench's chunk size, and the one huff_pick_chunk gives a shard (one wave of full decode blocks:
+        # small chunks, whose offsets cost ratio)
+        for chunk in dict.fromkeys((args.chunk, _lib.huff_pick_chunk(shards[0].numel()))):
+            streams = [codec.encode(x, cb, chunk) for x in shards]
+            enc = _timed(lambda: [codec.encode(x, cb, chunk) for x in shards], 3)
+            dec = _timed(lambda: [codec.decode(st, cb) for st in streams], 3)
+            # the same calls back to back, each with its own status, all statuses read once at the end
+            sts = [codec.new_status() for _ in shards]
+            outs = [torch.empty_like(x) for x in shards]
 
-        def enc_pipe():
-            for x, st in zip(shards, sts):
-                codec.encode(x, cb, args.chunk, status=st)
+            def enc_pipe():
+                for x, st in zip(shards, sts):
+                    codec.encode(x, cb, chunk, status=st)
 
-        def dec_pipe():
-            for s_, o, st in zip(streams, outs, sts):
-                codec.decode(s_, cb, out=o, status=st)
+            def dec_pipe():
+                for s_, o, st in zip(streams, outs, sts):
+                    codec.decode(s_, cb, out=o, status=st)
 
-        enc_p = _timed(enc_pipe, 3)
-        dec_p = _timed(dec_pipe, 3)
-        for st in sts:
-            codec.raise_on_status(st, "fixed-codebook shard")
-        for x, o in zip(shards, outs):
-            if not torch.equal(x, o):
-                raise RuntimeError("fixed-codebook decode differs")
-        fixed_bits = sum(st.total_bits() for st in streams)
+            enc_p = _timed(enc_pipe, 3)
+            dec_p = _timed(dec_pipe, 3)
+            for st in sts:
+                codec.raise_on_status(st, "fixed-codebook shard")
+            for x, o in zip(shards, outs):
+                if not torch.equal(x, o):
+                    raise RuntimeError("fixed-codebook decode differs")
+            fixed_bits = sum(st.total_bits() for st in streams)
+            container = sum(_lib.huff_container_size(x.numel(), chunk, st.total_bits(), False)
+                            for x, st in zip(shards, streams))
+            res[str(chunk)] = {"encode_gbs": round(n / enc / 1e6, 1), "decode_gbs": round(n / dec / 1e6, 1),
+                               "pipelined": {"encode_gbs": round(n / enc_p / 1e6, 1),
+                                             "decode_gbs": round(n / dec_p / 1e6, 1)},
+                               "container_ratio": round(n / container, 4)}
+            del streams, outs
         shard_bits, nh = 0, 0.0
-        for x in shards:
+        for x in shards:  # per-shard Huffman of each shard, through the library's own statistics
             h = codec.histogram(x).cpu().numpy().astype(np.uint64)
             ln = codec.build_codebook(torch.from_numpy(h.astype(np.int64)).cuda()).lengths()
-            shard_bits += oracle.total_bits(h, ln)
-            nh += oracle.entropy(h) * x.numel()
+            st_ = _lib.huff_code_stats(h, ln)
+            shard_bits += st_["total_bits"]
+            nh += st_["entropy_bits"] * x.numel()
+        first = res[str(args.chunk)]
         out.update({"elements": n, "shards": len(shards), "chunk_bytes": args.chunk,
-                    "encode_gbs": round(n / enc / 1e6, 1), "decode_gbs": round(n / dec / 1e6, 1),
-                    "pipelined": {"encode_gbs": round(n / enc_p / 1e6, 1), "decode_gbs": round(n / dec_p / 1e6, 1),
-                                  "how": "the 64 shard calls back to back, statuses read once at the end"},
+                    "encode_gbs": first["encode_gbs"], "decode_gbs": first["decode_gbs"],
+                    "pipelined": dict(first["pipelined"],
+                                      how="the 64 shard calls back to back, statuses read once at the end"),
+                    "picked_chunk": _lib.huff_pick_chunk(shards[0].numel()), "per_chunk_size": res,
                     "ratio": round(8 * n / fixed_bits, 4),
                     "gap_vs_per_shard_huffman": round((fixed_bits - shard_bits) / shard_bits, 5),
                     "gap_vs_entropy": round((fixed_bits - nh) / nh, 5)})
