@@ -4,8 +4,8 @@ With more than 448 chunk pairs per SM the decode runs one lane per chunk pair
 with the two planes decoded one after the other.  Three kernels cover that:
 the high plane decoded by table lookups (no 1-bit code), the high plane
 decoded as runs of its 1-bit code, and the same with x0 staged in shared
-memory (when x0 is given and the block's staging area fits; at 896 lanes per
-block it does not, and the run kernel without staging takes x0).  These tests
+memory (when x0 is given and the block's staging area fits, which it does up
+to the widest block, 896 lanes, next to the split low-plane table).  These tests
 size inputs (256-element chunks) to land in each, with ragged last chunks, a
 run symbol other than 0, long high-plane codes, and streams written by the
 oracle rather than by the GPU encoder.
@@ -58,7 +58,7 @@ def _round_trip(x1, x0):
 @pytest.mark.parametrize("lanes", [480, 832, 900])
 @pytest.mark.parametrize("delta", [True, False])
 def test_run_decoded_high_plane(lanes, delta):
-    """Snapshot delta (high plane with a 1-bit code for 0): the run kernels, staged x0 at <= 832 lanes."""
+    """Snapshot delta (high plane with a 1-bit code for 0): the run kernels (staged x0 with a delta)."""
     n = _n_for_lanes(lanes, 77)
     x0, x1 = _snapshot_like(n, lanes)
     if delta:
@@ -80,6 +80,32 @@ def test_table_decoded_high_plane(lanes):
     assert 1 not in s.cb_hi.lengths().astype(int).tolist()
     x0 = (torch.randn(n, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
     _round_trip(w, x0)  # a delta of unrelated tensors: no 1-bit code either
+
+
+@pytest.mark.parametrize("run_high", [True, False])
+def test_low_plane_windows_past_the_split_entry(run_high):
+    """A delta whose low plane has 2-bit codes (four symbols of about a quarter each, a thin tail, no
+    1-bit code): its 13-bit windows hold up to 6 symbols, more than the 4 a split table entry keeps,
+    so the rest go to the step's next lookup.  With a run-decoded high plane (staged x0) and with a
+    table-decoded one."""
+    n = _n_for_lanes(832, 123)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(31 + run_high)
+    main = torch.randint(0, 4, (n,), device="cuda", generator=g, dtype=torch.int32) * 17
+    tail = torch.randint(0, 256, (n,), device="cuda", generator=g, dtype=torch.int32)
+    lo = torch.where(torch.rand(n, device="cuda", generator=g) < 0.03, tail, main)
+    if run_high:  # 0 for about 98 % of elements: a 1-bit code
+        hi = torch.where(torch.rand(n, device="cuda", generator=g) < 0.02,
+                         torch.randint(0, 256, (n,), device="cuda", generator=g, dtype=torch.int32), 0)
+    else:  # spread over 40 values: no 1-bit code
+        hi = torch.randint(0, 40, (n,), device="cuda", generator=g, dtype=torch.int32)
+    d = ((hi << 8) | lo).to(torch.int16)
+    x0 = torch.randint(-32768, 32767, (n,), device="cuda", generator=g, dtype=torch.int32).to(torch.int16)
+    x1 = (d ^ x0).view(torch.bfloat16)
+    s = _round_trip(x1, x0.view(torch.bfloat16))
+    ln_lo = s.cb_lo.lengths().astype(int).tolist()
+    assert 1 not in ln_lo and ln_lo.count(2) >= 3  # the three-lookup steps, with 2-bit codes
+    assert (1 in s.cb_hi.lengths().astype(int).tolist()) == run_high
 
 
 def test_run_symbol_other_than_zero():
