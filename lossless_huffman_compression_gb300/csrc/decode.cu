@@ -643,8 +643,11 @@ __device__ __forceinline__ void fill_segment(PlaneDec &s, const uint8_t *p, size
 // a run costs no store at all.  One step takes at most one other code (it
 // starts with a 1 bit: the 1-bit code is 0; its symbol is stored as one byte)
 // and then the run of 1-bit codes after it: as many as the zero bits on top of
-// the buffer, up to the valid bits, the chunk's rest and the ring's room.  No
-// symbols are ever pending: st counts the symbols placed.
+// the buffer, up to the valid bits, the chunk's rest and the ring's room; then
+// a second such round, when the next code is in the first-code table and
+// within the valid bits (a warp-level simulation of the snapshot's high plane:
+// 1.13 steps per 32-symbol segment instead of 1.81).  No symbols are ever
+// pending: st counts the symbols placed.
 
 // The run tables of a codebook with a 1-bit code (every thread of the block
 // takes part).
@@ -720,6 +723,22 @@ __device__ __forceinline__ void step_zrun(PlaneDec &s, const uint8_t *p, size_t 
     r = go ? r : 0;
     consume64(s, static_cast<uint32_t>(r));
     s.st += one + r;
+    // a second round: the next code (when the first-code table has it and it lies within the valid
+    // bits) and the run after it
+    const int rem2 = cnt - s.st, room2 = limit - s.st;
+    const bool go2 = go && rem2 > 0 && room2 > 0;
+    const bool top1 = static_cast<int32_t>(s.bh) < 0;
+    const uint32_t f2 = T.zf[s.bh >> (32 - kZWin)];
+    const uint32_t L2 = f2 >> 8;
+    const bool nz2 = go2 && top1 && L2 != 0 && static_cast<int>(L2) <= s.nb;
+    if (nz2) ring[(s.st & (RING - 1)) ^ swz] = static_cast<uint8_t>(f2 & 0xffu);
+    const int one2 = nz2 ? 1 : 0;
+    s.consume(nz2 ? L2 : 0u);
+    const uint32_t z2 = s.bh != 0 ? __clz(s.bh) : 32u + __clz(s.bl);
+    int r2 = min(min(static_cast<int>(z2), s.nb), min(rem2, room2) - one2);
+    r2 = (go2 && (nz2 || !top1)) ? r2 : 0;
+    consume64(s, static_cast<uint32_t>(r2));
+    s.st += one2 + r2;
 }
 
 // Steps until every lane of the warp has placed symbols [.., need).
