@@ -439,7 +439,7 @@ int lmc_encode_bf16(const uint16_t *w, const uint16_t *x0, size_t n,
 
 /*
  * lmc_count_segment -- S, the elements per counted segment for n elements on
- * the current device: HUFF_COUNT_SEGMENT while the counted encode's warps (16
+ * the current device: HUFF_COUNT_SEGMENT while the counted encode's warps (20
  * per SM) outnumber segments of that size; otherwise the multiple of 512 in
  * [HUFF_COUNT_SEGMENT, 2 * HUFF_COUNT_SEGMENT) that gives every warp the same
  * number of segments.  lmc_histogram_bf16_counted and lmc_encode_bf16_counted

@@ -92,11 +92,11 @@ def test_counted_matches_oracle_and_two_pass(n, delta, chunk):
     assert torch.equal(back.view(torch.int16).cpu(), x1.view(torch.int16))
 
 
-def _enc_warps():
-    return torch.cuda.get_device_properties(0).multi_processor_count * 16
+def _enc_warps():  # the counted encode: one CTA of 20 warps per SM
+    return torch.cuda.get_device_properties(0).multi_processor_count * 20
 
 
-@pytest.mark.parametrize("n", [0, 1, SEG, 318_767_103, 318_767_104, 400_000_003, 2_000_027_648, 1 << 34])
+@pytest.mark.parametrize("n", [0, 1, SEG, 398_458_879, 398_458_880, 400_000_003, 2_000_027_648, 1 << 34])
 def test_count_segment_gives_every_encode_warp_the_same_rounds(n):
     """lmc_count_segment: SEG while the encode's warps outnumber SEG-element segments; otherwise the
     smallest whole number of 512-element tiles that splits the input into at most warps x rounds
@@ -111,8 +111,8 @@ def test_count_segment_gives_every_encode_warp_the_same_rounds(n):
     assert S % 512 == 0 and SEG <= S < 2 * SEG
     st = S // 512
     assert -(-tiles // st) <= warps * rounds < -(-tiles // (st - 1))
-    if n == 2_000_027_648 and warps == 152 * 16:
-        assert S == 268 * 512 and -(-n // S) == 14576  # 6 rounds of 2432 warps, 16 warps idle in the last
+    if n == 2_000_027_648 and warps == 152 * 20:
+        assert S == 257 * 512 and -(-n // S) == 15200  # exactly 5 rounds of 3040 warps
 
 
 def test_counted_segments_above_the_least_size():
