@@ -1198,11 +1198,17 @@ __device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uin
             fill_pair<kRing>(h, l, pay_hi, bytes_hi, pay_lo, bytes_lo, Th, Tl, hring, lring, swz, cnt, need, seg0 + kRing,
                              bad);
         } else {
+            // the high plane as runs (ZR >= 1) or by three-lookup steps (ZR == 0: no 1-bit code, the kernel's
+            // case); the low plane by three-lookup steps in every case (a 1-bit code there is decoded correctly
+            // by its table entries, only without the run shortcut), so each kernel holds one fill loop per plane
             if constexpr (zrun)
                 fill_zrun<kRing>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
             else
-                fill_segment<kRing, false, true>(h, pay_hi, bytes_hi, Th, hring, swz, cnt, need, seg0 + kRing, bad);
-            fill_segment<kRing, false, true>(l, pay_lo, bytes_lo, Tl, lring, swz, cnt, need, seg0 + kRing, bad);
+                fill_segment_t<kRing, false, 12, false, kSecMax, true, false>(h, pay_hi, bytes_hi, Th, hring, swz, cnt,
+                                                                            need, seg0 + kRing, bad);
+            fill_segment_t<kRing, false, 13, false, zrun ? kSecRun : kSecMax, true, true>(l, pay_lo, bytes_lo, Tl, lring,
+                                                                                         swz, cnt, need, seg0 + kRing,
+                                                                                         bad);
         }
         __syncwarp();
         if (whole && seg0 + kSeg <= warp_cnt) {
