@@ -1177,7 +1177,9 @@ __device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uin
     // x0 staging (warp-uniform): the warp's 2 KiB area, lane q's chunk at 64 q (32-bit shared addresses),
     // filled by each lane's own asynchronous 16-byte copies; xf: staging in use
     const uint32_t xst = stage ? smem_u32(stage_base) + (threadIdx.x - lane) * kStageLane : 0u;
-    bool xf = stage && whole && warp_cnt >= kSeg;
+    // (a warp past the last chunk has every count 0 and is whole too: it stages nothing; inside the
+    // full-segment merge below, where warp_cnt >= kSeg, xf is exactly `stage`)
+    const bool xf = stage && whole && warp_cnt >= kSeg;
     const auto stage_issue = [&](int seg) {  // x0 of segment [seg, seg + kSeg) of this lane's chunk
         const uint16_t *src = x0 + c * chunk + seg;
 #pragma unroll
@@ -1217,21 +1219,19 @@ __device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uin
             const size_t gs = 8 * chunk;
             const int q0 = lane >> 2;
             uint4 xv[4];
-            bool staged = false;
-            if (stage && xf) {
+            if constexpr (stage) {  // whole: the staging is in use (xf)
                 // this lane's copies have landed (issued a segment's decode ago); then every lane's
                 asm volatile("cp.async.wait_all;" ::: "memory");
                 __syncwarp();
-                staged = true;
-            }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (staged)
+                for (int i = 0; i < 4; ++i)
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(xv[i].x), "=r"(xv[i].y), "=r"(xv[i].z), "=r"(xv[i].w)
                                  : "r"(xst + (8 * i + q0) * kStageLane + 16 * (lane & 3))
                                  : "memory");
-                else
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
                     xv[i] = XOR ? __ldcs(reinterpret_cast<const uint4 *>(x0 + g0 + i * gs)) : make_uint4(0, 0, 0, 0);
             }
             const uint32_t o = ((seg0 + 8 * (lane & 3)) & (kRing - 1)) ^ ((q0 & 2) ? kRing / 2 : 0);
@@ -1250,7 +1250,7 @@ __device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uin
                 v.w ^= xv[i].w;
                 __stcs(reinterpret_cast<uint4 *>(out + g0 + i * gs), v);
             }
-            if (stage && xf && seg0 + 2 * kSeg <= warp_cnt) {
+            if (stage && seg0 + 2 * kSeg <= warp_cnt) {
                 // every lane has read its staged x0 (the values fed the stores above): refill the area
                 __syncwarp();
                 stage_issue(seg0 + kSeg);
