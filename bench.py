@@ -1010,10 +1010,10 @@ def relaunch_ranks(n: int) -> int:
     return subprocess.call(cmd)
 
 
-# The snapshot's chunk: 2.0e9 elements in 134 699 chunk pairs, 896-lane decode blocks (the widest whose x0
-# staging fits in shared memory; 7 warps per scheduler) on 151 SMs; huff_pick_chunk's choice for this size
-# with a delta.
-SNAPSHOT_CHUNK = 14848
+# The snapshot's chunk: 2.0e9 elements in 136 168 chunk pairs, 896-lane decode blocks (the widest whose x0
+# staging fits in shared memory; 7 warps per scheduler) on all 152 SMs; huff_pick_chunk's choice for this
+# size with a delta.
+SNAPSHOT_CHUNK = 14688
 
 
 def main():

@@ -69,7 +69,8 @@ typedef enum huff_status {
 #define HUFF_MAX_LEN 24          /* longest code the library produces or accepts */
 #define HUFF_MIN_MAX_LEN 8       /* smallest length limit that fits 256 symbols */
 #define HUFF_COVER_ALL 1u        /* raise zero counts to 1 before building (fixed codebooks) */
-#define HUFF_CHUNK_ALIGN 256     /* chunk_bytes must be a positive multiple of this */
+#define HUFF_CHUNK_ALIGN 32      /* chunk_bytes must be a positive multiple of this (the encode's lanes
+                                    take 32 byte-stream symbols or 16 bf16 elements of a tile) */
 #define HUFF_MAX_CHUNK (1u << 30) /* and at most this: a chunk's symbol count fits an int with room */
 #define HUFF_ALIGN 16            /* alignment (bytes) required of bulk device buffers */
 #define HUFF_LUT_BITS 12         /* first-level decode table index width */

@@ -30,7 +30,7 @@ HUFF_ERR_CUDA = -6
 HUFF_ERR_INVALID_CODEBOOK = -7
 HUFF_MAX_LEN = 24
 HUFF_COVER_ALL = 1
-HUFF_CHUNK_ALIGN = 256
+HUFF_CHUNK_ALIGN = 32
 HUFF_CODEBOOK_MAGIC = 0x48554642
 HUFF_NOALLOC_MAX_SYMBOLS = 1 << 30
 HUFF_COUNT_SEGMENT = 131072

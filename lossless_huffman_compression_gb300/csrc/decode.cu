@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
                     rings + sl * kRingU8 + ((e0 & (kRingU8 - 1)) ^ ((sl & 1) ? kRingU8 / 2 : 0));
                 uint8_t *dst = out + (c0 + sl) * chunk + e0;
                 const uint4 v = *reinterpret_cast<const uint4 *>(src);
-                if (e0 + 16 <= cs) {  // out is 16-byte aligned and chunk a multiple of 256
+                if (e0 + 16 <= cs) {  // out is 16-byte aligned and chunk a multiple of 32
                     __stcs(reinterpret_cast<uint4 *>(dst), v);
                 } else {
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -1281,7 +1281,7 @@ __device__ __forceinline__ void decode_bf16_body(const TH &Th, const TL &Tl, uin
                     uint4 v = make_uint4(__byte_perm(lv.x, hv.x, 0x5140), __byte_perm(lv.x, hv.x, 0x7362),
                                          __byte_perm(lv.y, hv.y, 0x5140), __byte_perm(lv.y, hv.y, 0x7362));
                     const size_t g = (c0 + q) * chunk + e0;  // first element of this group
-                    if (e0 + 8 <= cs) {  // x0 and out are 16-byte aligned, chunk a multiple of 256
+                    if (e0 + 8 <= cs) {  // x0 and out are 16-byte aligned, chunk a multiple of 32
                         v.x ^= xv[i].x;
                         v.y ^= xv[i].y;
                         v.z ^= xv[i].z;

@@ -125,8 +125,9 @@ __device__ uint64_t lookback(const uint64_t *desc, uint32_t t, int lane, int32_t
 }
 
 
-// The chunk size, as the encode kernels take it (chunks are multiples of 256
-// elements, so a chunk starts at the first symbol of some lane's group).
+// The chunk size, as the encode kernels take it (chunks are multiples of 32
+// symbols, so a chunk starts at the first symbol of some lane's group: 16
+// bf16 elements or 32 byte-stream symbols a lane).
 struct ChunkDiv {
     uint32_t chunk;  // < 2^31
 };
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(wenc::kThreads, 1)
             const uint32_t excl = incl - mine;
             const uint32_t ex0 = excl >> 16, ex1 = excl & 0xffffu, tot0 = tot >> 16, tot1 = tot & 0xffffu;
 
-            // chunk starts in this tile (chunks are multiples of 256 elements, so a chunk starts
+            // chunk starts in this tile (chunks are multiples of 32 elements, so a chunk starts
             // at the first element of some lane)
             if (to_next < wenc::kTile) {
                 do {

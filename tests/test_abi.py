@@ -76,7 +76,7 @@ def test_binding_fails_loudly_without_library(lib, tmp_path):
 
 
 def test_chunk_size_limits_rejected_before_any_device_work(lib):
-    """chunk_bytes must be a positive multiple of 256 and at most 2^30 (a chunk's symbol count
+    """chunk_bytes must be a positive multiple of 32 and at most 2^30 (a chunk's symbol count
     stays an int with room for the decoder's ring arithmetic).  Argument checks come before
     any CUDA call, so rejected calls run here without a GPU; the pointers are aligned
     placeholders that a rejected call never touches."""

@@ -83,7 +83,7 @@ def test_damaged_containers_are_rejected(lib):
     bad(lambda b: struct.pack_into("<H", b, 6, 3))                 # unknown flag
     bad(lambda b: struct.pack_into("<I", b, 12, 1))                # reserved field
     bad(lambda b: struct.pack_into("<Q", b, 32, 4))                # chunk count
-    bad(lambda b: struct.pack_into("<Q", b, 24, 1000))             # chunk size not a multiple of 256
+    bad(lambda b: struct.pack_into("<Q", b, 24, 1000))             # chunk size not a multiple of 32
     bad(lambda b: b.__setitem__(48 + 7, 25))                       # a length above max_len
     bad(lambda b: struct.pack_into("<Q", b, 48 + 256 + 8, 1 << 40))  # offsets not rising to T
     bad(lambda b: b.pop())                                         # truncated

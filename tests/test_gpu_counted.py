@@ -55,7 +55,7 @@ def _counted(dx1, dx0, chunk, cb_hi=None, cb_lo=None):
 
 @pytest.mark.parametrize("n", [1, 8, 4097, SEG - 1, SEG, SEG + 1, 3 * SEG + 4097, 1_000_003])
 @pytest.mark.parametrize("delta", [False, True])
-@pytest.mark.parametrize("chunk", [256, 16384])
+@pytest.mark.parametrize("chunk", [96, 256, 16384])
 def test_counted_matches_oracle_and_two_pass(n, delta, chunk):
     rng = np.random.default_rng(n * 2 + delta)
     x0, x1 = _pair(n, rng)

@@ -63,7 +63,7 @@ def test_one_lane_per_chunk_path(kind):
     _round_trip(x, cb, chunk)
 
 
-@pytest.mark.parametrize("n,chunk", [(1, 256), (1000, 256), (65_536, 65_536), (65_537, 65_536),
+@pytest.mark.parametrize("n,chunk", [(1, 256), (1000, 256), (1000, 32), (100_003, 96), (65_536, 65_536), (65_537, 65_536),
                                      (1_000_003, 1 << 20), (3_000_001, 1 << 22), (200_017, 16_384),
                                      (2_000_001, 1 << 30)])  # the largest chunk the ABI accepts
 def test_split_path_matches_oracle_payload(n, chunk):

@@ -164,7 +164,7 @@ SIZES = [1, 2, 100, 8191, 8192, 8193, 3 * 8192 + 123, 65536 + 4096 + 17, 300_001
 
 @pytest.mark.parametrize("n", SIZES)
 @pytest.mark.parametrize("kind", ["gauss", "uniform", "single", "skew"])
-@pytest.mark.parametrize("chunk", [256, 4096, 16384])
+@pytest.mark.parametrize("chunk", [32, 96, 256, 4064, 4096, 16384])  # multiples of 32, some not of 64
 def test_encode_decode_bit_exact(n, kind, chunk):
     x = _data(kind, n)
     h = oracle.histogram(x)
@@ -317,7 +317,7 @@ def test_host_side_argument_errors():
     cb = codec.build_codebook(codec.histogram(dev_u8(np.arange(256, dtype=np.uint8))))
     x = dev_u8(np.zeros(4096, np.uint8))
     with pytest.raises(_lib.HuffError) as e:
-        codec.encode(x, cb, 1000)          # chunk not a multiple of 256
+        codec.encode(x, cb, 1000)          # chunk not a multiple of 32
     assert e.value.status == _lib.HUFF_ERR_INVALID_ARG
     with pytest.raises(_lib.HuffError):
         codec.encode(x[1:], cb, 4096)      # misaligned input
@@ -369,7 +369,7 @@ def _bf16_pair(n, rng):
 
 @pytest.mark.parametrize("n", [1, 8, 4095, 4096, 4097, 3 * 4096 + 77, 100_001])
 @pytest.mark.parametrize("delta", [False, True])
-@pytest.mark.parametrize("chunk", [256, 16384])
+@pytest.mark.parametrize("chunk", [96, 256, 14688, 16384])  # 96 and 14 688 are multiples of 32, not of 256
 def test_fused_bf16_matches_split_then_encode(n, delta, chunk):
     rng = np.random.default_rng(n + delta)
     x0, x1 = _bf16_pair(n, rng)
