@@ -143,9 +143,10 @@ size_t huff_num_chunks(size_t n, size_t chunk_bytes);
  * for the decode that will run (delta != 0: lmc_decode_bf16 with x0, whose x0
  * staging takes shared memory; L = 896 either way on a GPU with 227 KiB of
  * shared memory per block).  This returns the smallest multiple of
- * HUFF_CHUNK_ALIGN that gives at most L chunks per SM (at least
- * HUFF_CHUNK_ALIGN, at most HUFF_MAX_CHUNK), so that one wave of blocks of
- * nearly L lanes covers the input on every SM.  (The chunk size is the
+ * HUFF_CHUNK_ALIGN that gives at most L chunks per SM (at least 256, so that
+ * the offsets, 8 bytes a chunk, stay within 1/32 of the symbols; at most
+ * HUFF_MAX_CHUNK), so that one wave of blocks of nearly L lanes covers the
+ * input on every SM.  (The chunk size is the
  * caller's choice on the pages' format; each chunk costs 8 bytes of offset
  * per stream.)  Returns 0 when the device cannot be queried.
  */

@@ -51,6 +51,8 @@ size_t huff_num_chunks(size_t n, size_t chunk_bytes) {
     return (n + chunk_bytes - 1) / chunk_bytes;
 }
 
+constexpr size_t kPickChunkMin = 256;
+
 size_t huff_pick_chunk(size_t n, int delta) {
     int dev = 0, sms = 0, smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -62,7 +64,7 @@ size_t huff_pick_chunk(size_t n, int delta) {
     const size_t lanes = static_cast<size_t>(sms) * static_cast<size_t>(decode_lanes(smem, delta != 0));
     size_t c = (n + lanes - 1) / lanes;
     c = (c + HUFF_CHUNK_ALIGN - 1) / HUFF_CHUNK_ALIGN * HUFF_CHUNK_ALIGN;
-    if (c < HUFF_CHUNK_ALIGN) c = HUFF_CHUNK_ALIGN;
+    if (c < kPickChunkMin) c = kPickChunkMin;  // offsets (8 bytes a chunk) stay within 1/32 of the symbols
     return c > HUFF_MAX_CHUNK ? HUFF_MAX_CHUNK : c;
 }
 

@@ -162,17 +162,17 @@ def test_corrupt_stream_is_reported_by_the_run_kernels():
 @pytest.mark.parametrize("delta", [True, False])
 @pytest.mark.parametrize("n", [0, 1, 1 << 20, 1 << 26, 536_870_912, 2_000_027_648, 1 << 36])
 def test_pick_chunk_gives_one_wave_of_full_blocks(n, delta):
-    """huff_pick_chunk: the smallest multiple of 32 that gives at most L chunks per SM, L the widest
-    decode block (896 lanes with or without a delta on a GPU with 227 KiB of shared memory per block:
-    the x0 staging fits next to the split low-plane table)."""
+    """huff_pick_chunk: the smallest multiple of 32, at least 256, that gives at most L chunks per SM, L
+    the widest decode block (896 lanes with or without a delta on a GPU with 227 KiB of shared memory per
+    block: the x0 staging fits next to the split low-plane table)."""
     c = _lib.huff_pick_chunk(n, delta)
     sms = _sms()
-    assert c % 32 == 0 and 32 <= c <= (1 << 30)
+    assert c % 32 == 0 and 256 <= c <= (1 << 30)
     if torch.cuda.get_device_properties(0).shared_memory_per_block_optin != 232448:
         pytest.skip("the lane count per SM is checked on a GPU with 227 KiB of shared memory per block")
     lanes = 896
     assert -(-n // c) <= sms * lanes
-    assert c == 32 or -(-n // (c - 32)) > sms * lanes  # the smallest such size
+    assert c == 256 or -(-n // (c - 32)) > sms * lanes  # the smallest such size
     if sms == 152 and (n, delta) in ((2_000_027_648, True), (536_870_912, False)):
         # the snapshot delta: 136 168 chunk pairs; the 1 GiB bf16 weights: 135 301; both in 896-lane blocks on
         # all 152 SMs
