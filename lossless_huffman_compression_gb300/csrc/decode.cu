@@ -9,10 +9,12 @@
 // GPU design:
 //   * one lane per chunk (per chunk pair for bf16), every lane of the grid
 //     resident at once; the block size follows the chunk count.  With fewer
-//     than 256 chunks per SM, byte streams instead split each chunk over a
-//     CTA by self-synchronisation (the section on few chunks below), and
-//     with at most 448 lanes per SM the fused bf16 decode steps both planes
-//     of a lane in one loop;
+//     than 768 chunks per SM, byte streams instead give each chunk a warp
+//     whose lanes take slices of its bits, and below 12 per SM a CTA whose
+//     threads do; both find the slices' code boundaries by
+//     self-synchronisation (the sections on fewer chunks below).  With at
+//     most 448 lanes per SM the fused bf16 decode steps both planes of a
+//     lane in one loop;
 //   * shared tables per plane: a window table of 2^W 64-bit entries (W = 12
 //     for the high plane, 13 for the low plane and byte streams), each
 //     listing the codes wholly inside the next W bits (up to six symbols,
@@ -1098,10 +1100,396 @@ __global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restr
     if (bad) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
+// ------------------------------------------------------------------ byte streams, a warp per chunk
+//
+// Between the two: chunks too few for one lane each, but enough for a warp
+// each.  A warp decodes its chunk in rounds of 32 slices of B bits, one per
+// lane.  Each slice is walked once from its first bit, which need not be a
+// code boundary (Huffman codes are self-synchronising: a walk started
+// anywhere falls onto the true boundaries within a few codes, as Klein and
+// Wiseman's parallel decoding and Weissenberger and Schmidt's GPU decoder
+// use).  The walk stages the symbols of the codes that start in the slice in
+// the lane's area of shared memory, and notes where its first kWsList table
+// steps start and how many symbols came before each.  Then each lane goes on
+// past its slice's end, one code at a time, until a code starts where a
+// noted step of the next slice starts: from there on the two walks are the
+// same, so once this slice is exact the next one is exact from that step,
+// and the codes in between are this slice's (staged after its own).  The
+// walk that reaches no noted step (about one slice in a few thousand on the
+// data measured) leaves the next slice to be walked again from this slice's
+// exit; its own end may then move, so the slice after it checks again, at
+// most 32 passes (slice 0 starts on the round's exact entry, and pass i
+// makes slice i exact).  A warp scan of the slices' counts places each
+// slice's symbols, which each lane copies from its area to the output.
+// B follows the chunk's mean code length so that a slice holds about
+// kWsTarget symbols; a slice with more than its area holds (a skewed part of
+// a chunk) is decoded once more from its entry, writing straight to the
+// output.  Slices start on multiples of the code lengths' greatest common
+// divisor from the chunk's start, as in the split decode.
+// A CTA per SM of kWsWarps warps shares one copy of the tables; its warps
+// take chunks blockIdx.x, blockIdx.x + gridDim.x, ... (interleaved, so every
+// CTA meets every part of the input alike) from a shared counter, a chunk at
+// a time, so warps that drew cheap chunks take more of them.
+constexpr int kWsWarps = 28;              // warps per CTA (7 per scheduler)
+constexpr int kWsStage = 84;              // staged symbols per slice
+constexpr int kWsStride = kWsStage + 4;   // bytes between two lanes' areas (22 words: lanes' columns spread over the banks)
+constexpr int kWsTarget = 56;             // symbols a slice is sized for
+constexpr int kWsList = 24;               // steps noted per walk
+static_assert(kWsStage % 4 == 0 && 4 * kWsList <= 255, "staging geometry");
+constexpr size_t kWsWarpBytes = 32 * (kWsStride + 3 * kWsList);  // a warp's areas and step notes
+
+__host__ size_t ws_smem() { return sizeof(U8Tables) + static_cast<size_t>(kWsWarps) * kWsWarpBytes + 16; }
+
+// A lane's step notes: where its first walk's first kWsList steps start
+// (relative to the slice's first bit) and the symbols before each; entry i
+// of lane l at i * 32 + l.
+struct WsNotes {
+    uint16_t *pos;
+    uint8_t *cnt;
+};
+
+// The first code of the window: its symbol and length (length 0 when the bits are no code).
+__device__ __forceinline__ void ws_code(const PlaneDec &s, const U8Tables &T, uint32_t &L, uint32_t &sym) {
+    const uint32_t win = s.bh >> (32 - 13);
+    uint64_t v;
+    uint32_t c, bits;
+    lut_get(T, win, v, c, bits);
+    if (c != 0) {
+        sym = static_cast<uint32_t>(v) & 0xffu;
+        L = T.len[sym];
+        return;
+    }
+    L = 0;
+    sym = 0;
+    if (T.sec_ok) {
+        if (T.sec_k > 0 && static_cast<int>(win) >= T.sec_first) {
+            const int k = T.sec_k;
+            const uint32_t e2 = T.sec[((win - static_cast<uint32_t>(T.sec_first)) << k) |
+                                      ((s.bh >> (32 - 13 - k)) & ((1u << k) - 1u))];
+            L = e2 >> 8;
+            sym = e2 & 0xffu;
+        }
+    } else {
+        const uint32_t lc = long_code(s.bh, &T);
+        L = lc >> 8;
+        sym = lc & 0xffu;
+    }
+}
+
+// One walk over [pos, lim) (positions relative to the round's entry; lo = the
+// slice's first bit): the count of the codes that start in it, and their
+// symbols: staged (the first kWsStage; NOTE: with the first kWsList steps
+// noted) or, DIRECT, written to dst[0, room).  pos ends at the walk's exit;
+// badpos is the last position (relative to lo) where the bits were no code.
+template <bool DIRECT, bool NOTE>
+__device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, size_t nbytes, const U8Tables &T,
+                                         uint32_t &pos, uint32_t lo, uint32_t lim, uint8_t *stg, WsNotes nt,
+                                         int &nsteps, int &badpos, uint8_t *dst, uint64_t room) {
+    PlaneDec s = s_io;  // a private copy, so that the stores below cannot alias the reader's state
+    const int seck = T.sec_k, secf = T.sec_first;
+    const bool use_sec = T.sec_ok;
+    uint32_t n = 0;
+    uint32_t a = 0;  // pending staged bytes (fewer than 4)
+    int fill = 0, st = 0, steps = 0;
+    WordOut wo;
+    if (DIRECT) wo.init(dst, room);
+    while (pos < lim) {
+        s.refill(p, nbytes);
+        const uint32_t win = s.bh >> (32 - 13);
+        uint64_t v;
+        uint32_t c, bits;
+        lut_get(T, win, v, c, bits);
+        if (NOTE && steps < kWsList) {
+            nt.pos[steps * 32] = static_cast<uint16_t>(pos - lo);
+            nt.cnt[steps * 32] = static_cast<uint8_t>(n);
+        }
+        ++steps;
+        // a code longer than the window: the secondary table's entry, looked up on every step (a
+        // predicated load rather than a branch that splits the warp where long and short codes mix)
+        uint32_t L2 = 0, sym2 = 0;
+        if (use_sec) {
+            const bool inr = seck > 0 && static_cast<int>(win) >= secf;
+            const uint32_t idx =
+                inr ? ((win - static_cast<uint32_t>(secf)) << seck) | ((s.bh >> (32 - 13 - seck)) & ((1u << seck) - 1u))
+                    : 0u;
+            const uint32_t e2 = T.sec[idx];
+            L2 = inr ? e2 >> 8 : 0u;
+            sym2 = e2 & 0xffu;
+        } else if (c == 0) {
+            const uint32_t lc = long_code(s.bh, &T);
+            L2 = lc >> 8;
+            sym2 = lc & 0xffu;
+        }
+        const bool lng = c == 0;
+        if (lng && L2 == 0) badpos = static_cast<int>(pos - lo);  // no code
+        v = lng ? sym2 : v;
+        bits = lng ? max(L2, 1u) : bits;
+        c = lng ? 1u : c;
+        if (c > 1 && pos + bits > lim) {  // codes past lim in the entry: only the first starts before it
+            v &= 0xffu;
+            c = 1;
+            bits = T.len[v];
+        }
+        bits = max(bits, 1u);  // only a corrupt codebook has a zero-length entry: every step moves on
+        if (DIRECT) {
+            wo.put(v, c);
+        } else {
+            const uint32_t sh = 8u * static_cast<uint32_t>(fill);
+            const uint32_t vl = static_cast<uint32_t>(v);
+            const uint32_t w0 = a | (vl << sh);
+            const int nf = fill + static_cast<int>(c);  // <= 7: at most one word completes
+            if (nf >= 4 && st + 4 <= kWsStage) *reinterpret_cast<uint32_t *>(stg + st) = w0;
+            a = nf >= 4 ? __funnelshift_l(vl, 0u, sh) : w0;  // the bytes past the completed word
+            st += nf >= 4 ? 4 : 0;
+            fill = nf & 3;
+        }
+        n += c;
+        pos += bits;
+        s.consume(bits);
+    }
+    if (DIRECT)
+        wo.finish();
+    else if (fill > 0 && st + 4 <= kWsStage)
+        *reinterpret_cast<uint32_t *>(stg + st) = a;
+    nsteps = min(steps, kWsList);
+    s_io = s;
+    return n;
+}
+
+// From the walk's exit pos (the reader is there), codes one at a time until
+// one starts where a noted step of the next slice starts (npos: its notes,
+// nns of them, relative to its first bit nlo): returns that step, or -1 when
+// the codes pass its last note.  The codes' symbols are staged from stg[n]
+// on, m of them; pb notes bits that are no code.
+__device__ __forceinline__ int ws_over(PlaneDec &s_io, const uint8_t *p, size_t nbytes, const U8Tables &T, uint32_t pos,
+                                    uint32_t nlo, const uint16_t *npos, int nns, uint8_t *stg, uint32_t n,
+                                    uint32_t &m, bool &pb) {
+    PlaneDec s = s_io;
+    int j = 0;
+    m = 0;
+    for (;;) {
+        const uint32_t d = pos - nlo;
+        while (j < nns && npos[j * 32] < d) ++j;
+        if (j == nns) break;
+        if (npos[j * 32] == d) {
+            s_io = s;
+            return j;
+        }
+        s.refill(p, nbytes);
+        uint32_t L, sym;
+        ws_code(s, T, L, sym);
+        if (L == 0) {
+            pb = true;
+            L = 1;
+        }
+        if (n + m < static_cast<uint32_t>(kWsStage)) stg[n + m] = static_cast<uint8_t>(sym);
+        ++m;
+        pos += L;
+        s.consume(L);
+    }
+    s_io = s;
+    return -1;
+}
+
+// Bytes stg[from, from + len) to dst[0, len): 4-byte stores between a head
+// and a tail of single bytes.  Reads stay below from + len rounded up to a
+// word, plus one word (the area's padding).
+__device__ __forceinline__ void ws_copy(const uint8_t *stg, uint32_t from, uint32_t len, uint8_t *dst) {
+    const uint32_t head = min(len, (4u - static_cast<uint32_t>(reinterpret_cast<uintptr_t>(dst) & 3u)) & 3u);
+    uint32_t i = 0;
+    for (; i < head; ++i) dst[i] = stg[from + i];
+    for (; i + 4 <= len; i += 4) {
+        const uint32_t at = from + i, wa = at & ~3u;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(stg + wa);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(stg + wa + 4);
+        *reinterpret_cast<uint32_t *>(dst + i) = __funnelshift_r(w0, w1, 8u * (at & 3u));
+    }
+    for (; i < len; ++i) dst[i] = stg[from + i];
+}
+
+__global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t *__restrict__ payload, size_t nbytes,
+                                                                  const uint64_t *__restrict__ off, size_t n,
+                                                                  size_t chunk, const huff_codebook *__restrict__ cb,
+                                                                  uint8_t *__restrict__ out, int32_t *status) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    U8Tables &T = *reinterpret_cast<U8Tables *>(dsm);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *const wbase = dsm + sizeof(U8Tables) + static_cast<size_t>(warp) * kWsWarpBytes;
+    uint8_t *const stg = wbase + lane * kWsStride;
+    WsNotes nt;
+    nt.pos = reinterpret_cast<uint16_t *>(wbase + 32 * kWsStride) + lane;
+    nt.cnt = wbase + 32 * kWsStride + 32 * 2 * kWsList + lane;
+    int *next = reinterpret_cast<int *>(dsm + sizeof(U8Tables) + static_cast<size_t>(kWsWarps) * kWsWarpBytes);
+    load_table_a(T, cb);
+    if (threadIdx.x == 0) *next = 0;
+    __syncthreads();
+    load_table_b(T, cb);
+    __syncthreads();
+    if (!T.ok) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, HUFF_ERR_INVALID_CODEBOOK);
+        return;
+    }
+    // g: the greatest common divisor of the code lengths
+    uint32_t g = 0;
+    for (int l = 1; l <= T.longest; ++l) {
+        if (T.bl_count[l] == 0) continue;
+        uint32_t x = static_cast<uint32_t>(l), y = g;
+        while (y) {
+            const uint32_t t = x % y;
+            x = y;
+            y = t;
+        }
+        g = x;
+    }
+    if (g == 0) g = 1;
+    const size_t n_chunks = (n + chunk - 1) / chunk;
+    bool bad = false;
+    for (;;) {
+        int jc = 0;
+        if (lane == 0) jc = atomicAdd(next, 1);
+        jc = __shfl_sync(0xffffffffu, jc, 0);
+        const size_t c = blockIdx.x + static_cast<size_t>(jc) * gridDim.x;
+        if (c >= n_chunks) break;
+        const size_t first = c * chunk;
+        const int cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
+        uint64_t start = 0, end = 0;
+        if (!chunk_bounds(off, c, nbytes, cnt, start, end)) {
+            if (lane == 0) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+            continue;
+        }
+        // slice length: about kWsTarget symbols at the chunk's mean code length, at least 32 bits, a multiple of g
+        uint32_t B = static_cast<uint32_t>((end - start) * kWsTarget / static_cast<uint64_t>(cnt));
+        B = max(B, 32u);
+        B = (B + g - 1) / g * g;
+        uint8_t *const dst0 = out + first;
+        uint64_t entry = start, written = 0;
+        while (entry < end) {
+            const uint64_t left = end - entry;
+            const uint32_t rlen = left < 32ull * B ? static_cast<uint32_t>(left) : 32u * B;
+            const uint32_t lo = static_cast<uint32_t>(lane) * B;
+            const uint32_t hi = lane == 31 ? rlen : min(lo + B, rlen);
+            const bool act = lo < rlen;
+            const int last = static_cast<int>((rlen - 1) / B);  // the last slice with bits
+            const bool has_next = lane < last;
+            PlaneDec s;
+            uint32_t ex = lo, cntw = 0;
+            int ns = 0, badpos = -1;
+            if (act) {
+                s.start(payload, nbytes, entry + lo);
+                cntw = ws_walk<false, true>(s, payload, nbytes, T, ex, lo, hi, stg, nt, ns, badpos, nullptr, 0);
+            }
+            __syncwarp();  // every lane's notes are in place
+            const int ns_next = __shfl_down_sync(0xffffffffu, ns, 1);
+            // past the slice's end until the next slice's walk is met
+            uint32_t m = 0;
+            bool pb = false;
+            int met = -1;
+            if (has_next) met = ws_over(s, payload, nbytes, T, ex, hi, nt.pos + 1, ns_next, stg, cntw, m, pb);
+            // each slice's entry: from the previous slice's meeting step (M), or walked again from its exit (R)
+            uint32_t skip = 0, ent = lo, seen_e = 0xffffffffu;
+            int seen_met = -2;
+            bool first_walk = true, used_m = false, own_bad = false, settled = false;
+            for (int pass = 0; pass <= 32; ++pass) {
+                uint32_t e = __shfl_up_sync(0xffffffffu, ex, 1);
+                int mp = __shfl_up_sync(0xffffffffu, met, 1);
+                if (lane == 0) {
+                    e = 0;
+                    mp = 0;  // slice 0 starts on the round's entry, its first noted step
+                }
+                const bool todo = act && (e != seen_e || mp != seen_met);
+                settled = !__any_sync(0xffffffffu, todo);
+                if (settled) break;
+                if (!todo) continue;
+                seen_e = e;
+                seen_met = mp;
+                if (e >= hi) {  // no code starts in the slice (only the last one can be this short)
+                    skip = cntw;
+                    ent = e;
+                    used_m = false;
+                    own_bad = false;
+                    continue;
+                }
+                if (mp >= 0 && first_walk) {
+                    skip = nt.cnt[mp * 32];
+                    ent = lo + nt.pos[mp * 32];
+                    used_m = true;
+                    own_bad = badpos >= static_cast<int>(ent - lo);
+                    continue;
+                }
+                // walk the slice again from its exact entry, then past its end again
+                s.start(payload, nbytes, entry + e);
+                ex = e;
+                badpos = -1;
+                int n2 = 0;
+                cntw = ws_walk<false, false>(s, payload, nbytes, T, ex, lo, hi, stg, nt, n2, badpos, nullptr, 0);
+                skip = 0;
+                ent = e;
+                used_m = false;
+                first_walk = false;
+                own_bad = badpos >= 0;
+                pb = false;
+                met = has_next ? ws_over(s, payload, nbytes, T, ex, hi, nt.pos + 1, ns_next, stg, cntw, m, pb) : -1;
+            }
+            if (!settled) bad = true;  // cannot happen: pass i makes slice i exact
+            // this slice's codes past its end are its own when the next slice starts at the meeting step
+            const bool next_m = __shfl_down_sync(0xffffffffu, used_m, 1) && has_next;
+            if (act && (own_bad || (next_m && pb))) bad = true;
+            const uint32_t own = act ? cntw - skip : 0u;
+            const uint32_t cw = own + (next_m ? m : 0u);
+            const bool thru = act && ent >= hi;
+            const uint32_t rex = __shfl_sync(0xffffffffu, thru ? ent : ex, last);
+            uint32_t incl = cw;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+            const uint64_t o = written + (incl - cw);
+            uint32_t len = cw;
+            if (o >= static_cast<uint64_t>(cnt))
+                len = 0;
+            else if (o + len > static_cast<uint64_t>(cnt))
+                len = static_cast<uint32_t>(cnt - o);  // only a corrupt chunk holds more symbols than cnt
+            if (len > 0) {
+                if (skip + cw > static_cast<uint32_t>(kWsStage)) {  // more than the staging area holds
+                    // from the slice's entry to where the next slice starts
+                    uint32_t lim = hi;
+                    if (next_m) lim = hi + nt.pos[met * 32 + 1];
+                    s.start(payload, nbytes, entry + ent);
+                    uint32_t rp = ent;
+                    int n2 = 0, b2 = -1;
+                    ws_walk<true, false>(s, payload, nbytes, T, rp, lo, lim, nullptr, nt, n2, b2, dst0 + o, len);
+                } else {
+                    ws_copy(stg, skip, len, dst0 + o);
+                }
+            }
+            written += total;
+            entry += rex;
+            __syncwarp();  // the notes and areas are reused by the next round
+        }
+        if (lane == 0 && (written != static_cast<uint64_t>(cnt) || entry != end)) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+    }
+    if (bad) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+}
+
+// A warp per chunk from kWsMinPerSm to kWsMaxPerSm chunks per SM.  Measured
+// on the 16 GiB sweep (fixed codebook): at 1 MiB chunks (108 per SM) 203
+// GB/s against 97 for the split decode; at 256 KiB (431 per SM) 195 against
+// 145 for one lane per chunk; at 128 KiB (862 per SM) both 234.  Below about
+// 12 per SM too few warps have a chunk (2 GiB at 1 MiB chunks, 13.5 per SM:
+// 83 against 82 for the split decode; 1 GiB, 6.7 per SM: 57 against 97).
+constexpr size_t kWsMinPerSm = 12;
+constexpr size_t kWsMaxPerSm = 768;
+__host__ bool ws_decode(size_t n_chunks, int sms) {
+    return n_chunks >= static_cast<size_t>(sms) * kWsMinPerSm && n_chunks < static_cast<size_t>(sms) * kWsMaxPerSm;
+}
+
 // Threads per chunk for the split decode, or 0 when one lane per chunk fills the GPU.
 __host__ int split_threads(size_t n_chunks, size_t chunk, int sms) {
     // the split decode walks every slice three times, so it pays where one lane per chunk would leave the
-    // SMs with fewer than about a third of the lanes they need to run at full rate (several hundred)
+    // SMs with fewer than about a third of the lanes they need to run at full rate (several hundred); a
+    // warp per chunk (above) takes the counts from kWsMinPerSm per SM up
     const size_t lanes = static_cast<size_t>(sms) * 256;
     if (n_chunks >= lanes) return 0;
     size_t t = (4 * lanes + n_chunks - 1) / n_chunks;     // about 1024 threads per SM in all
@@ -1387,7 +1775,17 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
                      const huff_codebook *cb, uint8_t *out, int32_t *status, cudaStream_t s) {
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    const int split = split_threads(n_chunks, chunk, dev_info().sms);
+    const int sms = dev_info().sms;
+    if (ws_decode(n_chunks, sms)) {
+        const size_t smem = ws_smem();
+        if (cudaFuncSetAttribute(k_decode_u8_ws, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+            return HUFF_ERR_CUDA;
+        k_decode_u8_ws<<<static_cast<unsigned>(sms), kWsWarps * 32, smem, s>>>(payload, bytes, off, n, chunk, cb, out,
+                                                                              status);
+        return launch_status();
+    }
+    const int split = split_threads(n_chunks, chunk, sms);
     if (split > 0) {
         const size_t smem = (static_cast<size_t>(split) + 32) * sizeof(uint64_t) + sizeof(SplitTab);
         k_decode_u8_split<<<static_cast<unsigned>(n_chunks), split, smem, s>>>(payload, bytes, off, n, chunk, cb, out,

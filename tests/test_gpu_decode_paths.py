@@ -1,11 +1,12 @@
-"""Both byte-stream decode paths, bit-exact.
+"""The byte-stream decode's one-lane and split paths, bit-exact.
 
 huff_decode gives every chunk one lane when there are enough chunks to fill
-the GPU (at least 256 per SM).  With fewer, it gives a chunk a CTA and each
-thread a slice of the chunk's bits, found by self-synchronisation (walks from
-arbitrary bits, then from the previous slice's exit until no exit changes).
-These tests size inputs on both sides of that threshold and give the split
-path the codes that make it work hardest:
+the GPU (at least 768 per SM), and a warp per chunk from 12 per SM (tested in
+test_gpu_decode_warp.py).  With fewer, it gives a chunk a CTA and each thread a
+slice of the chunk's bits, found by self-synchronisation (walks from arbitrary
+bits, then from the previous slice's exit until no exit changes).  These
+tests size inputs on both ends and give the split path the codes that make it
+work hardest:
 - codes of one length (slices start on the lengths' common divisor), and
   codes that resynchronise only rarely;
 - a single 1-bit code;
@@ -46,13 +47,13 @@ def _round_trip(x: np.ndarray, cb: codec.Codebook, chunk: int) -> None:
 
 
 def _lanes_threshold() -> int:
-    # twice the chunk count below which the split decode is taken
-    return torch.cuda.get_device_properties(0).multi_processor_count * 512
+    # a chunk count above the one from which every chunk gets one lane (768 per SM)
+    return torch.cuda.get_device_properties(0).multi_processor_count * 1024
 
 
 @pytest.mark.parametrize("kind", ["gauss", "skew"])
 def test_one_lane_per_chunk_path(kind):
-    """Enough chunks for one lane each (the split path is not taken), ragged tail."""
+    """Enough chunks for one lane each (neither the warp nor the split path), ragged tail."""
     chunk = 256
     n = _lanes_threshold() * chunk + 77
     if kind == "gauss":
