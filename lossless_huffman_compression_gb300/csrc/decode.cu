@@ -9,12 +9,11 @@
 // GPU design:
 //   * one lane per chunk (per chunk pair for bf16), every lane of the grid
 //     resident at once; the block size follows the chunk count.  With fewer
-//     than 768 chunks per SM, byte streams instead give each chunk a warp
-//     whose lanes take slices of its bits, and below 12 per SM a CTA whose
-//     threads do; both find the slices' code boundaries by
-//     self-synchronisation (the sections on fewer chunks below).  With at
-//     most 448 lanes per SM the fused bf16 decode steps both planes of a
-//     lane in one loop;
+//     than 768 chunks per SM, byte streams instead give each chunk a team of
+//     1 to 28 warps whose threads take slices of its bits and find their
+//     code boundaries by self-synchronisation (the section on fewer chunks
+//     below).  With at most 448 lanes per SM the fused bf16 decode steps
+//     both planes of a lane in one loop;
 //   * shared tables per plane: a window table of 2^W 64-bit entries (W = 12
 //     for the high plane, 13 for the low plane and byte streams), each
 //     listing the codes wholly inside the next W bits (up to six symbols,
@@ -862,44 +861,6 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     if (cnt > 0 && (bad || s.pos() != off[c + 1])) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
-// ------------------------------------------------------------------ byte streams, few chunks
-//
-// With fewer chunks than the GPU has lanes to spare, one lane per chunk
-// leaves most of the GPU idle.  Then a CTA takes one chunk and splits its bit
-// range into S slices, one thread each (S = blockDim.x).  It relies on
-// Huffman codes being self-synchronising: a decode started at an arbitrary
-// bit usually falls onto the true code boundaries within a few codes (the
-// observation behind Klein and Wiseman's parallel decoding and the GPU
-// decoder of Weissenberger and Schmidt).  Three walks over the slice:
-//   1. from the slice's first bit (a true boundary for slice 0; slices start
-//      on multiples of the code lengths' greatest common divisor, so for a
-//      code of one length every slice does) to the first boundary of that
-//      walk at or after the slice's end: the exit;
-//   2. from the previous slice's exit, counting the codes that start in the
-//      slice, to a new exit; repeated while any exit changes.  Slice 0 starts
-//      at the chunk's offset, so after round r slices 0..r are exact and a
-//      round that changes nothing has every exit exact: at most S + 1 rounds,
-//      whatever the code (one that never resynchronises costs a round per
-//      slice);
-//   3. a block scan of the counts gives each slice its first output index;
-//      each slice decodes again from its entry and stores its symbols.
-// The chunk is valid when the counts add up to its symbol count and the last
-// slice's exit is the next chunk's offset.
-constexpr int kSplitMinSyms = 16;  // symbols per slice at least, where the chunk allows 32 slices
-
-// The split decode's copy of a codebook's canonical arrays (shared memory).
-struct SplitTab {
-    uint32_t lim[32];
-    uint32_t first_code[32];
-    uint32_t first_index[32];
-    uint32_t bl_count[32];
-    uint8_t sorted[256];
-};
-
-// The codes that start in [pos, lim): their count, and with WRITE the symbols
-// stored to out[0, room).  pos ends at the walk's first boundary at or after
-// lim.  Every iteration takes at least one bit, so a walk over corrupt data
-// ends as well; `bad` notes bits that are no code.
 // A slice's output bytes, stored as aligned 8-byte words.  Its first and
 // last words may hold other slices' bytes, so those two are written byte by
 // byte (the slice's own bytes only); every word between them in one store.
@@ -944,6 +905,44 @@ struct WordOut {
     }
 };
 
+// ------------------------------------------------------------------ byte streams, few chunks
+//
+// With fewer chunks than the GPU has lanes to spare, one lane per chunk
+// leaves most of the GPU idle.  Then a CTA takes one chunk and splits its bit
+// range into S slices, one thread each (S = blockDim.x).  It relies on
+// Huffman codes being self-synchronising: a decode started at an arbitrary
+// bit usually falls onto the true code boundaries within a few codes (the
+// observation behind Klein and Wiseman's parallel decoding and the GPU
+// decoder of Weissenberger and Schmidt).  Three walks over the slice:
+//   1. from the slice's first bit (a true boundary for slice 0; slices start
+//      on multiples of the code lengths' greatest common divisor, so for a
+//      code of one length every slice does) to the first boundary of that
+//      walk at or after the slice's end: the exit;
+//   2. from the previous slice's exit, counting the codes that start in the
+//      slice, to a new exit; repeated while any exit changes.  Slice 0 starts
+//      at the chunk's offset, so after round r slices 0..r are exact and a
+//      round that changes nothing has every exit exact: at most S + 1 rounds,
+//      whatever the code (one that never resynchronises costs a round per
+//      slice);
+//   3. a block scan of the counts gives each slice its first output index;
+//      each slice decodes again from its entry and stores its symbols.
+// The chunk is valid when the counts add up to its symbol count and the last
+// slice's exit is the next chunk's offset.
+constexpr int kSplitMinSyms = 16;  // symbols per slice at least, where the chunk allows 32 slices
+
+// The split decode's copy of a codebook's canonical arrays (shared memory).
+struct SplitTab {
+    uint32_t lim[32];
+    uint32_t first_code[32];
+    uint32_t first_index[32];
+    uint32_t bl_count[32];
+    uint8_t sorted[256];
+};
+
+// The codes that start in [pos, lim): their count, and with WRITE the symbols
+// stored to out[0, room).  pos ends at the walk's first boundary at or after
+// lim.  Every iteration takes at least one bit, so a walk over corrupt data
+// ends as well; `bad` notes bits that are no code.
 // Positions are relative to the slice's first bit (32 bits: a chunk holds at
 // most 2^30 * 24 bits and has at least 32 slices).
 template <bool WRITE>
@@ -1100,49 +1099,50 @@ __global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restr
     if (bad) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
-// ------------------------------------------------------------------ byte streams, a warp per chunk
+// ------------------------------------------------------------------ byte streams, fewer chunks
 //
-// Between the two: chunks too few for one lane each, but enough for a warp
-// each.  A warp decodes its chunk in rounds of 32 slices of B bits, one per
-// lane.  Each slice is walked once from its first bit, which need not be a
+// With fewer chunks than one lane each needs to fill the GPU (or to balance
+// it: the chunks' decode costs can differ several times), a team of TW warps
+// (TW = 1 while there are enough chunks, up to the whole CTA when they are
+// few) decodes a chunk in rounds of TW * 32 slices of B bits, one per
+// thread.  Each slice is walked once from its first bit, which need not be a
 // code boundary (Huffman codes are self-synchronising: a walk started
 // anywhere falls onto the true boundaries within a few codes, as Klein and
 // Wiseman's parallel decoding and Weissenberger and Schmidt's GPU decoder
 // use).  The walk stages the symbols of the codes that start in the slice in
-// the lane's area of shared memory, and notes where its first kWsList table
-// steps start and how many symbols came before each.  Then each lane goes on
-// past its slice's end, one code at a time, until a code starts where a
-// noted step of the next slice starts: from there on the two walks are the
-// same, so once this slice is exact the next one is exact from that step,
-// and the codes in between are this slice's (staged after its own).  The
-// walk that reaches no noted step (about one slice in a few thousand on the
-// data measured) leaves the next slice to be walked again from this slice's
-// exit; its own end may then move, so the slice after it checks again, at
-// most 32 passes (slice 0 starts on the round's exact entry, and pass i
-// makes slice i exact).  A warp scan of the slices' counts places each
-// slice's symbols, which each lane copies from its area to the output.
+// the thread's area of shared memory, and notes where its first kWsList
+// table steps start and how many symbols came before each.  Then each thread
+// goes on past its slice's end, one code at a time, until a code starts
+// where a noted step of the next slice starts: from there on the two walks
+// are the same, so once this slice is exact the next one is exact from that
+// step, and the codes in between are this slice's (staged after its own).
+// The walk that reaches no noted step (about one slice in a few thousand on
+// the data measured) leaves the next slice to be walked again from this
+// slice's exit; its own end may then move, so the slice after it checks
+// again (slice 0 starts on the round's exact entry, and pass i makes slice i
+// exact).  A scan of the slices' counts places each slice's symbols, which
+// each thread copies from its area to the output.
 // B follows the chunk's mean code length so that a slice holds about
-// kWsTarget symbols; a slice with more than its area holds (a skewed part of
-// a chunk) is decoded once more from its entry, writing straight to the
-// output.  Slices start on multiples of the code lengths' greatest common
-// divisor from the chunk's start, as in the split decode.
-// A CTA per SM of kWsWarps warps shares one copy of the tables; its warps
+// kWsTarget symbols (with a team of several warps, no more than gives every
+// slice of one round some bits); a slice with more than its area holds (a
+// skewed part of a chunk) is decoded once more from its entry, writing
+// straight to the output.  Slices start on multiples of the code lengths'
+// greatest common divisor from the chunk's start: a code of one length (all
+// 8 bits, say) then starts every slice on a boundary.
+// A CTA per SM of kWsWarps warps shares one copy of the tables; its teams
 // take chunks blockIdx.x, blockIdx.x + gridDim.x, ... (interleaved, so every
 // CTA meets every part of the input alike) from a shared counter, a chunk at
-// a time, so warps that drew cheap chunks take more of them.
+// a time, so teams that drew cheap chunks take more of them.
 constexpr int kWsWarps = 28;              // warps per CTA (7 per scheduler)
 constexpr int kWsStage = 84;              // staged symbols per slice
 constexpr int kWsStride = kWsStage + 4;   // bytes between two lanes' areas (22 words: lanes' columns spread over the banks)
 constexpr int kWsTarget = 56;             // symbols a slice is sized for
 constexpr int kWsList = 24;               // steps noted per walk
 static_assert(kWsStage % 4 == 0 && 4 * kWsList <= 255, "staging geometry");
-constexpr size_t kWsWarpBytes = 32 * (kWsStride + 3 * kWsList);  // a warp's areas and step notes
-
-__host__ size_t ws_smem() { return sizeof(U8Tables) + static_cast<size_t>(kWsWarps) * kWsWarpBytes + 16; }
 
 // A lane's step notes: where its first walk's first kWsList steps start
 // (relative to the slice's first bit) and the symbols before each; entry i
-// of lane l at i * 32 + l.
+// of a team's slice l at i * (slices per round) + l.
 struct WsNotes {
     uint16_t *pos;
     uint8_t *cnt;
@@ -1181,7 +1181,7 @@ __device__ __forceinline__ void ws_code(const PlaneDec &s, const U8Tables &T, ui
 // symbols: staged (the first kWsStage; NOTE: with the first kWsList steps
 // noted) or, DIRECT, written to dst[0, room).  pos ends at the walk's exit;
 // badpos is the last position (relative to lo) where the bits were no code.
-template <bool DIRECT, bool NOTE>
+template <bool DIRECT, bool NOTE, int NS>
 __device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, size_t nbytes, const U8Tables &T,
                                          uint32_t &pos, uint32_t lo, uint32_t lim, uint8_t *stg, WsNotes nt,
                                          int &nsteps, int &badpos, uint8_t *dst, uint64_t room) {
@@ -1200,8 +1200,8 @@ __device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, si
         uint32_t c, bits;
         lut_get(T, win, v, c, bits);
         if (NOTE && steps < kWsList) {
-            nt.pos[steps * 32] = static_cast<uint16_t>(pos - lo);
-            nt.cnt[steps * 32] = static_cast<uint8_t>(n);
+            nt.pos[steps * NS] = static_cast<uint16_t>(pos - lo);
+            nt.cnt[steps * NS] = static_cast<uint8_t>(n);
         }
         ++steps;
         // a code longer than the window: the secondary table's entry, looked up on every step (a
@@ -1261,6 +1261,7 @@ __device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, si
 // nns of them, relative to its first bit nlo): returns that step, or -1 when
 // the codes pass its last note.  The codes' symbols are staged from stg[n]
 // on, m of them; pb notes bits that are no code.
+template <int NS>
 __device__ __forceinline__ int ws_over(PlaneDec &s_io, const uint8_t *p, size_t nbytes, const U8Tables &T, uint32_t pos,
                                     uint32_t nlo, const uint16_t *npos, int nns, uint8_t *stg, uint32_t n,
                                     uint32_t &m, bool &pb) {
@@ -1269,9 +1270,9 @@ __device__ __forceinline__ int ws_over(PlaneDec &s_io, const uint8_t *p, size_t 
     m = 0;
     for (;;) {
         const uint32_t d = pos - nlo;
-        while (j < nns && npos[j * 32] < d) ++j;
+        while (j < nns && npos[j * NS] < d) ++j;
         if (j == nns) break;
-        if (npos[j * 32] == d) {
+        if (npos[j * NS] == d) {
             s_io = s;
             return j;
         }
@@ -1307,19 +1308,135 @@ __device__ __forceinline__ void ws_copy(const uint8_t *stg, uint32_t from, uint3
     for (; i < len; ++i) dst[i] = stg[from + i];
 }
 
+// A team of TW warps decodes one chunk at a time; slice i of a round goes to
+// the team's thread i.  Exchanges between neighbouring slices, the count
+// scan and broadcasts use warp shuffles within one warp (TW = 1) and shared
+// memory with the team's own named barrier otherwise.
+template <int TW>
+struct WsTeam {
+    uint32_t *xa, *xb;  // L words each: values exchanged between neighbouring slices
+    uint32_t *xw;       // 32 words: warp totals and broadcasts
+    int tl, lane, wt, id;  // thread in the team, lane, warp in the team, team in the CTA
+    __device__ __forceinline__ void sync() const {
+        if constexpr (TW == 1)
+            __syncwarp();
+        else
+            asm volatile("barrier.sync %0, %1;" ::"r"(id + 1), "n"(TW * 32) : "memory");
+    }
+    __device__ __forceinline__ bool any(bool p) const {
+        if constexpr (TW == 1) {
+            return __any_sync(0xffffffffu, p);
+        } else {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\tbarrier.red.or.pred b, %2, %3, a;\n\t"
+                "selp.u32 %0, 1, 0, b;\n\t}"
+                : "=r"(r)
+                : "r"(static_cast<uint32_t>(p)), "r"(id + 1), "n"(TW * 32)
+                : "memory");
+            return r != 0;
+        }
+    }
+    // the previous slice's values (slice 0 gets its own)
+    __device__ __forceinline__ void prev2(uint32_t &a, uint32_t &b) const {
+        if constexpr (TW == 1) {
+            a = __shfl_up_sync(0xffffffffu, a, 1);
+            b = __shfl_up_sync(0xffffffffu, b, 1);
+        } else {
+            xa[tl] = a;
+            xb[tl] = b;
+            sync();
+            const int q = tl ? tl - 1 : 0;
+            a = xa[q];
+            b = xb[q];
+            sync();
+        }
+    }
+    // the next slice's value (the last slice gets its own)
+    __device__ __forceinline__ uint32_t next(uint32_t v) const {
+        if constexpr (TW == 1) {
+            return __shfl_down_sync(0xffffffffu, v, 1);
+        } else {
+            xa[tl] = v;
+            sync();
+            const uint32_t r = xa[tl + 1 < TW * 32 ? tl + 1 : tl];
+            sync();
+            return r;
+        }
+    }
+    __device__ __forceinline__ uint32_t from(uint32_t v, int src) const {
+        if constexpr (TW == 1) {
+            return __shfl_sync(0xffffffffu, v, src);
+        } else {
+            if (tl == src) xw[0] = v;
+            sync();
+            const uint32_t r = xw[0];
+            sync();
+            return r;
+        }
+    }
+    // exclusive prefix sum over the team's slices, and their total
+    __device__ __forceinline__ uint32_t scan(uint32_t v, uint32_t &total) const {
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if constexpr (TW == 1) {
+            total = __shfl_sync(0xffffffffu, incl, 31);
+            return incl - v;
+        } else {
+            if (lane == 31) xw[wt] = incl;
+            sync();
+            uint32_t before = 0, all = 0;
+            for (int w = 0; w < TW; ++w) {
+                const uint32_t t = xw[w];
+                all += t;
+                before += w < wt ? t : 0u;
+            }
+            sync();
+            total = all;
+            return before + incl - v;
+        }
+    }
+};
+
+// Shared memory of one team: the lanes' areas, the step notes and the exchange words.
+template <int TW>
+__host__ __device__ constexpr size_t ws_team_bytes() {
+    return static_cast<size_t>(TW) * 32 * (kWsStride + 3 * kWsList + 8) + 32 * 4;
+}
+template <int TW>
+__host__ size_t ws_smem() {
+    return sizeof(U8Tables) + static_cast<size_t>(kWsWarps / TW) * ws_team_bytes<TW>() + 16;
+}
+
+template <int TW>
 __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t *__restrict__ payload, size_t nbytes,
                                                                   const uint64_t *__restrict__ off, size_t n,
                                                                   size_t chunk, const huff_codebook *__restrict__ cb,
                                                                   uint8_t *__restrict__ out, int32_t *status) {
+    static_assert(kWsWarps % TW == 0 && (TW == 1 || kWsWarps / TW <= 15), "teams divide the CTA; one named barrier each");
+    constexpr int L = TW * 32;
     extern __shared__ __align__(16) uint8_t dsm[];
     U8Tables &T = *reinterpret_cast<U8Tables *>(dsm);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t *const wbase = dsm + sizeof(U8Tables) + static_cast<size_t>(warp) * kWsWarpBytes;
-    uint8_t *const stg = wbase + lane * kWsStride;
+    const int warp = threadIdx.x >> 5;
+    WsTeam<TW> tm;
+    tm.lane = threadIdx.x & 31;
+    tm.wt = warp % TW;
+    tm.id = warp / TW;
+    tm.tl = tm.wt * 32 + tm.lane;
+    const int tl = tm.tl;
+    uint8_t *const tbase = dsm + sizeof(U8Tables) + static_cast<size_t>(tm.id) * ws_team_bytes<TW>();
+    uint8_t *const stg = tbase + tl * kWsStride;
     WsNotes nt;
-    nt.pos = reinterpret_cast<uint16_t *>(wbase + 32 * kWsStride) + lane;
-    nt.cnt = wbase + 32 * kWsStride + 32 * 2 * kWsList + lane;
-    int *next = reinterpret_cast<int *>(dsm + sizeof(U8Tables) + static_cast<size_t>(kWsWarps) * kWsWarpBytes);
+    nt.pos = reinterpret_cast<uint16_t *>(tbase + L * kWsStride) + tl;
+    nt.cnt = tbase + L * kWsStride + L * 2 * kWsList + tl;
+    tm.xa = reinterpret_cast<uint32_t *>(tbase + L * (kWsStride + 3 * kWsList));
+    tm.xb = tm.xa + L;
+    tm.xw = tm.xb + L;
+    int *next = reinterpret_cast<int *>(dsm + sizeof(U8Tables) + static_cast<size_t>(kWsWarps / TW) * ws_team_bytes<TW>());
     load_table_a(T, cb);
     if (threadIdx.x == 0) *next = 0;
     __syncthreads();
@@ -1345,59 +1462,66 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
     const size_t n_chunks = (n + chunk - 1) / chunk;
     bool bad = false;
     for (;;) {
-        int jc = 0;
-        if (lane == 0) jc = atomicAdd(next, 1);
-        jc = __shfl_sync(0xffffffffu, jc, 0);
+        uint32_t jc = 0;
+        if (tl == 0) jc = static_cast<uint32_t>(atomicAdd(next, 1));
+        jc = tm.from(jc, 0);
         const size_t c = blockIdx.x + static_cast<size_t>(jc) * gridDim.x;
         if (c >= n_chunks) break;
         const size_t first = c * chunk;
         const int cnt = static_cast<int>(n - first < chunk ? n - first : chunk);
         uint64_t start = 0, end = 0;
         if (!chunk_bounds(off, c, nbytes, cnt, start, end)) {
-            if (lane == 0) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+            if (tl == 0) set_status(status, HUFF_ERR_CORRUPT_STREAM);
             continue;
         }
-        // slice length: about kWsTarget symbols at the chunk's mean code length, at least 32 bits, a multiple of g
-        uint32_t B = static_cast<uint32_t>((end - start) * kWsTarget / static_cast<uint64_t>(cnt));
+        // slice length: about kWsTarget symbols at the chunk's mean code length (a team of several warps:
+        // no more than gives every slice of one round some bits), at least 32 bits, a multiple of g
+        const uint64_t span = end - start;
+        uint32_t B = static_cast<uint32_t>(span * kWsTarget / static_cast<uint64_t>(cnt));
+        if (TW > 1) {
+            const uint64_t fit = (span + L - 1) / L;
+            if (fit < B) B = static_cast<uint32_t>(fit);
+        }
         B = max(B, 32u);
         B = (B + g - 1) / g * g;
         uint8_t *const dst0 = out + first;
         uint64_t entry = start, written = 0;
         while (entry < end) {
             const uint64_t left = end - entry;
-            const uint32_t rlen = left < 32ull * B ? static_cast<uint32_t>(left) : 32u * B;
-            const uint32_t lo = static_cast<uint32_t>(lane) * B;
-            const uint32_t hi = lane == 31 ? rlen : min(lo + B, rlen);
+            const uint32_t rlen = left < static_cast<uint64_t>(L) * B ? static_cast<uint32_t>(left) : L * B;
+            const uint32_t lo = static_cast<uint32_t>(tl) * B;
+            const uint32_t hi = tl == L - 1 ? rlen : min(lo + B, rlen);
             const bool act = lo < rlen;
             const int last = static_cast<int>((rlen - 1) / B);  // the last slice with bits
-            const bool has_next = lane < last;
+            const bool has_next = tl < last;
             PlaneDec s;
             uint32_t ex = lo, cntw = 0;
             int ns = 0, badpos = -1;
             if (act) {
                 s.start(payload, nbytes, entry + lo);
-                cntw = ws_walk<false, true>(s, payload, nbytes, T, ex, lo, hi, stg, nt, ns, badpos, nullptr, 0);
+                cntw = ws_walk<false, true, L>(s, payload, nbytes, T, ex, lo, hi, stg, nt, ns, badpos, nullptr, 0);
             }
-            __syncwarp();  // every lane's notes are in place
-            const int ns_next = __shfl_down_sync(0xffffffffu, ns, 1);
+            tm.sync();  // every slice's notes are in place
+            const int ns_next = static_cast<int>(tm.next(static_cast<uint32_t>(ns)));
             // past the slice's end until the next slice's walk is met
             uint32_t m = 0;
             bool pb = false;
             int met = -1;
-            if (has_next) met = ws_over(s, payload, nbytes, T, ex, hi, nt.pos + 1, ns_next, stg, cntw, m, pb);
+            if (has_next) met = ws_over<L>(s, payload, nbytes, T, ex, hi, nt.pos + 1, ns_next, stg, cntw, m, pb);
             // each slice's entry: from the previous slice's meeting step (M), or walked again from its exit (R)
             uint32_t skip = 0, ent = lo, seen_e = 0xffffffffu;
             int seen_met = -2;
             bool first_walk = true, used_m = false, own_bad = false, settled = false;
-            for (int pass = 0; pass <= 32; ++pass) {
-                uint32_t e = __shfl_up_sync(0xffffffffu, ex, 1);
-                int mp = __shfl_up_sync(0xffffffffu, met, 1);
-                if (lane == 0) {
+            for (int pass = 0; pass <= L; ++pass) {
+                uint32_t e = ex, mpu = static_cast<uint32_t>(met);
+                tm.prev2(e, mpu);
+                int mp = static_cast<int>(mpu);
+                if (tl == 0) {
                     e = 0;
                     mp = 0;  // slice 0 starts on the round's entry, its first noted step
                 }
                 const bool todo = act && (e != seen_e || mp != seen_met);
-                settled = !__any_sync(0xffffffffu, todo);
+                settled = !tm.any(todo);
                 if (settled) break;
                 if (!todo) continue;
                 seen_e = e;
@@ -1410,8 +1534,8 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
                     continue;
                 }
                 if (mp >= 0 && first_walk) {
-                    skip = nt.cnt[mp * 32];
-                    ent = lo + nt.pos[mp * 32];
+                    skip = nt.cnt[mp * L];
+                    ent = lo + nt.pos[mp * L];
                     used_m = true;
                     own_bad = badpos >= static_cast<int>(ent - lo);
                     continue;
@@ -1421,31 +1545,25 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
                 ex = e;
                 badpos = -1;
                 int n2 = 0;
-                cntw = ws_walk<false, false>(s, payload, nbytes, T, ex, lo, hi, stg, nt, n2, badpos, nullptr, 0);
+                cntw = ws_walk<false, false, L>(s, payload, nbytes, T, ex, lo, hi, stg, nt, n2, badpos, nullptr, 0);
                 skip = 0;
                 ent = e;
                 used_m = false;
                 first_walk = false;
                 own_bad = badpos >= 0;
                 pb = false;
-                met = has_next ? ws_over(s, payload, nbytes, T, ex, hi, nt.pos + 1, ns_next, stg, cntw, m, pb) : -1;
+                met = has_next ? ws_over<L>(s, payload, nbytes, T, ex, hi, nt.pos + 1, ns_next, stg, cntw, m, pb) : -1;
             }
             if (!settled) bad = true;  // cannot happen: pass i makes slice i exact
             // this slice's codes past its end are its own when the next slice starts at the meeting step
-            const bool next_m = __shfl_down_sync(0xffffffffu, used_m, 1) && has_next;
+            const bool next_m = tm.next(used_m ? 1u : 0u) != 0 && has_next;
             if (act && (own_bad || (next_m && pb))) bad = true;
             const uint32_t own = act ? cntw - skip : 0u;
             const uint32_t cw = own + (next_m ? m : 0u);
             const bool thru = act && ent >= hi;
-            const uint32_t rex = __shfl_sync(0xffffffffu, thru ? ent : ex, last);
-            uint32_t incl = cw;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-            const uint64_t o = written + (incl - cw);
+            const uint32_t rex = tm.from(thru ? ent : ex, last);
+            uint32_t total = 0;
+            const uint64_t o = written + tm.scan(cw, total);
             uint32_t len = cw;
             if (o >= static_cast<uint64_t>(cnt))
                 len = 0;
@@ -1455,41 +1573,60 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
                 if (skip + cw > static_cast<uint32_t>(kWsStage)) {  // more than the staging area holds
                     // from the slice's entry to where the next slice starts
                     uint32_t lim = hi;
-                    if (next_m) lim = hi + nt.pos[met * 32 + 1];
+                    if (next_m) lim = hi + nt.pos[met * L + 1];
                     s.start(payload, nbytes, entry + ent);
                     uint32_t rp = ent;
                     int n2 = 0, b2 = -1;
-                    ws_walk<true, false>(s, payload, nbytes, T, rp, lo, lim, nullptr, nt, n2, b2, dst0 + o, len);
+                    ws_walk<true, false, L>(s, payload, nbytes, T, rp, lo, lim, nullptr, nt, n2, b2, dst0 + o, len);
                 } else {
                     ws_copy(stg, skip, len, dst0 + o);
                 }
             }
             written += total;
             entry += rex;
-            __syncwarp();  // the notes and areas are reused by the next round
+            tm.sync();  // the notes and areas are reused by the next round
         }
-        if (lane == 0 && (written != static_cast<uint64_t>(cnt) || entry != end)) set_status(status, HUFF_ERR_CORRUPT_STREAM);
+        if (tl == 0 && (written != static_cast<uint64_t>(cnt) || entry != end)) set_status(status, HUFF_ERR_CORRUPT_STREAM);
     }
     if (bad) set_status(status, HUFF_ERR_CORRUPT_STREAM);
 }
 
-// A warp per chunk from kWsMinPerSm to kWsMaxPerSm chunks per SM.  Measured
-// on the 16 GiB sweep (fixed codebook): at 1 MiB chunks (108 per SM) 203
-// GB/s against 97 for the split decode; at 256 KiB (431 per SM) 195 against
-// 145 for one lane per chunk; at 128 KiB (862 per SM) both 234.  Below about
-// 12 per SM too few warps have a chunk (2 GiB at 1 MiB chunks, 13.5 per SM:
-// 83 against 82 for the split decode; 1 GiB, 6.7 per SM: 57 against 97).
-constexpr size_t kWsMinPerSm = 12;
+// The byte-stream decode's mode: 0, one lane per chunk; -1, a CTA per chunk
+// with three walks per slice (the split decode above); otherwise TW, a team
+// of TW warps per chunk.
+// One lane per chunk from kWsMaxPerSm chunks per SM.  Below, teams: the
+// fewest warps per team that leave at most about a tenth of the teams
+// without a chunk, provided a chunk is at least kWsMinRounds rounds of the
+// team (a round costs the same however few slices have bits); otherwise one
+// lane per chunk from 256 chunks per SM, the split decode below that.
+// Measured (CUDA events, one call): the 16 GiB sweep (fixed codebook) at
+// 1 MiB chunks (108 per SM) 203 GB/s with a warp per chunk against 97 with
+// the split decode, at 256 KiB (431 per SM) 232 against 145 with one lane per
+// chunk, at 128 KiB (862 per SM) both 234; 1024 chunks (6.7 per SM): 1 GiB of
+// the sweep at 1 MiB chunks 166 to 183 GB/s with teams of 4 to 28 warps
+// against 98 split, 256 MiB of N(0, 8) bytes at 256 KiB 258 (4 warps)
+// against 222 split, 64 MiB at 64 KiB (9 rounds of 4 warps) 206 against 214
+// split, 16 MiB at 16 KiB (2.3 rounds) 130 against 161 split; 64 chunks of
+// 16 KiB: 45 us with teams of 14 or 28 warps against 37 split.
 constexpr size_t kWsMaxPerSm = 768;
-__host__ bool ws_decode(size_t n_chunks, int sms) {
-    return n_chunks >= static_cast<size_t>(sms) * kWsMinPerSm && n_chunks < static_cast<size_t>(sms) * kWsMaxPerSm;
+constexpr size_t kWsMinRounds = 4;
+__host__ int u8_mode(size_t n_chunks, size_t chunk, int sms) {
+    if (n_chunks >= static_cast<size_t>(sms) * kWsMaxPerSm) return 0;
+    int tw = kWsWarps;
+    for (int d : {1, 2, 4, 7, 14})
+        if (10 * static_cast<size_t>(sms) * (kWsWarps / d) <= 11 * n_chunks) {
+            tw = d;
+            break;
+        }
+    if (chunk >= kWsMinRounds * static_cast<size_t>(tw) * 32 * kWsTarget) return tw;
+    return n_chunks >= static_cast<size_t>(sms) * 256 ? 0 : -1;
 }
 
 // Threads per chunk for the split decode, or 0 when one lane per chunk fills the GPU.
 __host__ int split_threads(size_t n_chunks, size_t chunk, int sms) {
     // the split decode walks every slice three times, so it pays where one lane per chunk would leave the
-    // SMs with fewer than about a third of the lanes they need to run at full rate (several hundred); a
-    // warp per chunk (above) takes the counts from kWsMinPerSm per SM up
+    // SMs with fewer than about a third of the lanes they need to run at full rate (several hundred); it
+    // takes the chunks too small for a team of warps (u8_mode)
     const size_t lanes = static_cast<size_t>(sms) * 256;
     if (n_chunks >= lanes) return 0;
     size_t t = (4 * lanes + n_chunks - 1) / n_chunks;     // about 1024 threads per SM in all
@@ -1776,29 +1913,39 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
     if (n == 0) return HUFF_OK;
     const size_t n_chunks = (n + chunk - 1) / chunk;
     const int sms = dev_info().sms;
-    if (ws_decode(n_chunks, sms)) {
-        const size_t smem = ws_smem();
-        if (cudaFuncSetAttribute(k_decode_u8_ws, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
-            return HUFF_ERR_CUDA;
-        k_decode_u8_ws<<<static_cast<unsigned>(sms), kWsWarps * 32, smem, s>>>(payload, bytes, off, n, chunk, cb, out,
-                                                                              status);
-        return launch_status();
-    }
-    const int split = split_threads(n_chunks, chunk, sms);
-    if (split > 0) {
+    const int tw = u8_mode(n_chunks, chunk, sms);
+    if (tw < 0) {
+        const int split = split_threads(n_chunks, chunk, sms);
         const size_t smem = (static_cast<size_t>(split) + 32) * sizeof(uint64_t) + sizeof(SplitTab);
         k_decode_u8_split<<<static_cast<unsigned>(n_chunks), split, smem, s>>>(payload, bytes, off, n, chunk, cb, out,
                                                                               status);
         return launch_status();
     }
-    const int block = decode_block(n_chunks, dev_info().sms);
-    const unsigned grid = static_cast<unsigned>((n_chunks + block - 1) / block);
+    const size_t teams = static_cast<size_t>(kWsWarps / (tw > 0 ? tw : 1));  // per CTA
+    const unsigned grid = static_cast<unsigned>(std::min<size_t>(sms, (n_chunks + teams - 1) / teams));
+    const auto ws = [&](auto kern, size_t smem) -> int {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+            return HUFF_ERR_CUDA;
+        kern<<<grid, kWsWarps * 32, smem, s>>>(payload, bytes, off, n, chunk, cb, out, status);
+        return launch_status();
+    };
+    switch (tw) {
+        case 1: return ws(k_decode_u8_ws<1>, ws_smem<1>());
+        case 2: return ws(k_decode_u8_ws<2>, ws_smem<2>());
+        case 4: return ws(k_decode_u8_ws<4>, ws_smem<4>());
+        case 7: return ws(k_decode_u8_ws<7>, ws_smem<7>());
+        case 14: return ws(k_decode_u8_ws<14>, ws_smem<14>());
+        case 28: return ws(k_decode_u8_ws<28>, ws_smem<28>());
+        default: break;
+    }
+    const int block = decode_block(n_chunks, sms);
+    const unsigned blocks = static_cast<unsigned>((n_chunks + block - 1) / block);
     const size_t smem = sizeof(U8Tables) + static_cast<size_t>(block) * kRingU8;
     if (cudaFuncSetAttribute(k_decode_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return HUFF_ERR_CUDA;
-    k_decode_u8<<<grid, block, smem, s>>>(payload, bytes, off, n, chunk, cb, out, status);
+    k_decode_u8<<<blocks, block, smem, s>>>(payload, bytes, off, n, chunk, cb, out, status);
     return launch_status();
 }
 

@@ -1,12 +1,13 @@
-"""The byte-stream decode's one-lane and split paths, bit-exact.
+"""The byte-stream decode's one-lane path and its few-chunk cases, bit-exact.
 
 huff_decode gives every chunk one lane when there are enough chunks to fill
-the GPU (at least 768 per SM), and a warp per chunk from 12 per SM (tested in
-test_gpu_decode_warp.py).  With fewer, it gives a chunk a CTA and each thread a
-slice of the chunk's bits, found by self-synchronisation (walks from arbitrary
-bits, then from the previous slice's exit until no exit changes).  These
-tests size inputs on both ends and give the split path the codes that make it
-work hardest:
+the GPU (at least 768 per SM).  With fewer, a team of warps takes each chunk
+(a whole CTA of 28 warps when chunks are as few as here; every team size is
+tested in test_gpu_decode_warp.py) and each thread a slice of its bits, whose
+code boundaries are found by self-synchronisation: one walk per slice from
+its first bit, then from its end until the next slice's walk is met.  These
+tests size inputs on both ends and give the few-chunk cases the codes that
+make them work hardest:
 - codes of one length (slices start on the lengths' common divisor), and
   codes that resynchronise only rarely;
 - a single 1-bit code;
@@ -53,7 +54,7 @@ def _lanes_threshold() -> int:
 
 @pytest.mark.parametrize("kind", ["gauss", "skew"])
 def test_one_lane_per_chunk_path(kind):
-    """Enough chunks for one lane each (neither the warp nor the split path), ragged tail."""
+    """Enough chunks for one lane each (not the team path), ragged tail."""
     chunk = 256
     n = _lanes_threshold() * chunk + 77
     if kind == "gauss":
@@ -67,8 +68,8 @@ def test_one_lane_per_chunk_path(kind):
 @pytest.mark.parametrize("n,chunk", [(1, 256), (1000, 256), (1000, 32), (100_003, 96), (65_536, 65_536), (65_537, 65_536),
                                      (1_000_003, 1 << 20), (3_000_001, 1 << 22), (200_017, 16_384),
                                      (2_000_001, 1 << 30)])  # the largest chunk the ABI accepts
-def test_split_path_matches_oracle_payload(n, chunk):
-    """The oracle's payload (not the GPU encoder's) decoded by the split path."""
+def test_few_chunks_matches_oracle_payload(n, chunk):
+    """The oracle's payload (not the GPU encoder's) decoded with few chunks."""
     x = _gauss(n, 8)
     ln, cd = oracle_codebook(oracle.histogram(x))
     pay, off = oracle.encode(x, ln, cd, chunk)
@@ -84,7 +85,7 @@ def test_split_path_matches_oracle_payload(n, chunk):
 
 
 @pytest.mark.parametrize("n", [1_000_003, 777_777])
-def test_split_path_codes_of_one_length(n):
+def test_few_chunks_codes_of_one_length(n):
     """256 codes of 8 bits: a walk that starts off the byte grid never meets it, so slices start on
     multiples of the lengths' common divisor (and the chunk is not a multiple of the slice count)."""
     cb = codec.build_codebook(torch.full((256,), 1000, dtype=torch.int64, device="cuda"))
@@ -94,10 +95,11 @@ def test_split_path_codes_of_one_length(n):
 
 
 @pytest.mark.parametrize("n", [1_000_003, 300_001])
-def test_split_path_slow_resynchronisation(n):
+def test_few_chunks_slow_resynchronisation(n):
     """Lengths 7, 8 and 9 (common divisor 1) on data of the 8-bit codes only: a walk off the byte
     grid moves onto it only when it happens to read the 7- or 9-bit code, about once in a hundred
-    codes, so many slices stay off the grid after the first walk and the exit rounds place them."""
+    codes, so many walks do not meet the next slice's noted steps and slices are walked again from
+    the previous exit."""
     h = torch.full((256,), 1000, dtype=torch.int64, device="cuda")
     h[0], h[254], h[255] = 2000, 1, 1
     cb = codec.build_codebook(h)
@@ -108,7 +110,7 @@ def test_split_path_slow_resynchronisation(n):
     _round_trip(x, cb, 1 << 20)
 
 
-def test_split_path_single_code_and_two_codes():
+def test_few_chunks_single_code_and_two_codes():
     n = 2_000_001
     x = np.full(n, 9, np.uint8)
     _round_trip(x, codec.build_codebook(codec.histogram(dev_u8(x))), 1 << 20)
@@ -116,7 +118,7 @@ def test_split_path_single_code_and_two_codes():
     _round_trip(y, codec.build_codebook(codec.histogram(dev_u8(y))), 1 << 20)
 
 
-def test_split_path_long_codes():
+def test_few_chunks_long_codes():
     """A floor-at-1 codebook from narrow data, used on wide data: most codes are 17 to 24 bits."""
     warm = _gauss(1 << 20, 4)
     cb = codec.build_codebook(codec.histogram(dev_u8(warm)), flags=_lib.HUFF_COVER_ALL)
@@ -124,8 +126,8 @@ def test_split_path_long_codes():
     _round_trip(x, cb, 1 << 18)
 
 
-def test_split_path_corrupt_streams_detected():
-    n, chunk = 600_000, 1 << 17
+@pytest.mark.parametrize("n,chunk", [(600_000, 1 << 17), (3_000_000, 1 << 19)])  # the split decode; teams of 28 warps
+def test_few_chunks_corrupt_streams_detected(n, chunk):
     x = _gauss(n, 8)
     d = dev_u8(x)
     cb = codec.build_codebook(codec.histogram(d))
