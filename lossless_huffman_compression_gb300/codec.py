@@ -192,10 +192,16 @@ def decode(s: Stream, cb: Codebook, out: torch.Tensor | None = None,
     return out
 
 
-def compress(x: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, max_len: int = 24, flags: int = 0):
-    """Per-shard Huffman: histogram, codebook and encode of one byte stream."""
-    cb = build_codebook(histogram(x), max_len, flags)
-    return cb, encode(x, cb, chunk_bytes, max_len)
+def compress(x: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, max_len: int = 24, flags: int = 0,
+             status: torch.Tensor | None = None):
+    """Per-shard Huffman: histogram, codebook and encode of one byte stream.  The three launches share
+    one status, read once at the end (a failed build leaves a codebook the encode rejects)."""
+    st = status if status is not None else new_status(x.device)
+    cb = build_codebook(histogram(x), max_len, flags, status=st)
+    s = encode(x, cb, chunk_bytes, max_len, status=st)
+    if status is None:
+        raise_on_status(st, "compress")
+    return cb, s
 
 
 def to_container(s: Stream, cb: Codebook | None = None, max_len: int = 24) -> bytes:
