@@ -1139,12 +1139,12 @@ __global__ void __launch_bounds__(1024) k_decode_u8_split(const uint8_t *__restr
 // a time, so teams that drew cheap chunks take more of them.
 constexpr int kWsWarps = 28;              // warps per CTA (7 per scheduler)
 constexpr int kWsStage = 84;              // staged symbols per slice
-constexpr int kWsStride = kWsStage + 4;   // bytes between two lanes' areas (22 words: lanes' columns spread over the banks)
+constexpr int kWsStride = kWsStage + 4;   // bytes between two threads' areas (a word of padding read by the copy)
 constexpr int kWsTarget = 56;             // symbols a slice is sized for
 constexpr int kWsList = 24;               // steps noted per walk
 static_assert(kWsStage % 4 == 0 && 4 * kWsList <= 255, "staging geometry");
 
-// A lane's step notes: where its first walk's first kWsList steps start
+// A thread's step notes: where its first walk's first kWsList steps start
 // (relative to the slice's first bit) and the symbols before each; entry i
 // of a team's slice l at i * (slices per round) + l.
 struct WsNotes {
