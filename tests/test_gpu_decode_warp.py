@@ -3,10 +3,11 @@
 huff_decode takes this path below 768 chunks per SM when a chunk is at least
 four rounds of the team: a team of 1, 2, 4, 7, 14 or 28 warps (the fewest
 that leave at most a tenth of the teams without a chunk) decodes a chunk in
-rounds of one slice per thread (about 56 symbols each), one walk per slice from the slice's first
-bit, noting where its first steps start; each thread then decodes past its
-slice's end until it meets a noted step of the next slice's walk (otherwise
-that slice is walked again from this slice's exit).  Inputs here are sized
+rounds of one slice per thread (about 56 symbols each), one walk per slice
+from the slice's first bit, noting where its first steps start; each thread
+then decodes past its slice's end until it meets a noted step of the next
+slice's walk (otherwise that slice is walked again from this slice's exit).
+Inputs here are sized
 into every team size and give the path the cases that make it work hardest:
 codes of one length, codes that resynchronise rarely, a single 1-bit code,
 long codes on data the codebook was not built for, chunks whose slices hold
@@ -122,7 +123,8 @@ def test_warp_path_codes_of_one_length():
     _round_trip(x, cb, CHUNK)
 
 
-def test_warp_path_slow_resynchronisation():
+@pytest.mark.parametrize("tw,per_sm,chunk", [(1, PER_SM, CHUNK), (7, 4, 1 << 16), (28, 0.05, 1 << 18)])
+def test_warp_path_slow_resynchronisation(tw, per_sm, chunk):
     """Lengths 7, 8 and 9 on data of the 8-bit codes only: most first walks stay off the byte grid,
     so slices are walked again from their predecessor's exit, pass after pass."""
     h = torch.full((256,), 1000, dtype=torch.int64, device="cuda")
@@ -131,8 +133,9 @@ def test_warp_path_slow_resynchronisation():
     ln = host_u8(cb.buf)[16:16 + 256]
     assert sorted(set(ln.tolist())) == [7, 8, 9]
     eight = np.flatnonzero(ln == 8).astype(np.uint8)
-    x = RNG.choice(eight, _n(PER_SM, CHUNK))
-    _round_trip(x, cb, CHUNK)
+    x = RNG.choice(eight, _n(per_sm, chunk))
+    assert _mode(-(-x.size // chunk), chunk) == tw
+    _round_trip(x, cb, chunk)
 
 
 def test_warp_path_single_code_and_two_codes():
@@ -152,12 +155,13 @@ def test_warp_path_long_codes():
     _round_trip(x, cb, CHUNK)
 
 
-def test_warp_path_slices_past_the_staging_area():
+@pytest.mark.parametrize("tw,per_sm,chunk", [(1, PER_SM, CHUNK), (4, 8, 1 << 15), (28, 1, 1 << 18)])
+def test_warp_path_slices_past_the_staging_area(tw, per_sm, chunk):
     """Each chunk: a run of the 1-bit code's symbol, then wide data.  Slices are sized from the
     chunk's mean code length, so those in the run hold hundreds of symbols and take the path that
-    writes them straight to the output."""
-    chunk = CHUNK
-    n = _n(PER_SM, chunk)
+    writes them straight to the output (a warp per chunk, and teams of 4 and 28 warps)."""
+    n = _n(per_sm, chunk)
+    assert _mode(-(-n // chunk), chunk) == tw
     x = RNG.integers(0, 256, n, dtype=np.uint8)
     x.reshape(-1)[: (n // chunk) * chunk].reshape(-1, chunk)[:, : chunk // 2] = 0
     h = torch.full((256,), 1, dtype=torch.int64, device="cuda")
@@ -180,15 +184,17 @@ def test_warp_path_mixed_distributions():
     _round_trip(x, cb, chunk)
 
 
-def test_warp_path_corrupt_streams_detected():
-    chunk = CHUNK
-    n = _n(PER_SM, chunk)
+@pytest.mark.parametrize("tw,per_sm,chunk", [(1, PER_SM, CHUNK), (28, 1, 1 << 18)])
+def test_warp_path_corrupt_streams_detected(tw, per_sm, chunk):
+    n = _n(per_sm, chunk)
+    n_chunks = -(-n // chunk)
+    assert _mode(n_chunks, chunk) == tw
     x = _gauss(n, 8)
     d = dev_u8(x)
     cb = codec.build_codebook(codec.histogram(d))
     s = codec.encode(d, cb, chunk)
     out = torch.empty(n, dtype=torch.uint8, device="cuda")
-    for at, bump in ((2, 1), (2, -1), (700, 8), (-2, -3)):
+    for at, bump in ((2, 1), (2, -1), (n_chunks // 2, 8), (-2, -3)):
         off = s.off.clone()
         off[at] += bump
         st = codec.new_status()
