@@ -1185,7 +1185,7 @@ __device__ __forceinline__ void ws_code(const PlaneDec &s, const U8Tables &T, ui
 // symbols: staged (the first kWsStage; NOTE: with the first kWsList steps
 // noted) or, DIRECT, written to dst[0, room).  pos ends at the walk's exit;
 // badpos is the last position (relative to lo) where the bits were no code.
-template <bool DIRECT, bool NOTE, int NS>
+template <bool DIRECT, bool NOTE, int NS, bool TWO = false>
 __device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, size_t nbytes, const U8Tables &T,
                                          uint32_t &pos, uint32_t lo, uint32_t lim, uint8_t *stg, WsNotes nt,
                                          int &nsteps, int &badpos, uint8_t *dst, uint64_t room) {
@@ -1229,10 +1229,22 @@ __device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, si
         v = lng ? sym2 : v;
         bits = lng ? max(L2, 1u) : bits;
         c = lng ? 1u : c;
-        if (c > 1 && pos + bits > lim) {  // codes past lim in the entry: only the first starts before it
+        const bool cut = c > 1 && pos + bits > lim;
+        if (cut) {  // codes past lim in the entry: only the first starts before it
             v &= 0xffu;
             c = 1;
             bits = T.len[v];
+        }
+        if constexpr (TWO && !DIRECT) {
+            // short codes: a second lookup on the bits after a simple first entry, when its codes end by lim
+            const uint32_t top2 = __funnelshift_l(s.bl, s.bh, bits);
+            uint64_t v2;
+            uint32_t c2, b2;
+            lut_get(T, top2 >> (32 - 13), v2, c2, b2);
+            const bool take2 = !lng && !cut && c2 != 0 && pos + bits + b2 <= lim;
+            v |= take2 ? v2 << (8 * c) : 0ull;
+            bits += take2 ? b2 : 0u;
+            c += take2 ? c2 : 0u;
         }
         bits = max(bits, 1u);  // only a corrupt codebook has a zero-length entry: every step moves on
         if (DIRECT) {
@@ -1241,10 +1253,18 @@ __device__ __forceinline__ uint32_t ws_walk(PlaneDec &s_io, const uint8_t *p, si
             const uint32_t sh = 8u * static_cast<uint32_t>(fill);
             const uint32_t vl = static_cast<uint32_t>(v);
             const uint32_t w0 = a | (vl << sh);
-            const int nf = fill + static_cast<int>(c);  // <= 7: at most one word completes
+            const int nf = fill + static_cast<int>(c);  // <= 7 (<= 11 with a second lookup)
             if (nf >= 4 && st + 4 <= kWsStage) *reinterpret_cast<uint32_t *>(stg + st) = w0;
-            a = nf >= 4 ? __funnelshift_l(vl, 0u, sh) : w0;  // the bytes past the completed word
-            st += nf >= 4 ? 4 : 0;
+            if constexpr (TWO) {
+                const uint32_t vh = static_cast<uint32_t>(v >> 32);
+                const uint32_t w1 = __funnelshift_l(vl, vh, sh);
+                if (nf >= 8 && st + 8 <= kWsStage) *reinterpret_cast<uint32_t *>(stg + st + 4) = w1;
+                a = nf >= 8 ? __funnelshift_l(vh, 0u, sh) : (nf >= 4 ? w1 : w0);
+                st += nf & ~3;
+            } else {
+                a = nf >= 4 ? __funnelshift_l(vl, 0u, sh) : w0;  // the bytes past the completed word
+                st += nf >= 4 ? 4 : 0;
+            }
             fill = nf & 3;
         }
         n += c;
@@ -1488,6 +1508,9 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
         }
         B = max(B, 32u);
         B = (B + g - 1) / g * g;
+        // short codes (a mean of at most 6 bits): a second lookup a step (N(0, 8) bytes at 64 and 256 KiB
+        // chunks: +10 and +9 %); longer ones gain nothing from it and pay for it
+        const bool two = span <= 6ull * static_cast<uint64_t>(cnt);
         uint8_t *const dst0 = out + first;
         uint64_t entry = start, written = 0;
         while (entry < end) {
@@ -1503,7 +1526,8 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
             int ns = 0, badpos = -1;
             if (act) {
                 s.start(payload, nbytes, entry + lo);
-                cntw = ws_walk<false, true, L>(s, payload, nbytes, T, ex, lo, hi, stg, nt, ns, badpos, nullptr, 0);
+                cntw = two ? ws_walk<false, true, L, true>(s, payload, nbytes, T, ex, lo, hi, stg, nt, ns, badpos, nullptr, 0)
+                           : ws_walk<false, true, L>(s, payload, nbytes, T, ex, lo, hi, stg, nt, ns, badpos, nullptr, 0);
             }
             tm.sync();  // every slice's notes are in place
             const int ns_next = static_cast<int>(tm.next(static_cast<uint32_t>(ns)));
@@ -1549,7 +1573,8 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
                 ex = e;
                 badpos = -1;
                 int n2 = 0;
-                cntw = ws_walk<false, false, L>(s, payload, nbytes, T, ex, lo, hi, stg, nt, n2, badpos, nullptr, 0);
+                cntw = two ? ws_walk<false, false, L, true>(s, payload, nbytes, T, ex, lo, hi, stg, nt, n2, badpos, nullptr, 0)
+                           : ws_walk<false, false, L>(s, payload, nbytes, T, ex, lo, hi, stg, nt, n2, badpos, nullptr, 0);
                 skip = 0;
                 ent = e;
                 used_m = false;
