@@ -1658,9 +1658,9 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
 // team (a round costs the same however few slices have bits); otherwise one
 // lane per chunk from 256 chunks per SM, the split decode below that.
 // Measured (CUDA events, one call): the 16 GiB sweep (fixed codebook) at
-// 1 MiB chunks (108 per SM) 203 GB/s with a warp per chunk against 97 with
-// the split decode, at 256 KiB (431 per SM) 232 against 145 with one lane per
-// chunk, at 128 KiB (862 per SM) both 234; 1024 chunks (6.7 per SM): 1 GiB of
+// 1 MiB chunks (108 per SM) 231 GB/s with a warp per chunk against 97 with
+// the split decode, at 256 KiB (431 per SM) 238 against 146 with one lane per
+// chunk, at 128 KiB (862 per SM) 237 against 258; 1024 chunks (6.7 per SM): 1 GiB of
 // the sweep at 1 MiB chunks 161 to 183 GB/s with teams of 4 to 28 warps
 // against 98 split, 256 MiB of N(0, 8) bytes at 256 KiB 281 (4 warps)
 // against 222 split, 64 MiB at 64 KiB (9 rounds of 4 warps) 227 against 214
