@@ -800,11 +800,34 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     }
     const int lane = threadIdx.x & 31;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    // a warp takes 32 consecutive chunks; with spread, the warps of a block take groups spread over the
+    // a warp takes 32 consecutive chunks; with spread (1), the warps of a block take groups spread over the
     // input (group warp * gridDim.x + block), so that blocks, and the SMs they run on, meet every part of
-    // it alike where there are too few waves of blocks for the block scheduler to even them out
-    const size_t c = spread ? (static_cast<size_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x) * 32 + lane
-                            : static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // it alike where there are too few waves of blocks for the block scheduler to even them out; by rank
+    // (2), block b takes the range of consecutive chunks with the b-th most bits, so that the block
+    // scheduler, which starts blocks in index order, starts the costly ones first and ends on cheap ones
+    size_t blk = blockIdx.x;
+    if (spread == 2) {
+        uint64_t *cost = reinterpret_cast<uint64_t *>(dsm + sizeof(U8Tables) + static_cast<size_t>(blockDim.x) * kRingU8);
+        uint32_t *pick = reinterpret_cast<uint32_t *>(cost + gridDim.x);
+        for (uint32_t r = threadIdx.x; r < gridDim.x; r += blockDim.x) {
+            const size_t a = static_cast<size_t>(r) * blockDim.x, b = min(a + blockDim.x, n_chunks);
+            cost[r] = off[b] - off[a];
+        }
+        __syncthreads();
+        for (uint32_t r = threadIdx.x; r < gridDim.x; r += blockDim.x) {
+            const uint64_t kr = cost[r];
+            uint32_t rank = 0;
+            for (uint32_t q = 0; q < gridDim.x; ++q) {
+                const uint64_t kq = cost[q];
+                rank += (kq > kr || (kq == kr && q < r)) ? 1u : 0u;
+            }
+            if (rank == blockIdx.x) *pick = r;
+        }
+        __syncthreads();
+        blk = *pick;
+    }
+    const size_t c = spread == 1 ? (static_cast<size_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x) * 32 + lane
+                                 : blk * blockDim.x + threadIdx.x;
     const size_t c0 = c - lane;  // the warp's first chunk
     uint64_t start = 0, end = 0;
     int cnt = 0;
@@ -1966,10 +1989,13 @@ int decode_lanes(int max_smem, bool delta) {
     return b;
 }
 
-// Measured on the 16 GiB sweep (blocks of 896 consecutive chunks lie in one 256 MiB segment): at 64 KiB
-// chunks (1.93 waves) spread blocks 265 GB/s against 246; at 16 KiB (7.7 waves) 268 against 335, each
-// block then waiting for its slowest warp while the block scheduler evens out consecutive ones.
-constexpr int kSpreadWaves = 2;
+// Measured on the 16 GiB sweep (blocks of 896 consecutive chunks lie in one 256 MiB segment), GB/s:
+// at 128 KiB chunks (one wave) spread blocks 258, ranked ranges 234, consecutive 234; at 64 KiB (1.93
+// waves) ranked 273, spread 265, consecutive 246; at 16 KiB (7.7 waves) ranked 346, consecutive 335,
+// spread 268 (each spread block waits for its slowest warp).  Ranking costs each block a pass over the
+// launch's block ranges, hence its limit.
+constexpr int kSpreadWaves = 1;
+constexpr unsigned kRankBlocks = 2048;
 
 int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, size_t n, size_t chunk,
                      const huff_codebook *cb, uint8_t *out, int32_t *status, cudaStream_t s) {
@@ -2004,12 +2030,14 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
     }
     const int block = decode_block(n_chunks, sms);
     const unsigned blocks = static_cast<unsigned>((n_chunks + block - 1) / block);
-    const size_t smem = sizeof(U8Tables) + static_cast<size_t>(block) * kRingU8;
+    // blocks take spread chunks when they run in at most kSpreadWaves waves, ranges by rank up to
+    // kRankBlocks blocks
+    const int spread = blocks <= static_cast<unsigned>(kSpreadWaves * sms) ? 1 : (blocks <= kRankBlocks ? 2 : 0);
+    const size_t smem = sizeof(U8Tables) + static_cast<size_t>(block) * kRingU8 +
+                        (spread == 2 ? static_cast<size_t>(blocks) * 8 + 16 : 0);
     if (cudaFuncSetAttribute(k_decode_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return HUFF_ERR_CUDA;
-    // blocks take spread chunks when they run in at most kSpreadWaves waves
-    const int spread = blocks <= static_cast<unsigned>(kSpreadWaves * sms) ? 1 : 0;
     k_decode_u8<<<blocks, block, smem, s>>>(payload, bytes, off, n, chunk, cb, out, status, spread);
     return launch_status();
 }
