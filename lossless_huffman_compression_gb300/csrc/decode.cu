@@ -1996,6 +1996,7 @@ int decode_lanes(int max_smem, bool delta) {
 // launch's block ranges, hence its limit.
 constexpr int kSpreadWaves = 1;
 constexpr unsigned kRankBlocks = 2048;
+constexpr size_t kRankChunk = 4096;
 
 int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, size_t n, size_t chunk,
                      const huff_codebook *cb, uint8_t *out, int32_t *status, cudaStream_t s) {
@@ -2031,8 +2032,11 @@ int launch_decode_u8(const uint8_t *payload, size_t bytes, const uint64_t *off, 
     const int block = decode_block(n_chunks, sms);
     const unsigned blocks = static_cast<unsigned>((n_chunks + block - 1) / block);
     // blocks take spread chunks when they run in at most kSpreadWaves waves, ranges by rank up to
-    // kRankBlocks blocks
-    const int spread = blocks <= static_cast<unsigned>(kSpreadWaves * sms) ? 1 : (blocks <= kRankBlocks ? 2 : 0);
+    // kRankBlocks blocks of chunks of at least kRankChunk symbols (a block's ranking pass then costs
+    // under 1 % of its decode)
+    const int spread = blocks <= static_cast<unsigned>(kSpreadWaves * sms)
+                           ? 1
+                           : (blocks <= kRankBlocks && chunk >= kRankChunk ? 2 : 0);
     const size_t smem = sizeof(U8Tables) + static_cast<size_t>(block) * kRingU8 +
                         (spread == 2 ? static_cast<size_t>(blocks) * 8 + 16 : 0);
     if (cudaFuncSetAttribute(k_decode_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
