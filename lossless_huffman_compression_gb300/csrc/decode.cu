@@ -809,6 +809,7 @@ __global__ void __launch_bounds__(kMaxBlock, 1) k_decode_u8(const uint8_t *__res
     if (spread == 2) {
         uint64_t *cost = reinterpret_cast<uint64_t *>(dsm + sizeof(U8Tables) + static_cast<size_t>(blockDim.x) * kRingU8);
         uint32_t *pick = reinterpret_cast<uint32_t *>(cost + gridDim.x);
+        if (threadIdx.x == 0) *pick = blockIdx.x;  // (the ranks are a permutation: some thread overwrites it)
         for (uint32_t r = threadIdx.x; r < gridDim.x; r += blockDim.x) {
             const size_t a = static_cast<size_t>(r) * blockDim.x, b = min(a + blockDim.x, n_chunks);
             cost[r] = off[b] - off[a];
