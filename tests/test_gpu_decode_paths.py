@@ -1,7 +1,9 @@
 """The byte-stream decode's one-lane path and its few-chunk cases, bit-exact.
 
 huff_decode gives every chunk one lane when there are enough chunks to fill
-the GPU (at least 768 per SM).  With fewer, a team of warps takes each chunk
+the GPU (at least 768 per SM); in one wave of blocks a block's warps spread
+over the input, in more waves block b takes the range with the b-th most
+bits.  With fewer, a team of warps takes each chunk
 (a whole CTA of 28 warps when chunks are as few as here; every team size is
 tested in test_gpu_decode_warp.py) and each thread a slice of its bits, whose
 code boundaries are found by self-synchronisation: one walk per slice from
@@ -63,6 +65,28 @@ def test_one_lane_per_chunk_path(kind):
         x = RNG.choice(np.array([0, 1, 2, 255], dtype=np.uint8), n, p=[0.95, 0.03, 0.019, 0.001])
     cb = codec.build_codebook(codec.histogram(dev_u8(x)))
     _round_trip(x, cb, chunk)
+
+
+@pytest.mark.parametrize("waves", [1.0, 2.3])
+def test_one_lane_spread_and_ranked_blocks(waves):
+    """One lane per chunk in one wave of 896-lane blocks (the warps of a block spread over the input)
+    and in 2.3 waves of chunks of 4096 symbols (block b takes the range with the b-th most bits).
+    Regions of three widths under one codebook make the ranges' bit counts differ; ragged tail."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunk = 4096
+    n = int(waves * sms * 896) * chunk + 77
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    x = torch.empty(n, dtype=torch.uint8, device="cuda")
+    step = 64 << 20
+    for k, a in enumerate(range(0, n, step)):
+        m = min(step, n - a)
+        v = torch.randn(m, device="cuda", generator=g) * (4.0, 16.0, 48.0)[k % 3]
+        x[a:a + m] = torch.clamp(torch.round(v), -128, 127).to(torch.int8).view(torch.uint8)
+    cb = codec.build_codebook(codec.histogram(x[: 64 << 20]), flags=_lib.HUFF_COVER_ALL)
+    s = codec.encode(x, cb, chunk)
+    out = codec.decode(s, cb)
+    assert torch.equal(out, x)
 
 
 @pytest.mark.parametrize("n,chunk", [(1, 256), (1000, 256), (1000, 32), (100_003, 96), (65_536, 65_536), (65_537, 65_536),
