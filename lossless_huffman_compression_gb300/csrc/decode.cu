@@ -1511,7 +1511,7 @@ __global__ void __launch_bounds__(kWsWarps * 32, 1) k_decode_u8_ws(const uint8_t
     }
     if (g == 0) g = 1;
     const size_t n_chunks = (n + chunk - 1) / chunk;
-    // the CTA's share, chunks blockIdx.x + gridDim.x j, taken largest first (by their bits): a warp that
+    // the CTA's share, chunks blockIdx.x + gridDim.x j, taken largest first (by their bits): the team that
     // takes the share's last chunks then takes cheap ones, and the teams finish closer together
     const uint32_t share =
         n_chunks > blockIdx.x ? static_cast<uint32_t>((n_chunks - blockIdx.x + gridDim.x - 1) / gridDim.x) : 0u;
