@@ -642,6 +642,37 @@ def materialised_delta_stages(path, args, peak):
     return out
 
 
+def host_link(h_a, h_b, h_out, d_a, d_b, d_out, s1, s2, s3):
+    """The host link of this machine, measured after the e2e run with its own pinned buffers (its rate
+    differs from box to box): host to device on two streams at once, device to host, and both
+    directions at once; GB/s, CUDA events, the best of three."""
+    def timed(copies):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s1)
+            for st in (s2, s3):
+                st.wait_event(a)
+            nbytes = 0
+            for st, dst, src in copies:
+                with torch.cuda.stream(st):
+                    dst.copy_(src, non_blocking=True)
+                nbytes += src.numel() * src.element_size()
+            for st in (s2, s3):
+                s1.wait_stream(st)
+            b.record(s1)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return round(nbytes / best / 1e6, 1)
+    return {"h2d_gbs": timed([(s1, d_a, h_a), (s2, d_b, h_b)]),
+            "d2h_gbs": timed([(s3, h_out, d_out)]),
+            "both_gbs": timed([(s1, d_a, h_a), (s2, d_b, h_b), (s3, h_out, d_out)]),
+            "how": "after the timed e2e steps: x1 and x0 to the device on two streams; the output to the host; "
+                   "all three at once"}
+
+
 def e2e_snapshot(path, x0, x1, args, dist, dev):
     """Same step through the public API with HOST buffers: copies inside the timed region.
 
@@ -742,9 +773,11 @@ def e2e_snapshot(path, x0, x1, args, dist, dev):
     total = sum_over_ranks(dist, float(2 * n), dev)
     h2d = 2 * n * 2 + cap_hi + cap_lo + 2 * 8 * (path.nc + 1)
     d2h = 2 * n + cap_hi + cap_lo + 2 * 8 * (path.nc + 1)
+    link = host_link(h_x1, h_x0, h_out, d_x1[0], d_x0[0], d_out[0], s_in, s_in2, s_out)
+    link["moved_gbs"] = round((h2d + d2h) / ms / 1e6, 1)  # both directions, the e2e step's own rate
     del d_x1, d_x0, d_out, paths
     return {"value": round(total / ms / 1e6, 2), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": steps,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "link": link,
             "api": "lmc_histogram_bf16_counted, huff_build_codebooks, lmc_encode_bf16_counted, lmc_decode_bf16 with pinned host "
                    "inputs, streams copied to host and back; a pipeline over six streams (input copies, compress, "
                    "round trip, decompress, output copy), consecutive steps on alternating buffer sets"}
